@@ -1,0 +1,110 @@
+/*
+ * dspark_oracle.h -- plain CPU oracle for the DSpark per-cycle hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This code exists to check the CUDA library.
+ * Only the test suite, the smoke check and the CPU-baseline leg of the
+ * benchmark may load it; the product path never does.
+ *
+ * Single-threaded, fp64 arithmetic, written to be read against the pages:
+ *   [D] "DSpark: confidence-scheduled speculative decoding" (ai-papers-daily
+ *       digest): eq. (4) causal block distribution, eq. (5) Markov head,
+ *       eq. (6) RNN head, eq. (7) confidence head, Module E + Algorithm 1
+ *       (hardware-aware prefix scheduler), Appendix A (non-anticipation),
+ *       production section (asynchronous top-K scheduler, flattened batch).
+ *   [E] "DSpark explained" (interactive explainer), section 06: single-token
+ *       rule accept with min(1, p/q), else resample from norm(max(0, p-q)).
+ *
+ * Random numbers: Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC'11), implemented here from its
+ * published definition.  Counter layout (a reading; the pages name no RNG):
+ *   key     = (seed low 32 bits, seed high 32 bits)
+ *   counter = (word0, word1, request, (cycle << 2) | stream)
+ *   stream 0: draft Gumbel noise      word0 = v / 4, word1 = step k (1..gamma),
+ *                                     output word v % 4 belongs to vocab entry v
+ *   stream 1: acceptance uniforms     word0 = 0, word1 = row position j, word 0
+ *   stream 2: residual / bonus Gumbel word0 = v / 4, word1 = row position
+ *   stream 3: reserved for synthetic-input noise
+ * Word to uniform: u = ((w >> 9) + 0.5) * 2^-23, strictly inside (0, 1).
+ *
+ * Parity pins for every function are in tests/test_oracle_*.py.
+ */
+#ifndef DSPARK_ORACLE_H
+#define DSPARK_ORACLE_H
+
+#include <stdint.h>
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types of the tensor inputs */
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* scheduler modes */
+#define ORACLE_SCHED_SYNC 0     /* Algorithm 1 with the early-stop break     */
+#define ORACLE_SCHED_ASYNC 1    /* top-K of the current order, K from t-2    */
+#define ORACLE_SCHED_NOBREAK 2  /* backtracking global search (lossy; tests) */
+
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+double oracle_uniform(uint32_t word);
+uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t req,
+                            uint64_t cycle, uint32_t stream, uint32_t lane);
+
+/* Markov-head draft (eqs. 4, 5, 7).  All requests independent; `reqs` lists
+ * the requests to compute (NULL = all R, in order), outputs are indexed by
+ * position in that list.  Optional outputs may be NULL.
+ *   U [R, gamma, V], h [R, gamma, d], W1 [V, r], W2t [V, r] (row v = column v
+ *   of W_2), w [d + r] f32, sts_T [gamma] f32 or NULL, anchor [R].
+ * Outputs: x [n, gamma], logq, lse, c [n, gamma], gap [n, gamma] = gap
+ * between the two largest Gumbel-perturbed scores, z [n, gamma, V] logits. */
+int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
+                        const void *U, const void *h, const void *W1, const void *W2t,
+                        const float *w, const float *sts_T, const int32_t *anchor,
+                        uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
+                        int32_t *x, double *logq, double *lse, double *c, double *gap,
+                        double *z);
+
+/* RNN-head draft (eq. 6).  W [3r, 2r + d]: rows [0, r) gate, [r, 2r) candidate,
+ * [2r, 3r) output.  s0 [R, r] f32 or NULL (zero).  Extra output: A [n, gamma, r],
+ * the vector tanh(W_o z_k) whose product with W_2 is the bias B_k. */
+int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
+                     const void *U, const void *h, const void *W1, const void *W2t,
+                     const void *W, const float *s0, const float *w, const float *sts_T,
+                     const int32_t *anchor, uint64_t seed, uint64_t cycle,
+                     const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
+                     double *lse, double *c, double *gap, double *z, double *A);
+
+/* Hardware-aware prefix scheduler (Module E, Algorithm 1; production async
+ * variant).  c [R, gamma] f32; sps[i] = SPS(B_min + i) for i < B_count.
+ * Outputs: ell [R], K_out (argmax of Theta over the sorted pool, no break),
+ * theta_best, a [R, gamma] f32 (may be NULL).  Returns 0, or -1 if the table
+ * does not cover B in [R, R(gamma + 1)]. */
+int oracle_schedule(int R, int gamma, const float *c, const double *sps, int B_min,
+                    int B_count, int mode, int K_in, int32_t *ell, int32_t *K_out,
+                    double *theta_best, float *a);
+
+/* Lossless verification ([E] section 06; [D] overview step 3).
+ *   T [N, V] target logits of the flattened batch, tags [N][2] = (request,
+ *   position), grouped by request with positions 0..ell_r ascending.
+ *   x [R, gamma] drafted tokens, logq / lse [R, gamma] f32 from the draft.
+ *   Residual bias: A [R, gamma, r] f32 if non-NULL (RNN head), else W1[x_n].
+ * Requests listed in `reqs` (NULL = all) are verified; outputs are full-size
+ * [R] / [R, gamma + 1] / [N] arrays, written only for those requests.
+ *   n_accept [R], out_tokens [R, gamma + 1] (-1 padded), next_anchor [R],
+ *   lse_p [N], logp [N] (NaN on rows without a test), margin [N] =
+ *   (log p - log q) - log u, gap [R] = top-two score gap of the final sample.
+ * Returns 0, or -1 on malformed tags. */
+int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *T,
+                  const int32_t *tags, const int32_t *anchor, const int32_t *x,
+                  const float *logq, const float *lse, const void *U, const void *W1,
+                  const void *W2t, const float *A, uint64_t seed, uint64_t cycle,
+                  const int32_t *reqs, int n_reqs, int32_t *n_accept, int32_t *out_tokens,
+                  int32_t *next_anchor, double *lse_p, double *logp, double *margin,
+                  double *gap);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
