@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark per-cycle hot path on GB300.
+
+One step = one decoding cycle of the workload: the gamma-step Markov draft
+(fused bias contraction + exact softmax normaliser + Gumbel-max sample +
+confidence, per step) followed by verification of every drafted token of the
+flattened batch (the qwen4b workload verifies all R * (gamma + 1) rows; workloads
+with a profiled SPS table also run the prefix scheduler and verify only the
+scheduled rows).
+
+Prints ONE JSON line (rank 0).  `value` is drafted-and-verified tokens per second
+of device time, R * gamma / (T_draft + T_schedule + T_verify), summed over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dspark|reference]
+                  [--workload qwen4b|heavy|prod|rnn|tiny]
+
+`--impl reference` times the CPU oracle (the plain single-threaded checker) on a
+bounded sample of requests of the same workload; it is the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_drafter_markov_gb300 import _lib as dsp  # noqa: E402
+from speculative_decoding_drafter_markov_gb300 import workloads as W  # noqa: E402
+
+METRIC = "drafted tok/s (R·γ) + verified tok/s at 1 GB300; % of HBM/TC roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
+    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def _workload_desc(wl):
+    return (f"{wl.name}: R={wl.R} gamma={wl.gamma} V={wl.V} r={wl.r} d={wl.d} {wl.dtype} "
+            f"{wl.head} head, scheduler={wl.sched}")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class Cycle:
+    """Preallocated buffers and the enqueue order of one decoding cycle."""
+
+    def __init__(self, wl, seed, device):
+        self.wl = wl
+        self.dev = device
+        inp = W.draft_inputs(wl, seed=seed, device=device)
+        self.inp = inp
+        R, gm, V = wl.R, wl.gamma, wl.V
+        self.out = {"x": torch.empty((R, gm), dtype=torch.int32, device=device),
+                    "logq": torch.empty((R, gm), dtype=torch.float32, device=device),
+                    "lse": torch.empty((R, gm), dtype=torch.float32, device=device),
+                    "c": torch.empty((R, gm), dtype=torch.float32, device=device)}
+        ws_bytes = dsp.draft_markov_workspace_size(inp["U"], inp["h"], inp["W1"], inp["W2t"],
+                                                   inp["w"], inp["anchor"])
+        self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+        # verification batch: every drafted token (no scheduler), or the capacity
+        # R (gamma + 1) with the scheduler's device-side row count
+        self.sched = wl.sched != "none"
+        cap = R * (gm + 1)
+        ell_all = np.full(R, gm)
+        self.tags = torch.as_tensor(W.tags_from_ell(ell_all), device=device)
+        self.T = W.target_logits(wl, inp["U"], inp["U_bonus"], W.tags_from_ell(ell_all), seed=seed)
+        assert self.T.shape[0] == cap
+        if self.sched:
+            B_min, _ = wl.B_range
+            self.B_min = B_min
+            self.sps = torch.as_tensor(W.sps_table(wl, seed), device=device)
+            self.K_hist = [torch.full((1,), -1, dtype=torch.int32, device=device) for _ in range(3)]
+            self.N_dev = torch.empty(1, dtype=torch.int32, device=device)
+            self.tags_sched = torch.empty((cap, 2), dtype=torch.int32, device=device)
+            self.sched_out = {"ell": torch.empty(R, dtype=torch.int32, device=device),
+                              "K_out": self.K_hist[0],
+                              "theta_best": torch.empty(1, dtype=torch.float64, device=device)}
+        self.vout = {"n_accept": torch.empty(R, dtype=torch.int32, device=device),
+                     "out_tokens": torch.empty((R, gm + 1), dtype=torch.int32, device=device),
+                     "next_anchor": torch.empty(R, dtype=torch.int32, device=device)}
+        if self.sched:
+            # target rows of the scheduled batch are gathered from the full grid
+            # (a stand-in for the target forward; not part of the timed stages)
+            self.T_sched = torch.empty_like(self.T)
+        nbytes = dsp.verify_workspace_size(self.T, self.tags, inp["anchor"], self.out["x"],
+                                           self.out["logq"], self.out["lse"], inp["U"], inp["W1"],
+                                           inp["W2t"])
+        self.vws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        self.launches_per_cycle = 2 * gm + 4 + (2 if self.sched else 0)
+
+    def draft_step(self, k, cycle):
+        i = self.inp
+        dsp.draft_markov_step(k, i["U"], i["h"], i["W1"], i["W2t"], i["w"], i["anchor"],
+                              out=self.out, ws=self.ws, seed=1234, cycle=cycle)
+
+    def schedule(self, cycle):
+        if not self.sched:
+            return
+        mode = dsp.SCHED_ASYNC if self.wl.sched == "async" else dsp.SCHED_SYNC
+        k_in = self.K_hist[(cycle + 1) % 3] if mode == dsp.SCHED_ASYNC else None
+        self.sched_out["K_out"] = self.K_hist[cycle % 3]
+        dsp.schedule(self.out["c"], self.sps, self.B_min, mode=mode, K_in=k_in, out=self.sched_out)
+        dsp.build_tags(self.sched_out["ell"], self.wl.gamma, tags=self.tags_sched, N_out=self.N_dev)
+
+    def target(self):
+        """Target logits of the scheduled rows (harness stand-in for the target model)."""
+        if self.sched:
+            t = self.tags_sched.long()
+            torch.index_select(self.T, 0, t[:, 0] * (self.wl.gamma + 1) + t[:, 1], out=self.T_sched)
+
+    def verify(self, cycle):
+        i = self.inp
+        tags = self.tags_sched if self.sched else self.tags
+        N_dev = self.N_dev if self.sched else None
+        T = self.T_sched if self.sched else self.T
+        dsp.verify(T, tags, i["anchor"], self.out["x"], self.out["logq"], self.out["lse"],
+                   i["U"], i["W1"], i["W2t"], N_dev=N_dev, seed=1234, cycle=cycle,
+                   out=self.vout, ws=self.vws)
+
+    def verified_tokens(self):
+        if self.sched:
+            return int(self.sched_out["ell"].sum().item())
+        return self.wl.R * self.wl.gamma
+
+
+def draft_step_bytes(wl):
+    """Algorithmic bytes of one draft step: U_k rows, W_2 streamed once, the
+    gathered W_1 rows, h_k and w (fp32)."""
+    es = 4 if wl.dtype == "f32" else 2
+    return (wl.R * wl.V + wl.V * wl.r + wl.R * wl.r + wl.R * wl.d) * es + (wl.d + wl.r) * 4
+
+
+def run_dspark(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.WORKLOADS[args.workload]
+    cyc = Cycle(wl, seed=1000 + rank, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    gm = wl.gamma
+
+    def one_cycle(c, ev=None):
+        for k in range(1, gm + 1):
+            if ev is not None:
+                ev["k0"][k - 1].record(stream)
+            cyc.draft_step(k, c)
+            if ev is not None:
+                ev["k1"][k - 1].record(stream)
+        if ev is not None:
+            ev["d"].record(stream)
+        cyc.schedule(c)
+        if ev is not None:
+            ev["s"].record(stream)
+        cyc.target()
+        if ev is not None:
+            ev["g"].record(stream)
+        cyc.verify(c)
+
+    for c in range(args.warmup):
+        flush.zero_()
+        one_cycle(c)
+    torch.cuda.synchronize()
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    events = [{"a": mk(), "b": mk(), "d": mk(), "s": mk(), "g": mk(), "k0": [mk() for _ in range(gm)],
+               "k1": [mk() for _ in range(gm)]} for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    verified = 0
+    for s in range(args.steps):
+        flush.zero_()  # L2 flush between timed iterations (outside the timed span)
+        ev = events[s]
+        ev["a"].record(stream)
+        one_cycle(args.warmup + s, ev)
+        ev["b"].record(stream)
+        if cyc.sched:
+            torch.cuda.synchronize()
+            verified += cyc.verified_tokens()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    if not cyc.sched:
+        verified = args.steps * wl.R * gm
+    t_draft = [e["a"].elapsed_time(e["d"]) for e in events]  # ms
+    t_sched = [e["d"].elapsed_time(e["s"]) for e in events]
+    t_verify = [e["g"].elapsed_time(e["b"]) for e in events]
+    # cycle time without the harness's target-row gather
+    t_cycle = [a + b + c for a, b, c in zip(t_draft, t_sched, t_verify)]
+    t_steps = [e["k0"][k].elapsed_time(e["k1"][k]) for e in events for k in range(gm)]
+    total_ms = sum(t_cycle)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    drafted = args.steps * wl.R * gm
+    value = world * drafted / (total_ms / 1e3)
+
+    hbm, tc, peak_kind = _peaks()
+    step_us = 1e3 * statistics.mean(t_steps)
+    bytes_step = draft_step_bytes(wl)
+    achieved = bytes_step / (step_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->f32" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": _workload_desc(wl),
+                   "verify_rows": "all R*(gamma+1)" if not cyc.sched else "scheduled",
+                   "l2": "256 MB buffer written between timed steps; U and T also exceed L2",
+                   "parallelism": f"replicas x{world} (requests independent)"},
+        "drafted_tok_s": world * drafted / (sum(t_draft) / 1e3),
+        "verified_tok_s": world * verified / ((sum(t_sched) + sum(t_verify)) / 1e3),
+        "stage_us": {"draft": 1e3 * statistics.mean(t_draft),
+                     "draft_step": step_us,
+                     "schedule": 1e3 * statistics.mean(t_sched),
+                     "verify": 1e3 * statistics.mean(t_verify)},
+        "roofline": {"kernel": "draft step (fused contraction + epilogue, then row merge)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes_per_launch": bytes_step, "traffic": None},
+        "gpu_launches": args.steps * cyc.launches_per_cycle,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(cyc, args, stream, flush)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+    return line, rank
+
+
+def run_e2e(cyc, args, stream, flush):
+    """Same cycle through the public API from pinned host buffers: per step the
+    H2D copy of that cycle's inputs (base logits, hidden states, anchors, target
+    logits) and the D2H read of the results are inside the timed span."""
+    wl, i = cyc.wl, cyc.inp
+    host_in = {k: i[k].cpu().pin_memory() for k in ("U", "h", "anchor")}
+    host_T = cyc.T.cpu().pin_memory()
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory()
+                for k, v in (("out_tokens", cyc.vout["out_tokens"]),
+                             ("n_accept", cyc.vout["n_accept"]), ("c", cyc.out["c"]))}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_T.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    total = 0.0
+    n = max(3, min(args.steps, 10))
+    for s in range(n + 2):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for k, t in host_in.items():
+            i[k].copy_(t, non_blocking=True)
+        cyc.T.copy_(host_T, non_blocking=True)
+        for k in range(1, wl.gamma + 1):
+            cyc.draft_step(k, 10_000 + s)
+        cyc.schedule(10_000 + s)
+        cyc.target()
+        cyc.verify(10_000 + s)
+        host_out["out_tokens"].copy_(cyc.vout["out_tokens"], non_blocking=True)
+        host_out["n_accept"].copy_(cyc.vout["n_accept"], non_blocking=True)
+        host_out["c"].copy_(cyc.out["c"], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if s >= 2:
+            total += a.elapsed_time(b)
+    return {"value": n * wl.R * wl.gamma / (total / 1e3), "unit": "tok/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def _oracle_sample(wl, n_req, seed=0):
+    """Host inputs of `n_req` requests of the workload (same shapes per request)."""
+    import dataclasses
+    sub = dataclasses.replace(wl, R=n_req)
+    inp = W.draft_inputs(sub, seed=seed, device="cpu")
+    to_np = W.bf16_bits
+    h = {k: to_np(v) for k, v in inp.items() if k not in ("U_bonus",)}
+    ell = np.full(n_req, wl.gamma)
+    tags = W.tags_from_ell(ell)
+    T = to_np(W.target_logits(sub, inp["U"], inp["U_bonus"], tags, seed=seed))
+    return h, tags, T
+
+
+def _oracle_cycle(orc, h, tags, T, cycle):
+    d = orc.draft_markov(h["U"], h["h"], h["W1"], h["W2t"], h["w"], h["anchor"], seed=1234,
+                         cycle=cycle)
+    orc.verify(T, tags, h["anchor"], d["x"], d["logq"].astype(np.float32),
+               d["lse"].astype(np.float32), h["U"], h["W1"], h["W2t"], seed=1234, cycle=cycle)
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle as it stands, one host core, on a bounded sample of requests of
+    the same workload (full vocabulary, full gamma, verify all): drafted and
+    verified tokens per second, extrapolated per request."""
+    import oracle as orc
+    orc.build()
+    h, tags, T = _oracle_sample(wl, 1)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_cycle(orc, h, tags, T, done)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 64:
+            break
+    return {"value": done * wl.gamma / el, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} request-cycles of {wl.name} (full V={wl.V}, gamma={wl.gamma}, "
+                      f"verify all), single-threaded C oracle, {el:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on each step's bounded sample (one request),
+    same metric and unit."""
+    if rank != 0:
+        return None
+    import oracle as orc
+    orc.build()
+    wl = W.WORKLOADS[args.workload]
+    h, tags, T = _oracle_sample(wl, 1)
+    for c in range(args.warmup):
+        _oracle_cycle(orc, h, tags, T, c)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        _oracle_cycle(orc, h, tags, T, args.warmup + s)
+    el = time.perf_counter() - t0
+    value = args.steps * wl.gamma / el
+    return {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": _workload_desc(wl), "sample": "1 request per step"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"1 request per step of {wl.name}, {args.steps} steps"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = _args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line, rank = run_dspark(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

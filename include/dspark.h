@@ -1,0 +1,221 @@
+/*
+ * dspark.h -- C ABI of the DSpark per-cycle hot path on one GB300 (sm_103a).
+ *
+ * The method is DSpark's semi-autoregressive draft + confidence-scheduled
+ * verification, as described in
+ *   [D] "DSpark: confidence-scheduled speculative decoding" (ai-papers-daily
+ *       digest): eq. (4) causal block distribution, eq. (5) Markov head,
+ *       eq. (6) RNN head, eq. (7) confidence head, Module D (sequential
+ *       temperature scaling), Module E + Algorithm 1 (prefix scheduler),
+ *       Appendix A, production section (async top-K, flattened batch);
+ *   [E] "DSpark explained" (interactive explainer), section 06 (single-token
+ *       rejection rule).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller; row-major,
+ *   contiguous, with the shapes given per field.  The library allocates no
+ *   device memory: scratch comes from the caller through `ws`, whose size the
+ *   matching *_workspace_size() function returns (256-byte aligned pointer).
+ * - Every call only enqueues work on `stream` (a cudaStream_t) and returns
+ *   without synchronising.  Calls on one stream run in order.
+ * - dtype: DSPARK_F32 or DSPARK_BF16 applies to U, h, W1, W2t, W and T.
+ *   Logits accumulate in fp32 whatever the storage type.
+ * - Return value: DSPARK_OK, or an error code for a problem the host can see
+ *   (bad shape, NULL pointer, unsupported size, CUDA launch failure); the
+ *   message is in dspark_last_error() (thread-local).  Problems only the
+ *   device can see (a token id >= V, malformed tags, a confidence outside
+ *   [0, 1], non-finite logits) are written as the first non-zero error code
+ *   into `*err` (a device int32 the caller zeroes; may be NULL to ignore) and
+ *   the outputs of the affected rows are then unspecified.
+ * - Sampling is deterministic given (seed, cycle): Philox-4x32-10 with
+ *   key = (seed lo, seed hi) and counter = (w0, w1, request, cycle << 2 | stream);
+ *   stream 0 draft Gumbel noise (w0 = v / 4, w1 = step k, word v % 4),
+ *   stream 1 acceptance uniforms (w0 = 0, w1 = position j, word 0),
+ *   stream 2 residual / bonus Gumbel noise (w0 = v / 4, w1 = position).
+ *   A word w maps to u = ((w >> 9) + 1/2) 2^-23.  Only the low 30 bits of
+ *   `cycle` enter the counter.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+typedef struct CUstream_st *dspark_stream_t; /* same type as cudaStream_t */
+
+enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVAL = 1,       /* bad argument: NULL pointer, shape, mode     */
+    DSPARK_ERR_RANGE = 2,       /* token id >= V, B outside the SPS table,     */
+                                /* confidence outside [0, 1]                   */
+    DSPARK_ERR_NONFINITE = 3,   /* NaN / Inf logits left no sample             */
+    DSPARK_ERR_CUDA = 4,        /* a CUDA runtime call failed                  */
+    DSPARK_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up          */
+    DSPARK_ERR_UNSUPPORTED = 6  /* size beyond what this build handles         */
+};
+
+enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
+enum { DSPARK_SCHED_SYNC = 0, DSPARK_SCHED_ASYNC = 1 };
+
+/* ------------------------------------------------------------------------ */
+/* Draft, Markov head.  [D] eq. (5) B(x_{k-1}, .) = W_1[x_{k-1}] W_2 added to  */
+/* the base logits U_k in eq. (4), sampled left to right for k = 1..gamma     */
+/* from the anchor x_0; confidence c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) */
+/* by eq. (7) with the Module D temperature T_k (1 when sts_T is NULL).       */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t R;            /* requests                                           */
+    int32_t gamma;        /* block length                                       */
+    int32_t V;            /* vocabulary                                         */
+    int32_t r;            /* rank of W_1 W_2                                    */
+    int32_t d;            /* hidden size of h                                   */
+    int32_t dtype;        /* DSPARK_F32 | DSPARK_BF16                           */
+    const void *U;        /* [R, gamma, V] base logits U_k                      */
+    const void *h;        /* [R, gamma, d] backbone hidden states h_k           */
+    const void *W1;       /* [V, r] embedding table W_1                         */
+    const void *W2t;      /* [V, r] W_2 transposed: row v is column v of W_2    */
+    const float *w;       /* [d + r] confidence weights (hidden part first)     */
+    const float *sts_T;   /* [gamma] temperatures T_k, or NULL for 1            */
+    const int32_t *anchor;/* [R] anchor tokens x_0                              */
+    uint64_t seed;        /* Philox key                                         */
+    uint64_t cycle;       /* decoding-cycle counter (Philox counter word 3)     */
+    int32_t *x;           /* out [R, gamma] drafted tokens x_1..x_gamma         */
+    float *logq;          /* out [R, gamma] log q_k(x_k)                        */
+    float *lse;           /* out [R, gamma] log sum_v exp(U_k(v) + B_k(v))      */
+    float *c;             /* out [R, gamma] confidences c_k                     */
+    int32_t *err;         /* device error word (see conventions), or NULL       */
+} dspark_draft_args;
+
+DSPARK_API size_t dspark_draft_markov_workspace_size(const dspark_draft_args *a);
+DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_stream_t stream);
+/* Step k (1..gamma) of the same loop alone: reads x_{k-1} (the anchor for
+ * k = 1, else column k-2 of a->x) and writes column k-1 of x, logq, lse, c.
+ * dspark_draft_markov equals calls for k = 1..gamma in order on one stream;
+ * the split lets an engine interleave other work between steps. */
+DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, void *ws,
+                                        dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Draft, RNN head.  [D] eq. (6): z_k = [s_{k-1}; W_1[x_{k-1}]; h_k],          */
+/* s_k = sigma(W_g z_k) s_{k-1} + (1 - sigma(W_g z_k)) tanh(W_c z_k),          */
+/* B_k = W_2^T tanh(W_o z_k); otherwise as the Markov head.                    */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    dspark_draft_args base; /* fields as for the Markov head                    */
+    const void *W;          /* [3r, 2r + d]: rows [0,r) W_g, [r,2r) W_c, [2r,3r) W_o */
+    const float *s0;        /* [R, r] initial state, or NULL for s_0 = 0        */
+    float *A;               /* out [R, gamma, r] A_k = tanh(W_o z_k), the vector */
+                            /* whose product with W_2 is B_k (verify needs it)  */
+    float *s_out;           /* out [R, r] final state s_gamma, or NULL          */
+} dspark_rnn_args;
+
+DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a);
+DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Hardware-aware prefix scheduler.  [D] Module E, Algorithm 1:               */
+/* a_{r,j} = prod_{i<=j} c_{r,i}; pool E = {(r,j): a_{r,j} > 0} sorted by a    */
+/* descending (ties: request, then position, ascending); scan with            */
+/* B = R + #admitted, tau = R + sum admitted a, Theta = tau * SPS(B).         */
+/*  - DSPARK_SCHED_SYNC: Algorithm 1 with the early-stop break.                */
+/*  - DSPARK_SCHED_ASYNC (production section): admit the top min(K, |E|)      */
+/*    entries of the current order, no break, with K read from *K_in (the     */
+/*    capacity computed two cycles earlier); *K_in < 0 or K_in == NULL falls  */
+/*    back to SYNC.  Both modes write *K_out = argmax_m Theta(m) over the     */
+/*    current pool without break (smallest m on ties), for use at cycle t+2.  */
+/* Number formats: a is an fp32 running product; tau is summed exactly as     */
+/* integers in units of 2^-32 (each a rounded to nearest-even on that grid);  */
+/* Theta = (tau units * 2^-32) * SPS(B) in fp64.  Results are bit-exact.      */
+/* Limits: R * gamma <= 8192.  The table must cover B in [R, R (gamma + 1)]   */
+/* (checked on the host: DSPARK_ERR_RANGE).                                   */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t R, gamma;
+    const float *c;        /* [R, gamma] confidences, each in [0, 1]            */
+    const double *sps;     /* [B_count] SPS(B_min + i), steps per second         */
+    int32_t B_min, B_count;
+    int32_t mode;          /* DSPARK_SCHED_SYNC | DSPARK_SCHED_ASYNC             */
+    const int32_t *K_in;   /* device scalar: async capacity, or NULL             */
+    int32_t *ell;          /* out [R] verify lengths l_r in 0..gamma             */
+    int32_t *K_out;        /* out device scalar: capacity for cycle t + 2        */
+    double *theta_best;    /* out device scalar: Theta at the admitted point     */
+    float *a;              /* out [R, gamma] survival products, or NULL          */
+    int32_t *err;
+} dspark_sched_args;
+
+DSPARK_API size_t dspark_schedule_workspace_size(const dspark_sched_args *a);
+DSPARK_API int dspark_schedule(const dspark_sched_args *a, void *ws, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Flattened batch layout ([D] production section, marker tensor): from     */
+/* ell [R] write tags [N, 2] = (request, position) for positions 0..l_r of   */
+/* each request in request order, and N = sum_r (1 + l_r) to *N_out (device).*/
+/* tags must hold R (gamma + 1) rows.                                         */
+/* ------------------------------------------------------------------------ */
+DSPARK_API int dspark_build_tags(int32_t R, int32_t gamma, const int32_t *ell, int32_t *tags,
+                                 int32_t *N_out, int32_t *err, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Lossless verification.  [E] section 06: accept x_{j+1} with probability    */
+/* min(1, p_j(x_{j+1}) / q_{j+1}(x_{j+1})), test: log u < log p - log q with */
+/* u from Philox stream 1; at the first rejection j* sample y from           */
+/* norm(max(0, p_{j*} - q_{j*+1})) (q recomputed from U, the bias operand and */
+/* W_2; p itself if the residual is empty); if all l_r tokens pass sample     */
+/* the bonus y from p_{l_r}.  Row i of T is the target's logits for position  */
+/* tags[i] = (r, j), i.e. the distribution of x_{j+1} given x_0..x_j; rows    */
+/* are grouped by request with positions 0..l_r ascending, every request      */
+/* present (violations: DSPARK_ERR_INVAL in *err).                            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t R, gamma, V, r, dtype;
+    int32_t N;              /* rows of T (the capacity when N_dev is given)     */
+    const int32_t *N_dev;   /* device scalar: rows in use, or NULL for N        */
+    const void *T;          /* [N, V] target logits, flattened                  */
+    const int32_t *tags;    /* [N, 2] (request, position)                       */
+    const int32_t *anchor;  /* [R] x_0                                          */
+    const int32_t *x;       /* [R, gamma] drafted tokens                        */
+    const float *logq;      /* [R, gamma] from the draft                        */
+    const float *lse;       /* [R, gamma] from the draft                        */
+    const void *U;          /* [R, gamma, V] base logits (residual recompute)   */
+    const void *W1;         /* [V, r] (Markov bias operand W_1[x_j])            */
+    const void *W2t;        /* [V, r]                                           */
+    const float *A;         /* [R, gamma, r] RNN bias operands, or NULL (Markov)*/
+    uint64_t seed, cycle;
+    int32_t *n_accept;      /* out [R] accepted draft tokens n_r                */
+    int32_t *out_tokens;    /* out [R, gamma + 1] x_1..x_{n_r}, y, then -1      */
+    int32_t *next_anchor;   /* out [R] y, the next cycle's anchor               */
+    float *lse_p;           /* out [N] log sum exp of each row, or NULL         */
+    float *logp;            /* out [N] log p_j(x_{j+1}) (NaN on last rows), or NULL */
+    int32_t *err;
+} dspark_verify_args;
+
+DSPARK_API size_t dspark_verify_workspace_size(const dspark_verify_args *a);
+DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Helpers                                                                    */
+/* ------------------------------------------------------------------------ */
+/* Message of the last failing call on this host thread ("" if none). */
+DSPARK_API const char *dspark_last_error(void);
+/* Library version as major * 10000 + minor * 100 + patch. */
+DSPARK_API int dspark_version(void);
+/* Philox-4x32-10 on the device: out[i][0..3] for counters ctr[i][0..3] and
+ * key (seed lo, seed hi), i < n.  Exposes the sampler's generator for checks. */
+DSPARK_API int dspark_philox(const uint32_t *ctr, uint64_t seed, int32_t n, uint32_t *out,
+                             dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

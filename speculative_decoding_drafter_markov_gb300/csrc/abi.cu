@@ -1,0 +1,271 @@
+// abi.cu -- the C ABI declared in include/dspark.h: argument checks, workspace
+// carving and kernel launches.  Nothing here synchronises or allocates.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+    return fail(DSPARK_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+int ok() {
+    g_last_error.clear();
+    return DSPARK_OK;
+}
+
+constexpr int kMaxRank = 512;  // shared-memory bound of the CUDA-core draft kernels
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_draft(const dspark_draft_args *a) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->R < 1 || a->gamma < 1 || a->V < 1 || a->r < 1 || a->d < 0)
+        return fail(DSPARK_ERR_INVAL, "bad shape R=%d gamma=%d V=%d r=%d d=%d", a->R, a->gamma, a->V,
+                    a->r, a->d);
+    if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16)
+        return fail(DSPARK_ERR_INVAL, "bad dtype %d", a->dtype);
+    if (a->r > kMaxRank) return fail(DSPARK_ERR_UNSUPPORTED, "rank r=%d above %d", a->r, kMaxRank);
+    if (!a->U || !a->W1 || !a->W2t || !a->w || !a->anchor || !a->x || !a->logq || !a->lse || !a->c ||
+        (a->d > 0 && !a->h))
+        return fail(DSPARK_ERR_INVAL, "null tensor pointer");
+    return DSPARK_OK;
+}
+
+size_t draft_partials_bytes(int R, int V) {
+    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)R * dspark::draft_step_nparts(V));
+}
+
+// the gamma sequential steps shared by both heads
+int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws, cudaStream_t s,
+                   const dspark::RnnStep *rnn, int k_first, int k_last) {
+    using namespace dspark;
+    DraftStep st{};
+    st.R = a->R; st.V = a->V; st.r = a->r; st.gamma = a->gamma; st.dtype = a->dtype;
+    st.U = a->U; st.W1 = a->W1; st.W2t = a->W2t;
+    st.seed = a->seed; st.cycle = a->cycle;
+    st.part = static_cast<DraftPartial *>(part_ws);
+    st.nparts = draft_step_nparts(a->V);
+    st.err = a->err;
+    DraftReduce rd{};
+    rd.R = a->R; rd.V = a->V; rd.r = a->r; rd.d = a->d; rd.gamma = a->gamma; rd.dtype = a->dtype;
+    rd.part = st.part; rd.nparts = st.nparts;
+    rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
+    rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
+    for (int k = k_first; k <= k_last; ++k) {
+        const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
+        const int xs = k == 1 ? 1 : a->gamma;
+        if (rnn) {
+            RnnStep rs = *rnn;
+            rs.k = k;
+            rs.x_prev = xp;
+            rs.x_stride = xs;
+            cudaError_t e = launch_rnn_step(rs, s);
+            if (e != cudaSuccess) return cuda_fail(e, "rnn step");
+            st.A_op = A_rnn + (size_t)(k - 1) * a->r;
+            st.a_stride = a->gamma * a->r;
+        }
+        st.k = k;
+        st.x_prev = xp;
+        st.x_stride = xs;
+        cudaError_t e = launch_draft_step(st, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft step");
+        rd.k = k;
+        rd.x_prev = xp;
+        rd.x_stride = xs;
+        e = launch_draft_reduce(rd, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft reduce");
+    }
+    return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+DSPARK_API const char *dspark_last_error(void) { return g_last_error.c_str(); }
+
+DSPARK_API int dspark_version(void) { return 100; }
+
+DSPARK_API size_t dspark_draft_markov_workspace_size(const dspark_draft_args *a) {
+    if (check_draft(a) != DSPARK_OK) return 0;
+    return draft_partials_bytes(a->R, a->V);
+}
+
+DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_stream_t stream) {
+    int rc = check_draft(a);
+    if (rc != DSPARK_OK) return rc;
+    if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
+    rc = run_draft_loop(a, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), nullptr, 1, a->gamma);
+    return rc == DSPARK_OK ? ok() : rc;
+}
+
+DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, void *ws,
+                                        dspark_stream_t stream) {
+    int rc = check_draft(a);
+    if (rc != DSPARK_OK) return rc;
+    if (k < 1 || k > a->gamma) return fail(DSPARK_ERR_INVAL, "step k=%d outside 1..%d", k, a->gamma);
+    if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
+    rc = run_draft_loop(a, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), nullptr, k, k);
+    return rc == DSPARK_OK ? ok() : rc;
+}
+
+DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a) {
+    if (!a || check_draft(&a->base) != DSPARK_OK) return 0;
+    const dspark_draft_args &b = a->base;
+    return draft_partials_bytes(b.R, b.V) + dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
+           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
+}
+
+DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_stream_t stream) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    int rc = check_draft(&a->base);
+    if (rc != DSPARK_OK) return rc;
+    if (!a->W || !a->A) return fail(DSPARK_ERR_INVAL, "null RNN tensor pointer");
+    if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
+    const dspark_draft_args &b = a->base;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *p = static_cast<char *>(ws);
+    void *part = p;
+    p += draft_partials_bytes(b.R, b.V);
+    float *state = reinterpret_cast<float *>(p);
+    p += dspark::align256(sizeof(float) * (size_t)b.R * b.r);
+    float *Hpre = reinterpret_cast<float *>(p);
+    cudaError_t e = a->s0 ? cudaMemcpyAsync(state, a->s0, sizeof(float) * (size_t)b.R * b.r,
+                                            cudaMemcpyDeviceToDevice, s)
+                          : cudaMemsetAsync(state, 0, sizeof(float) * (size_t)b.R * b.r, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rnn state init");
+    if (b.d > 0) {
+        e = dspark::launch_rnn_hproj(b.R * b.gamma, b.d, b.r, b.dtype, b.h, a->W, Hpre, s);
+    } else {
+        e = cudaMemsetAsync(Hpre, 0, sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "rnn h projection");
+    dspark::RnnStep rs{};
+    rs.R = b.R; rs.V = b.V; rs.r = b.r; rs.d = b.d; rs.gamma = b.gamma; rs.dtype = b.dtype;
+    rs.W = a->W; rs.W1 = b.W1; rs.Hpre = Hpre; rs.state = state; rs.A = a->A; rs.err = b.err;
+    rc = run_draft_loop(&b, a->A, part, s, &rs, 1, b.gamma);
+    if (rc != DSPARK_OK) return rc;
+    if (a->s_out) {
+        e = cudaMemcpyAsync(a->s_out, state, sizeof(float) * (size_t)b.R * b.r, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "rnn state out");
+    }
+    return ok();
+}
+
+DSPARK_API size_t dspark_schedule_workspace_size(const dspark_sched_args *a) {
+    (void)a;
+    return 0;
+}
+
+DSPARK_API int dspark_schedule(const dspark_sched_args *a, void *ws, dspark_stream_t stream) {
+    (void)ws;
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->R < 1 || a->gamma < 1) return fail(DSPARK_ERR_INVAL, "bad shape R=%d gamma=%d", a->R, a->gamma);
+    if ((long long)a->R * a->gamma > 8192)
+        return fail(DSPARK_ERR_UNSUPPORTED, "pool R*gamma=%lld above 8192", (long long)a->R * a->gamma);
+    if (a->mode != DSPARK_SCHED_SYNC && a->mode != DSPARK_SCHED_ASYNC)
+        return fail(DSPARK_ERR_INVAL, "bad mode %d", a->mode);
+    if (!a->c || !a->sps || !a->ell || !a->K_out || !a->theta_best)
+        return fail(DSPARK_ERR_INVAL, "null tensor pointer");
+    if (a->B_count < 1 || a->B_min > a->R ||
+        (long long)a->R * (a->gamma + 1) > (long long)a->B_min + a->B_count - 1)
+        return fail(DSPARK_ERR_RANGE, "SPS table [%d, %d] does not cover B in [%d, %lld]", a->B_min,
+                    a->B_min + a->B_count - 1, a->R, (long long)a->R * (a->gamma + 1));
+    cudaError_t e = dspark::launch_schedule(*a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "schedule");
+    return ok();
+}
+
+DSPARK_API int dspark_build_tags(int32_t R, int32_t gamma, const int32_t *ell, int32_t *tags,
+                                 int32_t *N_out, int32_t *err, dspark_stream_t stream) {
+    if (R < 1 || gamma < 0) return fail(DSPARK_ERR_INVAL, "bad shape R=%d gamma=%d", R, gamma);
+    if (!ell || !tags || !N_out) return fail(DSPARK_ERR_INVAL, "null tensor pointer");
+    cudaError_t e = dspark::launch_build_tags(R, gamma, ell, tags, N_out, err,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "build tags");
+    return ok();
+}
+
+static int check_verify(const dspark_verify_args *a) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->R < 1 || a->gamma < 1 || a->V < 1 || a->r < 1 || a->N < a->R ||
+        (long long)a->N > (long long)a->R * (a->gamma + 1))
+        return fail(DSPARK_ERR_INVAL, "bad shape R=%d gamma=%d V=%d r=%d N=%d", a->R, a->gamma, a->V,
+                    a->r, a->N);
+    if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16)
+        return fail(DSPARK_ERR_INVAL, "bad dtype %d", a->dtype);
+    if (a->r > kMaxRank) return fail(DSPARK_ERR_UNSUPPORTED, "rank r=%d above %d", a->r, kMaxRank);
+    if (!a->T || !a->tags || !a->anchor || !a->x || !a->logq || !a->lse || !a->U || !a->W1 ||
+        !a->W2t || !a->n_accept || !a->out_tokens || !a->next_anchor)
+        return fail(DSPARK_ERR_INVAL, "null tensor pointer");
+    if (!aligned16(a->T)) return fail(DSPARK_ERR_INVAL, "T must be 16-byte aligned");
+    return DSPARK_OK;
+}
+
+DSPARK_API size_t dspark_verify_workspace_size(const dspark_verify_args *a) {
+    if (check_verify(a) != DSPARK_OK) return 0;
+    return dspark::verify_ws_bytes(a->R, a->gamma, a->V, a->N);
+}
+
+DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_stream_t stream) {
+    int rc = check_verify(a);
+    if (rc != DSPARK_OK) return rc;
+    if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
+    const dspark::VerifyWs w = dspark::verify_ws_carve(ws, a->R, a->gamma, a->V, a->N);
+    cudaError_t e = dspark::launch_verify(*a, w, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "verify");
+    return ok();
+}
+
+DSPARK_API int dspark_philox(const uint32_t *ctr, uint64_t seed, int32_t n, uint32_t *out,
+                             dspark_stream_t stream) {
+    if (n < 0 || (n > 0 && (!ctr || !out))) return fail(DSPARK_ERR_INVAL, "bad philox arguments");
+    if (n == 0) return ok();
+    cudaError_t e = dspark::launch_philox(ctr, seed, n, out, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "philox");
+    return ok();
+}
+
+}  // extern "C"
+
+namespace dspark {
+
+namespace {
+__global__ void philox_kernel(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint4 w = philox4x32_10(make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]),
+                                  philox_key(seed));
+    out[4 * i] = w.x;
+    out[4 * i + 1] = w.y;
+    out[4 * i + 2] = w.z;
+    out[4 * i + 3] = w.w;
+}
+}  // namespace
+
+cudaError_t launch_philox(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out, cudaStream_t s) {
+    philox_kernel<<<(n + 255) / 256, 256, 0, s>>>(ctr, seed, n, out);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,212 @@
+// common.cuh -- device building blocks shared by the DSpark kernels.
+//
+// * Philox-4x32-10 (Salmon et al., SC'11) and the word -> uniform map.
+// * The running state of one row's fused epilogue: online max / sum-exp for the
+//   exact softmax normaliser of eq. (4) of the DSpark digest, and the Gumbel-max
+//   sample taken in "exponential race" form, argmax_v z_v - ln E_v with
+//   E_v = -ln u_v, which equals argmax_v z_v - ln(-ln u_v).
+// * Error reporting into the caller's device error word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// multiplicative slack of the race pre-filter (far above the few-ulp error of
+// the fp32 products it guards)
+constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
+
+// ---------------------------------------------------------------- errors
+__device__ __forceinline__ void set_err(int32_t *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------- fast exp2
+// MUFU ex2 (relative error ~2^-22); ex2(-inf) = +0, ex2(+inf) = +inf.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- Philox
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
+    return PhiloxKey{(uint32_t)seed, (uint32_t)(seed >> 32)};
+}
+
+// counter word 3: low 30 bits of the cycle, then the 2-bit stream id
+__device__ __forceinline__ uint32_t philox_ctr3(uint64_t cycle, uint32_t stream) {
+    return (uint32_t)(cycle << 2) | stream;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint32_t word_lane(const uint4 &w, int lane) {
+    return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
+}
+
+// u = ((w >> 9) + 1/2) 2^-23, exact in fp32
+__device__ __forceinline__ float uniform_of(uint32_t w) {
+    return __uint2float_rn(w >> 9) * (1.0f / 8388608.0f) + (1.0f / 16777216.0f);
+}
+
+// t = 1 - u, also exact: the lattice {(k + 1/2) 2^-23} is symmetric about 1/2.
+// Built from the bits: 1 + k' 2^-23 with k' = 2^23 - 1 - (w >> 9), minus
+// (1 - 2^-24); the subtraction is exact (Sterbenz).
+__device__ __forceinline__ float one_minus_uniform(uint32_t w) {
+    const uint32_t bits = ((~w) >> 9) | 0x3F800000u;
+    return __uint_as_float(bits) - (1.0f - 1.0f / 16777216.0f);
+}
+
+// E = -ln u = -ln(1 - t), the unit exponential variate behind the race
+__device__ __forceinline__ float exp_variate(float t) { return -log1pf(-t); }
+
+// ---------------------------------------------------------------- epilogue state
+// One row's running fused-epilogue state.  `C` caches exp(m - best) * slack so
+// the race pre-filter costs one multiply and one compare per element: element v
+// can only beat `best` if E_v < exp(z_v - best), and E_v >= t_v = 1 - u_v, so it
+// is skipped whenever t_v >= exp(z_v - m) * C.
+struct RowState {
+    float m;      // running max of z
+    float S;      // sum exp(z - m)
+    float best;   // best race score z - ln E
+    float zbest;  // z of the best element
+    int idx;      // its vocabulary index (-1: none yet)
+    float C;      // exp(m - best) * slack
+};
+
+__device__ __forceinline__ void row_init(RowState &s) {
+    s.m = -INFINITY;
+    s.S = 0.f;
+    s.best = -INFINITY;
+    s.zbest = 0.f;
+    s.idx = -1;
+    s.C = INFINITY;
+}
+
+__device__ __forceinline__ void row_refresh_C(RowState &s) {
+    s.C = ex2((s.m - s.best) * kLog2e) * kRaceSlack;
+}
+
+// Feed four consecutive vocabulary entries v0..v0+3 (one Philox call);
+// entries at or beyond V are ignored.
+__device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0, int V,
+                                          const uint4 &words) {
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (v0 + j < V) zmax = fmaxf(zmax, z[j]);
+    if (zmax > s.m) {
+        s.S *= ex2((s.m - zmax) * kLog2e);
+        s.m = zmax;
+        row_refresh_C(s);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (v0 + j >= V) continue;
+        const float e = ex2((z[j] - s.m) * kLog2e);
+        s.S += e;
+        const uint32_t w = word_lane(words, j);
+        const float t = one_minus_uniform(w);
+        if (!(t >= e * s.C)) {
+            const float score = z[j] - logf(exp_variate(t));
+            if (score > s.best) {
+                s.best = score;
+                s.idx = v0 + j;
+                s.zbest = z[j];
+                row_refresh_C(s);
+            }
+        }
+    }
+}
+
+// Combine two states (b into a).  Ties of the race go to the lower index.
+__device__ __forceinline__ void row_merge(RowState &a, float m, float S, float best, float zbest,
+                                          int idx) {
+    const float M = fmaxf(a.m, m);
+    if (M == -INFINITY) {
+        a.S = 0.f;
+    } else {
+        a.S = a.S * ex2((a.m - M) * kLog2e) + S * ex2((m - M) * kLog2e);
+    }
+    a.m = M;
+    if (idx >= 0 && (a.idx < 0 || best > a.best || (best == a.best && idx < a.idx))) {
+        a.best = best;
+        a.zbest = zbest;
+        a.idx = idx;
+    }
+}
+
+// Partial result of one (row, vocabulary slice) of a draft step.
+struct DraftPartial {
+    float m, S, best, zbest;
+    int idx;
+};
+
+// Partial result of one (row, vocabulary slice) of verification phase 2:
+// the race over the residual max(0, p - q) and, as fallback / bonus, over p.
+struct VerifyPartial {
+    float best_res, best_p;
+    int idx_res, idx_p;
+};
+
+// Race over weights w_v in (0, 1]: score ln w_v - ln E_v; the filter skips v
+// when t_v >= w_v * C with C = exp(-best) * slack.
+struct Race {
+    float best;
+    int idx;
+    float C;
+};
+
+__device__ __forceinline__ void race_init(Race &r) {
+    r.best = -INFINITY;
+    r.idx = -1;
+    r.C = INFINITY;
+}
+
+__device__ __forceinline__ void race_feed(Race &r, float w, float t, int v) {
+    if (!(w > 0.f)) return;
+    if (t >= w * r.C) return;
+    const float score = logf(w) - logf(exp_variate(t));
+    if (score > r.best) {
+        r.best = score;
+        r.idx = v;
+        r.C = ex2(-r.best * kLog2e) * kRaceSlack;
+    }
+}
+
+__device__ __forceinline__ void race_merge(float &best, int &idx, float b2, int i2) {
+    if (i2 >= 0 && (idx < 0 || b2 > best || (b2 == best && i2 < idx))) {
+        best = b2;
+        idx = i2;
+    }
+}
+
+}  // namespace dspark

@@ -1,0 +1,293 @@
+// draft.cu -- semi-autoregressive draft step kernels (CUDA cores).
+//
+// DSpark digest, eq. (4): p_k(v) is a softmax over U_k(v) + B_k(v); eq. (5)
+// Markov bias B_k = W_1[x_{k-1}] W_2; eq. (6) RNN bias B_k = W_2^T tanh(W_o z_k);
+// eq. (7) confidence c_k = sigma(w^T [h_k ; W_1[x_{k-1}]]).
+//
+// One draft step is two launches:
+//   draft_step_simt  vocabulary-sliced: each CTA owns 64 vocabulary entries,
+//                    keeps that slice of W_2 in shared memory, and for every
+//                    request contracts the bias operand with it, adds U_k and
+//                    folds the result into an online max / sum-exp and a
+//                    Gumbel race.  Output: one partial per (request, slice); no
+//                    logit ever reaches global memory.
+//   draft_reduce     one CTA per request merges its partials in a fixed order
+//                    (deterministic), writes x_k, log q_k(x_k), lse_k and the
+//                    confidence c_k.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kSliceV = 64;     // vocabulary entries per CTA
+constexpr int kRowsPerPass = 8; // requests per pass over the slice
+constexpr int kThreads = 128;   // 16 vocabulary quads x 8 requests
+
+template <typename T, bool kRnn>
+__global__ void __launch_bounds__(kThreads) draft_step_simt(const DraftStep p) {
+    extern __shared__ float smem[];
+    const int r = p.r, ld = r + 1;
+    float *W2s = smem;                    // [64][r + 1]
+    float *Es = smem + kSliceV * ld;      // [8][r + 1]
+    const T *W2t = static_cast<const T *>(p.W2t);
+    const T *W1 = static_cast<const T *>(p.W1);
+    const T *U = static_cast<const T *>(p.U);
+    const int slice = blockIdx.x, vbase = slice * kSliceV;
+
+    for (int e = threadIdx.x; e < kSliceV * r; e += kThreads) {
+        const int vv = e / r, i = e - vv * r, v = vbase + vv;
+        W2s[vv * ld + i] = v < p.V ? to_f32(W2t[(size_t)v * r + i]) : 0.f;
+    }
+    const int quad = threadIdx.x & 15, sub = threadIdx.x >> 4;
+    const int v0 = vbase + quad * 4;
+    const PhiloxKey key = philox_key(p.seed);
+    const uint32_t c3 = philox_ctr3(p.cycle, 0);
+
+    for (int row0 = 0; row0 < p.R; row0 += kRowsPerPass) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kRowsPerPass * r; e += kThreads) {
+            const int rr = e / r, i = e - rr * r, row = row0 + rr;
+            float val = 0.f;
+            if (row < p.R) {
+                if (kRnn) {
+                    val = p.A_op[(size_t)row * p.a_stride + i];
+                } else {
+                    int xp = p.x_prev[(size_t)row * p.x_stride];
+                    if (xp < 0 || xp >= p.V) {
+                        if (i == 0) set_err(p.err, DSPARK_ERR_RANGE);
+                        xp = 0;
+                    }
+                    val = to_f32(W1[(size_t)xp * r + i]);
+                }
+            }
+            Es[rr * ld + i] = val;
+        }
+        __syncthreads();
+
+        const int row = row0 + sub;
+        const float *e = Es + sub * ld;
+        const float *w0 = W2s + (quad * 4) * ld;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < r; ++i) {
+            const float ev = e[i];
+            acc[0] = fmaf(ev, w0[i], acc[0]);
+            acc[1] = fmaf(ev, w0[ld + i], acc[1]);
+            acc[2] = fmaf(ev, w0[2 * ld + i], acc[2]);
+            acc[3] = fmaf(ev, w0[3 * ld + i], acc[3]);
+        }
+        RowState st;
+        row_init(st);
+        if (row < p.R && v0 < p.V) {
+            const T *Urow = U + ((size_t)row * p.gamma + (p.k - 1)) * (size_t)p.V;
+            float z[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                z[j] = (v0 + j < p.V) ? acc[j] + to_f32(Urow[v0 + j]) : -INFINITY;
+            const uint4 words = philox4x32_10(
+                make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)row, c3), key);
+            row_feed4(st, z, v0, p.V, words);
+        }
+        // merge the 16 quads of this request (lanes differing in bits 0..3)
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) {
+            const float m = __shfl_xor_sync(0xffffffffu, st.m, off);
+            const float S = __shfl_xor_sync(0xffffffffu, st.S, off);
+            const float b = __shfl_xor_sync(0xffffffffu, st.best, off);
+            const float zb = __shfl_xor_sync(0xffffffffu, st.zbest, off);
+            const int ix = __shfl_xor_sync(0xffffffffu, st.idx, off);
+            row_merge(st, m, S, b, zb, ix);
+        }
+        if (quad == 0 && row < p.R)
+            p.part[(size_t)row * p.nparts + slice] = DraftPartial{st.m, st.S, st.best, st.zbest, st.idx};
+    }
+}
+
+constexpr int kReduceThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kReduceThreads) draft_reduce_kernel(const DraftReduce p) {
+    __shared__ float s_m[kReduceThreads], s_S[kReduceThreads], s_b[kReduceThreads],
+        s_z[kReduceThreads], s_dot[kReduceThreads];
+    __shared__ int s_i[kReduceThreads];
+    const int row = blockIdx.x, tid = threadIdx.x;
+    RowState st;
+    row_init(st);
+    for (int t = tid; t < p.nparts; t += kReduceThreads) {
+        const DraftPartial q = p.part[(size_t)row * p.nparts + t];
+        row_merge(st, q.m, q.S, q.best, q.zbest, q.idx);
+    }
+    // confidence logit w^T [h_k ; W_1[x_{k-1}]]
+    int xp = p.x_prev[(size_t)row * p.x_stride];
+    if (xp < 0 || xp >= p.V) xp = 0;  // reported by the step kernel
+    const T *h = static_cast<const T *>(p.h) + ((size_t)row * p.gamma + (p.k - 1)) * (size_t)p.d;
+    const T *e = static_cast<const T *>(p.W1) + (size_t)xp * p.r;
+    float dot = 0.f;
+    for (int j = tid; j < p.d; j += kReduceThreads) dot = fmaf(p.w[j], to_f32(h[j]), dot);
+    for (int i = tid; i < p.r; i += kReduceThreads) dot = fmaf(p.w[p.d + i], to_f32(e[i]), dot);
+
+    s_m[tid] = st.m; s_S[tid] = st.S; s_b[tid] = st.best; s_z[tid] = st.zbest; s_i[tid] = st.idx;
+    s_dot[tid] = dot;
+    __syncthreads();
+    for (int half = kReduceThreads / 2; half > 0; half >>= 1) {
+        if (tid < half) {
+            RowState a{s_m[tid], s_S[tid], s_b[tid], s_z[tid], s_i[tid], 0.f};
+            row_merge(a, s_m[tid + half], s_S[tid + half], s_b[tid + half], s_z[tid + half],
+                      s_i[tid + half]);
+            s_m[tid] = a.m; s_S[tid] = a.S; s_b[tid] = a.best; s_z[tid] = a.zbest; s_i[tid] = a.idx;
+            s_dot[tid] += s_dot[tid + half];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const size_t o = (size_t)row * p.gamma + (p.k - 1);
+        float lse = s_m[0] + logf(s_S[0]);
+        int idx = s_i[0];
+        if (idx < 0 || !isfinite(lse)) {
+            set_err(p.err, DSPARK_ERR_NONFINITE);
+            idx = 0;
+        }
+        p.x[o] = idx;
+        p.lse[o] = lse;
+        p.logq[o] = s_z[0] - lse;
+        const float T_k = p.sts_T ? p.sts_T[p.k - 1] : 1.0f;
+        p.c[o] = 1.0f / (1.0f + expf(-s_dot[0] / T_k));
+    }
+}
+
+// ---------------------------------------------------------------- RNN head
+template <typename T>
+__global__ void __launch_bounds__(256) rnn_hproj_kernel(int M, int d, int r, const T *h, const T *W,
+                                                        float *Hpre) {
+    __shared__ float As[16][68], Bs[16][68];
+    const int N = 3 * r, ldw = 2 * r + d;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < d; k0 += 16) {
+        for (int e = threadIdx.x; e < 1024; e += 256) {
+            const int mm = e >> 4, kk = e & 15;
+            As[kk][mm] = (m0 + mm < M && k0 + kk < d) ? to_f32(h[(size_t)(m0 + mm) * d + k0 + kk]) : 0.f;
+            Bs[kk][mm] = (n0 + mm < N && k0 + kk < d)
+                             ? to_f32(W[(size_t)(n0 + mm) * ldw + 2 * r + k0 + kk]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 4; ++j) {
+            const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+            if (m < M && n < N) Hpre[(size_t)m * N + n] = acc[i][j];
+        }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rnn_step_kernel(const RnnStep p) {
+    extern __shared__ float sh[];
+    const int r = p.r, row = blockIdx.x;
+    float *zsx = sh;          // [s_{k-1} ; W_1[x_{k-1}]]  (2r)
+    float *G = sh + 2 * r;    // W z_k                      (3r)
+    int xp = p.x_prev[(size_t)row * p.x_stride];
+    if (xp < 0 || xp >= p.V) {
+        if (threadIdx.x == 0) set_err(p.err, DSPARK_ERR_RANGE);
+        xp = 0;
+    }
+    const T *W1 = static_cast<const T *>(p.W1);
+    for (int i = threadIdx.x; i < r; i += blockDim.x) {
+        zsx[i] = p.state[(size_t)row * r + i];
+        zsx[r + i] = to_f32(W1[(size_t)xp * r + i]);
+    }
+    __syncthreads();
+    const T *W = static_cast<const T *>(p.W);
+    const int ldw = 2 * r + p.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const float *hp = p.Hpre + ((size_t)row * p.gamma + (p.k - 1)) * (size_t)(3 * r);
+    for (int o = warp; o < 3 * r; o += nwarps) {
+        const T *Wrow = W + (size_t)o * ldw;
+        float acc = 0.f;
+        for (int j = lane; j < 2 * r; j += 32) acc = fmaf(to_f32(Wrow[j]), zsx[j], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) G[o] = acc + hp[o];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < r; i += blockDim.x) {
+        const float g = 1.0f / (1.0f + expf(-G[i]));
+        const float cand = tanhf(G[r + i]);
+        const float s_prev = zsx[i];
+        p.state[(size_t)row * r + i] = g * s_prev + (1.0f - g) * cand;
+        p.A[((size_t)row * p.gamma + (p.k - 1)) * (size_t)r + i] = tanhf(G[2 * r + i]);
+    }
+}
+
+}  // namespace
+
+int draft_step_nparts(int V) { return (V + kSliceV - 1) / kSliceV; }
+
+template <typename T, bool kRnn>
+static cudaError_t launch_step_t(const DraftStep &p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)(kSliceV + kRowsPerPass) * (p.r + 1);
+    auto kern = draft_step_simt<T, kRnn>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<p.nparts, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s) {
+    const bool rnn = p.A_op != nullptr;
+    if (p.dtype == DSPARK_BF16)
+        return rnn ? launch_step_t<__nv_bfloat16, true>(p, s) : launch_step_t<__nv_bfloat16, false>(p, s);
+    return rnn ? launch_step_t<float, true>(p, s) : launch_step_t<float, false>(p, s);
+}
+
+cudaError_t launch_draft_reduce(const DraftReduce &p, cudaStream_t s) {
+    if (p.dtype == DSPARK_BF16)
+        draft_reduce_kernel<__nv_bfloat16><<<p.R, kReduceThreads, 0, s>>>(p);
+    else
+        draft_reduce_kernel<float><<<p.R, kReduceThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, const void *W,
+                             float *Hpre, cudaStream_t s) {
+    dim3 grid((3 * r + 63) / 64, (M + 63) / 64);
+    if (dtype == DSPARK_BF16)
+        rnn_hproj_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            M, d, r, static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(W), Hpre);
+    else
+        rnn_hproj_kernel<float><<<grid, 256, 0, s>>>(M, d, r, static_cast<const float *>(h),
+                                                     static_cast<const float *>(W), Hpre);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)(5 * p.r);
+    if (p.dtype == DSPARK_BF16) {
+        auto kern = rnn_step_kernel<__nv_bfloat16>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<p.R, 256, smem, s>>>(p);
+    } else {
+        auto kern = rnn_step_kernel<float>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<p.R, 256, smem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

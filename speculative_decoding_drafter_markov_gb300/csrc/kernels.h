@@ -1,0 +1,95 @@
+// kernels.h -- host-side launchers of the DSpark kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dspark {
+
+// ----- draft step (eqs. 4, 5): vocabulary-sliced partials of one step k ---------
+// The bias operand of row i is either W1[x_prev[i * x_stride]] (Markov head) or
+// the fp32 vector A_op + i * a_stride (RNN head).
+struct DraftStep {
+    int R, V, r, gamma, k;          // k = 1..gamma
+    int dtype;
+    const void *U;                   // [R, gamma, V]
+    const void *W1;                  // [V, r]
+    const void *W2t;                 // [V, r]
+    const int32_t *x_prev;           // Markov: token of row i at x_prev[i * x_stride]
+    int x_stride;
+    const float *A_op;               // RNN: operand of row i at A_op[i * a_stride]
+    int a_stride;
+    uint64_t seed, cycle;
+    DraftPartial *part;              // [R, nparts]
+    int nparts;
+    int32_t *err;
+};
+int draft_step_nparts(int V);
+cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
+
+// ----- reduce partials of step k, write x, logq, lse; confidence (eq. 7) -------
+struct DraftReduce {
+    int R, V, r, d, gamma, k, dtype;
+    const DraftPartial *part;
+    int nparts;
+    const void *h;                   // [R, gamma, d]
+    const void *W1;                  // [V, r]
+    const int32_t *x_prev;           // token x_{k-1} of row i at x_prev[i * x_stride]
+    int x_stride;
+    const float *w;                  // [d + r]
+    const float *sts_T;              // [gamma] or null
+    int32_t *x;
+    float *logq, *lse, *c;           // [R, gamma]
+    int32_t *err;
+};
+cudaError_t launch_draft_reduce(const DraftReduce &p, cudaStream_t s);
+
+// ----- RNN head (eq. 6) --------------------------------------------------------
+// Hpre[m, o] = sum_j h[m, j] W[o, 2r + j] for every (request, step) row m.
+cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, const void *W,
+                             float *Hpre, cudaStream_t s);
+// One recurrent step: gates from [s; W1[x_{k-1}]] and Hpre; updates state in
+// place, writes A[:, k-1, :] = tanh(W_o z_k).
+struct RnnStep {
+    int R, V, r, d, gamma, k, dtype;
+    const void *W;                   // [3r, 2r + d]
+    const void *W1;
+    const int32_t *x_prev;
+    int x_stride;
+    const float *Hpre;               // [R * gamma, 3r]
+    float *state;                    // [R, r]
+    float *A;                        // [R, gamma, r]
+    int32_t *err;
+};
+cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s);
+
+// ----- scheduler (Module E, Algorithm 1; async variant) ---------------------
+cudaError_t launch_schedule(const dspark_sched_args &a, cudaStream_t s);
+size_t schedule_smem_bytes(int R, int gamma);
+
+// ----- flattened batch tags ---------------------------------------------------
+cudaError_t launch_build_tags(int R, int gamma, const int32_t *ell, int32_t *tags, int32_t *N_out,
+                              int32_t *err, cudaStream_t s);
+
+// ----- verification -------------------------------------------------------------
+struct VerifyWs {
+    float *lse_p;          // [N]
+    int32_t *first_rej;    // [R]
+    int32_t *ell;          // [R]
+    int32_t *row_of;       // [R, gamma + 1]
+    VerifyPartial *part;   // [R, nparts]
+    int nparts;
+};
+size_t verify_ws_bytes(int R, int gamma, int V, int N);
+VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N);
+cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s);
+
+// ----- philox check ------------------------------------------------------------------
+cudaError_t launch_philox(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out, cudaStream_t s);
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace dspark

@@ -1,0 +1,128 @@
+"""GPU parity of the draft calls (Markov and RNN heads) against the oracle.
+
+Small cases run the oracle on every request; the standard full-size workloads
+(the launch configuration the benchmark times) run it on sampled requests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import compare_draft, host
+from speculative_decoding_drafter_markov_gb300 import _lib as dsp
+from speculative_decoding_drafter_markov_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_draft(inp, seed, cycle, sts_T=None, rnn=False):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sts = None if sts_T is None else torch.as_tensor(sts_T, device="cuda")
+    if rnn:
+        out = dsp.draft_rnn(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["W"], inp["w"],
+                            inp["anchor"], seed=seed, cycle=cycle, sts_T=sts, err=err)
+    else:
+        out = dsp.draft_markov(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["w"], inp["anchor"],
+                               seed=seed, cycle=cycle, sts_T=sts, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, dsp.ERROR_NAMES[int(err.item())]
+    return {k: host(v) for k, v in out.items()}
+
+
+def _oracle_draft(orc, inp, seed, cycle, reqs=None, sts_T=None, rnn=False):
+    args = [host(inp[k]) for k in ("U", "h", "W1", "W2t")]
+    if rnn:
+        return orc.draft_rnn(*args, host(inp["W"]), host(inp["w"]), host(inp["anchor"]), seed=seed,
+                             cycle=cycle, sts_T=sts_T, reqs=reqs)
+    return orc.draft_markov(*args, host(inp["w"]), host(inp["anchor"]), seed=seed, cycle=cycle,
+                            sts_T=sts_T, reqs=reqs)
+
+
+def _to_cuda(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+SMALL = [
+    W.WORKLOADS["tiny"],
+    W.small("qwen4b", R=10, gamma=3, V=1001, r=24, d=40),        # ragged V and r, bf16
+    W.small("heavy", R=33, gamma=5, V=2048 + 63, r=64, d=96),    # several slices + tail
+    W.small("prod", R=3, gamma=2, V=129, r=8, d=8, dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("seed,cycle", [(0, 0), (12345678901, 7)])
+def test_markov_small(orc, wl, seed, cycle):
+    inp = _to_cuda(W.draft_inputs(wl, seed=seed % 1000))
+    gpu = _gpu_draft(inp, seed, cycle)
+    ref = _oracle_draft(orc, inp, seed, cycle)
+    compare_draft(gpu, ref, list(range(wl.R)), wl.gamma)
+
+
+def test_markov_temperature(orc):
+    wl = W.small("qwen4b", R=6, gamma=4, V=700, r=16, d=32)
+    inp = _to_cuda(W.draft_inputs(wl, seed=3))
+    T = np.array([1.0, 1.7, 0.6, 2.5], np.float32)
+    gpu = _gpu_draft(inp, 5, 1, sts_T=T)
+    ref = _oracle_draft(orc, inp, 5, 1, sts_T=T)
+    compare_draft(gpu, ref, list(range(wl.R)), wl.gamma)
+
+
+def test_markov_deterministic():
+    wl = W.small("heavy", R=17, gamma=4, V=3000, r=32, d=16)
+    inp = _to_cuda(W.draft_inputs(wl, seed=4))
+    a = _gpu_draft(inp, 9, 2)
+    b = _gpu_draft(inp, 9, 2)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("name,reqs", [("qwen4b", [0, 37, 63]), ("heavy", [5, 200]),
+                                       ("prod", [511])])
+def test_markov_full_size_sampled(orc, name, reqs):
+    wl = W.WORKLOADS[name]
+    inp = W.draft_inputs(wl, seed=1, device="cuda")
+    gpu = _gpu_draft(inp, 2024, 3)
+    ref = _oracle_draft(orc, inp, 2024, 3, reqs=reqs)
+    compare_draft(gpu, ref, reqs, wl.gamma)
+    # every drafted token is a valid id and every confidence a probability
+    assert gpu["x"].min() >= 0 and gpu["x"].max() < wl.V
+    assert np.all((gpu["c"] > 0) & (gpu["c"] < 1))
+
+
+RNN_SMALL = [
+    W.small("rnn", R=5, gamma=4, V=900, r=16, d=24),
+    W.small("rnn", R=3, gamma=3, V=257, r=8, d=8, dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("wl", RNN_SMALL, ids=lambda w: f"{w.name}-{w.dtype}")
+def test_rnn_small(orc, wl):
+    inp = _to_cuda(W.draft_inputs(wl, seed=2))
+    gpu = _gpu_draft(inp, 77, 4, rnn=True)
+    ref = _oracle_draft(orc, inp, 77, 4, rnn=True)
+    compare_draft(gpu, ref, list(range(wl.R)), wl.gamma)
+    # the bias operand A_k = tanh(W_o z_k) until the first flip
+    for rq in range(wl.R):
+        for k in range(wl.gamma):
+            np.testing.assert_allclose(gpu["A"][rq, k], ref["A"][rq, k], atol=1e-4)
+            if gpu["x"][rq, k] != ref["x"][rq, k]:
+                break
+
+
+def test_rnn_full_size_sampled(orc):
+    wl = W.WORKLOADS["rnn"]
+    inp = W.draft_inputs(wl, seed=1, device="cuda")
+    gpu = _gpu_draft(inp, 11, 0, rnn=True)
+    reqs = [0, 127]
+    ref = _oracle_draft(orc, inp, 11, 0, reqs=reqs, rnn=True)
+    compare_draft(gpu, ref, reqs, wl.gamma)
+
+
+def test_bad_anchor_reports_range():
+    wl = W.small("qwen4b", R=4, gamma=2, V=300, r=8, d=8)
+    inp = _to_cuda(W.draft_inputs(wl, seed=0))
+    inp["anchor"][2] = wl.V + 5  # out of range: clamped on the device and reported
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dsp.draft_markov(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["w"], inp["anchor"], err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == dsp.ERR_RANGE
