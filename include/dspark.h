@@ -106,6 +106,32 @@ DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_
 DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, void *ws,
                                         dspark_stream_t stream);
 
+/* Markov-head draft that allocates nothing and takes no workspace.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: a plugin living inside another runtime whose
+ * caching allocator already owns the device's memory, a plain C host with no
+ * allocator of its own, or a code path that must not call cudaMalloc because
+ * that call can synchronise the device.  Such callers still pass every input
+ * and output tensor; only the scratch (the per-slice partial results the
+ * steps exchange) comes from a fixed array inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ *
+ * - Limit: the scratch needs R * ceil(V / 64) * 20 bytes and the array holds
+ *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB): e.g. R = 64 or R = 256 at
+ *   V = 151936 fit, R = 512 at V = 129280 does not.  Larger sizes return
+ *   DSPARK_ERR_UNSUPPORTED (message in dspark_last_error()) and launch nothing.
+ * - The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture on the device.
+ * - Every call on a device shares the one array.  Each step overwrites all
+ *   the scratch it reads, so nothing has to start at zero, but calls that
+ *   overlap on the GPU (different streams, or different host threads) race:
+ *   serialise them, e.g. by issuing them on one stream.
+ * Results equal dspark_draft_markov's for the same arguments. */
+#define DSPARK_NOALLOC_SCRATCH_BYTES (16u << 20)
+DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Draft, RNN head.  [D] eq. (6): z_k = [s_{k-1}; W_1[x_{k-1}]; h_k],          */
 /* s_k = sigma(W_g z_k) s_{k-1} + (1 - sigma(W_g z_k)) tanh(W_c z_k),          */

@@ -64,6 +64,7 @@ SYMBOLS = {
     "dspark_draft_markov_workspace_size": ([ctypes.POINTER(DraftArgs)], ctypes.c_size_t),
     "dspark_draft_markov": ([ctypes.POINTER(DraftArgs), P, P], ctypes.c_int),
     "dspark_draft_markov_step": ([ctypes.POINTER(DraftArgs), i32, P, P], ctypes.c_int),
+    "dspark_draft_markov_noalloc": ([ctypes.POINTER(DraftArgs), P], ctypes.c_int),
     "dspark_draft_rnn_workspace_size": ([ctypes.POINTER(RnnArgs)], ctypes.c_size_t),
     "dspark_draft_rnn": ([ctypes.POINTER(RnnArgs), P, P], ctypes.c_int),
     "dspark_schedule_workspace_size": ([ctypes.POINTER(SchedArgs)], ctypes.c_size_t),
@@ -180,6 +181,18 @@ def draft_markov_step(k, U, h, W1, W2t, w, anchor, *, out, ws, seed=0, cycle=0, 
     L = load()
     a = _draft_struct(U, h, W1, W2t, w, anchor, seed, cycle, sts_T, out, err)
     _check(L.dspark_draft_markov_step(ctypes.byref(a), int(k), _ptr(ws), _stream(stream)))
+    return out
+
+
+def draft_markov_noalloc(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, out=None,
+                         err=None, stream=None):
+    """Markov draft through the entry point that allocates nothing: its scratch
+    is a fixed array inside the library (R * ceil(V/64) * 20 bytes <= 16 MiB)."""
+    L = load()
+    R, gamma, _ = U.shape
+    out = _draft_outputs(R, gamma, U.device, out)
+    a = _draft_struct(U, h, W1, W2t, w, anchor, seed, cycle, sts_T, out, err)
+    _check(L.dspark_draft_markov_noalloc(ctypes.byref(a), _stream(stream)))
     return out
 
 

@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -126,6 +127,48 @@ DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, v
     if (k < 1 || k > a->gamma) return fail(DSPARK_ERR_INVAL, "step k=%d outside 1..%d", k, a->gamma);
     if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
     rc = run_draft_loop(a, nullptr, ws, reinterpret_cast<cudaStream_t>(stream), nullptr, k, k);
+    return rc == DSPARK_OK ? ok() : rc;
+}
+
+// Scratch of dspark_draft_markov_noalloc: a fixed device array, so that call
+// never allocates.  Host code may only use its address as looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSPARK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices];  // device address of the array, per device
+
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DSPARK_ERR_UNSUPPORTED, "noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DSPARK_OK;
+}
+}  // namespace
+
+DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_stream_t stream) {
+    int rc = check_draft(a);
+    if (rc != DSPARK_OK) return rc;
+    const size_t need = draft_partials_bytes(a->R, a->V);
+    if (need > (size_t)DSPARK_NOALLOC_SCRATCH_BYTES)
+        return fail(DSPARK_ERR_UNSUPPORTED,
+                    "noalloc draft needs %zu bytes of scratch for R=%d V=%d; the fixed array holds %u",
+                    need, a->R, a->V, (unsigned)DSPARK_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != DSPARK_OK) return rc;
+    rc = run_draft_loop(a, nullptr, scratch, reinterpret_cast<cudaStream_t>(stream), nullptr, 1,
+                        a->gamma);
     return rc == DSPARK_OK ? ok() : rc;
 }
 
