@@ -72,6 +72,12 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
     rd.part = st.part; rd.nparts = st.nparts;
     rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
     rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
+    const bool use_tc = rnn == nullptr && draft_step_tc_supported(st);
+    if (use_tc) {
+        int mt = 0;
+        draft_step_tc_shape(a->R, a->V, &st.nparts, &mt);
+        rd.nparts = st.nparts;
+    }
     for (int k = k_first; k <= k_last; ++k) {
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
         const int xs = k == 1 ? 1 : a->gamma;
@@ -88,8 +94,8 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         st.k = k;
         st.x_prev = xp;
         st.x_stride = xs;
-        cudaError_t e = launch_draft_step(st, s);
-        if (e != cudaSuccess) return cuda_fail(e, "draft step");
+        cudaError_t e = use_tc ? launch_draft_step_tc(st, s) : launch_draft_step(st, s);
+        if (e != cudaSuccess) return cuda_fail(e, use_tc ? "draft step (tensor cores)" : "draft step");
         rd.k = k;
         rd.x_prev = xp;
         rd.x_stride = xs;

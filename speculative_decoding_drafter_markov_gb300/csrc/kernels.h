@@ -27,8 +27,12 @@ struct DraftStep {
     int nparts;
     int32_t *err;
 };
-int draft_step_nparts(int V);
+int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
+// tensor-core path (bf16, r in {64, 128, 192, 256}, V % 8 == 0, Markov head)
+bool draft_step_tc_supported(const DraftStep &p);
+void draft_step_tc_shape(int R, int V, int *nparts, int *n_mtiles);
+cudaError_t launch_draft_step_tc(const DraftStep &p, cudaStream_t s);
 
 // ----- reduce partials of step k, write x, logq, lse; confidence (eq. 7) -------
 struct DraftReduce {

@@ -46,6 +46,10 @@ SMALL = [
     W.small("qwen4b", R=10, gamma=3, V=1001, r=24, d=40),        # ragged V and r, bf16
     W.small("heavy", R=33, gamma=5, V=2048 + 63, r=64, d=96),    # several slices + tail
     W.small("prod", R=3, gamma=2, V=129, r=8, d=8, dtype="f32"),
+    # tensor-core path: bf16, V % 8 == 0, r a multiple of 64 (partial tiles and M-tiles)
+    W.small("qwen4b", R=40, gamma=3, V=5000, r=64, d=32),
+    W.small("heavy", R=100, gamma=3, V=4104, r=128, d=16),
+    W.small("prod", R=300, gamma=2, V=8192 + 72, r=256, d=16),
 ]
 
 
