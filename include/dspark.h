@@ -117,17 +117,21 @@ DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, v
  * steps exchange) comes from a fixed array inside the library, which every
  * GPU that loads the library holds until the process exits.
  *
- * - Limit: the scratch needs R * ceil(V / 64) * 20 bytes and the array holds
- *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB): e.g. R = 64 or R = 256 at
- *   V = 151936 fit, R = 512 at V = 129280 does not.  Larger sizes return
+ * - Limit: the scratch is what dspark_draft_markov_workspace_size() returns
+ *   for the same arguments -- 32 bytes per (request, vocabulary range) plus
+ *   512; the ranges are one per SM on the tensor-core path (bf16, r a multiple
+ *   of 64 up to 256, V a multiple of 8: all the standard workloads, well under
+ *   1 MiB) and ceil(V / 64) on the CUDA-core path -- and the array holds
+ *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB).  Larger needs return
  *   DSPARK_ERR_UNSUPPORTED (message in dspark_last_error()) and launch nothing.
  * - The first call on each device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
  *   stream capture on the device.
- * - Every call on a device shares the one array.  Each step overwrites all
- *   the scratch it reads, so nothing has to start at zero, but calls that
- *   overlap on the GPU (different streams, or different host threads) race:
- *   serialise them, e.g. by issuing them on one stream.
+ * - Every call on a device shares the one array.  Each call first clears the
+ *   part that must start at zero (completion counters, with an asynchronous
+ *   memset on the stream) and every step overwrites the rest before reading
+ *   it, but calls that overlap on the GPU (different streams, or different
+ *   host threads) race: serialise them, e.g. by issuing them on one stream.
  * Results equal dspark_draft_markov's for the same arguments. */
 #define DSPARK_NOALLOC_SCRATCH_BYTES (16u << 20)
 DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_stream_t stream);

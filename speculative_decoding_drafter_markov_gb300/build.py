@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdspark.so")
-SOURCES = ["abi.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu"]
+SOURCES = ["abi.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu", "verify_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

@@ -52,31 +52,59 @@ int check_draft(const dspark_draft_args *a) {
     return DSPARK_OK;
 }
 
-size_t draft_partials_bytes(int R, int V) {
-    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)R * dspark::draft_step_nparts(V));
+// The step kernels' scratch: one partial per (request, vocabulary range) --
+// ceil(V / 64) ranges on the CUDA-core path, one per CTA on the tensor-core
+// path -- then the tensor-core step's per-M-tile completion counters.
+constexpr size_t kCounterBytes = 256;
+
+dspark::DraftStep step_template(const dspark_draft_args *a, const float *A_rnn) {
+    dspark::DraftStep st{};
+    st.R = a->R; st.V = a->V; st.r = a->r; st.gamma = a->gamma; st.dtype = a->dtype;
+    st.U = a->U; st.W1 = a->W1; st.W2t = a->W2t;
+    st.seed = a->seed; st.cycle = a->cycle;
+    st.err = a->err;
+    st.A_op = A_rnn;
+    st.a_stride = a->gamma * a->r;
+    st.h = a->h; st.d = a->d; st.w = a->w; st.sts_T = a->sts_T;
+    st.x_out = a->x; st.logq = a->logq; st.lse = a->lse; st.c = a->c;
+    return st;
+}
+
+bool use_tc_path(const dspark::DraftStep &st) {
+    return dspark::draft_step_tc_supported(st) && (size_t)((st.R + 63) / 64) * sizeof(int) <= kCounterBytes;
+}
+
+int step_nparts(const dspark::DraftStep &st, bool tc) {
+    if (!tc) return dspark::draft_step_nparts(st.V);
+    int np = 0, mt = 0;
+    dspark::draft_step_tc_shape(st.R, st.V, st.A_op != nullptr, &np, &mt);
+    return np;
+}
+
+size_t draft_ws_bytes(const dspark_draft_args *a, const float *A_rnn) {
+    const dspark::DraftStep st = step_template(a, A_rnn);
+    const int np = step_nparts(st, use_tc_path(st));
+    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)a->R * np) + kCounterBytes;
 }
 
 // the gamma sequential steps shared by both heads
 int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws, cudaStream_t s,
                    const dspark::RnnStep *rnn, int k_first, int k_last) {
     using namespace dspark;
-    DraftStep st{};
-    st.R = a->R; st.V = a->V; st.r = a->r; st.gamma = a->gamma; st.dtype = a->dtype;
-    st.U = a->U; st.W1 = a->W1; st.W2t = a->W2t;
-    st.seed = a->seed; st.cycle = a->cycle;
+    DraftStep st = step_template(a, rnn ? A_rnn : nullptr);
     st.part = static_cast<DraftPartial *>(part_ws);
-    st.nparts = draft_step_nparts(a->V);
-    st.err = a->err;
+    const bool use_tc = use_tc_path(st);
+    st.nparts = step_nparts(st, use_tc);
+    st.counters = reinterpret_cast<int *>(static_cast<char *>(part_ws) + draft_ws_bytes(a, st.A_op) -
+                                          kCounterBytes);
     DraftReduce rd{};
     rd.R = a->R; rd.V = a->V; rd.r = a->r; rd.d = a->d; rd.gamma = a->gamma; rd.dtype = a->dtype;
     rd.part = st.part; rd.nparts = st.nparts;
     rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
     rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
-    const bool use_tc = rnn == nullptr && draft_step_tc_supported(st);
     if (use_tc) {
-        int mt = 0;
-        draft_step_tc_shape(a->R, a->V, &st.nparts, &mt);
-        rd.nparts = st.nparts;
+        cudaError_t e = cudaMemsetAsync(st.counters, 0, kCounterBytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft counters");
     }
     for (int k = k_first; k <= k_last; ++k) {
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
@@ -89,13 +117,13 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
             cudaError_t e = launch_rnn_step(rs, s);
             if (e != cudaSuccess) return cuda_fail(e, "rnn step");
             st.A_op = A_rnn + (size_t)(k - 1) * a->r;
-            st.a_stride = a->gamma * a->r;
         }
         st.k = k;
         st.x_prev = xp;
         st.x_stride = xs;
         cudaError_t e = use_tc ? launch_draft_step_tc(st, s) : launch_draft_step(st, s);
         if (e != cudaSuccess) return cuda_fail(e, use_tc ? "draft step (tensor cores)" : "draft step");
+        if (use_tc) continue;  // merged and scored inside the tensor-core step
         rd.k = k;
         rd.x_prev = xp;
         rd.x_stride = xs;
@@ -115,7 +143,7 @@ DSPARK_API int dspark_version(void) { return 100; }
 
 DSPARK_API size_t dspark_draft_markov_workspace_size(const dspark_draft_args *a) {
     if (check_draft(a) != DSPARK_OK) return 0;
-    return draft_partials_bytes(a->R, a->V);
+    return draft_ws_bytes(a, nullptr);
 }
 
 DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_stream_t stream) {
@@ -165,7 +193,7 @@ int noalloc_scratch(void **out) {
 DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_stream_t stream) {
     int rc = check_draft(a);
     if (rc != DSPARK_OK) return rc;
-    const size_t need = draft_partials_bytes(a->R, a->V);
+    const size_t need = draft_ws_bytes(a, nullptr);
     if (need > (size_t)DSPARK_NOALLOC_SCRATCH_BYTES)
         return fail(DSPARK_ERR_UNSUPPORTED,
                     "noalloc draft needs %zu bytes of scratch for R=%d V=%d; the fixed array holds %u",
@@ -181,7 +209,7 @@ DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_st
 DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a) {
     if (!a || check_draft(&a->base) != DSPARK_OK) return 0;
     const dspark_draft_args &b = a->base;
-    return draft_partials_bytes(b.R, b.V) + dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
+    return draft_ws_bytes(&b, a->A) + dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
            dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
 }
 
@@ -195,7 +223,7 @@ DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_strea
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *p = static_cast<char *>(ws);
     void *part = p;
-    p += draft_partials_bytes(b.R, b.V);
+    p += draft_ws_bytes(&b, a->A);
     float *state = reinterpret_cast<float *>(p);
     p += dspark::align256(sizeof(float) * (size_t)b.R * b.r);
     float *Hpre = reinterpret_cast<float *>(p);

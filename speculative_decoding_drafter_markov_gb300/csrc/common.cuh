@@ -53,17 +53,17 @@ __device__ __forceinline__ uint32_t philox_ctr3(uint64_t cycle, uint32_t stream)
     return (uint32_t)(cycle << 2) | stream;
 }
 
+// The 32x32 -> 64-bit products are written as 64-bit multiplies (one wide
+// integer multiply each); the round keys k + i W depend only on the seed.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
-    uint32_t k0 = key.k0, k1 = key.k1;
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        if (round > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        const uint32_t k0 = key.k0 + (uint32_t)round * 0x9E3779B9u;
+        const uint32_t k1 = key.k1 + (uint32_t)round * 0xBB67AE85u;
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53ull;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57ull;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                       (uint32_t)p0);
     }
     return c;
 }
@@ -85,8 +85,26 @@ __device__ __forceinline__ float one_minus_uniform(uint32_t w) {
     return __uint_as_float(bits) - (1.0f - 1.0f / 16777216.0f);
 }
 
-// E = -ln u = -ln(1 - t), the unit exponential variate behind the race
-__device__ __forceinline__ float exp_variate(float t) { return -log1pf(-t); }
+// MUFU log2 (absolute error about 2^-22.6)
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ln E for the unit exponential variate E = -ln u = -ln(1 - t) behind the race.
+// For t < 2^-7, E = t + t^2/2 + t^3/3 + t^4/4 (truncation below 2^-28 relative);
+// otherwise E = -ln(2) log2(u) with u = 1 - t exact, whose absolute error
+// 2^-22.6 is at most 1.4e-5 relative because |log2 u| >= 2^-7 / ln 2.  The final
+// logarithm adds about 1e-7, so race scores carry an error below 2e-5.
+__device__ __forceinline__ float log_exp_variate(float t) {
+    float E;
+    if (t < 0.0078125f)
+        E = t * fmaf(t, fmaf(t, fmaf(t, 0.25f, 0.33333334f), 0.5f), 1.0f);
+    else
+        E = -kLn2 * lg2(1.0f - t);
+    return kLn2 * lg2(E);
+}
 
 // ---------------------------------------------------------------- epilogue state
 // One row's running fused-epilogue state.  `C` caches exp(m - best) * slack so
@@ -95,53 +113,72 @@ __device__ __forceinline__ float exp_variate(float t) { return -log1pf(-t); }
 // is skipped whenever t_v >= exp(z_v - m) * C.
 struct RowState {
     float m;      // running max of z
+    float mL;     // m * log2(e)
     float S;      // sum exp(z - m)
-    float best;   // best race score z - ln E
+    float best;   // best race score z - ln E of this thread's elements
     float zbest;  // z of the best element
     int idx;      // its vocabulary index (-1: none yet)
-    float C;      // exp(m - best) * slack
+    float thr;    // filter threshold: a score some element of the row reached (>= best)
+    float C;      // exp(m - thr) * slack
 };
 
 __device__ __forceinline__ void row_init(RowState &s) {
     s.m = -INFINITY;
+    s.mL = -INFINITY;
     s.S = 0.f;
     s.best = -INFINITY;
     s.zbest = 0.f;
     s.idx = -1;
+    s.thr = -INFINITY;
     s.C = INFINITY;
 }
 
 __device__ __forceinline__ void row_refresh_C(RowState &s) {
-    s.C = ex2((s.m - s.best) * kLog2e) * kRaceSlack;
+    s.C = ex2((s.m - s.thr) * kLog2e) * kRaceSlack;
 }
 
-// Feed four consecutive vocabulary entries v0..v0+3 (one Philox call);
-// entries at or beyond V are ignored.
+// Raise the filter threshold to a score reached elsewhere in the same row (an
+// element below it cannot be the row's winner).
+__device__ __forceinline__ void row_raise_thr(RowState &s, float thr) {
+    if (thr > s.thr) {
+        s.thr = thr;
+        row_refresh_C(s);
+    }
+}
+
+// Feed four consecutive vocabulary entries v0..v0+3 (one Philox call).
+// kFull: all four are below V; otherwise entries at or beyond V are ignored.
+template <bool kFull = false>
 __device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0, int V,
                                           const uint4 &words) {
-    float zmax = -INFINITY;
+    float zmax;
+    if (kFull) {
+        zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    } else {
+        zmax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (v0 + j < V) zmax = fmaxf(zmax, z[j]);
+        for (int j = 0; j < 4; ++j)
+            if (v0 + j < V) zmax = fmaxf(zmax, z[j]);
+    }
     if (zmax > s.m) {
         s.S *= ex2((s.m - zmax) * kLog2e);
         s.m = zmax;
+        s.mL = zmax * kLog2e;
         row_refresh_C(s);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if (v0 + j >= V) continue;
-        const float e = ex2((z[j] - s.m) * kLog2e);
+        if (!kFull && v0 + j >= V) continue;
+        const float e = ex2(fmaf(z[j], kLog2e, -s.mL));
         s.S += e;
-        const uint32_t w = word_lane(words, j);
-        const float t = one_minus_uniform(w);
+        const float t = one_minus_uniform(word_lane(words, j));
         if (!(t >= e * s.C)) {
-            const float score = z[j] - logf(exp_variate(t));
+            const float score = z[j] - log_exp_variate(t);
             if (score > s.best) {
                 s.best = score;
                 s.idx = v0 + j;
                 s.zbest = z[j];
-                row_refresh_C(s);
+                row_raise_thr(s, score);
             }
         }
     }
@@ -157,6 +194,7 @@ __device__ __forceinline__ void row_merge(RowState &a, float m, float S, float b
         a.S = a.S * ex2((a.m - M) * kLog2e) + S * ex2((m - M) * kLog2e);
     }
     a.m = M;
+    a.mL = M * kLog2e;
     if (idx >= 0 && (a.idx < 0 || best > a.best || (best == a.best && idx < a.idx))) {
         a.best = best;
         a.zbest = zbest;
@@ -164,11 +202,23 @@ __device__ __forceinline__ void row_merge(RowState &a, float m, float S, float b
     }
 }
 
-// Partial result of one (row, vocabulary slice) of a draft step.
-struct DraftPartial {
+// Partial result of one (row, vocabulary slice) of a draft step (32 bytes, so
+// a merge reads it with two 16-byte loads).
+struct __align__(16) DraftPartial {
     float m, S, best, zbest;
-    int idx;
+    int idx, pad0, pad1, pad2;
 };
+
+__device__ __forceinline__ DraftPartial make_partial(float m, float S, float best, float zbest, int idx) {
+    return DraftPartial{m, S, best, zbest, idx, 0, 0, 0};
+}
+
+// L2 read of a partial written by another CTA of the same launch
+__device__ __forceinline__ DraftPartial load_partial_cg(const DraftPartial *q) {
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(q));
+    const int4 b = __ldcg(reinterpret_cast<const int4 *>(q) + 1);
+    return DraftPartial{a.x, a.y, a.z, a.w, b.x, 0, 0, 0};
+}
 
 // Partial result of one (row, vocabulary slice) of verification phase 2:
 // the race over the residual max(0, p - q) and, as fallback / bonus, over p.
@@ -194,7 +244,7 @@ __device__ __forceinline__ void race_init(Race &r) {
 __device__ __forceinline__ void race_feed(Race &r, float w, float t, int v) {
     if (!(w > 0.f)) return;
     if (t >= w * r.C) return;
-    const float score = logf(w) - logf(exp_variate(t));
+    const float score = kLn2 * lg2(w) - log_exp_variate(t);
     if (score > r.best) {
         r.best = score;
         r.idx = v;

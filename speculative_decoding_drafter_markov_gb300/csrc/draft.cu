@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) draft_step_simt(const DraftStep p) {
             row_merge(st, m, S, b, zb, ix);
         }
         if (quad == 0 && row < p.R)
-            p.part[(size_t)row * p.nparts + slice] = DraftPartial{st.m, st.S, st.best, st.zbest, st.idx};
+            p.part[(size_t)row * p.nparts + slice] = make_partial(st.m, st.S, st.best, st.zbest, st.idx);
     }
 }
 
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kReduceThreads) draft_reduce_kernel(const Draf
     __syncthreads();
     for (int half = kReduceThreads / 2; half > 0; half >>= 1) {
         if (tid < half) {
-            RowState a{s_m[tid], s_S[tid], s_b[tid], s_z[tid], s_i[tid], 0.f};
+            RowState a{s_m[tid], s_m[tid] * kLog2e, s_S[tid], s_b[tid], s_z[tid], s_i[tid], s_b[tid], 0.f};
             row_merge(a, s_m[tid + half], s_S[tid + half], s_b[tid + half], s_z[tid + half],
                       s_i[tid + half]);
             s_m[tid] = a.m; s_S[tid] = a.S; s_b[tid] = a.best; s_z[tid] = a.zbest; s_i[tid] = a.idx;

@@ -1,6 +1,7 @@
 // kernels.h -- host-side launchers of the DSpark kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -26,13 +27,28 @@ struct DraftStep {
     DraftPartial *part;              // [R, nparts]
     int nparts;
     int32_t *err;
+    // used by the tensor-core step, which also merges the partials and computes
+    // the confidence itself
+    const void *h;                   // [R, gamma, d]
+    int d;
+    const float *w, *sts_T;
+    int32_t *x_out;
+    float *logq, *lse, *c;
+    int *counters;                   // [number of M-tiles], zero on entry
 };
 int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
-// tensor-core path (bf16, r in {64, 128, 192, 256}, V % 8 == 0, Markov head)
+// tensor-core path (bf16, r in {64, 128, 192, 256}, V % 8 == 0)
 bool draft_step_tc_supported(const DraftStep &p);
-void draft_step_tc_shape(int R, int V, int *nparts, int *n_mtiles);
+void draft_step_tc_shape(int R, int V, bool rnn, int *nparts, int *n_mtiles);
 cudaError_t launch_draft_step_tc(const DraftStep &p, cudaStream_t s);
+// shared tensor-core helpers
+int sm_count();
+bool tc_available();
+bool tc_kernels_enabled();
+bool encode_w2t_map(CUtensorMap *m, const void *W2t, int V, int r, int BN);
+bool encode_u_map(CUtensorMap *m, const void *U, int R, int gamma, int V, int MV);
+void tc_grid_shape(int R, int V, int MV, int BN, int *nparts, int *n_mtiles);
 
 // ----- reduce partials of step k, write x, logq, lse; confidence (eq. 7) -------
 struct DraftReduce {
@@ -90,6 +106,8 @@ struct VerifyWs {
 size_t verify_ws_bytes(int R, int gamma, int V, int N);
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N);
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s);
+bool verify_tc_supported(const dspark_verify_args &a);
+cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s);
 
 // ----- philox check ------------------------------------------------------------------
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out, cudaStream_t s);

@@ -339,12 +339,15 @@ cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaSt
         if (e != cudaSuccess) return e;
     }
     const bool rnn = a.A != nullptr;
-    if (a.dtype == DSPARK_BF16)
+    VerifyWs wf = w;  // the tensor-core path sets its own partial count
+    if (verify_tc_supported(a))
+        e = launch_verify_phase2_tc(a, wf, s);
+    else if (a.dtype == DSPARK_BF16)
         e = rnn ? launch_phase2<__nv_bfloat16, true>(a, w, s) : launch_phase2<__nv_bfloat16, false>(a, w, s);
     else
         e = rnn ? launch_phase2<float, true>(a, w, s) : launch_phase2<float, false>(a, w, s);
     if (e != cudaSuccess) return e;
-    verify_final<<<a.R, 256, 0, s>>>(a, w);
+    verify_final<<<a.R, 256, 0, s>>>(a, wf);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,236 @@
+// verify_tc.cu -- verification phase 2 on the tensor cores.
+//
+// "DSpark explained" section 06: at the first rejected position n of request
+// r the correction is drawn from norm(max(0, p_n - q_{n+1})); if every
+// scheduled token passed, the bonus token is drawn from p_{l_r}.  q_{n+1}
+// needs the draft logits of step n+1 again: U_{n+1} + (bias operand) W_2.
+// That contraction runs on tcgen05 exactly like the draft step (shared
+// pipeline in tc_pipeline.cuh); the epilogue streams the target row p_n and the
+// base-logit row U_{n+1} of each request from global memory and runs two Gumbel
+// races with the stream-2 noise: over the residual and over p (the bonus
+// sample, and the fallback for an empty residual).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tc_pipeline.cuh"
+
+namespace dspark {
+
+namespace {
+
+struct VerifyTcParams {
+    int R, V, r, gamma;
+    const __nv_bfloat16 *T, *U, *W1;
+    const float *A;  // RNN bias operands [R, gamma, r] or null
+    const int32_t *anchor, *x;
+    const float *lse;  // draft log-sum-exp [R, gamma]
+    VerifyWs w;
+    int nparts, n_mtiles, n_vtiles;
+    uint64_t seed, cycle;
+    int32_t *err;
+};
+
+template <class P>
+__global__ void __launch_bounds__(tcp::kThreads, 1)
+    verify_phase2_tc(const __grid_constant__ CUtensorMap tmB, const VerifyTcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ int s_mode[P::MV], s_n[P::MV], s_row[P::MV], s_xn[P::MV];
+    __shared__ float s_lsep[P::MV], s_lseq[P::MV];
+    typename P::State s = P::carve(smem_raw);
+    P::init(s);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
+    const int m0 = m_tile * P::MV;
+    int t_begin, ntiles;
+    tcp::tile_range(cv, p.nparts, p.n_vtiles, t_begin, ntiles);
+    const int kslabs = p.r / 64;
+
+    // per request: residual (1) or bonus (0) sample, its position and row
+    if (threadIdx.x < P::MV) {
+        const int rq = m0 + threadIdx.x;
+        int mode = -1, n = 0, row = 0, xn = 0;
+        float lsep = 0.f, lseq = 0.f;
+        if (rq < p.R) {
+            const int ell = p.w.ell[rq];
+            if (ell >= 0) {
+                const int fr = p.w.first_rej[rq];
+                mode = fr < ell ? 1 : 0;
+                n = fr < ell ? fr : ell;
+                row = p.w.row_of[rq * (p.gamma + 1) + n];
+                if (row < 0) {
+                    mode = -1;
+                } else {
+                    lsep = p.w.lse_p[row];
+                    if (mode == 1) {
+                        lseq = p.lse[(size_t)rq * p.gamma + n];
+                        xn = n == 0 ? p.anchor[rq] : p.x[(size_t)rq * p.gamma + n - 1];
+                        if (xn < 0 || xn >= p.V) xn = 0;
+                    }
+                }
+            } else if (cv == 0) {
+                set_err(p.err, DSPARK_ERR_INVAL);  // request missing from the batch
+            }
+        }
+        s_mode[threadIdx.x] = mode;
+        s_n[threadIdx.x] = n;
+        s_row[threadIdx.x] = row;
+        s_xn[threadIdx.x] = xn;
+        s_lsep[threadIdx.x] = lsep;
+        s_lseq[threadIdx.x] = lseq;
+    }
+    __syncthreads();  // row metadata, barriers and TMEM ready
+    P::ready(s);
+    if (warp == tcp::kProducerWarp) {
+        if (lane == 0) tc::prefetch_tmap(&tmB);
+        __syncwarp();
+        P::producer(s, &tmB, nullptr, t_begin, ntiles, kslabs, 0, m0, p.err);
+        __syncwarp();
+        P::teardown(s);
+        return;
+    }
+
+    // bias operand of q_{n+1}: W_1[x_n] (x_0 = anchor) or the RNN vector A_{n+1},
+    // by every thread except the producer warp
+    const int chunks_per_row = p.r / 8;
+    constexpr int kGather = tcp::kThreads - 32;
+    const int gt = threadIdx.x < tcp::kEpiThreads ? threadIdx.x : threadIdx.x - 32;
+    for (int e = gt; e < P::MV * chunks_per_row; e += kGather) {
+        const int row = e / chunks_per_row, c = e - row * chunks_per_row;
+        const int rq = m0 + row;
+        const bool live = s_mode[row] == 1;
+        if (P::KSPLIT == 1) {
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (live) val = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)s_xn[row] * p.r + c * 8);
+            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = val;
+        } else {
+            float xs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (live) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.A + ((size_t)rq * p.gamma + s_n[row]) * (size_t)p.r + c * 8);
+                const float4 a0 = src[0], a1 = src[1];
+                xs[0] = a0.x; xs[1] = a0.y; xs[2] = a0.z; xs[3] = a0.w;
+                xs[4] = a1.x; xs[5] = a1.y; xs[6] = a1.z; xs[7] = a1.w;
+            }
+            uint4 hi, lo;
+            tcp::split8(xs, hi, lo);
+            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = hi;
+            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 1)) = lo;
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::named_bar_sync(2, kGather);  // operand complete: the MMA warp may start
+
+    if (warp == tcp::kMmaWarp) {
+        if (lane == 0) P::mma(s, ntiles, kslabs, p.err);
+        __syncwarp();
+    } else {
+        const int et = threadIdx.x;
+        const int row = et / P::TPR, gi = et % P::TPR;
+        const int rq = m0 + row;
+        const int mode = s_mode[row], n = s_n[row];
+        const float lsep = s_lsep[row] * kLog2e, lseq = s_lseq[row] * kLog2e;
+        const __nv_bfloat16 *trow = p.T + (size_t)s_row[row] * p.V;
+        const __nv_bfloat16 *urow = p.U + ((size_t)rq * p.gamma + (mode == 1 ? n : 0)) * (size_t)p.V;
+        const PhiloxKey key = philox_key(p.seed);
+        const uint32_t c3 = philox_ctr3(p.cycle, 2);
+        Race res, pr;
+        race_init(res);
+        race_init(pr);
+        P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0) {
+            if (mode < 0) return;
+#pragma unroll
+            for (int j = 0; j < P::GPT; ++j) {
+                const int col = 4 * (gi + P::TPR * j);
+                const int v0 = n0 + col;
+                if (v0 >= p.V) continue;  // V % 4 == 0: a quad is all in or all out
+                const uint2 tt = *reinterpret_cast<const uint2 *>(trow + v0);
+                const float tv[4] = {tcp::bf16_lo(tt.x), tcp::bf16_hi(tt.x), tcp::bf16_lo(tt.y),
+                                     tcp::bf16_hi(tt.y)};
+                const uint4 words =
+                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), key);
+                float pv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
+                if (mode == 1) {
+                    const float4 acc = *reinterpret_cast<const float4 *>(s.staging + row * P::kPitch + col);
+                    const uint2 uu = *reinterpret_cast<const uint2 *>(urow + v0);
+                    const float zv[4] = {acc.x + tcp::bf16_lo(uu.x), acc.y + tcp::bf16_hi(uu.x),
+                                         acc.z + tcp::bf16_lo(uu.y), acc.w + tcp::bf16_hi(uu.y)};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float t = one_minus_uniform(word_lane(words, i));
+                        const float q = ex2(fmaf(zv[i], kLog2e, -lseq));
+                        race_feed(res, fmaxf(pv[i] - q, 0.f), t, v0 + i);
+                        race_feed(pr, pv[i], t, v0 + i);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        race_feed(pr, pv[i], one_minus_uniform(word_lane(words, i)), v0 + i);
+                }
+            }
+        });
+#pragma unroll
+        for (int off = P::TPR / 2; off > 0; off >>= 1) {
+            const float b1 = __shfl_xor_sync(0xffffffffu, res.best, off);
+            const int i1 = __shfl_xor_sync(0xffffffffu, res.idx, off);
+            const float b2 = __shfl_xor_sync(0xffffffffu, pr.best, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, pr.idx, off);
+            race_merge(res.best, res.idx, b1, i1);
+            race_merge(pr.best, pr.idx, b2, i2);
+        }
+        if (gi == 0 && rq < p.R)
+            p.w.part[(size_t)rq * p.nparts + cv] = VerifyPartial{res.best, pr.best, res.idx, pr.idx};
+    }
+    P::teardown(s);
+}
+
+// Pipe<rows, vocabulary tile, W_2^T ring, U ring (none), operand split>
+using VerifyM64 = tcp::Pipe<64, 128, 2, 0, 1>;
+using VerifyM128 = tcp::Pipe<128, 64, 3, 0, 1>;
+using VerifyRnn = tcp::Pipe<64, 64, 4, 0, 2>;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <class P>
+cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
+    int nparts = 0, mt = 0;
+    tc_grid_shape(a.R, a.V, P::MV, P::BN, &nparts, &mt);
+    CUtensorMap tmB;
+    if (!encode_w2t_map(&tmB, a.W2t, a.V, a.r, P::BN)) return cudaErrorInvalidValue;
+    w.nparts = nparts;
+    VerifyTcParams tp;
+    tp.R = a.R; tp.V = a.V; tp.r = a.r; tp.gamma = a.gamma;
+    tp.T = static_cast<const __nv_bfloat16 *>(a.T);
+    tp.U = static_cast<const __nv_bfloat16 *>(a.U);
+    tp.W1 = static_cast<const __nv_bfloat16 *>(a.W1);
+    tp.A = a.A;
+    tp.anchor = a.anchor; tp.x = a.x; tp.lse = a.lse;
+    tp.w = w;
+    tp.nparts = nparts; tp.n_mtiles = mt; tp.n_vtiles = (a.V + P::BN - 1) / P::BN;
+    tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
+    auto kern = verify_phase2_tc<P>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<mt * nparts, tcp::kThreads, P::kBytes, s>>>(tmB, tp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool verify_tc_supported(const dspark_verify_args &a) {
+    return tc_kernels_enabled() && a.dtype == DSPARK_BF16 && a.r % 64 == 0 && a.r >= 64 && a.r <= 256 &&
+           a.V % 8 == 0 && aligned16(a.T) && aligned16(a.U) && aligned16(a.W1) && aligned16(a.W2t) &&
+           (a.A == nullptr || aligned16(a.A)) && tc_available();
+}
+
+cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
+    if (a.A) return launch_cfg<VerifyRnn>(a, w, s);
+    if (a.R <= 64) return launch_cfg<VerifyM64>(a, w, s);
+    return launch_cfg<VerifyM128>(a, w, s);
+}
+
+}  // namespace dspark

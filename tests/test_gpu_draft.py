@@ -96,10 +96,11 @@ def test_markov_full_size_sampled(orc, name, reqs):
 RNN_SMALL = [
     W.small("rnn", R=5, gamma=4, V=900, r=16, d=24),
     W.small("rnn", R=3, gamma=3, V=257, r=8, d=8, dtype="f32"),
+    W.small("rnn", R=70, gamma=3, V=2000, r=64, d=24),   # tensor cores, 2 M-tiles
 ]
 
 
-@pytest.mark.parametrize("wl", RNN_SMALL, ids=lambda w: f"{w.name}-{w.dtype}")
+@pytest.mark.parametrize("wl", RNN_SMALL, ids=lambda w: f"{w.name}-{w.dtype}-r{w.r}")
 def test_rnn_small(orc, wl):
     inp = _to_cuda(W.draft_inputs(wl, seed=2))
     gpu = _gpu_draft(inp, 77, 4, rnn=True)

@@ -59,6 +59,9 @@ SMALL = [
     (W.small("qwen4b", R=12, gamma=4, V=1001, r=24, d=16), None),
     (W.small("heavy", R=20, gamma=6, V=4096 + 17, r=32, d=16), None),
     (W.small("prod", R=9, gamma=3, V=333, r=16, d=8, dtype="f32"), None),
+    # tensor-core phase 2: bf16, V % 8 == 0, r a multiple of 64
+    (W.small("qwen4b", R=12, gamma=4, V=1000, r=64, d=16), None),
+    (W.small("heavy", R=100, gamma=5, V=4096 + 8, r=128, d=16), None),
 ]
 
 
@@ -88,9 +91,11 @@ def test_verify_many_cycles_small(orc):
     assert total_rej > 0  # the residual path was exercised
 
 
-def test_verify_rnn_small(orc):
-    wl = W.small("rnn", R=6, gamma=4, V=640, r=16, d=16)
-    ell = np.array([4, 0, 2, 4, 1, 3])
+@pytest.mark.parametrize("wl", [W.small("rnn", R=6, gamma=4, V=640, r=16, d=16),
+                                W.small("rnn", R=70, gamma=3, V=1024, r=64, d=16)],
+                         ids=["cuda-cores", "tensor-cores"])
+def test_verify_rnn_small(orc, wl):
+    ell = np.random.default_rng(2).integers(0, wl.gamma + 1, wl.R)
     case = _case(orc, wl, 8, 2, ell, rnn=True)
     gpu = _gpu_verify(*case, 8, 2)
     ref = _oracle_verify(orc, *case, 8, 2)

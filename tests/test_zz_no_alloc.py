@@ -56,8 +56,8 @@ def test_noalloc_matches_workspace_version(wl):
 
 
 def test_noalloc_rejects_sizes_beyond_the_array():
-    wl = W.WORKLOADS["prod"]  # R=512, V=129280: 20.7 MB of scratch > 16 MiB
-    R, gamma, V, r, d = wl.R, 1, wl.V, wl.r, 8
+    # V not a multiple of 8 takes the CUDA-core path: 512 x ceil(V/64) x 32 B > 16 MiB
+    R, gamma, V, r, d = 512, 1, 129281, 256, 8
     z = lambda *s, dt=torch.bfloat16: torch.zeros(s, dtype=dt, device="cuda")
     inp = {"U": z(R, gamma, V), "h": z(R, gamma, d), "W1": z(V, r), "W2t": z(V, r),
            "w": z(d + r, dt=torch.float32), "anchor": z(R, dt=torch.int32)}
