@@ -101,8 +101,10 @@ DSPARK_API size_t dspark_draft_markov_workspace_size(const dspark_draft_args *a)
 DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_stream_t stream);
 /* Step k (1..gamma) of the same loop alone: reads x_{k-1} (the anchor for
  * k = 1, else column k-2 of a->x) and writes column k-1 of x, logq, lse, c.
- * dspark_draft_markov equals calls for k = 1..gamma in order on one stream;
- * the split lets an engine interleave other work between steps. */
+ * dspark_draft_markov equals calls for k = 1..gamma in order on one stream
+ * with one workspace; the split lets an engine interleave other work between
+ * steps.  Step 1 (re)starts the per-draft step counters kept in the
+ * workspace, so a step k > 1 must follow steps 1..k-1 of the same draft. */
 DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, void *ws,
                                         dspark_stream_t stream);
 

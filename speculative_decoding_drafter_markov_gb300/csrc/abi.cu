@@ -102,7 +102,7 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
     rd.part = st.part; rd.nparts = st.nparts;
     rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
     rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
-    if (use_tc) {
+    if (use_tc && k_first == 1) {  // step 1 starts the step counters; later steps continue them
         cudaError_t e = cudaMemsetAsync(st.counters, 0, kCounterBytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft counters");
     }
@@ -119,6 +119,7 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
             st.A_op = A_rnn + (size_t)(k - 1) * a->r;
         }
         st.k = k;
+        st.step_index = k;
         st.x_prev = xp;
         st.x_stride = xs;
         cudaError_t e = use_tc ? launch_draft_step_tc(st, s) : launch_draft_step(st, s);

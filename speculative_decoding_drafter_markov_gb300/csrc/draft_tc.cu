@@ -3,9 +3,9 @@
 // DSpark digest eq. (5): B_k = W_1[x_{k-1}] W_2 (Markov head) or eq. (6)
 // B_k = W_2^T tanh(W_o z_k) (RNN head), contracted on tcgen05 into TMEM and
 // consumed in place by the eq. (4) epilogue: U_k add, online max / sum-exp,
-// Philox Gumbel race.  No logit reaches global memory.  The pipeline (TMA ring
-// of W_2^T slabs and U_k tiles, MMA warp, TMEM staging) is tc_pipeline.cuh; this
-// file supplies the bias operand and the per-tile epilogue.
+// Philox Gumbel race.  No logit reaches global memory.  The pipeline (TMA rings
+// of W_2^T slabs and U_k tiles, MMA warp, per-warp TMEM epilogue) is tc_pipe.cuh;
+// this file supplies the bias operand, the per-tile epilogue and the merge.
 //
 // Markov head: the operand E = W_1[x_{k-1}] is exact in bf16.  RNN head: the
 // fp32 operand A_k is split into bf16 hi + lo parts (two MMAs per K-step).
@@ -19,7 +19,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
-#include "tc_pipeline.cuh"
+#include "tc_pipe.cuh"
 
 namespace dspark {
 
@@ -37,7 +37,8 @@ struct TcParams {
     const float *sts_T;      // [gamma] or null
     uint64_t seed, cycle;
     DraftPartial *part;
-    int *counters;           // [n_mtiles], zero on entry, left zero on exit
+    int *counters;           // [n_mtiles] completion counters, zeroed by the caller per call
+    int target;              // counter value once every CTA of this step has published
     int32_t *x;
     float *logq, *lse, *c;   // [R, gamma]
     int nparts;  // vocabulary ranges (CTAs per M-tile)
@@ -48,18 +49,30 @@ struct TcParams {
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request, by all
 // epilogue threads (16-byte chunks of h_k then of W_1[x_{k-1}]), reduced in a
-// fixed order through `red` (16 floats of shared memory).
-__device__ __forceinline__ void confidence_row(const TcParams &p, int grow, int et, float *red) {
-    int xp = p.x_prev[(size_t)grow * p.x_stride];
-    if (xp < 0 || xp >= p.V) xp = 0;
+// fixed order through `red` (16 floats of shared memory).  `pre` is thread et's
+// chunk et of h_k when `have_pre` (loaded early); E comes from shared memory
+// when the operand there is W_1[x_{k-1}] itself (`e_smem`, else null).
+template <class P>
+__device__ __forceinline__ void confidence_row(const TcParams &p, const typename P::State &s, int local_row,
+                                               int grow, int et, float *red, bool have_pre, uint4 pre,
+                                               bool e_smem) {
     const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (p.k - 1)) * (size_t)p.d;
-    const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
     float dot = 0.f;
     if ((p.d & 7) == 0) {
+        int xp = 0;
+        if (!e_smem) {
+            xp = p.x_prev[(size_t)grow * p.x_stride];
+            if (xp < 0 || xp >= p.V) xp = 0;
+        }
         const int hc = p.d / 8, nc = hc + p.r / 8;
         for (int ch = et; ch < nc; ch += tcp::kEpiThreads) {
-            const bool in_h = ch < hc;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(in_h ? h + ch * 8 : e + (ch - hc) * 8);
+            uint4 raw;
+            if (ch < hc)
+                raw = (have_pre && ch == et) ? pre : *reinterpret_cast<const uint4 *>(h + ch * 8);
+            else if (e_smem)
+                raw = *reinterpret_cast<const uint4 *>(P::a_chunk(s, local_row, ch - hc, 0));
+            else
+                raw = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xp * p.r + (ch - hc) * 8);
             const float *wv = p.w + ch * 8;  // w = [w_h ; w_e] lines up with [h ; e]
             const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -69,6 +82,9 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, int grow, int 
             }
         }
     } else {
+        int xp = p.x_prev[(size_t)grow * p.x_stride];
+        if (xp < 0 || xp >= p.V) xp = 0;
+        const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
         for (int j = et; j < p.d + p.r; j += tcp::kEpiThreads)
             dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
     }
@@ -85,6 +101,12 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, int grow, int 
     tc::named_bar_sync(1, tcp::kEpiThreads);
 }
 
+__device__ __forceinline__ int ld_acquire(const int *ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 template <class P>
 __global__ void __launch_bounds__(tcp::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
@@ -98,48 +120,39 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     int t_begin, ntiles;
     tcp::tile_range(cv, p.nparts, p.n_vtiles, t_begin, ntiles);
     const int kslabs = p.r / 64;
-
-    __syncthreads();  // barriers initialised, TMEM allocated
-    P::ready(s);
-    if (warp == tcp::kProducerWarp) {
-        // W_2^T and U_k do not depend on x_{k-1}: stream from the first cycle
-        if (lane == 0) {
-            tc::prefetch_tmap(&tmB);
-            tc::prefetch_tmap(&tmU);
-        }
-        __syncwarp();
-        P::producer(s, &tmB, &tmU, t_begin, ntiles, kslabs, p.k - 1, m0, p.err);
-        __syncwarp();
-        P::teardown(s);
-        return;
-    }
-
-    // bias operand of the M-tile's rows, in the swizzled K-major layout, by every
-    // thread except the producer warp
     const int chunks_per_row = p.r / 8;
-    constexpr int kGather = tcp::kThreads - 32;
-    const int gt = threadIdx.x < tcp::kEpiThreads ? threadIdx.x : threadIdx.x - 32;
-    int *s_tok = reinterpret_cast<int *>(s.staging);  // staging is free until the first tile
-    if (P::KSPLIT == 1) {
-        if (gt < P::MV) {  // the M-tile's tokens first: one load per row, all in flight together
-            const int grow = m0 + gt;
-            int xp = grow < p.R ? p.x_prev[(size_t)grow * p.x_stride] : -1;
-            if (grow < p.R && (xp < 0 || xp >= p.V)) {
-                set_err(p.err, DSPARK_ERR_RANGE);
-                xp = 0;
-            }
-            s_tok[gt] = xp;
+    int *s_tok = reinterpret_cast<int *>(P::merge_scratch(s));  // the rings are idle until the producer starts
+
+    // 1. the M-tile's tokens x_{k-1} (one load per row, all in flight together)
+    //    and this CTA's first chunk of h_k for the confidence
+    if (P::KSPLIT == 1 && threadIdx.x < P::MV) {
+        const int grow = m0 + threadIdx.x;
+        int xp = grow < p.R ? p.x_prev[(size_t)grow * p.x_stride] : -1;
+        if (grow < p.R && (xp < 0 || xp >= p.V)) {
+            set_err(p.err, DSPARK_ERR_RANGE);
+            xp = 0;
         }
-        tc::named_bar_sync(2, kGather);
+        s_tok[threadIdx.x] = xp;
     }
-    for (int e = gt; e < P::MV * chunks_per_row; e += kGather) {
+    const bool conf_row = cv < P::MV && m0 + cv < p.R;
+    const bool have_pre = conf_row && threadIdx.x < tcp::kEpiThreads && (p.d & 7) == 0 && threadIdx.x < p.d / 8;
+    uint4 pre = make_uint4(0u, 0u, 0u, 0u);
+    if (have_pre)
+        pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (p.k - 1)) * (size_t)p.d +
+                                               threadIdx.x * 8);
+    __syncthreads();  // tokens, barriers, thresholds, TMEM
+    P::ready(s);
+
+    // 2. bias operand in the swizzled K-major layout, before the W_2 / U streams
+    //    compete for memory bandwidth
+    for (int e = threadIdx.x; e < P::MV * chunks_per_row; e += tcp::kThreads) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int grow = m0 + row;
         if (P::KSPLIT == 1) {
             const int xp = s_tok[row];
             const uint4 val = xp >= 0 ? *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xp * p.r + c * 8)
                                       : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = val;
+            P::put_a(s, row, c, 0, val);
         } else {
             float xs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (grow < p.R) {
@@ -150,41 +163,52 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             }
             uint4 hi, lo;
             tcp::split8(xs, hi, lo);
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = hi;
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 1)) = lo;
+            P::put_a(s, row, c, 0, hi);
+            P::put_a(s, row, c, 1, lo);
         }
     }
     tc::fence_proxy_async_smem();
-    tc::named_bar_sync(2, kGather);  // operand complete: the MMA warp may start
+    __syncthreads();  // operand complete
 
-    if (warp == tcp::kMmaWarp) {
+    if (warp == tcp::kProducerWarp) {
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmB);
+            tc::prefetch_tmap(&tmU);
+        }
+        __syncwarp();
+        P::producer(s, &tmB, &tmU, t_begin, ntiles, kslabs, p.k - 1, m0, p.err);
+        __syncwarp();
+    } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, p.err);
         __syncwarp();
     } else {
         const int et = threadIdx.x;
-        const int row = et / P::TPR, gi = et % P::TPR;
+        const int row = P::epi_row(), col0 = P::epi_col0();
         const int grow = m0 + row;
         const bool row_live = grow < p.R;
-        // confidences of this CTA's share of the M-tile's rows (local rows cv,
-        // cv + nparts, ...) while the first tile is in flight; the staging tile
-        // is still free and holds the reduction
-        for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) confidence_row(p, m0 + i, et, s.staging);
+        // confidences of this CTA's rows (local rows cv, cv + nparts, ...) while
+        // the first tile is in flight
+        for (int i = cv, j = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++j)
+            confidence_row<P>(p, s, i, m0 + i, et, s.red, j == 0 && have_pre, pre, P::KSPLIT == 1);
 
         const PhiloxKey key = philox_key(p.seed);
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         RowState st;
         row_init(st);
-        P::epilogue(s, t_begin, ntiles, p.err, [&](int t, int n0) {
-            const unsigned char *sU = P::u_tile(s, t);
+        P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *sU) {
+            if (!row_live) return;
+            // the row's best score so far, wherever in the CTA it was found, filters this thread
+            row_raise_thr(st, P::read_thr(s, row));
+            const float best0 = st.best;
             const bool full_tile = n0 + P::BN <= p.V;
 #pragma unroll
-            for (int j = 0; j < P::GPT; ++j) {
-                if (!row_live) break;
-                const int col = 4 * (gi + P::TPR * j);
-                const float4 acc = *reinterpret_cast<const float4 *>(s.staging + row * P::kPitch + col);
+            for (int g = 0; g < P::CW / 4; ++g) {
+                const int col = col0 + 4 * g;
                 const uint2 uu = P::u_quad(sU, row, col);
-                float z[4] = {acc.x + tcp::bf16_lo(uu.x), acc.y + tcp::bf16_hi(uu.x), acc.z + tcp::bf16_lo(uu.y),
-                              acc.w + tcp::bf16_hi(uu.y)};
+                float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
+                              __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
+                              __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
+                              __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
                 const int v0 = n0 + col;
                 const uint4 words =
                     philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)grow, c3), key);
@@ -193,83 +217,103 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                 else
                     row_feed4<false>(st, z, v0, p.V, words);
             }
-            // the row's best score so far filters all TPR threads of the row
-            float thr = st.thr;
-#pragma unroll
-            for (int off = P::TPR / 2; off > 0; off >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, off));
-            row_raise_thr(st, thr);
+            if (st.best > best0) P::publish_thr(s, row, st.best);
         });
-        // merge the TPR threads of each row (consecutive lanes)
-#pragma unroll
-        for (int off = P::TPR / 2; off > 0; off >>= 1) {
-            const float m = __shfl_xor_sync(0xffffffffu, st.m, off);
-            const float S = __shfl_xor_sync(0xffffffffu, st.S, off);
-            const float bb = __shfl_xor_sync(0xffffffffu, st.best, off);
-            const float zb = __shfl_xor_sync(0xffffffffu, st.zbest, off);
-            const int ix = __shfl_xor_sync(0xffffffffu, st.idx, off);
-            row_merge(st, m, S, bb, zb, ix);
-        }
-        if (gi == 0 && row_live)
-            p.part[(size_t)grow * p.nparts + cv] = make_partial(st.m, st.S, st.best, st.zbest, st.idx);
 
-        // the last CTA of the M-tile to finish merges all vocabulary ranges in a
-        // fixed order: lse_k, x_k and log q_k(x_k)
+        // merge the TPR threads of each request (fixed warp order) into this CTA's partial
+        float *mg = P::merge_scratch(s);
+        mg[et] = st.m;
+        mg[tcp::kEpiThreads + et] = st.S;
+        mg[2 * tcp::kEpiThreads + et] = st.best;
+        mg[3 * tcp::kEpiThreads + et] = st.zbest;
+        reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + et] = st.idx;
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        if (et < P::MV && m0 + et < p.R) {
+            RowState f;
+            row_init(f);
+            const int q0 = P::DUAL ? (et >> 5) : (et >> 5);  // first warp holding this request
+            const int wstep = P::DUAL ? 2 : 4;
+            for (int w = q0; w < tcp::kEpiWarps; w += wstep) {
+                const int src = w * 32 + (et & 31);
+                row_merge(f, mg[src], mg[tcp::kEpiThreads + src], mg[2 * tcp::kEpiThreads + src],
+                          mg[3 * tcp::kEpiThreads + src], reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + src]);
+            }
+            p.part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
+        }
+
+        // publish, then wait (bounded) until every CTA of the M-tile has published;
+        // the launch is cooperative, so all of them are resident
         __threadfence();
         tc::named_bar_sync(1, tcp::kEpiThreads);
-        if (et == 0) *s.flag = atomicAdd(&p.counters[m_tile], 1) == p.nparts - 1 ? 1 : 0;
+        if (et == 0) {
+            atomicAdd(&p.counters[m_tile], 1);
+            int ok = 1;
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (ld_acquire(&p.counters[m_tile]) < p.target) {
+                if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+                    set_err(p.err, DSPARK_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(256);
+            }
+            *s.flag = ok;
+        }
         tc::named_bar_sync(1, tcp::kEpiThreads);
+        // every CTA finalises its share of the rows: one partial per thread,
+        // merged in a fixed tree (lanes, then warps in order)
         if (*s.flag) {
             __threadfence();
-            RowState fin;
-            row_init(fin);
-            if (row_live) {
-                // batches of independent 16-byte loads, merged in index order
-                constexpr int kBatch = 8;
-                const DraftPartial *base = p.part + (size_t)grow * p.nparts;
-                for (int i0 = gi; i0 < p.nparts; i0 += P::TPR * kBatch) {
-                    DraftPartial q[kBatch];
+            float *wm = mg, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
+            int *wi = reinterpret_cast<int *>(wz + 16);
+            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) {
+                const int gr = m0 + i;
+                RowState f;
+                row_init(f);
+                if (et < p.nparts) {
+                    const DraftPartial q = load_partial_cg(p.part + (size_t)gr * p.nparts + et);
+                    row_merge(f, q.m, q.S, q.best, q.zbest, q.idx);
+                }
 #pragma unroll
-                    for (int b = 0; b < kBatch; ++b) {
-                        const int i = i0 + b * P::TPR;
-                        q[b] = i < p.nparts ? load_partial_cg(base + i)
-                                            : make_partial(-INFINITY, 0.f, -INFINITY, 0.f, -1);
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float m = __shfl_xor_sync(0xffffffffu, f.m, off);
+                    const float S = __shfl_xor_sync(0xffffffffu, f.S, off);
+                    const float bb = __shfl_xor_sync(0xffffffffu, f.best, off);
+                    const float zb = __shfl_xor_sync(0xffffffffu, f.zbest, off);
+                    const int ix = __shfl_xor_sync(0xffffffffu, f.idx, off);
+                    row_merge(f, m, S, bb, zb, ix);
+                }
+                if (lane == 0) {
+                    wm[warp] = f.m; wS[warp] = f.S; wb[warp] = f.best; wz[warp] = f.zbest; wi[warp] = f.idx;
+                }
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                if (et == 0) {
+                    RowState g;
+                    row_init(g);
+                    for (int w = 0; w < tcp::kEpiWarps; ++w) row_merge(g, wm[w], wS[w], wb[w], wz[w], wi[w]);
+                    const size_t o = (size_t)gr * p.gamma + (p.k - 1);
+                    const float lse = g.m + logf(g.S);
+                    int idx = g.idx;
+                    if (idx < 0 || !isfinite(lse)) {
+                        set_err(p.err, DSPARK_ERR_NONFINITE);
+                        idx = 0;
                     }
-#pragma unroll
-                    for (int b = 0; b < kBatch; ++b) row_merge(fin, q[b].m, q[b].S, q[b].best, q[b].zbest, q[b].idx);
+                    p.x[o] = idx;
+                    p.lse[o] = lse;
+                    p.logq[o] = g.zbest - lse;
                 }
+                tc::named_bar_sync(1, tcp::kEpiThreads);
             }
-#pragma unroll
-            for (int off = P::TPR / 2; off > 0; off >>= 1) {
-                const float m = __shfl_xor_sync(0xffffffffu, fin.m, off);
-                const float S = __shfl_xor_sync(0xffffffffu, fin.S, off);
-                const float bb = __shfl_xor_sync(0xffffffffu, fin.best, off);
-                const float zb = __shfl_xor_sync(0xffffffffu, fin.zbest, off);
-                const int ix = __shfl_xor_sync(0xffffffffu, fin.idx, off);
-                row_merge(fin, m, S, bb, zb, ix);
-            }
-            if (gi == 0 && row_live) {
-                const size_t o = (size_t)grow * p.gamma + (p.k - 1);
-                const float lse = fin.m + logf(fin.S);
-                int idx = fin.idx;
-                if (idx < 0 || !isfinite(lse)) {
-                    set_err(p.err, DSPARK_ERR_NONFINITE);
-                    idx = 0;
-                }
-                p.x[o] = idx;
-                p.lse[o] = lse;
-                p.logq[o] = fin.zbest - lse;
-            }
-            if (et == 0) p.counters[m_tile] = 0;
         }
     }
     P::teardown(s);
 }
 
 // pipeline configurations
-// Pipe<rows, vocabulary tile, W_2^T ring, U ring, operand split>
-using DraftM64 = tcp::Pipe<64, 128, 2, 2, 1>;   // Markov, R <= 64 per M-tile
-using DraftM128 = tcp::Pipe<128, 64, 2, 2, 1>;  // Markov, 128 rows per M-tile
-using DraftRnn = tcp::Pipe<64, 64, 3, 3, 2>;    // RNN (fp32 operand split hi/lo)
+// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
+using DraftM64 = tcp::Pipe<64, 128, 8, 2, 1>;   // Markov, R <= 64
+using DraftM128 = tcp::Pipe<128, 128, 6, 2, 1>; // Markov, 128 requests per M-tile
+using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -291,11 +335,14 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.n_mtiles = n_mtiles;
     tp.n_vtiles = (p.V + P::BN - 1) / P::BN;
     tp.err = p.err;
+    tp.target = p.step_index * nparts;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;
-    kern<<<n_mtiles * nparts, tcp::kThreads, P::kBytes, s>>>(tmB, tmU, tp);
-    return cudaGetLastError();
+    // cooperative: the CTAs wait for one another at the end of the step
+    void *args[] = {&tmB, &tmU, &tp};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(n_mtiles * nparts),
+                                       dim3(tcp::kThreads), args, (size_t)P::kBytes, s);
 }
 
 }  // namespace

@@ -1,0 +1,331 @@
+// tc_pipe.cuh -- the contraction pipeline shared by the tensor-core kernels.
+//
+// D = A . W_2^T[tile]^T on tcgen05, where A (the bias operand of each request:
+// W_1[x] or the RNN vector A_k, bf16, K-major, 128-byte swizzle) is resident in
+// shared memory and W_2^T streams through a ring of 64-wide K slabs.  One CTA
+// owns one M-tile of MV requests and a contiguous range of BN-wide vocabulary
+// tiles.  Warp roles (576 threads):
+//   warps 0..15  epilogue: every warp reads its own block of the accumulator
+//                straight from TMEM (no staging) and runs the caller's
+//                functor on it; synchronisation is per warp, through mbarriers.
+//   warp 16      TMA producer: lane 0 streams the W_2^T slab ring (each slot
+//                freed by the MMA commit that consumed it), lane 1 the U ring
+//                (freed when all 16 epilogue warps have used a tile).
+//   warp 17      TMEM allocator and MMA issuer, NACC accumulators of BN columns.
+// MV = 128: quadrant q of the accumulator holds requests 32q..32q+31 and the
+// four warps of a quadrant split the BN columns.  MV = 64: A holds the 64
+// requests twice (rows i and 64 + i), so quadrants 0-1 and 2-3 hold the same
+// requests; quadrants 0-1 take the first BN/2 columns and 2-3 the second half,
+// which keeps all 16 warps busy with only 64 requests.
+// KSPLIT = 2: A = A_hi + A_lo in bf16 (an fp32 operand kept to ~2^-16 relative),
+// two MMAs per K-step against the same W_2^T slab.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace dspark {
+namespace tcp {
+
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = kEpiThreads + 64;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+
+template <int MV_, int BN_, int NS_, int SU_, int KSPLIT_>
+struct Pipe {
+    static constexpr int MV = MV_, BN = BN_, NS = NS_, SU = SU_, KSPLIT = KSPLIT_;
+    static constexpr bool DUAL = MV == 64;
+    static constexpr bool WITH_U = SU > 0;
+    static constexpr int kArows = 128;                  // MMA rows (A duplicated when DUAL)
+    static constexpr int kSlabA = kArows * 128;         // one 64-wide K slab of A
+    static constexpr int kABytes = 4 * KSPLIT * kSlabA; // r <= 256
+    static constexpr int kSlabB = BN * 128;             // one 64-wide K slab of W_2^T
+    static constexpr int kUBox = MV * 128;              // 64 vocabulary columns of U
+    static constexpr int kUBytes = (BN / 64) * kUBox;
+    static constexpr int NACC = 512 / BN > 4 ? 4 : 512 / BN;  // TMEM accumulators
+    static constexpr int kTmemCols = NACC * BN;
+    static constexpr int CW = DUAL ? BN / 8 : BN / 4;  // accumulator columns per warp
+    static constexpr int TPR = DUAL ? 8 : 4;           // epilogue threads per request
+    static constexpr int kOffB = kABytes;
+    static constexpr int kOffU = kOffB + NS * kSlabB;
+    static constexpr int kOffBar = kOffU + SU * kUBytes;
+    static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC;
+    static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
+    static constexpr int kOffMisc = kOffThr + 4 * MV;
+    static constexpr int kOffRed = kOffMisc + 64;           // 16-float reduction scratch
+    static constexpr int kBytes = kOffRed + 64 + 1024;      // + alignment slack
+    // scratch for the per-CTA merge at the end (the rings are idle by then)
+    static constexpr int kMergeBytes = kEpiThreads * 5 * 4;
+    static_assert(kBytes <= 232448, "shared memory budget");
+    static_assert(kMergeBytes <= NS * kSlabB, "merge scratch");
+    static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
+    static_assert(CW == 16 || CW == 32, "TMEM load width");
+    static_assert(MV == 64 || MV == 128, "M-tile rows");
+
+    struct State {
+        unsigned char *smem, *sA;
+        uint64_t *fullB, *emptyB, *fullU, *emptyU, *tfull, *tempty;
+        unsigned *thr;  // ordered-uint encoded row thresholds
+        uint32_t *tmem_slot;
+        volatile int *abort_flag, *flag;
+        float *red;  // 16 floats
+        uint32_t tmem_base;
+    };
+
+    __device__ static State carve(unsigned char *raw) {
+        State s;
+        s.smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                                   ~static_cast<uintptr_t>(1023));
+        s.sA = s.smem;
+        uint64_t *bars = reinterpret_cast<uint64_t *>(s.smem + kOffBar);
+        s.fullB = bars;
+        s.emptyB = bars + NS;
+        s.fullU = bars + 2 * NS;
+        s.emptyU = bars + 2 * NS + SU;
+        s.tfull = bars + 2 * NS + 2 * SU;
+        s.tempty = s.tfull + NACC;
+        s.thr = reinterpret_cast<unsigned *>(s.smem + kOffThr);
+        s.tmem_slot = reinterpret_cast<uint32_t *>(s.smem + kOffMisc);
+        s.abort_flag = reinterpret_cast<volatile int *>(s.smem + kOffMisc + 4);
+        s.flag = reinterpret_cast<volatile int *>(s.smem + kOffMisc + 8);
+        s.red = reinterpret_cast<float *>(s.smem + kOffRed);
+        s.tmem_base = 0;
+        return s;
+    }
+
+    // all threads: barrier init, thresholds (thread 0 / first MV threads) and TMEM allocation
+    __device__ static void init(State &s) {
+        const int warp = threadIdx.x >> 5;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < NS; ++i) {
+                tc::mbar_init(&s.fullB[i], 1);
+                tc::mbar_init(&s.emptyB[i], 1);  // the MMA commit that consumed the slab
+            }
+            for (int i = 0; i < SU; ++i) {
+                tc::mbar_init(&s.fullU[i], 1);
+                tc::mbar_init(&s.emptyU[i], kEpiWarps);
+            }
+            for (int b = 0; b < NACC; ++b) {
+                tc::mbar_init(&s.tfull[b], 1);
+                tc::mbar_init(&s.tempty[b], kEpiWarps);
+            }
+            *s.abort_flag = 0;
+            *s.flag = 0;
+            tc::fence_mbar_init();
+        }
+        if (threadIdx.x < MV) s.thr[threadIdx.x] = ord_encode(-INFINITY);
+        if (warp == kMmaWarp) {
+            tc::tmem_alloc(s.tmem_slot, kTmemCols);
+            tc::tmem_relinquish();
+            tc::tc_fence_before();
+        }
+    }
+
+    // after the CTA barrier that follows init
+    __device__ static void ready(State &s) {
+        tc::tc_fence_after();
+        s.tmem_base = *s.tmem_slot;
+    }
+
+    // order-preserving float <-> unsigned (for atomicMax on scores)
+    __device__ static unsigned ord_encode(float f) {
+        const unsigned b = __float_as_uint(f);
+        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    __device__ static float ord_decode(unsigned u) {
+        return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+    }
+
+    // 16-byte chunk c (8 bf16 along K) of MMA row `row` of split part `part` of A
+    __device__ static unsigned char *a_chunk(const State &s, int row, int c, int part) {
+        const int slab = (c >> 3) + 4 * part, cc = c & 7;
+        return s.sA + slab * kSlabA + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4);
+    }
+
+    // write operand chunk c of request row `row` (both copies when DUAL)
+    __device__ static void put_a(const State &s, int row, int c, int part, const uint4 &v) {
+        *reinterpret_cast<uint4 *>(a_chunk(s, row, c, part)) = v;
+        if (DUAL) *reinterpret_cast<uint4 *>(a_chunk(s, row + 64, c, part)) = v;
+    }
+
+    // the U tile of tile t and one quad of it (64-column boxes, 128-byte swizzle)
+    __device__ static const unsigned char *u_tile(const State &s, int t) {
+        return s.smem + kOffU + (SU > 0 ? t % SU : 0) * kUBytes;
+    }
+    __device__ static uint2 u_quad(const unsigned char *sU, int row, int col) {
+        const int h = col >> 6, cc = col & 63;
+        return *reinterpret_cast<const uint2 *>(sU + h * kUBox + row * 128 +
+                                                ((((cc >> 3) ^ (row & 7))) << 4) + ((cc & 7) << 1));
+    }
+
+    // epilogue thread geometry: request row within the M-tile and first column
+    // (within the vocabulary tile) of this warp's accumulator block
+    __device__ static int epi_row() {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        return DUAL ? lane + 32 * (warp & 1) : lane + 32 * (warp & 3);
+    }
+    __device__ static int epi_col0() {
+        const int warp = threadIdx.x >> 5, q = warp & 3, j = warp >> 2;
+        return DUAL ? (q >= 2 ? BN / 2 : 0) + j * CW : j * CW;
+    }
+
+    // warp 16 (all lanes call): lane 0 streams W_2^T slabs, lane 1 the U tiles
+    __device__ static void producer(State &s, const CUtensorMap *tmB, const CUtensorMap *tmU, int t_begin,
+                                    int ntiles, int kslabs, int u_k, int m0, int32_t *err) {
+        const int lane = threadIdx.x & 31;
+        if (lane == 0) {
+            const int total = ntiles * kslabs;
+            int issued = 0;
+            for (int g = 0; g < total; ++g) {
+                const int slot = g % NS, t = g / kslabs, j = g - t * kslabs;
+                if (!tc::mbar_wait(&s.emptyB[slot], ((uint32_t)(g / NS) & 1u) ^ 1u, s.abort_flag, err)) break;
+                tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
+                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, (t_begin + t) * BN);
+                ++issued;
+            }
+            for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
+                tc::mbar_wait(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, s.abort_flag, err);
+        } else if (lane == 1 && SU > 0) {
+            constexpr int su = SU > 0 ? SU : 1;
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t % su;
+                if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(t / su) & 1u) ^ 1u, s.abort_flag, err)) break;
+                unsigned char *dst = s.smem + kOffU + st * kUBytes;
+                const int n0 = (t_begin + t) * BN;
+                tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
+                for (int h = 0; h < BN / 64; ++h)
+                    tc::tma_load_3d(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k, m0);
+                ++issued;
+            }
+            for (int t = issued - su < 0 ? 0 : issued - su; t < issued; ++t)
+                tc::mbar_wait(&s.fullU[t % su], (uint32_t)(t / su) & 1u, s.abort_flag, err);
+        }
+    }
+
+    // warp 17, lane 0
+    __device__ static void mma(State &s, int ntiles, int kslabs, int32_t *err) {
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
+        const uint32_t a_base = tc::smem_u32(s.sA);
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int b = t % NACC;
+            if (!tc::mbar_wait(&s.tempty[b], ((uint32_t)(t / NACC) & 1u) ^ 1u, s.abort_flag, err)) break;
+            tc::tc_fence_after();
+            const uint32_t d = s.tmem_base + (uint32_t)(b * BN);
+            for (int j = 0; j < kslabs; ++j) {
+                const int g = t * kslabs + j, slot = g % NS;
+                if (!tc::mbar_wait(&s.fullB[slot], (uint32_t)(g / NS) & 1u, s.abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t b_slab = tc::smem_u32(s.smem + kOffB + slot * kSlabB);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bd = tc::smem_desc_k128(b_slab + kk * 32);
+#pragma unroll
+                    for (int part = 0; part < KSPLIT; ++part)
+                        tc::umma_bf16(d, tc::smem_desc_k128(a_base + (j + 4 * part) * kSlabA + kk * 32), bd, idesc,
+                                      (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                }
+                tc::umma_commit(&s.emptyB[slot]);
+            }
+            if (!ok) break;
+            tc::umma_commit(&s.tfull[b]);
+            ++issued;
+        }
+        if (issued > 0) {  // the last MMAs must finish before TMEM is freed
+            const int t = issued - 1;
+            tc::mbar_wait(&s.tfull[t % NACC], (uint32_t)(t / NACC) & 1u, s.abort_flag, err);
+        }
+    }
+
+    // warps 0..15: per tile, load this warp's CW accumulator columns of its 32
+    // rows and call f(t, n0, acc, sU) (n0: first vocabulary entry of the tile;
+    // sU: the tile's U, or null).  Per-warp flow, no CTA barrier.
+    template <class F>
+    __device__ static void epilogue(State &s, int t_begin, int ntiles, int32_t *err, F &&f) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const uint32_t taddr0 = s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)epi_col0();
+        for (int t = 0; t < ntiles; ++t) {
+            const int b = t % NACC;
+            int ok = 1;
+            if (lane == 0) {
+                ok = tc::mbar_wait(&s.tfull[b], (uint32_t)(t / NACC) & 1u, s.abort_flag, err) ? 1 : 0;
+                if (ok && SU > 0)
+                    ok = tc::mbar_wait(&s.fullU[t % (SU > 0 ? SU : 1)], (uint32_t)(t / (SU > 0 ? SU : 1)) & 1u,
+                                       s.abort_flag, err) ? 1 : 0;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc::tc_fence_after();
+            uint32_t acc[CW];
+            tc::tmem_ld16(taddr0 + (uint32_t)(b * BN), *reinterpret_cast<uint32_t(*)[16]>(acc));
+            if constexpr (CW == 32)
+                tc::tmem_ld16(taddr0 + (uint32_t)(b * BN + 16), *reinterpret_cast<uint32_t(*)[16]>(acc + 16));
+            tc::tmem_wait_ld();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
+            f(t, (t_begin + t) * BN, acc, SU > 0 ? u_tile(s, t) : nullptr);
+            __syncwarp();
+            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[t % (SU > 0 ? SU : 1)]);
+        }
+    }
+
+    // raise row r's shared threshold to `score`
+    __device__ static void publish_thr(State &s, int r, float score) {
+        atomicMax(&s.thr[r], ord_encode(score));
+    }
+    __device__ static float read_thr(const State &s, int r) {
+        return ord_decode(*reinterpret_cast<volatile unsigned *>(&s.thr[r]));
+    }
+
+    // per-CTA merge scratch (valid once every epilogue warp has left its loop)
+    __device__ static float *merge_scratch(const State &s) {
+        return reinterpret_cast<float *>(s.smem + kOffB);
+    }
+
+    // all threads, at the very end
+    __device__ static void teardown(State &s) {
+        __syncthreads();
+        if ((threadIdx.x >> 5) == kMmaWarp) {
+            tc::tc_fence_after();
+            tc::tmem_dealloc(s.tmem_base, kTmemCols);
+        }
+    }
+};
+
+// vocabulary tile range of CTA cv out of nparts
+__device__ __forceinline__ void tile_range(int cv, int nparts, int n_vtiles, int &t_begin, int &ntiles) {
+    t_begin = (int)((long long)cv * n_vtiles / nparts);
+    ntiles = (int)((long long)(cv + 1) * n_vtiles / nparts) - t_begin;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// split 8 fp32 values into bf16 hi and lo parts (x = hi + lo + O(2^-16 |x|))
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]), h1 = __float2bfloat16_rn(x[2 * i + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(x[2 * i] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(x[2 * i + 1] - __bfloat162float(h1));
+        h[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        l[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+}  // namespace tcp
+}  // namespace dspark

@@ -5,7 +5,7 @@
 // scheduled token passed, the bonus token is drawn from p_{l_r}.  q_{n+1}
 // needs the draft logits of step n+1 again: U_{n+1} + (bias operand) W_2.
 // That contraction runs on tcgen05 exactly like the draft step (shared
-// pipeline in tc_pipeline.cuh); the epilogue streams the target row p_n and the
+// pipeline in tc_pipe.cuh); the epilogue streams the target row p_n and the
 // base-logit row U_{n+1} of each request from global memory and runs two Gumbel
 // races with the stream-2 noise: over the residual and over p (the bonus
 // sample, and the fallback for an empty residual).
@@ -15,7 +15,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
-#include "tc_pipeline.cuh"
+#include "tc_pipe.cuh"
 
 namespace dspark {
 
@@ -83,28 +83,17 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     }
     __syncthreads();  // row metadata, barriers and TMEM ready
     P::ready(s);
-    if (warp == tcp::kProducerWarp) {
-        if (lane == 0) tc::prefetch_tmap(&tmB);
-        __syncwarp();
-        P::producer(s, &tmB, nullptr, t_begin, ntiles, kslabs, 0, m0, p.err);
-        __syncwarp();
-        P::teardown(s);
-        return;
-    }
 
-    // bias operand of q_{n+1}: W_1[x_n] (x_0 = anchor) or the RNN vector A_{n+1},
-    // by every thread except the producer warp
+    // bias operand of q_{n+1}: W_1[x_n] (x_0 = anchor) or the RNN vector A_{n+1}
     const int chunks_per_row = p.r / 8;
-    constexpr int kGather = tcp::kThreads - 32;
-    const int gt = threadIdx.x < tcp::kEpiThreads ? threadIdx.x : threadIdx.x - 32;
-    for (int e = gt; e < P::MV * chunks_per_row; e += kGather) {
+    for (int e = threadIdx.x; e < P::MV * chunks_per_row; e += tcp::kThreads) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int rq = m0 + row;
         const bool live = s_mode[row] == 1;
         if (P::KSPLIT == 1) {
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
             if (live) val = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)s_xn[row] * p.r + c * 8);
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = val;
+            P::put_a(s, row, c, 0, val);
         } else {
             float xs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (live) {
@@ -116,19 +105,24 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             }
             uint4 hi, lo;
             tcp::split8(xs, hi, lo);
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 0)) = hi;
-            *reinterpret_cast<uint4 *>(P::a_chunk(s, row, c, 1)) = lo;
+            P::put_a(s, row, c, 0, hi);
+            P::put_a(s, row, c, 1, lo);
         }
     }
     tc::fence_proxy_async_smem();
-    tc::named_bar_sync(2, kGather);  // operand complete: the MMA warp may start
+    __syncthreads();  // operand complete
 
-    if (warp == tcp::kMmaWarp) {
+    if (warp == tcp::kProducerWarp) {
+        if (lane == 0) tc::prefetch_tmap(&tmB);
+        __syncwarp();
+        P::producer(s, &tmB, nullptr, t_begin, ntiles, kslabs, 0, m0, p.err);
+        __syncwarp();
+    } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, p.err);
         __syncwarp();
     } else {
         const int et = threadIdx.x;
-        const int row = et / P::TPR, gi = et % P::TPR;
+        const int row = P::epi_row(), col0 = P::epi_col0();
         const int rq = m0 + row;
         const int mode = s_mode[row], n = s_n[row];
         const float lsep = s_lsep[row] * kLog2e, lseq = s_lseq[row] * kLog2e;
@@ -139,26 +133,38 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         Race res, pr;
         race_init(res);
         race_init(pr);
-        P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0) {
+        P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *) {
             if (mode < 0) return;
+            const int vb = n0 + col0;
+            // this block of the target row (and of U_{n+1}), 8 columns per load; V % 8 == 0
+            // makes every 8-column chunk entirely in or out of range
+            uint4 tq[P::CW / 8], uq[P::CW / 8];
 #pragma unroll
-            for (int j = 0; j < P::GPT; ++j) {
-                const int col = 4 * (gi + P::TPR * j);
-                const int v0 = n0 + col;
-                if (v0 >= p.V) continue;  // V % 4 == 0: a quad is all in or all out
-                const uint2 tt = *reinterpret_cast<const uint2 *>(trow + v0);
-                const float tv[4] = {tcp::bf16_lo(tt.x), tcp::bf16_hi(tt.x), tcp::bf16_lo(tt.y),
-                                     tcp::bf16_hi(tt.y)};
+            for (int c = 0; c < P::CW / 8; ++c) {
+                const bool in = vb + 8 * c < p.V;
+                tq[c] = in ? *reinterpret_cast<const uint4 *>(trow + vb + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+                uq[c] = (in && mode == 1) ? *reinterpret_cast<const uint4 *>(urow + vb + 8 * c)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int g = 0; g < P::CW / 4; ++g) {
+                const int v0 = vb + 4 * g;
+                if (v0 >= p.V) break;
+                const uint4 &tt = tq[g >> 1];
+                const uint32_t t0 = (g & 1) ? tt.z : tt.x, t1 = (g & 1) ? tt.w : tt.y;
+                const float tv[4] = {tcp::bf16_lo(t0), tcp::bf16_hi(t0), tcp::bf16_lo(t1), tcp::bf16_hi(t1)};
                 const uint4 words =
                     philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), key);
                 float pv[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
                 if (mode == 1) {
-                    const float4 acc = *reinterpret_cast<const float4 *>(s.staging + row * P::kPitch + col);
-                    const uint2 uu = *reinterpret_cast<const uint2 *>(urow + v0);
-                    const float zv[4] = {acc.x + tcp::bf16_lo(uu.x), acc.y + tcp::bf16_hi(uu.x),
-                                         acc.z + tcp::bf16_lo(uu.y), acc.w + tcp::bf16_hi(uu.y)};
+                    const uint4 &uu = uq[g >> 1];
+                    const uint32_t u0 = (g & 1) ? uu.z : uu.x, u1 = (g & 1) ? uu.w : uu.y;
+                    const float zv[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(u0),
+                                         __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(u0),
+                                         __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(u1),
+                                         __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(u1)};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float t = one_minus_uniform(word_lane(words, i));
@@ -173,25 +179,32 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                 }
             }
         });
-#pragma unroll
-        for (int off = P::TPR / 2; off > 0; off >>= 1) {
-            const float b1 = __shfl_xor_sync(0xffffffffu, res.best, off);
-            const int i1 = __shfl_xor_sync(0xffffffffu, res.idx, off);
-            const float b2 = __shfl_xor_sync(0xffffffffu, pr.best, off);
-            const int i2 = __shfl_xor_sync(0xffffffffu, pr.idx, off);
-            race_merge(res.best, res.idx, b1, i1);
-            race_merge(pr.best, pr.idx, b2, i2);
+        // merge the TPR threads of each request (fixed warp order) into this CTA's partial
+        float *mg = P::merge_scratch(s);
+        int *mgi = reinterpret_cast<int *>(mg);
+        mg[et] = res.best;
+        mgi[tcp::kEpiThreads + et] = res.idx;
+        mg[2 * tcp::kEpiThreads + et] = pr.best;
+        mgi[3 * tcp::kEpiThreads + et] = pr.idx;
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        if (et < P::MV && m0 + et < p.R) {
+            float b1 = -INFINITY, b2 = -INFINITY;
+            int i1 = -1, i2 = -1;
+            for (int w = et >> 5; w < tcp::kEpiWarps; w += P::DUAL ? 2 : 4) {
+                const int src = w * 32 + (et & 31);
+                race_merge(b1, i1, mg[src], mgi[tcp::kEpiThreads + src]);
+                race_merge(b2, i2, mg[2 * tcp::kEpiThreads + src], mgi[3 * tcp::kEpiThreads + src]);
+            }
+            p.w.part[(size_t)(m0 + et) * p.nparts + cv] = VerifyPartial{b1, b2, i1, i2};
         }
-        if (gi == 0 && rq < p.R)
-            p.w.part[(size_t)rq * p.nparts + cv] = VerifyPartial{res.best, pr.best, res.idx, pr.idx};
     }
     P::teardown(s);
 }
 
-// Pipe<rows, vocabulary tile, W_2^T ring, U ring (none), operand split>
-using VerifyM64 = tcp::Pipe<64, 128, 2, 0, 1>;
-using VerifyM128 = tcp::Pipe<128, 64, 3, 0, 1>;
-using VerifyRnn = tcp::Pipe<64, 64, 4, 0, 2>;
+// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>
+using VerifyM64 = tcp::Pipe<64, 128, 9, 0, 1>;  // + static row metadata: within 227 KB
+using VerifyM128 = tcp::Pipe<128, 64, 10, 0, 1>;
+using VerifyRnn = tcp::Pipe<128, 64, 10, 0, 2>;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
