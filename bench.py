@@ -312,6 +312,8 @@ def run_dspark(args, world, rank, local):
     # cycle time without the harness's target-row gather
     t_cycle = [a + b + c for a, b, c in zip(t_draft, t_sched, t_verify)]
     t_steps = [e["k0"][k].elapsed_time(e["k1"][k]) for e in events for k in range(gm)]
+    t_first = [e["k0"][0].elapsed_time(e["k1"][0]) for e in events]
+    t_rest = [e["k0"][k].elapsed_time(e["k1"][k]) for e in events for k in range(1, gm)]
     total_ms = sum(t_cycle)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -337,6 +339,8 @@ def run_dspark(args, world, rank, local):
         "verified_tok_s": world * verified / ((sum(t_sched) + sum(t_verify)) / 1e3),
         "stage_us": {"draft": 1e3 * statistics.mean(t_draft),
                      "draft_step": step_us,
+                     "draft_step_first": 1e3 * statistics.mean(t_first),
+                     "draft_step_rest": 1e3 * statistics.mean(t_rest) if t_rest else None,
                      "schedule": 1e3 * statistics.mean(t_sched),
                      "verify": 1e3 * statistics.mean(t_verify)},
         "roofline": {"kernel": "draft step (fused contraction + epilogue, then row merge)",

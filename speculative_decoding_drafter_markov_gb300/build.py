@@ -19,6 +19,7 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdspark.so")
 SOURCES = ["abi.cu", "draft.cu", "draft_tc.cu", "sched.cu", "verify.cu", "verify_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+TU_FLAGS = {}
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
 
@@ -46,7 +47,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(OUT, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        extra = TU_FLAGS.get(src, [])
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)

@@ -184,6 +184,60 @@ __device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0,
     }
 }
 
+// Feed N consecutive vocabulary entries v0..v0+N-1 (all below V; N a multiple
+// of 4, words[j] the Philox word of entry v0 + j).  Written for instruction-level
+// parallelism: one max and one rescale per block, independent exponentials
+// summed in a fixed tree, independent filter tests; the rare candidates that pass
+// the filter are scored exactly in index order.
+template <int N>
+__device__ __forceinline__ void row_feed_block(RowState &s, const float (&z)[N], int v0,
+                                               const uint32_t (&words)[N]) {
+    float mx[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) mx[j] = z[j];
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+    if (mx[0] > s.m) {
+        s.S *= ex2((s.m - mx[0]) * kLog2e);
+        s.m = mx[0];
+        s.mL = mx[0] * kLog2e;
+        row_refresh_C(s);
+    }
+    float e[N], sum[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        e[j] = ex2(fmaf(z[j], kLog2e, -s.mL));
+        sum[j] = e[j];
+    }
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) sum[j] += sum[j + w];
+    s.S += sum[0];
+    unsigned pass = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float t = one_minus_uniform(words[j]);
+        if (!(t >= e[j] * s.C)) pass |= 1u << j;
+    }
+    if (pass) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            if (pass & (1u << j)) {
+                const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
+                if (score > s.best) {
+                    s.best = score;
+                    s.idx = v0 + j;
+                    s.zbest = z[j];
+                    row_raise_thr(s, score);
+                }
+            }
+        }
+    }
+}
+
 // Combine two states (b into a).  Ties of the race go to the lower index.
 __device__ __forceinline__ void row_merge(RowState &a, float m, float S, float best, float zbest,
                                           int idx) {

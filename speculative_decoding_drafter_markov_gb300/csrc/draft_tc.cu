@@ -200,22 +200,42 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             // the row's best score so far, wherever in the CTA it was found, filters this thread
             row_raise_thr(st, P::read_thr(s, row));
             const float best0 = st.best;
-            const bool full_tile = n0 + P::BN <= p.V;
+            const int vb = n0 + col0;
+            if (vb + P::CW <= p.V) {
+                // whole block in range: per 16 columns, the Philox words first (independent
+                // chains), then the block
 #pragma unroll
-            for (int g = 0; g < P::CW / 4; ++g) {
-                const int col = col0 + 4 * g;
-                const uint2 uu = P::u_quad(sU, row, col);
-                float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
-                              __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
-                              __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
-                              __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
-                const int v0 = n0 + col;
-                const uint4 words =
-                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)grow, c3), key);
-                if (full_tile)
-                    row_feed4<true>(st, z, v0, p.V, words);
-                else
+                for (int h = 0; h < P::CW / 16; ++h) {
+                    uint32_t words[16];
+                    float z[16];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int gg = 4 * h + g;
+                        const uint4 w4 = philox4x32_10(
+                            make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)p.k, (uint32_t)grow, c3), key);
+                        words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
+                        const uint2 uu = P::u_quad(sU, row, col0 + 4 * gg);
+                        z[4 * g] = __uint_as_float(acc[4 * gg]) + tcp::bf16_lo(uu.x);
+                        z[4 * g + 1] = __uint_as_float(acc[4 * gg + 1]) + tcp::bf16_hi(uu.x);
+                        z[4 * g + 2] = __uint_as_float(acc[4 * gg + 2]) + tcp::bf16_lo(uu.y);
+                        z[4 * g + 3] = __uint_as_float(acc[4 * gg + 3]) + tcp::bf16_hi(uu.y);
+                    }
+                    row_feed_block<16>(st, z, vb + 16 * h, words);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < P::CW / 4; ++g) {
+                    const int col = col0 + 4 * g;
+                    const uint2 uu = P::u_quad(sU, row, col);
+                    float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
+                                  __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
+                                  __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
+                                  __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
+                    const int v0 = n0 + col;
+                    const uint4 words =
+                        philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)grow, c3), key);
                     row_feed4<false>(st, z, v0, p.V, words);
+                }
             }
             if (st.best > best0) P::publish_thr(s, row, st.best);
         });
@@ -312,7 +332,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
 using DraftM64 = tcp::Pipe<64, 128, 8, 2, 1>;   // Markov, R <= 64
-using DraftM128 = tcp::Pipe<128, 128, 6, 2, 1>; // Markov, 128 requests per M-tile
+using DraftM128 = tcp::Pipe<128, 64, 12, 3, 1>; // Markov, 128 requests per M-tile
 using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -191,6 +191,8 @@ struct Pipe {
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
                 tc::mbar_wait(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, s.abort_flag, err);
         } else if (lane == 1 && SU > 0) {
+            // U is read once: keep it from displacing W_2^T, which the next steps reuse
+            const uint64_t pol = tc::policy_evict_first();
             constexpr int su = SU > 0 ? SU : 1;
             int issued = 0;
             for (int t = 0; t < ntiles; ++t) {
@@ -200,7 +202,7 @@ struct Pipe {
                 const int n0 = (t_begin + t) * BN;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
                 for (int h = 0; h < BN / 64; ++h)
-                    tc::tma_load_3d(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k, m0);
+                    tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k, m0, pol);
                 ++issued;
             }
             for (int t = issued - su < 0 ? 0 : issued - su; t < issued; ++t)

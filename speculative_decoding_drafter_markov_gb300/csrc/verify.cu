@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace dspark {
 
@@ -73,8 +74,9 @@ __global__ void __launch_bounds__(256) verify_phase1(const dspark_verify_args a,
     if (a.V % kVec == 0) {
         const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
         const int nv = a.V / kVec;
+        const uint64_t pol = tc::policy_evict_first();  // each target row is read once here
         for (int c = tid; c < nv; c += blockDim.x) {
-            const uint4 raw = row4[c];
+            const uint4 raw = tc::ld_global_hint(row4 + c, pol);
             const T *vals = reinterpret_cast<const T *>(&raw);
             float x[kVec];
 #pragma unroll

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         Race res, pr;
         race_init(res);
         race_init(pr);
+        const uint64_t pol = tc::policy_evict_first();  // target and base rows are read once
         P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *) {
             if (mode < 0) return;
             const int vb = n0 + col0;
@@ -142,9 +143,8 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < P::CW / 8; ++c) {
                 const bool in = vb + 8 * c < p.V;
-                tq[c] = in ? *reinterpret_cast<const uint4 *>(trow + vb + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-                uq[c] = (in && mode == 1) ? *reinterpret_cast<const uint4 *>(urow + vb + 8 * c)
-                                          : make_uint4(0u, 0u, 0u, 0u);
+                tq[c] = in ? tc::ld_global_hint(trow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                uq[c] = (in && mode == 1) ? tc::ld_global_hint(urow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int g = 0; g < P::CW / 4; ++g) {
