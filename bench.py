@@ -175,8 +175,16 @@ class Cycle:
                     "logq": torch.empty((R, gm), dtype=torch.float32, device=device),
                     "lse": torch.empty((R, gm), dtype=torch.float32, device=device),
                     "c": torch.empty((R, gm), dtype=torch.float32, device=device)}
-        ws_bytes = dsp.draft_markov_workspace_size(inp["U"], inp["h"], inp["W1"], inp["W2t"],
-                                                   inp["w"], inp["anchor"])
+        self.rnn = wl.head == "rnn"
+        if self.rnn:
+            r = wl.r
+            self.out["A"] = torch.empty((R, gm, r), dtype=torch.float32, device=device)
+            self.out["s_out"] = torch.empty((R, r), dtype=torch.float32, device=device)
+            ws_bytes = dsp.draft_rnn_workspace_size(inp["U"], inp["h"], inp["W1"], inp["W2t"],
+                                                    inp["W"], inp["w"], inp["anchor"])
+        else:
+            ws_bytes = dsp.draft_markov_workspace_size(inp["U"], inp["h"], inp["W1"], inp["W2t"],
+                                                       inp["w"], inp["anchor"])
         self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
         # verification batch: every drafted token (no scheduler), or the capacity
         # R (gamma + 1) with the scheduler's device-side row count
@@ -205,14 +213,22 @@ class Cycle:
             self.T_sched = torch.empty_like(self.T)
         nbytes = dsp.verify_workspace_size(self.T, self.tags, inp["anchor"], self.out["x"],
                                            self.out["logq"], self.out["lse"], inp["U"], inp["W1"],
-                                           inp["W2t"])
+                                           inp["W2t"], A=self.out.get("A"))
         self.vws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
-        self.launches_per_cycle = 2 * gm + 4 + (2 if self.sched else 0)
+        # library kernels per cycle: the gamma Markov draft steps (one launch) or,
+        # RNN head, the h projection then per step the state update and the step;
+        # schedule + build_tags; verify (init, phase 1, phase 2, final)
+        n_draft = 1 + 2 * gm if self.rnn else 1
+        self.launches_per_cycle = n_draft + 4 + (2 if self.sched else 0)
 
-    def draft_step(self, k, cycle):
+    def draft(self, cycle):
         i = self.inp
-        dsp.draft_markov_step(k, i["U"], i["h"], i["W1"], i["W2t"], i["w"], i["anchor"],
-                              out=self.out, ws=self.ws, seed=1234, cycle=cycle)
+        if self.rnn:
+            dsp.draft_rnn(i["U"], i["h"], i["W1"], i["W2t"], i["W"], i["w"], i["anchor"],
+                          out=self.out, ws=self.ws, seed=1234, cycle=cycle)
+        else:
+            dsp.draft_markov(i["U"], i["h"], i["W1"], i["W2t"], i["w"], i["anchor"],
+                             out=self.out, ws=self.ws, seed=1234, cycle=cycle)
 
     def schedule(self, cycle):
         if not self.sched:
@@ -235,8 +251,8 @@ class Cycle:
         N_dev = self.N_dev if self.sched else None
         T = self.T_sched if self.sched else self.T
         dsp.verify(T, tags, i["anchor"], self.out["x"], self.out["logq"], self.out["lse"],
-                   i["U"], i["W1"], i["W2t"], N_dev=N_dev, seed=1234, cycle=cycle,
-                   out=self.vout, ws=self.vws)
+                   i["U"], i["W1"], i["W2t"], A=self.out.get("A"), N_dev=N_dev, seed=1234,
+                   cycle=cycle, out=self.vout, ws=self.vws)
 
     def verified_tokens(self):
         if self.sched:
@@ -244,11 +260,18 @@ class Cycle:
         return self.wl.R * self.wl.gamma
 
 
-def draft_step_bytes(wl):
+def draft_step_bytes(wl, with_w2=True):
     """Algorithmic bytes of one draft step: U_k rows, W_2 streamed once, the
     gathered W_1 rows, h_k and w (fp32)."""
     es = 4 if wl.dtype == "f32" else 2
-    return (wl.R * wl.V + wl.V * wl.r + wl.R * wl.r + wl.R * wl.d) * es + (wl.d + wl.r) * 4
+    w2 = wl.V * wl.r if with_w2 else 0
+    return (wl.R * wl.V + w2 + wl.R * wl.r + wl.R * wl.d) * es + (wl.d + wl.r) * 4
+
+
+def draft_cycle_bytes_strict(wl):
+    """The stricter per-cycle count: W_2 read from memory once for all gamma steps."""
+    es = 4 if wl.dtype == "f32" else 2
+    return wl.gamma * draft_step_bytes(wl, with_w2=False) + wl.V * wl.r * es
 
 
 def run_dspark(args, world, rank, local):
@@ -261,12 +284,7 @@ def run_dspark(args, world, rank, local):
     gm = wl.gamma
 
     def one_cycle(c, ev=None):
-        for k in range(1, gm + 1):
-            if ev is not None:
-                ev["k0"][k - 1].record(stream)
-            cyc.draft_step(k, c)
-            if ev is not None:
-                ev["k1"][k - 1].record(stream)
+        cyc.draft(c)
         if ev is not None:
             ev["d"].record(stream)
         cyc.schedule(c)
@@ -283,8 +301,7 @@ def run_dspark(args, world, rank, local):
     torch.cuda.synchronize()
 
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    events = [{"a": mk(), "b": mk(), "d": mk(), "s": mk(), "g": mk(), "k0": [mk() for _ in range(gm)],
-               "k1": [mk() for _ in range(gm)]} for _ in range(args.steps)]
+    events = [{"a": mk(), "b": mk(), "d": mk(), "s": mk(), "g": mk()} for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
@@ -311,9 +328,6 @@ def run_dspark(args, world, rank, local):
     t_verify = [e["g"].elapsed_time(e["b"]) for e in events]
     # cycle time without the harness's target-row gather
     t_cycle = [a + b + c for a, b, c in zip(t_draft, t_sched, t_verify)]
-    t_steps = [e["k0"][k].elapsed_time(e["k1"][k]) for e in events for k in range(gm)]
-    t_first = [e["k0"][0].elapsed_time(e["k1"][0]) for e in events]
-    t_rest = [e["k0"][k].elapsed_time(e["k1"][k]) for e in events for k in range(1, gm)]
     total_ms = sum(t_cycle)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -323,9 +337,12 @@ def run_dspark(args, world, rank, local):
     value = world * drafted / (total_ms / 1e3)
 
     hbm, tc, peak_kind = _peaks()
-    step_us = 1e3 * statistics.mean(t_steps)
-    bytes_step = draft_step_bytes(wl)
-    achieved = bytes_step / (step_us * 1e-6) / 1e9
+    draft_us = 1e3 * statistics.mean(t_draft)
+    bytes_launch = gm * draft_step_bytes(wl)  # W_2 counted once per step
+    if cyc.rnn:  # + the recurrent projection W [3r, 2r + d], read once per cycle
+        bytes_launch += 3 * wl.r * (2 * wl.r + wl.d) * 2
+    achieved = bytes_launch / (draft_us * 1e-6) / 1e9
+    strict = draft_cycle_bytes_strict(wl) / (draft_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -337,16 +354,23 @@ def run_dspark(args, world, rank, local):
                    "parallelism": f"replicas x{world} (requests independent)"},
         "drafted_tok_s": world * drafted / (sum(t_draft) / 1e3),
         "verified_tok_s": world * verified / ((sum(t_sched) + sum(t_verify)) / 1e3),
-        "stage_us": {"draft": 1e3 * statistics.mean(t_draft),
-                     "draft_step": step_us,
-                     "draft_step_first": 1e3 * statistics.mean(t_first),
-                     "draft_step_rest": 1e3 * statistics.mean(t_rest) if t_rest else None,
+        "stage_us": {"draft": draft_us,
+                     "draft_step": draft_us / gm,
                      "schedule": 1e3 * statistics.mean(t_sched),
                      "verify": 1e3 * statistics.mean(t_verify)},
-        "roofline": {"kernel": "draft step (fused contraction + epilogue, then row merge)",
+        "roofline": {"kernel": (f"draft: h projection + {gm} x (state update, draft_step_tc)"
+                                if cyc.rnn else
+                                f"draft_step_tc: the {gm} draft steps of a cycle in one launch "
+                                "(fused contraction + epilogue + row merge per step)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "algorithmic_bytes_per_launch": bytes_step, "traffic": None},
+                     "algorithmic_bytes_per_launch": bytes_launch,
+                     "bytes_rule": "per step: U_k + W_2 + W_1 rows + h_k + w; x gamma steps",
+                     "timing": "CUDA events around the whole draft call",
+                     "traffic": None},
+        "roofline_w2_once_per_cycle": {"achieved": strict, "peak": hbm, "unit": "GB/s",
+                                       "frac": strict / hbm,
+                                       "algorithmic_bytes_per_launch": draft_cycle_bytes_strict(wl)},
         "gpu_launches": args.steps * cyc.launches_per_cycle,
         "clocks": clk,
     }
@@ -380,8 +404,7 @@ def run_e2e(cyc, args, stream, flush):
         for k, t in host_in.items():
             i[k].copy_(t, non_blocking=True)
         cyc.T.copy_(host_T, non_blocking=True)
-        for k in range(1, wl.gamma + 1):
-            cyc.draft_step(k, 10_000 + s)
+        cyc.draft(10_000 + s)
         cyc.schedule(10_000 + s)
         cyc.target()
         cyc.verify(10_000 + s)

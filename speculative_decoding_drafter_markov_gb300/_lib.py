@@ -187,7 +187,8 @@ def draft_markov_step(k, U, h, W1, W2t, w, anchor, *, out, ws, seed=0, cycle=0, 
 def draft_markov_noalloc(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, out=None,
                          err=None, stream=None):
     """Markov draft through the entry point that allocates nothing: its scratch
-    is a fixed array inside the library (R * ceil(V/64) * 20 bytes <= 16 MiB)."""
+    is a fixed array inside the library (the draft workspace size -- 32 bytes per
+    (request, vocabulary range) plus 256 -- must be <= 16 MiB)."""
     L = load()
     R, gamma, _ = U.shape
     out = _draft_outputs(R, gamma, U.device, out)
@@ -221,6 +222,19 @@ def draft_rnn(U, h, W1, W2t, W, w, anchor, *, s0=None, seed=0, cycle=0, sts_T=No
     ws = _workspace(L.dspark_draft_rnn_workspace_size(ctypes.byref(a)), U.device, ws)
     _check(L.dspark_draft_rnn(ctypes.byref(a), _ptr(ws), _stream(stream)))
     return out
+
+
+def draft_rnn_workspace_size(U, h, W1, W2t, W, w, anchor):
+    """Scratch bytes dspark_draft_rnn needs for this shape."""
+    L = load()
+    R, gamma, _ = U.shape
+    r = W1.shape[1]
+    out = _draft_outputs(R, gamma, U.device, None)
+    a = RnnArgs()
+    a.base = _draft_struct(U, h, W1, W2t, w, anchor, 0, 0, None, out, None)
+    a.W, a.s0 = _ptr(W), None
+    a.A = a.s_out = None
+    return L.dspark_draft_rnn_workspace_size(ctypes.byref(a))
 
 
 # --------------------------------------------------------------------- schedule

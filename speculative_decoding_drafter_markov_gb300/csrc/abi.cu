@@ -71,7 +71,10 @@ dspark::DraftStep step_template(const dspark_draft_args *a, const float *A_rnn) 
 }
 
 bool use_tc_path(const dspark::DraftStep &st) {
-    return dspark::draft_step_tc_supported(st) && (size_t)((st.R + 63) / 64) * sizeof(int) <= kCounterBytes;
+    if (!dspark::draft_step_tc_supported(st)) return false;
+    int np = 0, mt = 0;
+    dspark::draft_step_tc_shape(st.R, st.V, st.A_op != nullptr, &np, &mt);
+    return (size_t)2 * mt * sizeof(int) <= kCounterBytes;  // two counters per M-tile
 }
 
 int step_nparts(const dspark::DraftStep &st, bool tc) {
@@ -106,6 +109,16 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         cudaError_t e = cudaMemsetAsync(st.counters, 0, kCounterBytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft counters");
     }
+    if (use_tc && !rnn) {
+        // Markov head on the tensor cores: all the steps in one launch
+        st.k = k_first;
+        st.step_index = k_first;
+        st.nsteps = k_last - k_first + 1;
+        st.x_prev = k_first == 1 ? a->anchor : a->x + (k_first - 2);
+        st.x_stride = k_first == 1 ? 1 : a->gamma;
+        cudaError_t e = launch_draft_step_tc(st, s);
+        return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft steps (tensor cores)");
+    }
     for (int k = k_first; k <= k_last; ++k) {
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
         const int xs = k == 1 ? 1 : a->gamma;
@@ -120,6 +133,7 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         }
         st.k = k;
         st.step_index = k;
+        st.nsteps = 1;
         st.x_prev = xp;
         st.x_stride = xs;
         cudaError_t e = use_tc ? launch_draft_step_tc(st, s) : launch_draft_step(st, s);

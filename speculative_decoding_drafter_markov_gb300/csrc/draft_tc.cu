@@ -26,9 +26,12 @@ namespace dspark {
 namespace {
 
 struct TcParams {
-    int R, V, r, d, gamma, k;
+    int R, V, r, d, gamma;
+    int k;       // first step of the launch (1..gamma)
+    int nsteps;  // steps k .. k + nsteps - 1 (Markov head; 1 for the RNN head)
+    int step_index;  // counter index of step k (1 for the first step since the counters were zeroed)
     const __nv_bfloat16 *W1;
-    const int32_t *x_prev;
+    const int32_t *x_prev;  // token x_{k-1} of row i at x_prev[i * x_stride]
     int x_stride;
     const float *A_op;  // RNN: operand of row i at A_op[i * a_stride], else null
     int a_stride;
@@ -37,8 +40,7 @@ struct TcParams {
     const float *sts_T;      // [gamma] or null
     uint64_t seed, cycle;
     DraftPartial *part;
-    int *counters;           // [n_mtiles] completion counters, zeroed by the caller per call
-    int target;              // counter value once every CTA of this step has published
+    int *counters;  // [2 * n_mtiles]: partials published, rows finalised (per M-tile)
     int32_t *x;
     float *logq, *lse, *c;   // [R, gamma]
     int nparts;  // vocabulary ranges (CTAs per M-tile)
@@ -51,12 +53,13 @@ struct TcParams {
 // epilogue threads (16-byte chunks of h_k then of W_1[x_{k-1}]), reduced in a
 // fixed order through `red` (16 floats of shared memory).  `pre` is thread et's
 // chunk et of h_k when `have_pre` (loaded early); E comes from shared memory
-// when the operand there is W_1[x_{k-1}] itself (`e_smem`, else null).
+// when the operand there is W_1[x_{k-1}] itself (`e_smem`), else from the
+// launch's x_prev (RNN head, one step per launch).
 template <class P>
-__device__ __forceinline__ void confidence_row(const TcParams &p, const typename P::State &s, int local_row,
-                                               int grow, int et, float *red, bool have_pre, uint4 pre,
-                                               bool e_smem) {
-    const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (p.k - 1)) * (size_t)p.d;
+__device__ __forceinline__ void confidence_row(const TcParams &p, const typename P::State &s, int k,
+                                               int local_row, int grow, int et, float *red, bool have_pre,
+                                               uint4 pre, bool e_smem) {
+    const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
     float dot = 0.f;
     if ((p.d & 7) == 0) {
         int xp = 0;
@@ -82,8 +85,13 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, const typename
             }
         }
     } else {
-        int xp = p.x_prev[(size_t)grow * p.x_stride];
-        if (xp < 0 || xp >= p.V) xp = 0;
+        int xp = 0;
+        if (e_smem) {
+            xp = s.tok[local_row];
+        } else {
+            xp = p.x_prev[(size_t)grow * p.x_stride];
+            if (xp < 0 || xp >= p.V) xp = 0;
+        }
         const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
         for (int j = et; j < p.d + p.r; j += tcp::kEpiThreads)
             dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
@@ -95,8 +103,8 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, const typename
     if (et == 0) {
         float sum = 0.f;
         for (int i = 0; i < tcp::kEpiThreads / 32; ++i) sum += red[i];
-        const float T_k = p.sts_T ? p.sts_T[p.k - 1] : 1.0f;
-        p.c[(size_t)grow * p.gamma + (p.k - 1)] = 1.0f / (1.0f + expf(-sum / T_k));
+        const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
+        p.c[(size_t)grow * p.gamma + (k - 1)] = 1.0f / (1.0f + expf(-sum / T_k));
     }
     tc::named_bar_sync(1, tcp::kEpiThreads);
 }
@@ -107,49 +115,43 @@ __device__ __forceinline__ int ld_acquire(const int *ptr) {
     return v;
 }
 
-template <class P>
-__global__ void __launch_bounds__(tcp::kThreads, 1)
-    draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
-                  const TcParams p) {
-    extern __shared__ unsigned char smem_raw[];
-    typename P::State s = P::carve(smem_raw);
-    P::init(s);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
-    const int m0 = m_tile * P::MV;
-    int t_begin, ntiles;
-    tcp::tile_range(cv, p.nparts, p.n_vtiles, t_begin, ntiles);
-    const int kslabs = p.r / 64;
-    const int chunks_per_row = p.r / 8;
-    int *s_tok = reinterpret_cast<int *>(P::merge_scratch(s));  // the rings are idle until the producer starts
-
-    // 1. the M-tile's tokens x_{k-1} (one load per row, all in flight together)
-    //    and this CTA's first chunk of h_k for the confidence
-    if (P::KSPLIT == 1 && threadIdx.x < P::MV) {
-        const int grow = m0 + threadIdx.x;
-        int xp = grow < p.R ? p.x_prev[(size_t)grow * p.x_stride] : -1;
-        if (grow < p.R && (xp < 0 || xp >= p.V)) {
-            set_err(p.err, DSPARK_ERR_RANGE);
-            xp = 0;
+// bounded wait until *ctr >= target (a counter other CTAs of the launch raise)
+__device__ __forceinline__ bool wait_counter(const int *ctr, int target, int32_t *err) {
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (ld_acquire(ctr) < target) {
+        if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+            set_err(err, DSPARK_ERR_TIMEOUT);
+            return false;
         }
-        s_tok[threadIdx.x] = xp;
+        __nanosleep(128);
     }
-    const bool conf_row = cv < P::MV && m0 + cv < p.R;
-    const bool have_pre = conf_row && threadIdx.x < tcp::kEpiThreads && (p.d & 7) == 0 && threadIdx.x < p.d / 8;
-    uint4 pre = make_uint4(0u, 0u, 0u, 0u);
-    if (have_pre)
-        pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (p.k - 1)) * (size_t)p.d +
-                                               threadIdx.x * 8);
-    __syncthreads();  // tokens, barriers, thresholds, TMEM
-    P::ready(s);
+    return true;
+}
 
-    // 2. bias operand in the swizzled K-major layout, before the W_2 / U streams
-    //    compete for memory bandwidth
-    for (int e = threadIdx.x; e < P::MV * chunks_per_row; e += tcp::kThreads) {
+// token x_{k-1} of request grow (held in s.tok), checked against the vocabulary
+__device__ __forceinline__ int load_token(const TcParams &p, int grow, const int32_t *xp, int stride,
+                                          bool from_l2) {
+    if (grow >= p.R) return -1;
+    const int32_t *ptr = xp + (size_t)grow * stride;
+    int x = from_l2 ? __ldcg(ptr) : *ptr;
+    if (x < 0 || x >= p.V) {
+        set_err(p.err, DSPARK_ERR_RANGE);
+        x = 0;
+    }
+    return x;
+}
+
+// the bias operand of the M-tile in the swizzled K-major layout: W_1[x_{k-1}]
+// (tokens in s.tok) or the split fp32 RNN operand; threads tid, tid + nthr, ...
+template <class P>
+__device__ __forceinline__ void gather_operand(const TcParams &p, const typename P::State &s, int m0, int tid,
+                                               int nthr) {
+    const int chunks_per_row = p.r / 8;
+    for (int e = tid; e < P::MV * chunks_per_row; e += nthr) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int grow = m0 + row;
         if (P::KSPLIT == 1) {
-            const int xp = s_tok[row];
+            const int xp = s.tok[row];
             const uint4 val = xp >= 0 ? *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xp * p.r + c * 8)
                                       : make_uint4(0u, 0u, 0u, 0u);
             P::put_a(s, row, c, 0, val);
@@ -167,6 +169,47 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             P::put_a(s, row, c, 1, lo);
         }
     }
+}
+
+// One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
+// (m_tile, cv) owns requests m0 .. m0 + MV - 1 and vocabulary range cv of
+// nparts.  Per step: contraction + eq. (4) epilogue over the range, a merge
+// into one partial per request, then -- once every CTA of the M-tile has
+// published (bounded wait; the launch is cooperative, so all are resident) --
+// each CTA finalises rows cv, cv + nparts, ... (x_k, lse_k, log q_k).  The next
+// step's operand needs x_k of all the M-tile's rows, hence a second bounded
+// wait on the finalised-rows counter; meanwhile the producer already streams
+// the next step's W_2^T slabs and U tiles.
+template <class P>
+__global__ void __launch_bounds__(tcp::kThreads, 1)
+    draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
+                  const TcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    typename P::State s = P::carve(smem_raw);
+    P::init(s);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
+    const int m0 = m_tile * P::MV;
+    int t_begin, ntiles;
+    tcp::tile_range(cv, p.nparts, p.n_vtiles, t_begin, ntiles);
+    const int kslabs = p.r / 64;
+    int *ctr_part = p.counters + m_tile, *ctr_fin = p.counters + p.n_mtiles + m_tile;
+
+    // 1. the M-tile's tokens x_{k-1} (one load per row, all in flight together)
+    //    and this CTA's first chunk of h_k for the confidence
+    if (P::KSPLIT == 1 && threadIdx.x < P::MV) s.tok[threadIdx.x] = load_token(p, m0 + threadIdx.x, p.x_prev, p.x_stride, false);
+    const bool conf_row = cv < P::MV && m0 + cv < p.R;
+    const bool pre_ok = conf_row && (p.d & 7) == 0;
+    bool have_pre = pre_ok && threadIdx.x < tcp::kEpiThreads && threadIdx.x < p.d / 8;
+    uint4 pre = make_uint4(0u, 0u, 0u, 0u);
+    if (have_pre)
+        pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (p.k - 1)) * (size_t)p.d +
+                                               threadIdx.x * 8);
+    __syncthreads();  // tokens, barriers, thresholds, TMEM
+    P::ready(s);
+
+    // 2. first bias operand, before the W_2 / U streams compete for bandwidth
+    gather_operand<P>(p, s, m0, threadIdx.x, tcp::kThreads);
     tc::fence_proxy_async_smem();
     __syncthreads();  // operand complete
 
@@ -176,123 +219,136 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             tc::prefetch_tmap(&tmU);
         }
         __syncwarp();
-        P::producer(s, &tmB, &tmU, t_begin, ntiles, kslabs, p.k - 1, m0, p.err);
+        P::producer(s, &tmB, &tmU, t_begin, ntiles, kslabs, p.nsteps, p.k - 1, m0, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
-        if (lane == 0) P::mma(s, ntiles, kslabs, p.err);
+        if (lane == 0) P::mma(s, ntiles, kslabs, p.nsteps, p.err);
         __syncwarp();
     } else {
         const int et = threadIdx.x;
         const int row = P::epi_row(), col0 = P::epi_col0();
         const int grow = m0 + row;
         const bool row_live = grow < p.R;
-        // confidences of this CTA's rows (local rows cv, cv + nparts, ...) while
-        // the first tile is in flight
-        for (int i = cv, j = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++j)
-            confidence_row<P>(p, s, i, m0 + i, et, s.red, j == 0 && have_pre, pre, P::KSPLIT == 1);
-
         const PhiloxKey key = philox_key(p.seed);
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
-        RowState st;
-        row_init(st);
-        P::epilogue(s, t_begin, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *sU) {
-            if (!row_live) return;
-            // the row's best score so far, wherever in the CTA it was found, filters this thread
-            row_raise_thr(st, P::read_thr(s, row));
-            const float best0 = st.best;
-            const int vb = n0 + col0;
-            if (vb + P::CW <= p.V) {
-                // whole block in range: per 16 columns, the Philox words first (independent
-                // chains), then the block
-#pragma unroll
-                for (int h = 0; h < P::CW / 16; ++h) {
-                    uint32_t words[16];
-                    float z[16];
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int gg = 4 * h + g;
-                        const uint4 w4 = philox4x32_10(
-                            make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)p.k, (uint32_t)grow, c3), key);
-                        words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
-                        const uint2 uu = P::u_quad(sU, row, col0 + 4 * gg);
-                        z[4 * g] = __uint_as_float(acc[4 * gg]) + tcp::bf16_lo(uu.x);
-                        z[4 * g + 1] = __uint_as_float(acc[4 * gg + 1]) + tcp::bf16_hi(uu.x);
-                        z[4 * g + 2] = __uint_as_float(acc[4 * gg + 2]) + tcp::bf16_lo(uu.y);
-                        z[4 * g + 3] = __uint_as_float(acc[4 * gg + 3]) + tcp::bf16_hi(uu.y);
-                    }
-                    row_feed_block<16>(st, z, vb + 16 * h, words);
-                }
-            } else {
-#pragma unroll
-                for (int g = 0; g < P::CW / 4; ++g) {
-                    const int col = col0 + 4 * g;
-                    const uint2 uu = P::u_quad(sU, row, col);
-                    float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
-                                  __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
-                                  __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
-                                  __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
-                    const int v0 = n0 + col;
-                    const uint4 words =
-                        philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)grow, c3), key);
-                    row_feed4<false>(st, z, v0, p.V, words);
-                }
-            }
-            if (st.best > best0) P::publish_thr(s, row, st.best);
-        });
-
-        // merge the TPR threads of each request (fixed warp order) into this CTA's partial
         float *mg = P::merge_scratch(s);
-        mg[et] = st.m;
-        mg[tcp::kEpiThreads + et] = st.S;
-        mg[2 * tcp::kEpiThreads + et] = st.best;
-        mg[3 * tcp::kEpiThreads + et] = st.zbest;
-        reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + et] = st.idx;
-        tc::named_bar_sync(1, tcp::kEpiThreads);
-        if (et < P::MV && m0 + et < p.R) {
-            RowState f;
-            row_init(f);
-            const int q0 = P::DUAL ? (et >> 5) : (et >> 5);  // first warp holding this request
-            const int wstep = P::DUAL ? 2 : 4;
-            for (int w = q0; w < tcp::kEpiWarps; w += wstep) {
-                const int src = w * 32 + (et & 31);
-                row_merge(f, mg[src], mg[tcp::kEpiThreads + src], mg[2 * tcp::kEpiThreads + src],
-                          mg[3 * tcp::kEpiThreads + src], reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + src]);
-            }
-            p.part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
-        }
-
-        // publish, then wait (bounded) until every CTA of the M-tile has published;
-        // the launch is cooperative, so all of them are resident
-        __threadfence();
-        tc::named_bar_sync(1, tcp::kEpiThreads);
-        if (et == 0) {
-            atomicAdd(&p.counters[m_tile], 1);
-            int ok = 1;
-            const uint64_t t0 = tc::globaltimer_ns();
-            while (ld_acquire(&p.counters[m_tile]) < p.target) {
-                if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
-                    set_err(p.err, DSPARK_ERR_TIMEOUT);
-                    ok = 0;
+        for (int step = 0; step < p.nsteps; ++step) {
+            const int k = p.k + step, q = p.step_index + step;
+            if (step > 0) {
+                // x_{k-1} of every row of the M-tile is final once all its CTAs finalised step k-1
+                if (pre_ok && et < p.d / 8)
+                    pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (k - 1)) * (size_t)p.d +
+                                                           et * 8);
+                have_pre = pre_ok && et < p.d / 8;
+                if (et == 0) *s.flag = !*s.abort_flag && wait_counter(ctr_fin, (q - 1) * p.nparts, p.err) ? 1 : 0;
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                if (!*s.flag) {
+                    *s.abort_flag = 1;
                     break;
                 }
-                __nanosleep(256);
+                if (et < P::MV) s.tok[et] = load_token(p, m0 + et, p.x + (k - 2), p.gamma, true);
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                gather_operand<P>(p, s, m0, et, tcp::kEpiThreads);
+                P::operand_written(s, et);
             }
-            *s.flag = ok;
-        }
-        tc::named_bar_sync(1, tcp::kEpiThreads);
-        // every CTA finalises its share of the rows: one partial per thread,
-        // merged in a fixed tree (lanes, then warps in order)
-        if (*s.flag) {
+            // confidences of this CTA's rows (local rows cv, cv + nparts, ...) while
+            // the first tile is in flight
+            for (int i = cv, j = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++j)
+                confidence_row<P>(p, s, k, i, m0 + i, et, s.red, j == 0 && have_pre, pre, P::KSPLIT == 1);
+
+            RowState st;
+            row_init(st);
+            P::epilogue(s, step * ntiles, t_begin, ntiles, p.err,
+                        [&](int, int n0, const uint32_t *acc, const unsigned char *sU) {
+                if (!row_live) return;
+                // the row's best score so far, wherever in the CTA it was found, filters this thread
+                row_raise_thr(st, P::read_thr(s, row));
+                const float best0 = st.best;
+                const int vb = n0 + col0;
+                if (vb + P::CW <= p.V) {
+                    // whole block in range: per 16 columns, the Philox words first (independent
+                    // chains), then the block
+#pragma unroll
+                    for (int h = 0; h < P::CW / 16; ++h) {
+                        uint32_t words[16];
+                        float z[16];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int gg = 4 * h + g;
+                            const uint4 w4 = philox4x32_10(
+                                make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)k, (uint32_t)grow, c3), key);
+                            words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
+                            const uint2 uu = P::u_quad(sU, row, col0 + 4 * gg);
+                            z[4 * g] = __uint_as_float(acc[4 * gg]) + tcp::bf16_lo(uu.x);
+                            z[4 * g + 1] = __uint_as_float(acc[4 * gg + 1]) + tcp::bf16_hi(uu.x);
+                            z[4 * g + 2] = __uint_as_float(acc[4 * gg + 2]) + tcp::bf16_lo(uu.y);
+                            z[4 * g + 3] = __uint_as_float(acc[4 * gg + 3]) + tcp::bf16_hi(uu.y);
+                        }
+                        row_feed_block<16>(st, z, vb + 16 * h, words);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < P::CW / 4; ++g) {
+                        const int col = col0 + 4 * g;
+                        const uint2 uu = P::u_quad(sU, row, col);
+                        float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
+                                      __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
+                                      __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
+                                      __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
+                        const int v0 = n0 + col;
+                        const uint4 words =
+                            philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), key);
+                        row_feed4<false>(st, z, v0, p.V, words);
+                    }
+                }
+                if (st.best > best0) P::publish_thr(s, row, st.best);
+            });
+
+            // merge the TPR threads of each request (fixed warp order) into this CTA's partial
+            tc::named_bar_sync(1, tcp::kEpiThreads);  // every warp past its last accumulator
+            mg[et] = st.m;
+            mg[tcp::kEpiThreads + et] = st.S;
+            mg[2 * tcp::kEpiThreads + et] = st.best;
+            mg[3 * tcp::kEpiThreads + et] = st.zbest;
+            reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + et] = st.idx;
+            tc::named_bar_sync(1, tcp::kEpiThreads);
+            if (et < P::MV) s.thr[et] = P::ord_encode(-INFINITY);  // the next step starts afresh
+            if (et < P::MV && m0 + et < p.R) {
+                RowState f;
+                row_init(f);
+                const int wstep = P::DUAL ? 2 : 4;  // warps holding the same request
+                for (int w = et >> 5; w < tcp::kEpiWarps; w += wstep) {
+                    const int src = w * 32 + (et & 31);
+                    row_merge(f, mg[src], mg[tcp::kEpiThreads + src], mg[2 * tcp::kEpiThreads + src],
+                              mg[3 * tcp::kEpiThreads + src], reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + src]);
+                }
+                p.part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
+            }
+
+            // publish, then wait (bounded) until every CTA of the M-tile has published
             __threadfence();
-            float *wm = mg, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
+            tc::named_bar_sync(1, tcp::kEpiThreads);
+            if (et == 0) {
+                atomicAdd(ctr_part, 1);
+                *s.flag = wait_counter(ctr_part, q * p.nparts, p.err) ? 1 : 0;
+            }
+            tc::named_bar_sync(1, tcp::kEpiThreads);
+            if (!*s.flag) {
+                *s.abort_flag = 1;
+                break;
+            }
+            // every CTA finalises its share of the rows: one partial per thread,
+            // merged in a fixed tree (lanes, then warps in order)
+            __threadfence();
+            float *wm = mg + 5 * tcp::kEpiThreads, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
             int *wi = reinterpret_cast<int *>(wz + 16);
             for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) {
                 const int gr = m0 + i;
                 RowState f;
                 row_init(f);
                 if (et < p.nparts) {
-                    const DraftPartial q = load_partial_cg(p.part + (size_t)gr * p.nparts + et);
-                    row_merge(f, q.m, q.S, q.best, q.zbest, q.idx);
+                    const DraftPartial pq = load_partial_cg(p.part + (size_t)gr * p.nparts + et);
+                    row_merge(f, pq.m, pq.S, pq.best, pq.zbest, pq.idx);
                 }
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -311,7 +367,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                     RowState g;
                     row_init(g);
                     for (int w = 0; w < tcp::kEpiWarps; ++w) row_merge(g, wm[w], wS[w], wb[w], wz[w], wi[w]);
-                    const size_t o = (size_t)gr * p.gamma + (p.k - 1);
+                    const size_t o = (size_t)gr * p.gamma + (k - 1);
                     const float lse = g.m + logf(g.S);
                     int idx = g.idx;
                     if (idx < 0 || !isfinite(lse)) {
@@ -323,6 +379,13 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                     p.logq[o] = g.zbest - lse;
                 }
                 tc::named_bar_sync(1, tcp::kEpiThreads);
+            }
+            // rows finalised: the M-tile's next step may gather x_k.  (The barrier
+            // also keeps s.flag from being rewritten before every thread read it.)
+            tc::named_bar_sync(1, tcp::kEpiThreads);
+            if (et == 0) {
+                __threadfence();
+                atomicAdd(ctr_fin, 1);
             }
         }
     }
@@ -344,6 +407,8 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     if (!encode_u_map(&tmU, p.U, p.R, p.gamma, p.V, P::MV)) return cudaErrorInvalidValue;
     TcParams tp;
     tp.R = p.R; tp.V = p.V; tp.r = p.r; tp.d = p.d; tp.gamma = p.gamma; tp.k = p.k;
+    tp.nsteps = p.A_op ? 1 : (p.nsteps > 0 ? p.nsteps : 1);
+    tp.step_index = p.step_index;
     tp.h = static_cast<const __nv_bfloat16 *>(p.h); tp.w = p.w; tp.sts_T = p.sts_T;
     tp.counters = p.counters;
     tp.x = p.x_out; tp.logq = p.logq; tp.lse = p.lse; tp.c = p.c;
@@ -355,7 +420,6 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.n_mtiles = n_mtiles;
     tp.n_vtiles = (p.V + P::BN - 1) / P::BN;
     tp.err = p.err;
-    tp.target = p.step_index * nparts;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;

@@ -34,8 +34,9 @@ struct DraftStep {
     const float *w, *sts_T;
     int32_t *x_out;
     float *logq, *lse, *c;
-    int *counters;                   // [number of M-tiles], zero at the start of the call
+    int *counters;                   // [2 x number of M-tiles], zero at the start of the call
     int step_index;                  // 1 for the first step launched since the counters were zeroed
+    int nsteps;                      // tensor-core Markov step: steps k .. k + nsteps - 1 in one launch
 };
 int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);

@@ -75,6 +75,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     return false;
 }
 
+// Bounded wait that ignores the abort flag: used to let this CTA's own copies
+// and MMAs in flight land before its shared memory or TMEM is released.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(64);
+        }
+    }
+    set_err(err, DSPARK_ERR_TIMEOUT);
+    return false;
+}
+
 // ---------------------------------------------------------------- proxies, barriers
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -54,15 +54,17 @@ struct Pipe {
     static constexpr int kOffB = kABytes;
     static constexpr int kOffU = kOffB + NS * kSlabB;
     static constexpr int kOffBar = kOffU + SU * kUBytes;
-    static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC;
+    static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC + 1;
     static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
-    static constexpr int kOffMisc = kOffThr + 4 * MV;
+    static constexpr int kOffTok = kOffThr + 4 * MV;        // per-request tokens / metadata
+    static constexpr int kOffMisc = kOffTok + 4 * MV;
     static constexpr int kOffRed = kOffMisc + 64;           // 16-float reduction scratch
     static constexpr int kBytes = kOffRed + 64 + 1024;      // + alignment slack
-    // scratch for the per-CTA merge at the end (the rings are idle by then)
+    // scratch for the per-CTA merge after the tile loop: the operand region,
+    // which no MMA reads once the last accumulator has been consumed
     static constexpr int kMergeBytes = kEpiThreads * 5 * 4;
     static_assert(kBytes <= 232448, "shared memory budget");
-    static_assert(kMergeBytes <= NS * kSlabB, "merge scratch");
+    static_assert(kMergeBytes <= kABytes, "merge scratch");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
     static_assert(CW == 16 || CW == 32, "TMEM load width");
     static_assert(MV == 64 || MV == 128, "M-tile rows");
@@ -70,7 +72,9 @@ struct Pipe {
     struct State {
         unsigned char *smem, *sA;
         uint64_t *fullB, *emptyB, *fullU, *emptyU, *tfull, *tempty;
-        unsigned *thr;  // ordered-uint encoded row thresholds
+        uint64_t *aready;  // operand of the next step written (multi-step launches)
+        unsigned *thr;     // ordered-uint encoded row thresholds
+        int *tok;          // MV ints of per-request scratch
         uint32_t *tmem_slot;
         volatile int *abort_flag, *flag;
         float *red;  // 16 floats
@@ -89,7 +93,9 @@ struct Pipe {
         s.emptyU = bars + 2 * NS + SU;
         s.tfull = bars + 2 * NS + 2 * SU;
         s.tempty = s.tfull + NACC;
+        s.aready = s.tempty + NACC;
         s.thr = reinterpret_cast<unsigned *>(s.smem + kOffThr);
+        s.tok = reinterpret_cast<int *>(s.smem + kOffTok);
         s.tmem_slot = reinterpret_cast<uint32_t *>(s.smem + kOffMisc);
         s.abort_flag = reinterpret_cast<volatile int *>(s.smem + kOffMisc + 4);
         s.flag = reinterpret_cast<volatile int *>(s.smem + kOffMisc + 8);
@@ -114,6 +120,7 @@ struct Pipe {
                 tc::mbar_init(&s.tfull[b], 1);
                 tc::mbar_init(&s.tempty[b], kEpiWarps);
             }
+            tc::mbar_init(s.aready, 1);
             *s.abort_flag = 0;
             *s.flag = 0;
             tc::fence_mbar_init();
@@ -153,10 +160,7 @@ struct Pipe {
         if (DUAL) *reinterpret_cast<uint4 *>(a_chunk(s, row + 64, c, part)) = v;
     }
 
-    // the U tile of tile t and one quad of it (64-column boxes, 128-byte swizzle)
-    __device__ static const unsigned char *u_tile(const State &s, int t) {
-        return s.smem + kOffU + (SU > 0 ? t % SU : 0) * kUBytes;
-    }
+    // one quad of a U tile (64-column boxes, 128-byte swizzle)
     __device__ static uint2 u_quad(const unsigned char *sU, int row, int col) {
         const int h = col >> 6, cc = col & 63;
         return *reinterpret_cast<const uint2 *>(sU + h * kUBox + row * 128 +
@@ -174,96 +178,121 @@ struct Pipe {
         return DUAL ? (q >= 2 ? BN / 2 : 0) + j * CW : j * CW;
     }
 
-    // warp 16 (all lanes call): lane 0 streams W_2^T slabs, lane 1 the U tiles
+    // warp 16 (all lanes call): lane 0 streams W_2^T slabs, lane 1 the U tiles,
+    // for `nsteps` consecutive draft steps over the same tile range (W_2^T does
+    // not depend on the step, so the next step's slabs stream in while the
+    // current one is merged); U of step i is position u_k0 + i.
     __device__ static void producer(State &s, const CUtensorMap *tmB, const CUtensorMap *tmU, int t_begin,
-                                    int ntiles, int kslabs, int u_k, int m0, int32_t *err) {
+                                    int ntiles, int kslabs, int nsteps, int u_k0, int m0, int32_t *err) {
         const int lane = threadIdx.x & 31;
         if (lane == 0) {
-            const int total = ntiles * kslabs;
+            const int per_step = ntiles * kslabs, total = nsteps * per_step;
             int issued = 0;
             for (int g = 0; g < total; ++g) {
-                const int slot = g % NS, t = g / kslabs, j = g - t * kslabs;
+                const int slot = g % NS, rem = g % per_step, t = rem / kslabs, j = rem - t * kslabs;
                 if (!tc::mbar_wait(&s.emptyB[slot], ((uint32_t)(g / NS) & 1u) ^ 1u, s.abort_flag, err)) break;
                 tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
                 tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, (t_begin + t) * BN);
                 ++issued;
             }
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
-                tc::mbar_wait(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, s.abort_flag, err);
+                tc::mbar_wait_drain(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, err);
         } else if (lane == 1 && SU > 0) {
             // U is read once: keep it from displacing W_2^T, which the next steps reuse
             const uint64_t pol = tc::policy_evict_first();
             constexpr int su = SU > 0 ? SU : 1;
+            const int total = nsteps * ntiles;
             int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int st = t % su;
-                if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(t / su) & 1u) ^ 1u, s.abort_flag, err)) break;
+            for (int g = 0; g < total; ++g) {
+                const int st = g % su, step = g / ntiles, t = g - step * ntiles;
+                if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(g / su) & 1u) ^ 1u, s.abort_flag, err)) break;
                 unsigned char *dst = s.smem + kOffU + st * kUBytes;
                 const int n0 = (t_begin + t) * BN;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
                 for (int h = 0; h < BN / 64; ++h)
-                    tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k, m0, pol);
+                    tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k0 + step, m0, pol);
                 ++issued;
             }
-            for (int t = issued - su < 0 ? 0 : issued - su; t < issued; ++t)
-                tc::mbar_wait(&s.fullU[t % su], (uint32_t)(t / su) & 1u, s.abort_flag, err);
+            for (int g = issued - su < 0 ? 0 : issued - su; g < issued; ++g)
+                tc::mbar_wait_drain(&s.fullU[g % su], (uint32_t)(g / su) & 1u, err);
         }
     }
 
-    // warp 17, lane 0
-    __device__ static void mma(State &s, int ntiles, int kslabs, int32_t *err) {
+    // warp 17, lane 0: `nsteps` steps of `ntiles` tiles.  Step i > 0 starts once
+    // the epilogue has written its operand (phase i - 1 of `aready`).
+    __device__ static void mma(State &s, int ntiles, int kslabs, int nsteps, int32_t *err) {
         constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
         const uint32_t a_base = tc::smem_u32(s.sA);
         int issued = 0;
         bool ok = true;
-        for (int t = 0; t < ntiles && ok; ++t) {
-            const int b = t % NACC;
-            if (!tc::mbar_wait(&s.tempty[b], ((uint32_t)(t / NACC) & 1u) ^ 1u, s.abort_flag, err)) break;
-            tc::tc_fence_after();
-            const uint32_t d = s.tmem_base + (uint32_t)(b * BN);
-            for (int j = 0; j < kslabs; ++j) {
-                const int g = t * kslabs + j, slot = g % NS;
-                if (!tc::mbar_wait(&s.fullB[slot], (uint32_t)(g / NS) & 1u, s.abort_flag, err)) {
+        for (int step = 0; step < nsteps && ok; ++step) {
+            if (step > 0) {
+                if (!tc::mbar_wait(s.aready, (uint32_t)(step - 1) & 1u, s.abort_flag, err)) break;
+                tc::tc_fence_after();
+            }
+            for (int tl = 0; tl < ntiles && ok; ++tl) {
+                const int t = step * ntiles + tl;
+                const int b = t % NACC;
+                if (!tc::mbar_wait(&s.tempty[b], ((uint32_t)(t / NACC) & 1u) ^ 1u, s.abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t b_slab = tc::smem_u32(s.smem + kOffB + slot * kSlabB);
+                const uint32_t d = s.tmem_base + (uint32_t)(b * BN);
+                for (int j = 0; j < kslabs; ++j) {
+                    const int g = t * kslabs + j, slot = g % NS;
+                    if (!tc::mbar_wait(&s.fullB[slot], (uint32_t)(g / NS) & 1u, s.abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t b_slab = tc::smem_u32(s.smem + kOffB + slot * kSlabB);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = tc::smem_desc_k128(b_slab + kk * 32);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = tc::smem_desc_k128(b_slab + kk * 32);
 #pragma unroll
-                    for (int part = 0; part < KSPLIT; ++part)
-                        tc::umma_bf16(d, tc::smem_desc_k128(a_base + (j + 4 * part) * kSlabA + kk * 32), bd, idesc,
-                                      (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                        for (int part = 0; part < KSPLIT; ++part)
+                            tc::umma_bf16(d, tc::smem_desc_k128(a_base + (j + 4 * part) * kSlabA + kk * 32), bd,
+                                          idesc, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                    }
+                    tc::umma_commit(&s.emptyB[slot]);
                 }
-                tc::umma_commit(&s.emptyB[slot]);
+                if (!ok) break;
+                tc::umma_commit(&s.tfull[b]);
+                ++issued;
             }
-            if (!ok) break;
-            tc::umma_commit(&s.tfull[b]);
-            ++issued;
         }
         if (issued > 0) {  // the last MMAs must finish before TMEM is freed
             const int t = issued - 1;
-            tc::mbar_wait(&s.tfull[t % NACC], (uint32_t)(t / NACC) & 1u, s.abort_flag, err);
+            tc::mbar_wait_drain(&s.tfull[t % NACC], (uint32_t)(t / NACC) & 1u, err);
         }
     }
 
+    // epilogue side of the operand hand-off: called by all epilogue threads after
+    // they wrote the next step's operand with generic stores
+    __device__ static void operand_written(State &s, int et) {
+        tc::fence_proxy_async_smem();
+        tc::named_bar_sync(1, kEpiThreads);
+        if (et == 0) tc::mbar_arrive(s.aready);
+    }
+
     // warps 0..15: per tile, load this warp's CW accumulator columns of its 32
-    // rows and call f(t, n0, acc, sU) (n0: first vocabulary entry of the tile;
-    // sU: the tile's U, or null).  Per-warp flow, no CTA barrier.
+    // rows and call f(t, n0, acc, sU) (t: tile within this call; n0: first
+    // vocabulary entry of the tile; sU: the tile's U, or null).  Barrier phases
+    // continue from tile number tg0 (the tiles of earlier steps of the launch).
+    // Per-warp flow, no CTA barrier.
     template <class F>
-    __device__ static void epilogue(State &s, int t_begin, int ntiles, int32_t *err, F &&f) {
+    __device__ static void epilogue(State &s, int tg0, int t_begin, int ntiles, int32_t *err, F &&f) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const uint32_t taddr0 = s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)epi_col0();
+        constexpr int su = SU > 0 ? SU : 1;
         for (int t = 0; t < ntiles; ++t) {
-            const int b = t % NACC;
+            const int tg = tg0 + t, b = tg % NACC;
             int ok = 1;
             if (lane == 0) {
-                ok = tc::mbar_wait(&s.tfull[b], (uint32_t)(t / NACC) & 1u, s.abort_flag, err) ? 1 : 0;
+                ok = tc::mbar_wait(&s.tfull[b], (uint32_t)(tg / NACC) & 1u, s.abort_flag, err) ? 1 : 0;
                 if (ok && SU > 0)
-                    ok = tc::mbar_wait(&s.fullU[t % (SU > 0 ? SU : 1)], (uint32_t)(t / (SU > 0 ? SU : 1)) & 1u,
-                                       s.abort_flag, err) ? 1 : 0;
+                    ok = tc::mbar_wait(&s.fullU[tg % su], (uint32_t)(tg / su) & 1u, s.abort_flag, err) ? 1 : 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -276,9 +305,9 @@ struct Pipe {
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
-            f(t, (t_begin + t) * BN, acc, SU > 0 ? u_tile(s, t) : nullptr);
+            f(t, (t_begin + t) * BN, acc, SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr);
             __syncwarp();
-            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[t % (SU > 0 ? SU : 1)]);
+            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
         }
     }
 
@@ -290,9 +319,10 @@ struct Pipe {
         return ord_decode(*reinterpret_cast<volatile unsigned *>(&s.thr[r]));
     }
 
-    // per-CTA merge scratch (valid once every epilogue warp has left its loop)
+    // per-CTA merge scratch in the operand region (valid once every epilogue
+    // warp has consumed its last accumulator, until the next operand is written)
     __device__ static float *merge_scratch(const State &s) {
-        return reinterpret_cast<float *>(s.smem + kOffB);
+        return reinterpret_cast<float *>(s.sA);
     }
 
     // all threads, at the very end

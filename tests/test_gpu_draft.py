@@ -50,6 +50,7 @@ SMALL = [
     W.small("qwen4b", R=40, gamma=3, V=5000, r=64, d=32),
     W.small("heavy", R=100, gamma=3, V=4104, r=128, d=16),
     W.small("prod", R=300, gamma=2, V=8192 + 72, r=256, d=16),
+    W.small("heavy", R=65, gamma=5, V=2056, r=64, d=20),          # d % 8 != 0, 1 M-tile of 128
 ]
 
 
@@ -78,6 +79,33 @@ def test_markov_deterministic():
     b = _gpu_draft(inp, 9, 2)
     for k in a:
         assert np.array_equal(a[k], b[k]), k
+
+
+STEP_CASES = [
+    W.small("qwen4b", R=40, gamma=3, V=5000, r=64, d=32),
+    W.small("heavy", R=130, gamma=4, V=4104, r=128, d=20),
+    W.WORKLOADS["qwen4b"],
+]
+
+
+@pytest.mark.parametrize("wl", STEP_CASES, ids=lambda w: f"{w.name}-R{w.R}")
+def test_step_calls_match_one_call(wl):
+    """gamma single-step calls and the all-steps call give identical outputs."""
+    inp = W.draft_inputs(wl, seed=6, device="cuda")
+    whole = _gpu_draft(inp, 31, 2)
+    out = {k: torch.empty((wl.R, wl.gamma), dtype=torch.int32 if k == "x" else torch.float32,
+                          device="cuda") for k in ("x", "logq", "lse", "c")}
+    nbytes = dsp.draft_markov_workspace_size(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["w"],
+                                             inp["anchor"])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k in range(1, wl.gamma + 1):
+        dsp.draft_markov_step(k, inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["w"], inp["anchor"],
+                              out=out, ws=ws, seed=31, cycle=2, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for k in ("x", "logq", "lse", "c"):
+        assert np.array_equal(host(out[k]), whole[k]), k
 
 
 @pytest.mark.parametrize("name,reqs", [("qwen4b", [0, 37, 63]), ("heavy", [5, 200]),
