@@ -68,6 +68,34 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     return c;
 }
 
+// The 20 round keys of one seed, k + i W for i = 0..9.  The tensor-core kernels
+// get them in their launch parameters (computed on the host), so each round's
+// key xor takes its operand straight from the parameter bank: a Philox call is
+// then two wide multiplies and two three-way xors per round.
+struct PhiloxRoundKeys {
+    uint32_t k0[10], k1[10];
+};
+
+__host__ __device__ inline PhiloxRoundKeys philox_round_keys(uint64_t seed) {
+    PhiloxRoundKeys rk;
+    for (int i = 0; i < 10; ++i) {
+        rk.k0[i] = (uint32_t)seed + (uint32_t)i * 0x9E3779B9u;
+        rk.k1[i] = (uint32_t)(seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
+    return rk;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys &rk) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53ull;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57ull;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk.k0[round], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ rk.k1[round], (uint32_t)p0);
+    }
+    return c;
+}
+
 __device__ __forceinline__ uint32_t word_lane(const uint4 &w, int lane) {
     return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

@@ -39,6 +39,7 @@ struct TcParams {
     const float *w;          // [d + r]
     const float *sts_T;      // [gamma] or null
     uint64_t seed, cycle;
+    PhiloxRoundKeys rk;  // of seed
     DraftPartial *part;
     int *counters;  // [2 * n_mtiles]: partials published, rows finalised (per M-tile)
     int32_t *x;
@@ -229,7 +230,6 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         const int row = P::epi_row(), col0 = P::epi_col0();
         const int grow = m0 + row;
         const bool row_live = grow < p.R;
-        const PhiloxKey key = philox_key(p.seed);
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         float *mg = P::merge_scratch(s);
         for (int step = 0; step < p.nsteps; ++step) {
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                         for (int g = 0; g < 4; ++g) {
                             const int gg = 4 * h + g;
                             const uint4 w4 = philox4x32_10(
-                                make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)k, (uint32_t)grow, c3), key);
+                                make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)k, (uint32_t)grow, c3), p.rk);
                             words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
                             const uint2 uu = P::u_quad(sU, row, col0 + 4 * gg);
                             z[4 * g] = __uint_as_float(acc[4 * gg]) + tcp::bf16_lo(uu.x);
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                                       __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
                         const int v0 = n0 + col;
                         const uint4 words =
-                            philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), key);
+                            philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), p.rk);
                         row_feed4<false>(st, z, v0, p.V, words);
                     }
                 }
@@ -416,6 +416,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.x_prev = p.x_prev; tp.x_stride = p.x_stride;
     tp.A_op = p.A_op; tp.a_stride = p.a_stride;
     tp.seed = p.seed; tp.cycle = p.cycle;
+    tp.rk = philox_round_keys(p.seed);
     tp.part = p.part; tp.nparts = nparts;
     tp.n_mtiles = n_mtiles;
     tp.n_vtiles = (p.V + P::BN - 1) / P::BN;

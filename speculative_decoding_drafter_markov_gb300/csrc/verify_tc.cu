@@ -30,6 +30,7 @@ struct VerifyTcParams {
     VerifyWs w;
     int nparts, n_mtiles, n_vtiles;
     uint64_t seed, cycle;
+    PhiloxRoundKeys rk;  // of seed
     int32_t *err;
 };
 
@@ -128,7 +129,6 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         const float lsep = s_lsep[row] * kLog2e, lseq = s_lseq[row] * kLog2e;
         const __nv_bfloat16 *trow = p.T + (size_t)s_row[row] * p.V;
         const __nv_bfloat16 *urow = p.U + ((size_t)rq * p.gamma + (mode == 1 ? n : 0)) * (size_t)p.V;
-        const PhiloxKey key = philox_key(p.seed);
         const uint32_t c3 = philox_ctr3(p.cycle, 2);
         Race res, pr;
         race_init(res);
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                 const uint32_t t0 = (g & 1) ? tt.z : tt.x, t1 = (g & 1) ? tt.w : tt.y;
                 const float tv[4] = {tcp::bf16_lo(t0), tcp::bf16_hi(t0), tcp::bf16_lo(t1), tcp::bf16_hi(t1)};
                 const uint4 words =
-                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), key);
+                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), p.rk);
                 float pv[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
@@ -225,6 +225,7 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.w = w;
     tp.nparts = nparts; tp.n_mtiles = mt; tp.n_vtiles = (a.V + P::BN - 1) / P::BN;
     tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
+    tp.rk = philox_round_keys(a.seed);
     auto kern = verify_phase2_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;
