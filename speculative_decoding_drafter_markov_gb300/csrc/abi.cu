@@ -123,7 +123,12 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
         const int xs = k == 1 ? 1 : a->gamma;
         if (rnn) {
+            // state double buffer: s_{k-1} in buffer (k - 1) % 2, s_k into buffer k % 2
             RnnStep rs = *rnn;
+            if ((k & 1) == 0) {
+                rs.s_in = rnn->s_out;
+                rs.s_out = const_cast<float *>(rnn->s_in);
+            }
             rs.k = k;
             rs.x_prev = xp;
             rs.x_stride = xs;
@@ -221,11 +226,19 @@ DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_st
     return rc == DSPARK_OK ? ok() : rc;
 }
 
+namespace {
+constexpr size_t kLtWorkspaceBytes = 4u << 20;  // cuBLASLt scratch of the h projection
+
+size_t rnn_ws_bytes(const dspark_rnn_args *a) {
+    const dspark_draft_args &b = a->base;
+    return draft_ws_bytes(&b, a->A) + 2 * dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
+           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r) + kLtWorkspaceBytes;
+}
+}  // namespace
+
 DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a) {
     if (!a || check_draft(&a->base) != DSPARK_OK) return 0;
-    const dspark_draft_args &b = a->base;
-    return draft_ws_bytes(&b, a->A) + dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
-           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
+    return rnn_ws_bytes(a);
 }
 
 DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_stream_t stream) {
@@ -236,29 +249,39 @@ DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_strea
     if (!ws) return fail(DSPARK_ERR_INVAL, "null workspace");
     const dspark_draft_args &b = a->base;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t state_bytes = sizeof(float) * (size_t)b.R * b.r;
     char *p = static_cast<char *>(ws);
     void *part = p;
     p += draft_ws_bytes(&b, a->A);
-    float *state = reinterpret_cast<float *>(p);
-    p += dspark::align256(sizeof(float) * (size_t)b.R * b.r);
+    float *state0 = reinterpret_cast<float *>(p);
+    p += dspark::align256(state_bytes);
+    float *state1 = reinterpret_cast<float *>(p);
+    p += dspark::align256(state_bytes);
     float *Hpre = reinterpret_cast<float *>(p);
-    cudaError_t e = a->s0 ? cudaMemcpyAsync(state, a->s0, sizeof(float) * (size_t)b.R * b.r,
-                                            cudaMemcpyDeviceToDevice, s)
-                          : cudaMemsetAsync(state, 0, sizeof(float) * (size_t)b.R * b.r, s);
+    p += dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
+    void *lt_ws = p;
+    cudaError_t e = a->s0 ? cudaMemcpyAsync(state0, a->s0, state_bytes, cudaMemcpyDeviceToDevice, s)
+                          : cudaMemsetAsync(state0, 0, state_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn state init");
     if (b.d > 0) {
-        e = dspark::launch_rnn_hproj(b.R * b.gamma, b.d, b.r, b.dtype, b.h, a->W, Hpre, s);
+        if (b.dtype == DSPARK_BF16 && dspark::hproj_lt_available())
+            e = dspark::launch_hproj_lt(b.R * b.gamma, b.d, b.r, b.h, a->W, Hpre, lt_ws, kLtWorkspaceBytes, s);
+        else
+            e = dspark::launch_rnn_hproj(b.R * b.gamma, b.d, b.r, b.dtype, b.h, a->W, Hpre, s);
     } else {
         e = cudaMemsetAsync(Hpre, 0, sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "rnn h projection");
     dspark::RnnStep rs{};
     rs.R = b.R; rs.V = b.V; rs.r = b.r; rs.d = b.d; rs.gamma = b.gamma; rs.dtype = b.dtype;
-    rs.W = a->W; rs.W1 = b.W1; rs.Hpre = Hpre; rs.state = state; rs.A = a->A; rs.err = b.err;
+    rs.W = a->W; rs.W1 = b.W1; rs.Hpre = Hpre; rs.A = a->A; rs.err = b.err;
+    rs.s_in = state0;
+    rs.s_out = state1;
     rc = run_draft_loop(&b, a->A, part, s, &rs, 1, b.gamma);
     if (rc != DSPARK_OK) return rc;
     if (a->s_out) {
-        e = cudaMemcpyAsync(a->s_out, state, sizeof(float) * (size_t)b.R * b.r, cudaMemcpyDeviceToDevice, s);
+        const float *last = (b.gamma & 1) ? state1 : state0;
+        e = cudaMemcpyAsync(a->s_out, last, state_bytes, cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "rnn state out");
     }
     return ok();

@@ -194,42 +194,68 @@ __global__ void __launch_bounds__(256) rnn_hproj_kernel(int M, int d, int r, con
         }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) rnn_step_kernel(const RnnStep p) {
+// One step of eq. (6) after the h_k part: G = W[:, :2r] [s_{k-1}; W_1[x_{k-1}]]
+// + Hpre_k, then s_k = sigma(G_g) s_{k-1} + (1 - sigma(G_g)) tanh(G_c) and the
+// bias operand A_k = tanh(G_o).  CTA (ib, qb) computes entries i0 .. i0 + IB - 1
+// of the three gates for requests q0 .. q0 + RB - 1: the 3 IB rows of W and the
+// RB vectors z are staged in shared memory as fp32 (rows padded by one word,
+// so the lanes of a warp read distinct banks), one thread per (request, i).
+// The state is double-buffered (s_in -> s_out) since every CTA reads whole
+// rows of s_{k-1}.
+constexpr int kRnnIB = 8;
+
+template <typename T, int RB>
+__global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) {
     extern __shared__ float sh[];
-    const int r = p.r, row = blockIdx.x;
-    float *zsx = sh;          // [s_{k-1} ; W_1[x_{k-1}]]  (2r)
-    float *G = sh + 2 * r;    // W z_k                      (3r)
-    int xp = p.x_prev[(size_t)row * p.x_stride];
-    if (xp < 0 || xp >= p.V) {
-        if (threadIdx.x == 0) set_err(p.err, DSPARK_ERR_RANGE);
-        xp = 0;
-    }
-    const T *W1 = static_cast<const T *>(p.W1);
-    for (int i = threadIdx.x; i < r; i += blockDim.x) {
-        zsx[i] = p.state[(size_t)row * r + i];
-        zsx[r + i] = to_f32(W1[(size_t)xp * r + i]);
-    }
-    __syncthreads();
+    const int r = p.r, K = 2 * r, ld = K + 1;
+    float *Ws = sh;                    // [3 IB][K + 1]: rows g r + i0 + ii, g = gate
+    float *Zs = sh + 3 * kRnnIB * ld;  // [RB][K + 1]
+    const int i0 = blockIdx.x * kRnnIB, q0 = blockIdx.y * RB;
+    const int ldw = 2 * r + p.d;
     const T *W = static_cast<const T *>(p.W);
-    const int ldw = 2 * r + p.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    const float *hp = p.Hpre + ((size_t)row * p.gamma + (p.k - 1)) * (size_t)(3 * r);
-    for (int o = warp; o < 3 * r; o += nwarps) {
-        const T *Wrow = W + (size_t)o * ldw;
-        float acc = 0.f;
-        for (int j = lane; j < 2 * r; j += 32) acc = fmaf(to_f32(Wrow[j]), zsx[j], acc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) G[o] = acc + hp[o];
+    const T *W1 = static_cast<const T *>(p.W1);
+    for (int e = threadIdx.x; e < 3 * kRnnIB * K; e += blockDim.x) {
+        const int row = e / K, j = e - row * K;
+        const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
+        Ws[row * ld + j] = i < r ? to_f32(W[(size_t)(g * r + i) * ldw + j]) : 0.f;
+    }
+    for (int e = threadIdx.x; e < RB * K; e += blockDim.x) {
+        const int q = e / K, j = e - q * K, rq = q0 + q;
+        float v = 0.f;
+        if (rq < p.R) {
+            if (j < r) {
+                v = p.s_in[(size_t)rq * r + j];
+            } else {
+                int xp = p.x_prev[(size_t)rq * p.x_stride];
+                if (xp < 0 || xp >= p.V) {
+                    if (j == r) set_err(p.err, DSPARK_ERR_RANGE);
+                    xp = 0;
+                }
+                v = to_f32(W1[(size_t)xp * r + (j - r)]);
+            }
+        }
+        Zs[q * ld + j] = v;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < r; i += blockDim.x) {
-        const float g = 1.0f / (1.0f + expf(-G[i]));
-        const float cand = tanhf(G[r + i]);
-        const float s_prev = zsx[i];
-        p.state[(size_t)row * r + i] = g * s_prev + (1.0f - g) * cand;
-        p.A[((size_t)row * p.gamma + (p.k - 1)) * (size_t)r + i] = tanhf(G[2 * r + i]);
+    const int q = threadIdx.x / kRnnIB, ii = threadIdx.x - q * kRnnIB;
+    const int rq = q0 + q, i = i0 + ii;
+    const float *z = Zs + q * ld;
+    const float *wg = Ws + ii * ld, *wc = Ws + (kRnnIB + ii) * ld, *wo = Ws + (2 * kRnnIB + ii) * ld;
+    float gg = 0.f, gc = 0.f, go = 0.f;
+    for (int j = 0; j < K; ++j) {
+        const float zj = z[j];
+        gg = fmaf(wg[j], zj, gg);
+        gc = fmaf(wc[j], zj, gc);
+        go = fmaf(wo[j], zj, go);
+    }
+    if (rq < p.R && i < r) {
+        const float *hp = p.Hpre + ((size_t)rq * p.gamma + (p.k - 1)) * (size_t)(3 * r);
+        gg += hp[i];
+        gc += hp[r + i];
+        go += hp[2 * r + i];
+        const float g = 1.0f / (1.0f + expf(-gg));
+        p.s_out[(size_t)rq * r + i] = g * z[i] + (1.0f - g) * tanhf(gc);
+        p.A[((size_t)rq * p.gamma + (p.k - 1)) * (size_t)r + i] = tanhf(go);
     }
 }
 
@@ -274,20 +300,22 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
     return cudaGetLastError();
 }
 
-cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)(5 * p.r);
-    if (p.dtype == DSPARK_BF16) {
-        auto kern = rnn_step_kernel<__nv_bfloat16>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<p.R, 256, smem, s>>>(p);
-    } else {
-        auto kern = rnn_step_kernel<float>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<p.R, 256, smem, s>>>(p);
-    }
+template <typename T, int RB>
+static cudaError_t launch_rnn_step_t(const RnnStep &p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 1);
+    auto kern = rnn_step_kernel<T, RB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((p.r + kRnnIB - 1) / kRnnIB, (p.R + RB - 1) / RB);
+    kern<<<grid, RB * kRnnIB, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s) {
+    // 32 requests per CTA up to r = 256 (120 KB of shared memory), 16 above
+    if (p.dtype == DSPARK_BF16)
+        return p.r <= 256 ? launch_rnn_step_t<__nv_bfloat16, 32>(p, s) : launch_rnn_step_t<__nv_bfloat16, 16>(p, s);
+    return p.r <= 256 ? launch_rnn_step_t<float, 32>(p, s) : launch_rnn_step_t<float, 16>(p, s);
 }
 
 }  // namespace dspark

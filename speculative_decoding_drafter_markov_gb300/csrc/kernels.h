@@ -82,11 +82,16 @@ struct RnnStep {
     const int32_t *x_prev;
     int x_stride;
     const float *Hpre;               // [R * gamma, 3r]
-    float *state;                    // [R, r]
+    const float *s_in;               // [R, r] state s_{k-1}
+    float *s_out;                    // [R, r] state s_k (a different buffer)
     float *A;                        // [R, gamma, r]
     int32_t *err;
 };
 cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s);
+// Hpre [M, 3r] = h [M, d] W[:, 2r:]^T on the tensor cores (bf16), through cuBLASLt
+bool hproj_lt_available();
+cudaError_t launch_hproj_lt(int M, int d, int r, const void *h, const void *W, float *Hpre, void *lt_ws,
+                            size_t lt_ws_bytes, cudaStream_t s);
 
 // ----- scheduler (Module E, Algorithm 1; async variant) ---------------------
 cudaError_t launch_schedule(const dspark_sched_args &a, cudaStream_t s);
