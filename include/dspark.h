@@ -104,7 +104,9 @@ DSPARK_API int dspark_draft_markov(const dspark_draft_args *a, void *ws, dspark_
  * dspark_draft_markov equals calls for k = 1..gamma in order on one stream
  * with one workspace; the split lets an engine interleave other work between
  * steps.  Step 1 (re)starts the per-draft step counters kept in the
- * workspace, so a step k > 1 must follow steps 1..k-1 of the same draft. */
+ * workspace, so a step k > 1 must follow steps 1..k-1 of the same draft.
+ * (dspark_draft_markov itself runs all gamma steps in one launch on the
+ * tensor-core path.) */
 DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, void *ws,
                                         dspark_stream_t stream);
 
@@ -120,10 +122,12 @@ DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, v
  * GPU that loads the library holds until the process exits.
  *
  * - Limit: the scratch is what dspark_draft_markov_workspace_size() returns
- *   for the same arguments -- 32 bytes per (request, vocabulary range) plus
- *   512; the ranges are one per SM on the tensor-core path (bf16, r a multiple
- *   of 64 up to 256, V a multiple of 8: all the standard workloads, well under
- *   1 MiB) and ceil(V / 64) on the CUDA-core path -- and the array holds
+ *   for the same arguments -- 32 bytes per (request, vocabulary range), twice
+ *   on the tensor-core path, plus 8 bytes per (request, step) and 256, each
+ *   part rounded up to 256 bytes; the ranges are one per SM on the tensor-core
+ *   path (bf16, r a multiple of 64 up to 256, V a multiple of 8: all the
+ *   standard workloads, under 2 MiB) and ceil(V / 64) on the CUDA-core path --
+ *   and the array holds
  *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB).  Larger needs return
  *   DSPARK_ERR_UNSUPPORTED (message in dspark_last_error()) and launch nothing.
  * - The first call on each device looks up the array's device address (with

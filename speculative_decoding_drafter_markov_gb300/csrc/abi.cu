@@ -53,8 +53,10 @@ int check_draft(const dspark_draft_args *a) {
 }
 
 // The step kernels' scratch: one partial per (request, vocabulary range) --
-// ceil(V / 64) ranges on the CUDA-core path, one per CTA on the tensor-core
-// path -- then the tensor-core step's per-M-tile completion counters.
+// ceil(V / 64) ranges on the CUDA-core path; one per CTA on the tensor-core
+// path, twice (double-buffered by step parity) -- then the tensor-core step's
+// per-M-tile completion counters and its [gamma, R] packed race winners, the
+// part cleared at the start of a call.
 constexpr size_t kCounterBytes = 256;
 
 dspark::DraftStep step_template(const dspark_draft_args *a, const float *A_rnn) {
@@ -74,7 +76,7 @@ bool use_tc_path(const dspark::DraftStep &st) {
     if (!dspark::draft_step_tc_supported(st)) return false;
     int np = 0, mt = 0;
     dspark::draft_step_tc_shape(st.R, st.V, st.A_op != nullptr, &np, &mt);
-    return (size_t)2 * mt * sizeof(int) <= kCounterBytes;  // two counters per M-tile
+    return (size_t)mt * sizeof(int) <= kCounterBytes;  // one counter per M-tile
 }
 
 int step_nparts(const dspark::DraftStep &st, bool tc) {
@@ -84,10 +86,19 @@ int step_nparts(const dspark::DraftStep &st, bool tc) {
     return np;
 }
 
-size_t draft_ws_bytes(const dspark_draft_args *a, const float *A_rnn) {
+size_t winners_bytes(const dspark_draft_args *a) {
+    return dspark::align256(sizeof(unsigned long long) * (size_t)a->R * a->gamma);
+}
+
+size_t partials_bytes(const dspark_draft_args *a, const float *A_rnn) {
     const dspark::DraftStep st = step_template(a, A_rnn);
-    const int np = step_nparts(st, use_tc_path(st));
-    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)a->R * np) + kCounterBytes;
+    const bool tc = use_tc_path(st);
+    const int np = step_nparts(st, tc);
+    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)a->R * np * (tc ? 2 : 1));
+}
+
+size_t draft_ws_bytes(const dspark_draft_args *a, const float *A_rnn) {
+    return partials_bytes(a, A_rnn) + kCounterBytes + winners_bytes(a);
 }
 
 // the gamma sequential steps shared by both heads
@@ -98,15 +109,17 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
     st.part = static_cast<DraftPartial *>(part_ws);
     const bool use_tc = use_tc_path(st);
     st.nparts = step_nparts(st, use_tc);
-    st.counters = reinterpret_cast<int *>(static_cast<char *>(part_ws) + draft_ws_bytes(a, st.A_op) -
-                                          kCounterBytes);
+    char *cleared = static_cast<char *>(part_ws) + partials_bytes(a, st.A_op);
+    const size_t cleared_bytes = kCounterBytes + winners_bytes(a);
+    st.counters = reinterpret_cast<int *>(cleared);
+    st.winners = reinterpret_cast<unsigned long long *>(cleared + kCounterBytes);
     DraftReduce rd{};
     rd.R = a->R; rd.V = a->V; rd.r = a->r; rd.d = a->d; rd.gamma = a->gamma; rd.dtype = a->dtype;
     rd.part = st.part; rd.nparts = st.nparts;
     rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
     rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
     if (use_tc && k_first == 1) {  // step 1 starts the step counters; later steps continue them
-        cudaError_t e = cudaMemsetAsync(st.counters, 0, kCounterBytes, s);
+        cudaError_t e = cudaMemsetAsync(cleared, 0, cleared_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft counters");
     }
     if (use_tc && !rnn) {

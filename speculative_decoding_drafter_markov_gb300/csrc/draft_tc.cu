@@ -40,43 +40,28 @@ struct TcParams {
     const float *sts_T;      // [gamma] or null
     uint64_t seed, cycle;
     PhiloxRoundKeys rk;  // of seed
-    DraftPartial *part;
-    int *counters;  // [2 * n_mtiles]: partials published, rows finalised (per M-tile)
+    DraftPartial *part;  // [2][R][nparts]: step partials, double-buffered by step parity
+    unsigned long long *winners;  // [gamma][R] packed race winners, zero at the start of the call
+    int *counters;  // [n_mtiles]: partials published (per M-tile), zero at the start of the call
     int32_t *x;
     float *logq, *lse, *c;   // [R, gamma]
     int nparts;  // vocabulary ranges (CTAs per M-tile)
     int n_mtiles;
-    int n_vtiles;
     int32_t *err;
 };
 
-// eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request, by all
-// epilogue threads (16-byte chunks of h_k then of W_1[x_{k-1}]), reduced in a
-// fixed order through `red` (16 floats of shared memory).  `pre` is thread et's
-// chunk et of h_k when `have_pre` (loaded early); E comes from shared memory
-// when the operand there is W_1[x_{k-1}] itself (`e_smem`), else from the
-// launch's x_prev (RNN head, one step per launch).
-template <class P>
-__device__ __forceinline__ void confidence_row(const TcParams &p, const typename P::State &s, int k,
-                                               int local_row, int grow, int et, float *red, bool have_pre,
-                                               uint4 pre, bool e_smem) {
+// eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
+// xp = x_{k-1}), by all epilogue threads, reduced in a fixed order through
+// `red` (16 floats of shared memory).
+__device__ __forceinline__ void confidence_row(const TcParams &p, int k, int grow, int xp, int et, float *red) {
     const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
+    const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
     float dot = 0.f;
     if ((p.d & 7) == 0) {
-        int xp = 0;
-        if (!e_smem) {
-            xp = p.x_prev[(size_t)grow * p.x_stride];
-            if (xp < 0 || xp >= p.V) xp = 0;
-        }
         const int hc = p.d / 8, nc = hc + p.r / 8;
         for (int ch = et; ch < nc; ch += tcp::kEpiThreads) {
-            uint4 raw;
-            if (ch < hc)
-                raw = (have_pre && ch == et) ? pre : *reinterpret_cast<const uint4 *>(h + ch * 8);
-            else if (e_smem)
-                raw = *reinterpret_cast<const uint4 *>(P::a_chunk(s, local_row, ch - hc, 0));
-            else
-                raw = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xp * p.r + (ch - hc) * 8);
+            const uint4 raw = ch < hc ? *reinterpret_cast<const uint4 *>(h + ch * 8)
+                                      : *reinterpret_cast<const uint4 *>(e + (ch - hc) * 8);
             const float *wv = p.w + ch * 8;  // w = [w_h ; w_e] lines up with [h ; e]
             const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -86,14 +71,6 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, const typename
             }
         }
     } else {
-        int xp = 0;
-        if (e_smem) {
-            xp = s.tok[local_row];
-        } else {
-            xp = p.x_prev[(size_t)grow * p.x_stride];
-            if (xp < 0 || xp >= p.V) xp = 0;
-        }
-        const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
         for (int j = et; j < p.d + p.r; j += tcp::kEpiThreads)
             dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
     }
@@ -130,17 +107,25 @@ __device__ __forceinline__ bool wait_counter(const int *ctr, int target, int32_t
 }
 
 // token x_{k-1} of request grow (held in s.tok), checked against the vocabulary
-__device__ __forceinline__ int load_token(const TcParams &p, int grow, const int32_t *xp, int stride,
-                                          bool from_l2) {
+__device__ __forceinline__ int load_token(const TcParams &p, int grow, const int32_t *xp, int stride) {
     if (grow >= p.R) return -1;
-    const int32_t *ptr = xp + (size_t)grow * stride;
-    int x = from_l2 ? __ldcg(ptr) : *ptr;
+    int x = xp[(size_t)grow * stride];
     if (x < 0 || x >= p.V) {
         set_err(p.err, DSPARK_ERR_RANGE);
         x = 0;
     }
     return x;
 }
+
+// The race winner of a row as one 64-bit word whose unsigned order is the
+// merge order (higher score, then lower index): order-preserving score bits
+// on top, the complemented index below.  Zero means "no candidate".
+__device__ __forceinline__ unsigned long long pack_winner(float best, int idx) {
+    const uint32_t b = __float_as_uint(best);
+    const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)ob << 32) | (uint32_t)~(uint32_t)idx;
+}
+__device__ __forceinline__ int winner_index(unsigned long long w) { return (int)~(uint32_t)w; }
 
 // the bias operand of the M-tile in the swizzled K-major layout: W_1[x_{k-1}]
 // (tokens in s.tok) or the split fp32 RNN operand; threads tid, tid + nthr, ...
@@ -172,15 +157,62 @@ __device__ __forceinline__ void gather_operand(const TcParams &p, const typename
     }
 }
 
+// Finalise row gr of step k from its nparts partials (one per thread, merged
+// in a fixed tree: lanes, then warps in order): x_k, lse_k, log q_k(x_k).
+__device__ __forceinline__ void finalise_row(const TcParams &p, const DraftPartial *part, int gr, int k, int et,
+                                             float *wsc) {
+    const int warp = et >> 5, lane = et & 31;
+    float *wm = wsc, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
+    int *wi = reinterpret_cast<int *>(wz + 16);
+    RowState f;
+    row_init(f);
+    for (int i = et; i < p.nparts; i += tcp::kEpiThreads) {
+        const DraftPartial pq = load_partial_cg(part + (size_t)gr * p.nparts + i);
+        row_merge(f, pq.m, pq.S, pq.best, pq.zbest, pq.idx);
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float m = __shfl_xor_sync(0xffffffffu, f.m, off);
+        const float S = __shfl_xor_sync(0xffffffffu, f.S, off);
+        const float bb = __shfl_xor_sync(0xffffffffu, f.best, off);
+        const float zb = __shfl_xor_sync(0xffffffffu, f.zbest, off);
+        const int ix = __shfl_xor_sync(0xffffffffu, f.idx, off);
+        row_merge(f, m, S, bb, zb, ix);
+    }
+    if (lane == 0) {
+        wm[warp] = f.m; wS[warp] = f.S; wb[warp] = f.best; wz[warp] = f.zbest; wi[warp] = f.idx;
+    }
+    tc::named_bar_sync(1, tcp::kEpiThreads);
+    if (et == 0) {
+        RowState g;
+        row_init(g);
+        for (int w = 0; w < tcp::kEpiWarps; ++w) row_merge(g, wm[w], wS[w], wb[w], wz[w], wi[w]);
+        const size_t o = (size_t)gr * p.gamma + (k - 1);
+        const float lse = g.m + logf(g.S);
+        int idx = g.idx;
+        if (idx < 0 || !isfinite(lse)) {
+            set_err(p.err, DSPARK_ERR_NONFINITE);
+            idx = 0;
+        }
+        p.x[o] = idx;
+        p.lse[o] = lse;
+        p.logq[o] = g.zbest - lse;
+    }
+    tc::named_bar_sync(1, tcp::kEpiThreads);
+}
+
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
-// (m_tile, cv) owns requests m0 .. m0 + MV - 1 and vocabulary range cv of
-// nparts.  Per step: contraction + eq. (4) epilogue over the range, a merge
-// into one partial per request, then -- once every CTA of the M-tile has
-// published (bounded wait; the launch is cooperative, so all are resident) --
-// each CTA finalises rows cv, cv + nparts, ... (x_k, lse_k, log q_k).  The next
-// step's operand needs x_k of all the M-tile's rows, hence a second bounded
-// wait on the finalised-rows counter; meanwhile the producer already streams
-// the next step's W_2^T slabs and U tiles.
+// (m_tile, cv) owns requests m0 .. m0 + MV - 1 and vocabulary columns
+// [c0, c1), an equal share.  Per step: contraction + eq. (4) epilogue over the
+// columns, a merge into one partial per request (double-buffered by step
+// parity) and the race winner folded into a per-(step, request) 64-bit maximum.
+// Once every CTA of the M-tile has published (bounded wait; the launch is
+// cooperative, so all are resident) each reads the winners x_k of its rows and
+// gathers the next operand W_1[x_k] right away -- the producer has already
+// streamed the next step's first W_2^T slabs and U tiles -- and only then
+// finalises its share of rows (cv, cv + nparts, ...: lse_k, log q_k) while the
+// MMAs of the next step run.  The confidences of its rows are computed while
+// it waits for the other CTAs.
 template <class P>
 __global__ void __launch_bounds__(tcp::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
@@ -191,21 +223,14 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
     const int m0 = m_tile * P::MV;
-    int t_begin, ntiles;
-    tcp::tile_range(cv, p.nparts, p.n_vtiles, t_begin, ntiles);
+    int c0, c1;
+    tcp::col_range(cv, p.nparts, p.V, c0, c1);
+    const int ntiles = (c1 - c0 + P::BN - 1) / P::BN;
     const int kslabs = p.r / 64;
-    int *ctr_part = p.counters + m_tile, *ctr_fin = p.counters + p.n_mtiles + m_tile;
+    int *ctr = p.counters + m_tile;
 
     // 1. the M-tile's tokens x_{k-1} (one load per row, all in flight together)
-    //    and this CTA's first chunk of h_k for the confidence
-    if (P::KSPLIT == 1 && threadIdx.x < P::MV) s.tok[threadIdx.x] = load_token(p, m0 + threadIdx.x, p.x_prev, p.x_stride, false);
-    const bool conf_row = cv < P::MV && m0 + cv < p.R;
-    const bool pre_ok = conf_row && (p.d & 7) == 0;
-    bool have_pre = pre_ok && threadIdx.x < tcp::kEpiThreads && threadIdx.x < p.d / 8;
-    uint4 pre = make_uint4(0u, 0u, 0u, 0u);
-    if (have_pre)
-        pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (p.k - 1)) * (size_t)p.d +
-                                               threadIdx.x * 8);
+    if (threadIdx.x < P::MV) s.tok[threadIdx.x] = load_token(p, m0 + threadIdx.x, p.x_prev, p.x_stride);
     __syncthreads();  // tokens, barriers, thresholds, TMEM
     P::ready(s);
 
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             tc::prefetch_tmap(&tmU);
         }
         __syncwarp();
-        P::producer(s, &tmB, &tmU, t_begin, ntiles, kslabs, p.nsteps, p.k - 1, m0, p.err);
+        P::producer(s, &tmB, &tmU, c0, ntiles, kslabs, p.nsteps, p.k - 1, m0, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, p.nsteps, p.err);
@@ -232,40 +257,22 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         const bool row_live = grow < p.R;
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         float *mg = P::merge_scratch(s);
+        float *wsc = mg + 5 * tcp::kEpiThreads;  // 80 floats of finalise scratch
         for (int step = 0; step < p.nsteps; ++step) {
             const int k = p.k + step, q = p.step_index + step;
-            if (step > 0) {
-                // x_{k-1} of every row of the M-tile is final once all its CTAs finalised step k-1
-                if (pre_ok && et < p.d / 8)
-                    pre = *reinterpret_cast<const uint4 *>(p.h + ((size_t)(m0 + cv) * p.gamma + (k - 1)) * (size_t)p.d +
-                                                           et * 8);
-                have_pre = pre_ok && et < p.d / 8;
-                if (et == 0) *s.flag = !*s.abort_flag && wait_counter(ctr_fin, (q - 1) * p.nparts, p.err) ? 1 : 0;
-                tc::named_bar_sync(1, tcp::kEpiThreads);
-                if (!*s.flag) {
-                    *s.abort_flag = 1;
-                    break;
-                }
-                if (et < P::MV) s.tok[et] = load_token(p, m0 + et, p.x + (k - 2), p.gamma, true);
-                tc::named_bar_sync(1, tcp::kEpiThreads);
-                gather_operand<P>(p, s, m0, et, tcp::kEpiThreads);
-                P::operand_written(s, et);
-            }
-            // confidences of this CTA's rows (local rows cv, cv + nparts, ...) while
-            // the first tile is in flight
-            for (int i = cv, j = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++j)
-                confidence_row<P>(p, s, k, i, m0 + i, et, s.red, j == 0 && have_pre, pre, P::KSPLIT == 1);
+            DraftPartial *part = p.part + (size_t)(q & 1) * p.R * p.nparts;
+            unsigned long long *win = p.winners + (size_t)(q - 1) * p.R;
 
             RowState st;
             row_init(st);
-            P::epilogue(s, step * ntiles, t_begin, ntiles, p.err,
+            P::epilogue(s, step * ntiles, c0, ntiles, p.err,
                         [&](int, int n0, const uint32_t *acc, const unsigned char *sU) {
                 if (!row_live) return;
                 // the row's best score so far, wherever in the CTA it was found, filters this thread
                 row_raise_thr(st, P::read_thr(s, row));
                 const float best0 = st.best;
                 const int vb = n0 + col0;
-                if (vb + P::CW <= p.V) {
+                if (vb + P::CW <= c1) {
                     // whole block in range: per 16 columns, the Philox words first (independent
                     // chains), then the block
 #pragma unroll
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                         }
                         row_feed_block<16>(st, z, vb + 16 * h, words);
                     }
-                } else {
+                } else if (vb < c1) {
 #pragma unroll
                     for (int g = 0; g < P::CW / 4; ++g) {
                         const int col = col0 + 4 * g;
@@ -298,13 +305,14 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                         const int v0 = n0 + col;
                         const uint4 words =
                             philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), p.rk);
-                        row_feed4<false>(st, z, v0, p.V, words);
+                        row_feed4<false>(st, z, v0, c1, words);
                     }
                 }
                 if (st.best > best0) P::publish_thr(s, row, st.best);
             });
 
-            // merge the TPR threads of each request (fixed warp order) into this CTA's partial
+            // merge the TPR threads of each request (fixed warp order) into this CTA's
+            // partial and fold its winner into the step's per-request maximum
             tc::named_bar_sync(1, tcp::kEpiThreads);  // every warp past its last accumulator
             mg[et] = st.m;
             mg[tcp::kEpiThreads + et] = st.S;
@@ -322,71 +330,41 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                     row_merge(f, mg[src], mg[tcp::kEpiThreads + src], mg[2 * tcp::kEpiThreads + src],
                               mg[3 * tcp::kEpiThreads + src], reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + src]);
                 }
-                p.part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
+                part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
+                if (f.idx >= 0) atomicMax(win + m0 + et, pack_winner(f.best, f.idx));
             }
-
-            // publish, then wait (bounded) until every CTA of the M-tile has published
             __threadfence();
             tc::named_bar_sync(1, tcp::kEpiThreads);
-            if (et == 0) {
-                atomicAdd(ctr_part, 1);
-                *s.flag = wait_counter(ctr_part, q * p.nparts, p.err) ? 1 : 0;
-            }
+            if (et == 0) atomicAdd(ctr, 1);
+
+            // while the other CTAs finish: confidences c_k of this CTA's rows
+            // (local rows cv, cv + nparts, ...; x_{k-1} is still in s.tok)
+            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) confidence_row(p, k, m0 + i, s.tok[i], et, s.red);
+
+            // wait (bounded) until every CTA of the M-tile has published this step
+            if (et == 0) *s.flag = !*s.abort_flag && wait_counter(ctr, q * p.nparts, p.err) ? 1 : 0;
             tc::named_bar_sync(1, tcp::kEpiThreads);
             if (!*s.flag) {
                 *s.abort_flag = 1;
                 break;
             }
-            // every CTA finalises its share of the rows: one partial per thread,
-            // merged in a fixed tree (lanes, then warps in order)
             __threadfence();
-            float *wm = mg + 5 * tcp::kEpiThreads, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
-            int *wi = reinterpret_cast<int *>(wz + 16);
-            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) {
-                const int gr = m0 + i;
-                RowState f;
-                row_init(f);
-                if (et < p.nparts) {
-                    const DraftPartial pq = load_partial_cg(p.part + (size_t)gr * p.nparts + et);
-                    row_merge(f, pq.m, pq.S, pq.best, pq.zbest, pq.idx);
-                }
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float m = __shfl_xor_sync(0xffffffffu, f.m, off);
-                    const float S = __shfl_xor_sync(0xffffffffu, f.S, off);
-                    const float bb = __shfl_xor_sync(0xffffffffu, f.best, off);
-                    const float zb = __shfl_xor_sync(0xffffffffu, f.zbest, off);
-                    const int ix = __shfl_xor_sync(0xffffffffu, f.idx, off);
-                    row_merge(f, m, S, bb, zb, ix);
-                }
-                if (lane == 0) {
-                    wm[warp] = f.m; wS[warp] = f.S; wb[warp] = f.best; wz[warp] = f.zbest; wi[warp] = f.idx;
-                }
-                tc::named_bar_sync(1, tcp::kEpiThreads);
-                if (et == 0) {
-                    RowState g;
-                    row_init(g);
-                    for (int w = 0; w < tcp::kEpiWarps; ++w) row_merge(g, wm[w], wS[w], wb[w], wz[w], wi[w]);
-                    const size_t o = (size_t)gr * p.gamma + (k - 1);
-                    const float lse = g.m + logf(g.S);
-                    int idx = g.idx;
-                    if (idx < 0 || !isfinite(lse)) {
-                        set_err(p.err, DSPARK_ERR_NONFINITE);
-                        idx = 0;
+            if (step + 1 < p.nsteps) {
+                // x_k of the M-tile's rows -> the next operand W_1[x_k], then the MMA warp goes
+                if (et < P::MV) {
+                    int x = -1;
+                    if (m0 + et < p.R) {
+                        x = winner_index(__ldcg(win + m0 + et));
+                        if (x < 0 || x >= p.V) x = 0;  // no winner: reported by the finaliser
                     }
-                    p.x[o] = idx;
-                    p.lse[o] = lse;
-                    p.logq[o] = g.zbest - lse;
+                    s.tok[et] = x;
                 }
                 tc::named_bar_sync(1, tcp::kEpiThreads);
+                gather_operand<P>(p, s, m0, et, tcp::kEpiThreads);
+                P::operand_written(s, et);
             }
-            // rows finalised: the M-tile's next step may gather x_k.  (The barrier
-            // also keeps s.flag from being rewritten before every thread read it.)
-            tc::named_bar_sync(1, tcp::kEpiThreads);
-            if (et == 0) {
-                __threadfence();
-                atomicAdd(ctr_fin, 1);
-            }
+            // finalise this CTA's share of the step's rows (scratch outside the operand)
+            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) finalise_row(p, part, m0 + i, k, et, s.red);
         }
     }
     P::teardown(s);
@@ -418,8 +396,8 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.seed = p.seed; tp.cycle = p.cycle;
     tp.rk = philox_round_keys(p.seed);
     tp.part = p.part; tp.nparts = nparts;
+    tp.winners = p.winners;
     tp.n_mtiles = n_mtiles;
-    tp.n_vtiles = (p.V + P::BN - 1) / P::BN;
     tp.err = p.err;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);

@@ -24,7 +24,7 @@ struct DraftStep {
     const float *A_op;               // RNN: operand of row i at A_op[i * a_stride]
     int a_stride;
     uint64_t seed, cycle;
-    DraftPartial *part;              // [R, nparts]
+    DraftPartial *part;              // [R, nparts] (tensor-core step: [2, R, nparts])
     int nparts;
     int32_t *err;
     // used by the tensor-core step, which also merges the partials and computes
@@ -34,7 +34,8 @@ struct DraftStep {
     const float *w, *sts_T;
     int32_t *x_out;
     float *logq, *lse, *c;
-    int *counters;                   // [2 x number of M-tiles], zero at the start of the call
+    int *counters;                   // [number of M-tiles], zero at the start of the call
+    unsigned long long *winners;     // [gamma, R] packed race winners, zero at the start of the call
     int step_index;                  // 1 for the first step launched since the counters were zeroed
     int nsteps;                      // tensor-core Markov step: steps k .. k + nsteps - 1 in one launch
 };

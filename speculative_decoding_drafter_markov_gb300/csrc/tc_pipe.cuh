@@ -58,8 +58,8 @@ struct Pipe {
     static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
     static constexpr int kOffTok = kOffThr + 4 * MV;        // per-request tokens / metadata
     static constexpr int kOffMisc = kOffTok + 4 * MV;
-    static constexpr int kOffRed = kOffMisc + 64;           // 16-float reduction scratch
-    static constexpr int kBytes = kOffRed + 64 + 1024;      // + alignment slack
+    static constexpr int kOffRed = kOffMisc + 64;           // 80-float reduction scratch
+    static constexpr int kBytes = kOffRed + 320 + 1024;     // + alignment slack
     // scratch for the per-CTA merge after the tile loop: the operand region,
     // which no MMA reads once the last accumulator has been consumed
     static constexpr int kMergeBytes = kEpiThreads * 5 * 4;
@@ -77,7 +77,7 @@ struct Pipe {
         int *tok;          // MV ints of per-request scratch
         uint32_t *tmem_slot;
         volatile int *abort_flag, *flag;
-        float *red;  // 16 floats
+        float *red;  // 80 floats
         uint32_t tmem_base;
     };
 
@@ -182,7 +182,7 @@ struct Pipe {
     // for `nsteps` consecutive draft steps over the same tile range (W_2^T does
     // not depend on the step, so the next step's slabs stream in while the
     // current one is merged); U of step i is position u_k0 + i.
-    __device__ static void producer(State &s, const CUtensorMap *tmB, const CUtensorMap *tmU, int t_begin,
+    __device__ static void producer(State &s, const CUtensorMap *tmB, const CUtensorMap *tmU, int col0,
                                     int ntiles, int kslabs, int nsteps, int u_k0, int m0, int32_t *err) {
         const int lane = threadIdx.x & 31;
         if (lane == 0) {
@@ -192,7 +192,7 @@ struct Pipe {
                 const int slot = g % NS, rem = g % per_step, t = rem / kslabs, j = rem - t * kslabs;
                 if (!tc::mbar_wait(&s.emptyB[slot], ((uint32_t)(g / NS) & 1u) ^ 1u, s.abort_flag, err)) break;
                 tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
-                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, (t_begin + t) * BN);
+                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, col0 + t * BN);
                 ++issued;
             }
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
@@ -207,7 +207,7 @@ struct Pipe {
                 const int st = g % su, step = g / ntiles, t = g - step * ntiles;
                 if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(g / su) & 1u) ^ 1u, s.abort_flag, err)) break;
                 unsigned char *dst = s.smem + kOffU + st * kUBytes;
-                const int n0 = (t_begin + t) * BN;
+                const int n0 = col0 + t * BN;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
                 for (int h = 0; h < BN / 64; ++h)
                     tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k0 + step, m0, pol);
@@ -277,12 +277,12 @@ struct Pipe {
     }
 
     // warps 0..15: per tile, load this warp's CW accumulator columns of its 32
-    // rows and call f(t, n0, acc, sU) (t: tile within this call; n0: first
-    // vocabulary entry of the tile; sU: the tile's U, or null).  Barrier phases
-    // continue from tile number tg0 (the tiles of earlier steps of the launch).
-    // Per-warp flow, no CTA barrier.
+    // rows and call f(t, n0, acc, sU) (t: tile within this call; n0 = col0 +
+    // t BN: first vocabulary entry of the tile; sU: the tile's U, or null).
+    // Barrier phases continue from tile number tg0 (the tiles of earlier steps
+    // of the launch).  Per-warp flow, no CTA barrier.
     template <class F>
-    __device__ static void epilogue(State &s, int tg0, int t_begin, int ntiles, int32_t *err, F &&f) {
+    __device__ static void epilogue(State &s, int tg0, int col0, int ntiles, int32_t *err, F &&f) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const uint32_t taddr0 = s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)epi_col0();
         constexpr int su = SU > 0 ? SU : 1;
@@ -305,7 +305,7 @@ struct Pipe {
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
-            f(t, (t_begin + t) * BN, acc, SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr);
+            f(t, col0 + t * BN, acc, SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr);
             __syncwarp();
             if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
         }
@@ -339,6 +339,14 @@ struct Pipe {
 __device__ __forceinline__ void tile_range(int cv, int nparts, int n_vtiles, int &t_begin, int &ntiles) {
     t_begin = (int)((long long)cv * n_vtiles / nparts);
     ntiles = (int)((long long)(cv + 1) * n_vtiles / nparts) - t_begin;
+}
+
+// vocabulary column range [c0, c1) of CTA cv out of nparts: equal shares with
+// boundaries on multiples of 8 (a TMA box's first column must sit on a 16-byte
+// boundary); tiles of BN columns start at c0, the last one cut at c1
+__device__ __forceinline__ void col_range(int cv, int nparts, int V, int &c0, int &c1) {
+    c0 = (int)(((long long)cv * V / nparts) & ~7ll);
+    c1 = cv + 1 == nparts ? V : (int)(((long long)(cv + 1) * V / nparts) & ~7ll);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     if (warp == tcp::kProducerWarp) {
         if (lane == 0) tc::prefetch_tmap(&tmB);
         __syncwarp();
-        P::producer(s, &tmB, nullptr, t_begin, ntiles, kslabs, 1, 0, m0, p.err);
+        P::producer(s, &tmB, nullptr, t_begin * P::BN, ntiles, kslabs, 1, 0, m0, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, 1, p.err);
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         race_init(res);
         race_init(pr);
         const uint64_t pol = tc::policy_evict_first();  // target and base rows are read once
-        P::epilogue(s, 0, t_begin, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *) {
+        P::epilogue(s, 0, t_begin * P::BN, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *) {
             if (mode < 0) return;
             const int vb = n0 + col0;
             // this block of the target row (and of U_{n+1}), 8 columns per load; V % 8 == 0
