@@ -43,12 +43,17 @@ __global__ void verify_init(int R, int gamma, VerifyWs w) {
 template <typename T>
 __device__ __forceinline__ void feed_lse(float &m, float &S, const float *x, int n) {
     float cm = -INFINITY;
+#pragma unroll
     for (int j = 0; j < n; ++j) cm = fmaxf(cm, x[j]);
     if (cm > m) {
         S *= ex2((m - cm) * kLog2e);
         m = cm;
     }
-    for (int j = 0; j < n; ++j) S += ex2((x[j] - m) * kLog2e);
+    const float mL = m * kLog2e;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < n; ++j) acc += ex2(fmaf(x[j], kLog2e, -mL));
+    S += acc;
 }
 
 template <typename T>
@@ -75,7 +80,24 @@ __global__ void __launch_bounds__(256) verify_phase1(const dspark_verify_args a,
         const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
         const int nv = a.V / kVec;
         const uint64_t pol = tc::policy_evict_first();  // each target row is read once here
-        for (int c = tid; c < nv; c += blockDim.x) {
+        // kLoads 16-byte loads in flight per thread, then one max / rescale for all of them
+        constexpr int kLoads = 4;
+        const int step = kLoads * (int)blockDim.x;
+        int c0 = tid;
+        for (; c0 + (kLoads - 1) * (int)blockDim.x < nv; c0 += step) {
+            uint4 raw[kLoads];
+#pragma unroll
+            for (int q = 0; q < kLoads; ++q) raw[q] = tc::ld_global_hint(row4 + c0 + q * blockDim.x, pol);
+            float x[kLoads * kVec];
+#pragma unroll
+            for (int q = 0; q < kLoads; ++q) {
+                const T *vals = reinterpret_cast<const T *>(&raw[q]);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) x[q * kVec + j] = to_f32(vals[j]);
+            }
+            feed_lse<T>(m, S, x, kLoads * kVec);
+        }
+        for (int c = c0; c < nv; c += blockDim.x) {
             const uint4 raw = tc::ld_global_hint(row4 + c, pol);
             const T *vals = reinterpret_cast<const T *>(&raw);
             float x[kVec];
