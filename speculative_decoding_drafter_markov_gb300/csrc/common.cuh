@@ -334,6 +334,31 @@ __device__ __forceinline__ void race_feed(Race &r, float w, float t, int v) {
     }
 }
 
+// Four consecutive entries v0..v0+3 of one race (weights w[i] >= 0, words
+// from one Philox call): the filter for all four first, then the rare
+// survivors scored exactly in index order.
+__device__ __forceinline__ void race_feed4(Race &r, const float (&w)[4], const uint4 &words, int v0) {
+    unsigned pass = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float t = one_minus_uniform(word_lane(words, i));
+        if (w[i] > 0.f && t < w[i] * r.C) pass |= 1u << i;
+    }
+    if (pass) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (pass & (1u << i)) {
+                const float score = kLn2 * lg2(w[i]) - log_exp_variate(one_minus_uniform(word_lane(words, i)));
+                if (score > r.best) {
+                    r.best = score;
+                    r.idx = v0 + i;
+                    r.C = ex2(-r.best * kLog2e) * kRaceSlack;
+                }
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void race_merge(float &best, int &idx, float b2, int i2) {
     if (i2 >= 0 && (idx < 0 || b2 > best || (b2 == best && i2 < idx))) {
         best = b2;

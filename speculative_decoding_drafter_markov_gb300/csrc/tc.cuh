@@ -137,10 +137,15 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
 // 16-byte global load with an L2 cache policy
 __device__ __forceinline__ uint4 ld_global_hint(const void *ptr, uint64_t policy) {
     uint4 v;
-    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(policy));
+    asm("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "l"(policy));
     return v;
+}
+
+// start pulling the line that holds `ptr` into L2
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {

@@ -291,6 +291,45 @@ __global__ void __launch_bounds__(256) verify_final(const dspark_verify_args a, 
         }
         __syncthreads();
     }
+    // A rejected position whose residual max(0, p - q) came out empty (p equal to
+    // q to rounding everywhere) samples p instead, with the same stream-2 noise:
+    // when the slices did not run that race, this CTA runs it over the whole row.
+    __shared__ int s_fallback;
+    if (tid == 0) {
+        const int ell = w.ell[rq];
+        s_fallback = ell >= 0 && w.first_rej[rq] < ell && s_i1[0] < 0 && s_i2[0] < 0;
+    }
+    __syncthreads();
+    if (s_fallback) {
+        const int n = w.first_rej[rq];
+        const int row = w.row_of[rq * (a.gamma + 1) + n];
+        Race pr;
+        race_init(pr);
+        if (row >= 0) {
+            const float lsep = w.lse_p[row] * kLog2e;
+            const PhiloxKey key = philox_key(a.seed);
+            const uint32_t c3 = philox_ctr3(a.cycle, 2);
+            for (int v0 = 4 * tid; v0 < a.V; v0 += 4 * blockDim.x) {
+                const uint4 words =
+                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), key);
+                for (int j = 0; j < 4 && v0 + j < a.V; ++j) {
+                    const size_t at = (size_t)row * a.V + v0 + j;
+                    const float tv = a.dtype == DSPARK_BF16
+                                         ? __bfloat162float(static_cast<const __nv_bfloat16 *>(a.T)[at])
+                                         : static_cast<const float *>(a.T)[at];
+                    race_feed(pr, ex2(fmaf(tv, kLog2e, -lsep)), one_minus_uniform(word_lane(words, j)), v0 + j);
+                }
+            }
+        }
+        __syncthreads();
+        s_b2[tid] = pr.best;
+        s_i2[tid] = pr.idx;
+        __syncthreads();
+        for (int half = blockDim.x / 2; half > 0; half >>= 1) {
+            if (tid < half) race_merge(s_b2[tid], s_i2[tid], s_b2[tid + half], s_i2[tid + half]);
+            __syncthreads();
+        }
+    }
     if (tid != 0) return;
     const int ell = w.ell[rq];
     int32_t *out = a.out_tokens + (size_t)rq * (a.gamma + 1);

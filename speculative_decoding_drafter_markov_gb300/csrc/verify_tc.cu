@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                 const float tv[4] = {tcp::bf16_lo(t0), tcp::bf16_hi(t0), tcp::bf16_lo(t1), tcp::bf16_hi(t1)};
                 const uint4 words =
                     philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), p.rk);
-                float pv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
+                // rejected position: race over the residual max(0, p - q) only (the race
+                // over p is its fallback for an empty residual and is run by the final
+                // kernel in that case); bonus position: race over p
+                float wv[4];
                 if (mode == 1) {
                     const uint4 &uu = uq[g >> 1];
                     const uint32_t u0 = (g & 1) ? uu.z : uu.x, u1 = (g & 1) ? uu.w : uu.y;
@@ -166,16 +167,13 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                                          __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(u1),
                                          __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(u1)};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float t = one_minus_uniform(word_lane(words, i));
-                        const float q = ex2(fmaf(zv[i], kLog2e, -lseq));
-                        race_feed(res, fmaxf(pv[i] - q, 0.f), t, v0 + i);
-                        race_feed(pr, pv[i], t, v0 + i);
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        wv[i] = fmaxf(ex2(fmaf(tv[i], kLog2e, -lsep)) - ex2(fmaf(zv[i], kLog2e, -lseq)), 0.f);
+                    race_feed4(res, wv, words, v0);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        race_feed(pr, pv[i], one_minus_uniform(word_lane(words, i)), v0 + i);
+                    for (int i = 0; i < 4; ++i) wv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
+                    race_feed4(pr, wv, words, v0);
                 }
             }
         });
