@@ -260,6 +260,12 @@ class Cycle:
         return self.wl.R * self.wl.gamma
 
 
+# DRAM bytes (read + write) of one draft launch from the committed ncu capture
+# (profiles/draft_step_tc_qwen4b.md); only for the kernel version that capture
+# measured -- set to None whenever the draft kernel changes
+DRAFT_TRAFFIC_NCU = {"qwen4b": 262_230_784 + 3_811_328}
+
+
 def draft_step_bytes(wl, with_w2=True):
     """Algorithmic bytes of one draft step: U_k rows, W_2 streamed once, the
     gathered W_1 rows, h_k and w (fp32)."""
@@ -303,6 +309,7 @@ def run_dspark(args, world, rank, local):
     mk = lambda: torch.cuda.Event(enable_timing=True)
     events = [{"a": mk(), "b": mk(), "d": mk(), "s": mk(), "g": mk()} for _ in range(args.steps)]
     clocks = ClockSampler(local)
+    accepted_dev = torch.zeros((), dtype=torch.int64, device=dev)  # sum of (n_accept + 1)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -314,6 +321,7 @@ def run_dspark(args, world, rank, local):
         ev["a"].record(stream)
         one_cycle(args.warmup + s, ev)
         ev["b"].record(stream)
+        accepted_dev += cyc.vout["n_accept"].sum() + wl.R  # outside the timed span
         if cyc.sched:
             torch.cuda.synchronize()
             verified += cyc.verified_tokens()
@@ -335,6 +343,7 @@ def run_dspark(args, world, rank, local):
         total_ms = float(t.item())
     drafted = args.steps * wl.R * gm
     value = world * drafted / (total_ms / 1e3)
+    accepted = int(accepted_dev.item())
 
     hbm, tc, peak_kind = _peaks()
     draft_us = 1e3 * statistics.mean(t_draft)
@@ -354,6 +363,9 @@ def run_dspark(args, world, rank, local):
                    "parallelism": f"replicas x{world} (requests independent)"},
         "drafted_tok_s": world * drafted / (sum(t_draft) / 1e3),
         "verified_tok_s": world * verified / ((sum(t_sched) + sum(t_verify)) / 1e3),
+        "accepted_tok_s": world * accepted / (total_ms / 1e3),
+        "mean_tau": accepted / (args.steps * wl.R),
+        "mean_ell": verified / (args.steps * wl.R),
         "stage_us": {"draft": draft_us,
                      "draft_step": draft_us / gm,
                      "schedule": 1e3 * statistics.mean(t_sched),
@@ -367,7 +379,8 @@ def run_dspark(args, world, rank, local):
                      "algorithmic_bytes_per_launch": bytes_launch,
                      "bytes_rule": "per step: U_k + W_2 + W_1 rows + h_k + w; x gamma steps",
                      "timing": "CUDA events around the whole draft call",
-                     "traffic": None},
+                     "traffic": DRAFT_TRAFFIC_NCU.get(wl.name),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"},
         "roofline_w2_once_per_cycle": {"achieved": strict, "peak": hbm, "unit": "GB/s",
                                        "frac": strict / hbm,
                                        "algorithmic_bytes_per_launch": draft_cycle_bytes_strict(wl)},

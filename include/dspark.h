@@ -251,6 +251,18 @@ DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_strea
 DSPARK_API const char *dspark_last_error(void);
 /* Library version as major * 10000 + minor * 100 + patch. */
 DSPARK_API int dspark_version(void);
+/* Self-check of the device-side failure detection (no counterpart in the
+ * pages).  Every spin-wait in the tensor-core kernels -- a CTA waiting for the
+ * other CTAs of its M-tile, a role waiting on an mbarrier -- gives up after a
+ * wall-clock limit, writes DSPARK_ERR_TIMEOUT into the error word and returns.
+ * This call runs the same two waits on a condition that nothing satisfies
+ * unless the caller set it: mode 0 waits for *flag >= target (a device int32);
+ * mode 1 waits on a fresh mbarrier that completes only when target <= 0.
+ * limit_ns in (0, 2e9].  After the stream reaches it, *err holds
+ * DSPARK_ERR_TIMEOUT if the wait ran out, else it is unchanged. */
+DSPARK_API int dspark_wait_selfcheck(const int32_t *flag, int32_t target, int32_t mode, uint64_t limit_ns,
+                                     int32_t *err, dspark_stream_t stream);
+
 /* Philox-4x32-10 on the device: out[i][0..3] for counters ctr[i][0..3] and
  * key (seed lo, seed hi), i < n.  Exposes the sampler's generator for checks. */
 DSPARK_API int dspark_philox(const uint32_t *ctr, uint64_t seed, int32_t n, uint32_t *out,

@@ -75,6 +75,7 @@ SYMBOLS = {
     "dspark_last_error": ([], ctypes.c_char_p),
     "dspark_version": ([], ctypes.c_int),
     "dspark_philox": ([P, u64, i32, P, P], ctypes.c_int),
+    "dspark_wait_selfcheck": ([P, i32, i32, u64, P, P], ctypes.c_int),
 }
 
 
@@ -330,3 +331,10 @@ def philox(ctr, seed, stream=None):
     out = torch.empty((n, 4), dtype=torch.int32, device=ctr.device)
     _check(L.dspark_philox(_ptr(ctr), int(seed), n, _ptr(out), _stream(stream)))
     return out
+
+
+def wait_selfcheck(flag, target, mode, limit_ns, err, stream=None):
+    """Run the kernels' bounded wait on `flag` (see include/dspark.h)."""
+    L = load()
+    _check(L.dspark_wait_selfcheck(_ptr(flag), int(target), int(mode), int(limit_ns), _ptr(err),
+                                   _stream(stream)))

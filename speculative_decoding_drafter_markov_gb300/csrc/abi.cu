@@ -365,6 +365,17 @@ DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_strea
     return ok();
 }
 
+DSPARK_API int dspark_wait_selfcheck(const int32_t *flag, int32_t target, int32_t mode, uint64_t limit_ns,
+                                     int32_t *err, dspark_stream_t stream) {
+    if (!flag || !err) return fail(DSPARK_ERR_INVAL, "null pointer");
+    if (mode != 0 && mode != 1) return fail(DSPARK_ERR_INVAL, "bad mode %d", mode);
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return fail(DSPARK_ERR_INVAL, "limit outside (0, 2 s]");
+    cudaError_t e = dspark::launch_wait_selfcheck(flag, target, mode, limit_ns, err,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-check");
+    return ok();
+}
+
 DSPARK_API int dspark_philox(const uint32_t *ctr, uint64_t seed, int32_t n, uint32_t *out,
                              dspark_stream_t stream) {
     if (n < 0 || (n > 0 && (!ctr || !out))) return fail(DSPARK_ERR_INVAL, "bad philox arguments");

@@ -94,10 +94,11 @@ __device__ __forceinline__ int ld_acquire(const int *ptr) {
 }
 
 // bounded wait until *ctr >= target (a counter other CTAs of the launch raise)
-__device__ __forceinline__ bool wait_counter(const int *ctr, int target, int32_t *err) {
+__device__ __forceinline__ bool wait_counter(const int *ctr, int target, int32_t *err,
+                                             uint64_t limit_ns = tc::kWaitLimitNs) {
     const uint64_t t0 = tc::globaltimer_ns();
     while (ld_acquire(ctr) < target) {
-        if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+        if (tc::globaltimer_ns() - t0 > limit_ns) {
             set_err(err, DSPARK_ERR_TIMEOUT);
             return false;
         }
@@ -370,10 +371,30 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     P::teardown(s);
 }
 
+// Self-check of the two bounded waits the tensor-core kernels use, on a
+// condition that nothing satisfies unless the caller set it: mode 0 waits for
+// *flag >= target like the cross-CTA counter waits; mode 1 waits on an
+// mbarrier phase that completes only when target <= 0 (one arrival), like the
+// pipeline waits.  Either returns after limit_ns with DSPARK_ERR_TIMEOUT in
+// *err instead of hanging.
+__global__ void wait_selfcheck_kernel(const int *flag, int target, int mode, uint64_t limit_ns, int32_t *err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (mode == 0) {
+        wait_counter(flag, target, err, limit_ns);
+        return;
+    }
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+    if (target <= 0) tc::mbar_arrive(&bar);
+    tc::mbar_wait(&bar, 0u, &abort_flag, err, limit_ns);
+}
+
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
-using DraftM64 = tcp::Pipe<64, 128, 8, 2, 1>;   // Markov, R <= 64
-using DraftM128 = tcp::Pipe<128, 64, 12, 3, 1>; // Markov, 128 requests per M-tile
+using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;   // Markov, R <= 64
+using DraftM128 = tcp::Pipe<128, 64, 8, 6, 1>;  // Markov, 128 requests per M-tile
 using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -488,6 +509,12 @@ void draft_step_tc_shape(int R, int V, bool rnn, int *nparts, int *n_mtiles) {
     if (rnn) tc_grid_shape(R, V, DraftRnn::MV, DraftRnn::BN, nparts, n_mtiles);
     else if (R <= 64) tc_grid_shape(R, V, DraftM64::MV, DraftM64::BN, nparts, n_mtiles);
     else tc_grid_shape(R, V, DraftM128::MV, DraftM128::BN, nparts, n_mtiles);
+}
+
+cudaError_t launch_wait_selfcheck(const int *flag, int target, int mode, uint64_t limit_ns, int32_t *err,
+                                  cudaStream_t s) {
+    wait_selfcheck_kernel<<<1, 1, 0, s>>>(flag, target, mode, limit_ns, err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_draft_step_tc(const DraftStep &p, cudaStream_t s) {

@@ -45,6 +45,8 @@ cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
 bool draft_step_tc_supported(const DraftStep &p);
 void draft_step_tc_shape(int R, int V, bool rnn, int *nparts, int *n_mtiles);
 cudaError_t launch_draft_step_tc(const DraftStep &p, cudaStream_t s);
+cudaError_t launch_wait_selfcheck(const int *flag, int target, int mode, uint64_t limit_ns, int32_t *err,
+                                  cudaStream_t s);
 // shared tensor-core helpers
 int sm_count();
 bool tc_available();

@@ -59,14 +59,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // raises the CTA's abort flag and reports DSPARK_ERR_TIMEOUT) or when another
 // role already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *err) {
+                                          int32_t *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0u) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            if (globaltimer_ns() - t0 > limit_ns) break;
             __nanosleep(64);
         }
     }
