@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(256) rnn_hproj_kernel(int M, int d, int r, con
 // of the three gates for requests q0 .. q0 + RB - 1: the 3 IB rows of W and the
 // RB vectors z are staged in shared memory as fp32 (rows padded by one word,
 // so the lanes of a warp read distinct banks), one thread per (request, i).
+// Rows are padded by 4 words: 16-byte aligned for vector reads, and the 8
+// weight rows of a warp start 4 banks apart.
 // The state is double-buffered (s_in -> s_out) since every CTA reads whole
 // rows of s_{k-1}.
 constexpr int kRnnIB = 8;
@@ -207,34 +209,76 @@ constexpr int kRnnIB = 8;
 template <typename T, int RB>
 __global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) {
     extern __shared__ float sh[];
-    const int r = p.r, K = 2 * r, ld = K + 1;
+    const int r = p.r, K = 2 * r, ld = K + 4;
     float *Ws = sh;                    // [3 IB][K + 1]: rows g r + i0 + ii, g = gate
     float *Zs = sh + 3 * kRnnIB * ld;  // [RB][K + 1]
     const int i0 = blockIdx.x * kRnnIB, q0 = blockIdx.y * RB;
     const int ldw = 2 * r + p.d;
     const T *W = static_cast<const T *>(p.W);
     const T *W1 = static_cast<const T *>(p.W1);
-    for (int e = threadIdx.x; e < 3 * kRnnIB * K; e += blockDim.x) {
-        const int row = e / K, j = e - row * K;
-        const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
-        Ws[row * ld + j] = i < r ? to_f32(W[(size_t)(g * r + i) * ldw + j]) : 0.f;
+    __shared__ int s_xp[RB];
+    if (threadIdx.x < RB) {
+        const int rq = q0 + threadIdx.x;
+        int xp = rq < p.R ? p.x_prev[(size_t)rq * p.x_stride] : 0;
+        if (xp < 0 || xp >= p.V) {
+            if (rq < p.R) set_err(p.err, DSPARK_ERR_RANGE);
+            xp = 0;
+        }
+        s_xp[threadIdx.x] = xp;
     }
-    for (int e = threadIdx.x; e < RB * K; e += blockDim.x) {
-        const int q = e / K, j = e - q * K, rq = q0 + q;
-        float v = 0.f;
-        if (rq < p.R) {
-            if (j < r) {
-                v = p.s_in[(size_t)rq * r + j];
+    __syncthreads();
+    constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
+    if (r % kVec == 0 && ldw % kVec == 0) {
+        // 16-byte loads, several in flight per thread (the loops are unrolled)
+        const int cpr = K / kVec;  // chunks per staged row
+#pragma unroll 4
+        for (int e = threadIdx.x; e < 3 * kRnnIB * cpr; e += blockDim.x) {
+            const int row = e / cpr, c = e - row * cpr;
+            const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
+            float *dst = Ws + row * ld + c * kVec;
+            if (i < r) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(W + (size_t)(g * r + i) * ldw + c * kVec);
+                const T *vals = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) dst[k] = to_f32(vals[k]);
             } else {
-                int xp = p.x_prev[(size_t)rq * p.x_stride];
-                if (xp < 0 || xp >= p.V) {
-                    if (j == r) set_err(p.err, DSPARK_ERR_RANGE);
-                    xp = 0;
-                }
-                v = to_f32(W1[(size_t)xp * r + (j - r)]);
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) dst[k] = 0.f;
             }
         }
-        Zs[q * ld + j] = v;
+#pragma unroll 4
+        for (int e = threadIdx.x; e < RB * cpr; e += blockDim.x) {
+            const int q = e / cpr, c = e - q * cpr, rq = q0 + q, j = c * kVec;
+            float *dst = Zs + q * ld + j;
+            if (rq >= p.R) {
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) dst[k] = 0.f;
+            } else if (j < r) {
+                const float *src = p.s_in + (size_t)rq * r + j;
+#pragma unroll
+                for (int k = 0; k < kVec; k += 4) {
+                    const float4 f = *reinterpret_cast<const float4 *>(src + k);
+                    dst[k] = f.x; dst[k + 1] = f.y; dst[k + 2] = f.z; dst[k + 3] = f.w;
+                }
+            } else {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(W1 + (size_t)s_xp[q] * r + (j - r));
+                const T *vals = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) dst[k] = to_f32(vals[k]);
+            }
+        }
+    } else {
+        for (int e = threadIdx.x; e < 3 * kRnnIB * K; e += blockDim.x) {
+            const int row = e / K, j = e - row * K;
+            const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
+            Ws[row * ld + j] = i < r ? to_f32(W[(size_t)(g * r + i) * ldw + j]) : 0.f;
+        }
+        for (int e = threadIdx.x; e < RB * K; e += blockDim.x) {
+            const int q = e / K, j = e - q * K, rq = q0 + q;
+            float v = 0.f;
+            if (rq < p.R) v = j < r ? p.s_in[(size_t)rq * r + j] : to_f32(W1[(size_t)s_xp[q] * r + (j - r)]);
+            Zs[q * ld + j] = v;
+        }
     }
     __syncthreads();
     const int q = threadIdx.x / kRnnIB, ii = threadIdx.x - q * kRnnIB;
@@ -242,7 +286,17 @@ __global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) 
     const float *z = Zs + q * ld;
     const float *wg = Ws + ii * ld, *wc = Ws + (kRnnIB + ii) * ld, *wo = Ws + (2 * kRnnIB + ii) * ld;
     float gg = 0.f, gc = 0.f, go = 0.f;
-    for (int j = 0; j < K; ++j) {
+    int j = 0;
+    for (; j + 4 <= K; j += 4) {
+        const float4 zv = *reinterpret_cast<const float4 *>(z + j);
+        const float4 a = *reinterpret_cast<const float4 *>(wg + j);
+        const float4 b = *reinterpret_cast<const float4 *>(wc + j);
+        const float4 c = *reinterpret_cast<const float4 *>(wo + j);
+        gg = fmaf(a.x, zv.x, gg); gg = fmaf(a.y, zv.y, gg); gg = fmaf(a.z, zv.z, gg); gg = fmaf(a.w, zv.w, gg);
+        gc = fmaf(b.x, zv.x, gc); gc = fmaf(b.y, zv.y, gc); gc = fmaf(b.z, zv.z, gc); gc = fmaf(b.w, zv.w, gc);
+        go = fmaf(c.x, zv.x, go); go = fmaf(c.y, zv.y, go); go = fmaf(c.z, zv.z, go); go = fmaf(c.w, zv.w, go);
+    }
+    for (; j < K; ++j) {
         const float zj = z[j];
         gg = fmaf(wg[j], zj, gg);
         gc = fmaf(wc[j], zj, gc);
@@ -302,7 +356,7 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
 
 template <typename T, int RB>
 static cudaError_t launch_rnn_step_t(const RnnStep &p, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 1);
+    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 4);
     auto kern = rnn_step_kernel<T, RB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
