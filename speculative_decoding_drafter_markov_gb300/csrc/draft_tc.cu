@@ -158,19 +158,23 @@ __device__ __forceinline__ void gather_operand(const TcParams &p, const typename
     }
 }
 
-// Finalise row gr of step k from its nparts partials (one per thread, merged
-// in a fixed tree: lanes, then warps in order): x_k, lse_k, log q_k(x_k).
-__device__ __forceinline__ void finalise_row(const TcParams &p, const DraftPartial *part, int gr, int k, int et,
-                                             float *wsc) {
-    const int warp = et >> 5, lane = et & 31;
-    float *wm = wsc, *wS = wm + 16, *wb = wS + 16, *wz = wb + 16;
-    int *wi = reinterpret_cast<int *>(wz + 16);
+// Finalise row gr of step k from its nparts partials, by one warp (lanes stride
+// over the partials, then a fixed shuffle tree): x_k, lse_k, log q_k(x_k),
+// written by lane 0.
+__device__ __forceinline__ void finalise_row(const TcParams &p, const DraftPartial *part, int gr, int k, int lane) {
     RowState f;
     row_init(f);
-    for (int i = et; i < p.nparts; i += tcp::kEpiThreads) {
-        const DraftPartial pq = load_partial_cg(part + (size_t)gr * p.nparts + i);
-        row_merge(f, pq.m, pq.S, pq.best, pq.zbest, pq.idx);
+    // all of a lane's partials in flight at once (nparts <= 8 x 32), then merged in order
+    constexpr int kPer = 8;
+    DraftPartial pq[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int i = lane + 32 * q;
+        if (i < p.nparts) pq[q] = load_partial_cg(part + (size_t)gr * p.nparts + i);
     }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+        if (lane + 32 * q < p.nparts) row_merge(f, pq[q].m, pq[q].S, pq[q].best, pq[q].zbest, pq[q].idx);
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float m = __shfl_xor_sync(0xffffffffu, f.m, off);
@@ -181,25 +185,17 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
         row_merge(f, m, S, bb, zb, ix);
     }
     if (lane == 0) {
-        wm[warp] = f.m; wS[warp] = f.S; wb[warp] = f.best; wz[warp] = f.zbest; wi[warp] = f.idx;
-    }
-    tc::named_bar_sync(1, tcp::kEpiThreads);
-    if (et == 0) {
-        RowState g;
-        row_init(g);
-        for (int w = 0; w < tcp::kEpiWarps; ++w) row_merge(g, wm[w], wS[w], wb[w], wz[w], wi[w]);
         const size_t o = (size_t)gr * p.gamma + (k - 1);
-        const float lse = g.m + logf(g.S);
-        int idx = g.idx;
+        const float lse = f.m + logf(f.S);
+        int idx = f.idx;
         if (idx < 0 || !isfinite(lse)) {
             set_err(p.err, DSPARK_ERR_NONFINITE);
             idx = 0;
         }
         p.x[o] = idx;
         p.lse[o] = lse;
-        p.logq[o] = g.zbest - lse;
+        p.logq[o] = f.zbest - lse;
     }
-    tc::named_bar_sync(1, tcp::kEpiThreads);
 }
 
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
@@ -365,7 +361,8 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                 P::operand_written(s, et);
             }
             // finalise this CTA's share of the step's rows (scratch outside the operand)
-            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) finalise_row(p, part, m0 + i, k, et, s.red);
+            for (int i = cv, n = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++n)
+                if (warp == n % tcp::kEpiWarps) finalise_row(p, part, m0 + i, k, lane);
         }
     }
     P::teardown(s);
