@@ -62,6 +62,18 @@ def _dist():
     return world, rank, local
 
 
+def aggregate_ranks(local_ms, local_units, world, device):
+    """Whole-job figures of a weak-scaling run: the timed span is the maximum
+    over ranks, the work is every rank's (each rank runs its own replica of the
+    workload).  Returns (max_ms, units per second summed over ranks)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * local_units / (total_ms / 1e3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -336,13 +348,8 @@ def run_dspark(args, world, rank, local):
     t_verify = [e["g"].elapsed_time(e["b"]) for e in events]
     # cycle time without the harness's target-row gather
     t_cycle = [a + b + c for a, b, c in zip(t_draft, t_sched, t_verify)]
-    total_ms = sum(t_cycle)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     drafted = args.steps * wl.R * gm
-    value = world * drafted / (total_ms / 1e3)
+    total_ms, value = aggregate_ranks(sum(t_cycle), drafted, world, dev)
     accepted = int(accepted_dev.item())
 
     hbm, tc, peak_kind = _peaks()
