@@ -251,20 +251,18 @@ __device__ __forceinline__ void row_feed_block(RowState &s, const float (&z)[N],
         if (!(t >= e[j] * s.C)) pass |= 1u << j;
     }
     if (pass) {
-        // survivors scored exactly in index order; the filter constant is
-        // refreshed once after the block (it only filters the next blocks)
-        const float best0 = s.best;
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             if (pass & (1u << j)) {
                 const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
-                const bool better = score > s.best;
-                s.best = better ? score : s.best;
-                s.idx = better ? v0 + j : s.idx;
-                s.zbest = better ? z[j] : s.zbest;
+                if (score > s.best) {
+                    s.best = score;
+                    s.idx = v0 + j;
+                    s.zbest = z[j];
+                    row_raise_thr(s, score);
+                }
             }
         }
-        if (s.best > best0) row_raise_thr(s, s.best);
     }
 }
 

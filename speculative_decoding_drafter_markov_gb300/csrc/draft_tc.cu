@@ -164,17 +164,20 @@ __device__ __forceinline__ void gather_operand(const TcParams &p, const typename
 __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftPartial *part, int gr, int k, int lane) {
     RowState f;
     row_init(f);
-    // all of a lane's partials in flight at once (nparts <= 8 x 32), then merged in order
-    constexpr int kPer = 8;
-    DraftPartial pq[kPer];
+    // a lane's partials four at a time: the loads of a batch in flight together,
+    // then merged in order
+    constexpr int kBatch = 4;
+    for (int q0 = 0; lane + 32 * q0 < p.nparts; q0 += kBatch) {
+        DraftPartial pq[kBatch];
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        const int i = lane + 32 * q;
-        if (i < p.nparts) pq[q] = load_partial_cg(part + (size_t)gr * p.nparts + i);
+        for (int q = 0; q < kBatch; ++q) {
+            const int i = lane + 32 * (q0 + q);
+            if (i < p.nparts) pq[q] = load_partial_cg(part + (size_t)gr * p.nparts + i);
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            if (lane + 32 * (q0 + q) < p.nparts) row_merge(f, pq[q].m, pq[q].S, pq[q].best, pq[q].zbest, pq[q].idx);
     }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q)
-        if (lane + 32 * q < p.nparts) row_merge(f, pq[q].m, pq[q].S, pq[q].best, pq[q].zbest, pq[q].idx);
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float m = __shfl_xor_sync(0xffffffffu, f.m, off);
