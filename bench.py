@@ -229,9 +229,9 @@ class Cycle:
         self.vws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         # library kernels per cycle: the gamma Markov draft steps (one launch) or,
         # RNN head, the h projection then per step the state update and the step;
-        # schedule + build_tags; verify (init, phase 1, phase 2, final)
+        # schedule + build_tags; verify (init, phase 1, phase 2 with the final merge)
         n_draft = 1 + 2 * gm if self.rnn else 1
-        self.launches_per_cycle = n_draft + 4 + (2 if self.sched else 0)
+        self.launches_per_cycle = n_draft + 3 + (2 if self.sched else 0)
 
     def draft(self, cycle):
         i = self.inp

@@ -111,8 +111,10 @@ struct VerifyWs {
     int32_t *ell;          // [R]
     int32_t *row_of;       // [R, gamma + 1]
     VerifyPartial *part;   // [R, nparts]
+    int *done;             // [kVerifyMaxMTiles] CTAs of an M-tile that published (tensor-core phase 2)
     int nparts;
 };
+constexpr int kVerifyMaxMTiles = 64;
 size_t verify_ws_bytes(int R, int gamma, int V, int N);
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N);
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s);

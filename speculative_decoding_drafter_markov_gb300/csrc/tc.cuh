@@ -90,6 +90,27 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     return false;
 }
 
+// ---------------------------------------------------------------- cross-CTA counters
+__device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// bounded wait until *ctr >= target (a counter other CTAs of the launch raise)
+__device__ __forceinline__ bool wait_counter_ge(const int *ctr, int target, int32_t *err,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(ctr) < target) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            set_err(err, DSPARK_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- proxies, barriers
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

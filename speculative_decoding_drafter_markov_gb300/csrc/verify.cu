@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "verify_common.cuh"
 
 namespace dspark {
 
@@ -34,6 +35,7 @@ constexpr int kNone = 0x7fffffff;
 __global__ void verify_init(int R, int gamma, VerifyWs w) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < R * (gamma + 1)) w.row_of[i] = -1;
+    if (i < kVerifyMaxMTiles) w.done[i] = 0;
     if (i < R) {
         w.first_rej[i] = kNone;
         w.ell[i] = -1;
@@ -331,26 +333,7 @@ __global__ void __launch_bounds__(256) verify_final(const dspark_verify_args a, 
         }
     }
     if (tid != 0) return;
-    const int ell = w.ell[rq];
-    int32_t *out = a.out_tokens + (size_t)rq * (a.gamma + 1);
-    if (ell < 0) {
-        a.n_accept[rq] = 0;
-        for (int j = 0; j <= a.gamma; ++j) out[j] = -1;
-        a.next_anchor[rq] = -1;
-        return;
-    }
-    const int fr = w.first_rej[rq];
-    const bool residual = fr < ell;
-    const int n = residual ? fr : ell;
-    int y = (residual && s_i1[0] >= 0) ? s_i1[0] : s_i2[0];
-    if (y < 0) {
-        set_err(a.err, DSPARK_ERR_NONFINITE);
-        y = 0;
-    }
-    a.n_accept[rq] = n;
-    for (int j = 0; j <= a.gamma; ++j)
-        out[j] = j < n ? a.x[(size_t)rq * a.gamma + j] : (j == n ? y : -1);
-    a.next_anchor[rq] = y;
+    write_outcome(a, w, rq, s_i1[0], s_i2[0]);
 }
 
 template <typename T, bool kRnn>
@@ -369,7 +352,7 @@ size_t verify_ws_bytes(int R, int gamma, int V, int N) {
     const int nparts = (V + kSliceV - 1) / kSliceV;
     return align256(sizeof(float) * (size_t)N) + align256(sizeof(int32_t) * (size_t)R) * 2 +
            align256(sizeof(int32_t) * (size_t)R * (gamma + 1)) +
-           align256(sizeof(VerifyPartial) * (size_t)R * nparts);
+           align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles);
 }
 
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
@@ -385,11 +368,13 @@ VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
     w.row_of = reinterpret_cast<int32_t *>(p);
     p += align256(sizeof(int32_t) * (size_t)R * (gamma + 1));
     w.part = reinterpret_cast<VerifyPartial *>(p);
+    p += align256(sizeof(VerifyPartial) * (size_t)R * w.nparts);
+    w.done = reinterpret_cast<int *>(p);
     return w;
 }
 
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s) {
-    const int n_init = a.R * (a.gamma + 1);
+    const int n_init = a.R * (a.gamma + 1) > kVerifyMaxMTiles ? a.R * (a.gamma + 1) : kVerifyMaxMTiles;
     verify_init<<<(n_init + 255) / 256, 256, 0, s>>>(a.R, a.gamma, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -403,9 +388,12 @@ cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaSt
     }
     const bool rnn = a.A != nullptr;
     VerifyWs wf = w;  // the tensor-core path sets its own partial count
-    if (verify_tc_supported(a))
+    if (verify_tc_supported(a)) {
+        // the last CTA of each M-tile merges the slices and writes the outcome itself
         e = launch_verify_phase2_tc(a, wf, s);
-    else if (a.dtype == DSPARK_BF16)
+        return e;
+    }
+    if (a.dtype == DSPARK_BF16)
         e = rnn ? launch_phase2<__nv_bfloat16, true>(a, w, s) : launch_phase2<__nv_bfloat16, false>(a, w, s);
     else
         e = rnn ? launch_phase2<float, true>(a, w, s) : launch_phase2<float, false>(a, w, s);

@@ -16,6 +16,7 @@
 #include "kernels.h"
 #include "tc.cuh"
 #include "tc_pipe.cuh"
+#include "verify_common.cuh"
 
 namespace dspark {
 
@@ -32,6 +33,7 @@ struct VerifyTcParams {
     uint64_t seed, cycle;
     PhiloxRoundKeys rk;  // of seed
     int32_t *err;
+    dspark_verify_args a;  // outputs and the rest of the call (the outcome writer)
 };
 
 template <class P>
@@ -195,6 +197,80 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             }
             p.w.part[(size_t)(m0 + et) * p.nparts + cv] = VerifyPartial{b1, b2, i1, i2};
         }
+
+        // Every CTA of the M-tile publishes, waits (bounded; the launch is cooperative,
+        // so all are resident) until all have, then finalises its share of the
+        // requests: rows cv, cv + nparts, ..., one warp per request.
+        __threadfence();
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        if (et == 0) {
+            atomicAdd(p.w.done + m_tile, 1);
+            *s.flag = tc::wait_counter_ge(p.w.done + m_tile, p.nparts, p.err) ? 1 : 0;
+        }
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        if (*s.flag) {
+            __threadfence();
+            for (int i = cv, n = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++n) {
+                if (warp != n % tcp::kEpiWarps) continue;
+                const int rq2 = m0 + i;
+                float b1 = -INFINITY, b2 = -INFINITY;
+                int i1 = -1, i2 = -1;
+                // a lane's slices four at a time, the loads of a batch in flight together
+                for (int q0 = lane; q0 < p.nparts; q0 += 4 * 32) {
+                    float4 vp[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q0 + 32 * q < p.nparts)
+                            vp[q] = __ldcg(reinterpret_cast<const float4 *>(p.w.part + (size_t)rq2 * p.nparts + q0 + 32 * q));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q0 + 32 * q < p.nparts) {
+                            race_merge(b1, i1, vp[q].x, __float_as_int(vp[q].z));
+                            race_merge(b2, i2, vp[q].y, __float_as_int(vp[q].w));
+                        }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float c1 = __shfl_xor_sync(0xffffffffu, b1, off);
+                    const int j1 = __shfl_xor_sync(0xffffffffu, i1, off);
+                    const float c2 = __shfl_xor_sync(0xffffffffu, b2, off);
+                    const int j2 = __shfl_xor_sync(0xffffffffu, i2, off);
+                    race_merge(b1, i1, c1, j1);
+                    race_merge(b2, i2, c2, j2);
+                }
+                // a rejected position whose residual max(0, p - q) came out empty (p equal
+                // to q to rounding everywhere) samples p with the same noise: this warp
+                // runs that race over the whole row
+                const int ell = p.w.ell[rq2], fr = p.w.first_rej[rq2];
+                if (ell >= 0 && fr < ell && i1 < 0 && i2 < 0) {
+                    const int row = p.w.row_of[rq2 * (p.gamma + 1) + fr];
+                    Race fb;
+                    race_init(fb);
+                    if (row >= 0) {
+                        const float lsep2 = p.w.lse_p[row] * kLog2e;
+                        const uint32_t c3b = philox_ctr3(p.cycle, 2);
+                        const __nv_bfloat16 *trow2 = p.T + (size_t)row * p.V;
+                        for (int v0 = 4 * lane; v0 < p.V; v0 += 128) {
+                            const uint4 words =
+                                philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)fr, (uint32_t)rq2, c3b), p.rk);
+                            for (int j = 0; j < 4 && v0 + j < p.V; ++j)
+                                race_feed(fb, ex2(fmaf(__bfloat162float(trow2[v0 + j]), kLog2e, -lsep2)),
+                                          one_minus_uniform(word_lane(words, j)), v0 + j);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float c2 = __shfl_xor_sync(0xffffffffu, fb.best, off);
+                        const int j2 = __shfl_xor_sync(0xffffffffu, fb.idx, off);
+                        race_merge(fb.best, fb.idx, c2, j2);
+                    }
+                    i2 = fb.idx;
+                }
+                if (lane == 0) write_outcome(p.a, p.w, rq2, i1, i2);
+            }
+        } else {
+            *s.abort_flag = 1;
+        }
     }
     P::teardown(s);
 }
@@ -224,17 +300,21 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.nparts = nparts; tp.n_mtiles = mt; tp.n_vtiles = (a.V + P::BN - 1) / P::BN;
     tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
     tp.rk = philox_round_keys(a.seed);
+    tp.a = a;
     auto kern = verify_phase2_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;
-    kern<<<mt * nparts, tcp::kThreads, P::kBytes, s>>>(tmB, tp);
-    return cudaGetLastError();
+    // cooperative: the CTAs of an M-tile wait for one another before the final merge
+    void *args[] = {&tmB, &tp};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(mt * nparts), dim3(tcp::kThreads),
+                                       args, (size_t)P::kBytes, s);
 }
 
 }  // namespace
 
 bool verify_tc_supported(const dspark_verify_args &a) {
     return tc_kernels_enabled() && a.dtype == DSPARK_BF16 && a.r % 64 == 0 && a.r >= 64 && a.r <= 256 &&
+           (a.R + 63) / 64 <= kVerifyMaxMTiles &&
            a.V % 8 == 0 && aligned16(a.T) && aligned16(a.U) && aligned16(a.W1) && aligned16(a.W2t) &&
            (a.A == nullptr || aligned16(a.A)) && tc_available();
 }
