@@ -275,7 +275,7 @@ class Cycle:
 # DRAM bytes (read + write) of one draft launch from the committed ncu capture
 # (profiles/draft_step_tc_qwen4b.md); only for the kernel version that capture
 # measured -- set to None whenever the draft kernel changes
-DRAFT_TRAFFIC_NCU = {}
+DRAFT_TRAFFIC_NCU = {"qwen4b": 263274240 + 4504064}
 
 
 def draft_step_bytes(wl, with_w2=True):
