@@ -57,14 +57,16 @@ def lib():
         L.oracle_uniform.restype = ctypes.c_double
         L.oracle_philox_word.argtypes = [u64, u32, u32, u32, u64, u32, u32]
         L.oracle_philox_word.restype = u32
-        L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 6
+        L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 7
         L.oracle_draft_markov.restype = i32
-        L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 7
+        L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 8
         L.oracle_draft_rnn.restype = i32
         L.oracle_schedule.argtypes = [i32, i32, P, P, i32, i32, i32, i32, P, P, P, P]
         L.oracle_schedule.restype = i32
         L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 7
         L.oracle_verify.restype = i32
+        L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P]
+        L.oracle_sts_fit.restype = i32
         _lib = L
     return _lib
 
@@ -117,14 +119,14 @@ def draft_markov(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, reqs=
     n = R if rl is None else len(rl)
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
-    gap = np.zeros((n, gamma))
+    gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma))
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_markov(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(w),
                                    _p(sts), _p(anchor), seed, cycle, _p(rl), n, _p(x), _p(logq),
-                                   _p(lse), _p(c), _p(gap), _p(z))
+                                   _p(lse), _p(c), _p(gap), _p(z), _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_markov failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out
@@ -149,14 +151,15 @@ def draft_rnn(U, h, W1, W2t, W, w, anchor, *, s0=None, seed=0, cycle=0, sts_T=No
     n = R if rl is None else len(rl)
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
-    gap = np.zeros((n, gamma)); A = np.zeros((n, gamma, r))
+    gap = np.zeros((n, gamma)); A = np.zeros((n, gamma, r)); logit = np.zeros((n, gamma))
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_rnn(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(W),
                                 _p(s0a), _p(w), _p(sts), _p(anchor), seed, cycle, _p(rl), n,
-                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(z), _p(A))
+                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(z), _p(A),
+                                _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_rnn failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, A=A)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, A=A, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out
@@ -209,3 +212,23 @@ def verify(T, tags, anchor, x, logq, lse, U, W1, W2t, *, A=None, seed=0, cycle=0
         raise ValueError(f"oracle_verify failed ({rc})")
     return dict(n_accept=n_acc, out_tokens=out, next_anchor=nxt, lse_p=lse_p, logp=logp,
                 margin=margin, gap=gap)
+
+
+def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None):
+    """[D] Module D: sequential temperature scaling, one grid search per position,
+    left to right, minimising the ECE of the cumulative products prod_{i<=k} c_i
+    against the held-out outcome 1[n_accept >= k]."""
+    logit = np.ascontiguousarray(logit, dtype=np.float32)
+    M, gamma = logit.shape
+    n_accept = np.ascontiguousarray(n_accept, dtype=np.int32)
+    grid = np.ascontiguousarray(grid, dtype=np.float32)
+    G = len(grid)
+    Tp = None if T_prefix is None else np.ascontiguousarray(T_prefix, dtype=np.float32)
+    T = np.zeros(gamma, np.float32)
+    ece = np.zeros(gamma)
+    curve = np.zeros((gamma, G))
+    rc = lib().oracle_sts_fit(M, gamma, _p(logit), _p(n_accept), G, _p(grid), int(n_bins), _p(Tp),
+                              _p(T), _p(ece), _p(curve))
+    if rc != 0:
+        raise ValueError(f"oracle_sts_fit failed ({rc})")
+    return dict(T=T, ece=ece, curve=curve, index=np.argmin(curve, axis=1).astype(np.int32))

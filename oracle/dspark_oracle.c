@@ -117,10 +117,11 @@ static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, ui
  * temperature T_k is the sequential temperature scaling of Module D applied
  * to the logit (T_k = 1 when not given). */
 static double confidence(const float *w, const void *h_k, int d, const double *e, int r,
-                         int dtype, double T_k) {
+                         int dtype, double T_k, double *logit) {
     double dot = 0.0;
     for (int j = 0; j < d; ++j) dot += (double)w[j] * load_elem(h_k, (size_t)j, dtype);
     for (int i = 0; i < r; ++i) dot += (double)w[d + i] * e[i];
+    if (logit) *logit = dot;
     return 1.0 / (1.0 + exp(-dot / T_k));
 }
 
@@ -133,7 +134,7 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        double *z_out) {
+                        double *z_out, double *logit) {
     int n = reqs ? n_reqs : R;
     double *e = (double *)malloc(sizeof(double) * (size_t)r);
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
@@ -160,7 +161,8 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
             const void *h_k = dtype == ORACLE_F32
                                   ? (const void *)((const float *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d)
                                   : (const void *)((const uint16_t *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d);
-            c[o] = confidence(w, h_k, d, e, r, dtype, sts_T ? (double)sts_T[k - 1] : 1.0);
+            c[o] = confidence(w, h_k, d, e, r, dtype, sts_T ? (double)sts_T[k - 1] : 1.0,
+                              logit ? &logit[o] : NULL);
             x_prev = x[o];
         }
     }
@@ -183,7 +185,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, double *z_out, double *A_out) {
+                     double *lse, double *c, double *gap, double *z_out, double *A_out,
+                     double *logit) {
     int n = reqs ? n_reqs : R;
     int zlen = 2 * r + d;
     double *s = (double *)malloc(sizeof(double) * (size_t)r);
@@ -232,7 +235,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
             /* eq. (7) reads the embedding W_1[x_{k-1}], i.e. the middle block of z_k */
             const void *h_k = dtype == ORACLE_F32 ? (const void *)((const float *)h + hrow)
                                                   : (const void *)((const uint16_t *)h + hrow);
-            c[o] = confidence(w, h_k, d, zk + r, r, dtype, sts_T ? (double)sts_T[k - 1] : 1.0);
+            c[o] = confidence(w, h_k, d, zk + r, r, dtype, sts_T ? (double)sts_T[k - 1] : 1.0,
+                              logit ? &logit[o] : NULL);
             memcpy(s, s_next, sizeof(double) * (size_t)r);
             x_prev = x[o];
         }
@@ -489,4 +493,67 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
     }
     free(first); free(count); free(w); free(b);
     return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sequential temperature scaling, [D] Module D.                             */
+/* c_i is the probability that position i is accepted given that every      */
+/* earlier position was, so by the chain rule the probability that the      */
+/* first k drafted tokens are all accepted is P_k = prod_{i<=k} c_i with     */
+/* c_i = sigma(s_i / T_i).  Left to right, T_k is the grid point whose       */
+/* P_k has the smallest expected calibration error against the held-out     */
+/* outcome y_k = 1[n >= k] (n = accepted prefix length of the sample), with  */
+/* T_1..T_{k-1} held at the values already chosen.                          */
+/* ECE (the pages fix no binning; the usual equal-width reading): n_bins     */
+/* bins of [0, 1], bin(P) = min(floor(P n_bins), n_bins - 1), and           */
+/*   ECE = sum_b (|b| / M) |mean_b P - mean_b y| = (1/M) sum_b |sum_b (P - y)|. */
+/* Ties between grid points go to the lowest index.                         */
+/* ------------------------------------------------------------------------ */
+int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept, int G,
+                   const float *grid, int n_bins, const float *T_prefix, float *T_out,
+                   double *ece_out, double *curve) {
+    if (M < 1 || gamma < 1 || G < 1 || n_bins < 1) return -1;
+    for (int g = 0; g < G; ++g)
+        if (!(grid[g] > 0.0f) || !isfinite(grid[g])) return -1;
+    for (int m = 0; m < M; ++m) {
+        if (n_accept[m] < 0 || n_accept[m] > gamma) return -1;
+        for (int k = 0; k < gamma; ++k)
+            if (isnan(logit[(size_t)m * gamma + k])) return -1;
+    }
+    double *prefix = (double *)malloc(sizeof(double) * (size_t)M);   /* P_{k-1} per sample */
+    double *bin_sum = (double *)malloc(sizeof(double) * (size_t)n_bins);
+    if (!prefix || !bin_sum) { free(prefix); free(bin_sum); return -1; }
+    for (int m = 0; m < M; ++m) prefix[m] = 1.0;
+    for (int k = 1; k <= gamma; ++k) {
+        int best = 0;
+        double best_ece = 0.0;
+        for (int g = 0; g < G; ++g) {
+            double T = (double)grid[g];
+            for (int b = 0; b < n_bins; ++b) bin_sum[b] = 0.0;
+            for (int m = 0; m < M; ++m) {
+                double s = (double)logit[(size_t)m * gamma + (k - 1)];
+                double P = prefix[m] * (1.0 / (1.0 + exp(-s / T)));
+                int b = (int)floor(P * n_bins);
+                if (b > n_bins - 1) b = n_bins - 1;
+                double y = n_accept[m] >= k ? 1.0 : 0.0;
+                bin_sum[b] += P - y;
+            }
+            double ece = 0.0;
+            for (int b = 0; b < n_bins; ++b) ece += fabs(bin_sum[b]);
+            ece /= (double)M;
+            if (curve) curve[(size_t)(k - 1) * G + g] = ece;
+            if (g == 0 || ece < best_ece) { best = g; best_ece = ece; }
+        }
+        T_out[k - 1] = grid[best];
+        ece_out[k - 1] = best_ece;
+        /* hold T_k for the later positions (a caller may impose its own) */
+        double T_k = T_prefix ? (double)T_prefix[k - 1] : (double)grid[best];
+        for (int m = 0; m < M; ++m) {
+            double s = (double)logit[(size_t)m * gamma + (k - 1)];
+            prefix[m] *= 1.0 / (1.0 + exp(-s / T_k));
+        }
+    }
+    free(prefix);
+    free(bin_sum);
+    return 0;
 }

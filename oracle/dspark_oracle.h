@@ -10,7 +10,8 @@
  *       digest): eq. (4) causal block distribution, eq. (5) Markov head,
  *       eq. (6) RNN head, eq. (7) confidence head, Module E + Algorithm 1
  *       (hardware-aware prefix scheduler), Appendix A (non-anticipation),
- *       production section (asynchronous top-K scheduler, flattened batch).
+ *       production section (asynchronous top-K scheduler, flattened batch),
+ *       Module D (sequential temperature scaling of the confidences).
  *   [E] "DSpark explained" (interactive explainer), section 06: single-token
  *       rule accept with min(1, p/q), else resample from norm(max(0, p-q)).
  *
@@ -58,13 +59,14 @@ uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t re
  *   U [R, gamma, V], h [R, gamma, d], W1 [V, r], W2t [V, r] (row v = column v
  *   of W_2), w [d + r] f32, sts_T [gamma] f32 or NULL, anchor [R].
  * Outputs: x [n, gamma], logq, lse, c [n, gamma], gap [n, gamma] = gap
- * between the two largest Gumbel-perturbed scores, z [n, gamma, V] logits. */
+ * between the two largest Gumbel-perturbed scores, z [n, gamma, V] logits,
+ * logit [n, gamma] = w^T [h_k ; W_1[x_{k-1}]] (the confidence logit). */
 int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const void *U, const void *h, const void *W1, const void *W2t,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        double *z);
+                        double *z, double *logit);
 
 /* RNN-head draft (eq. 6).  W [3r, 2r + d]: rows [0, r) gate, [r, 2r) candidate,
  * [2r, 3r) output.  s0 [R, r] f32 or NULL (zero).  Extra output: A [n, gamma, r],
@@ -74,7 +76,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, double *z, double *A);
+                     double *lse, double *c, double *gap, double *z, double *A,
+                     double *logit);
 
 /* Hardware-aware prefix scheduler (Module E, Algorithm 1; production async
  * variant).  c [R, gamma] f32; sps[i] = SPS(B_min + i) for i < B_count.
@@ -103,6 +106,19 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
                   const int32_t *reqs, int n_reqs, int32_t *n_accept, int32_t *out_tokens,
                   int32_t *next_anchor, double *lse_p, double *logp, double *margin,
                   double *gap);
+
+/* Sequential temperature scaling ([D] Module D).  logit [M, gamma] f32
+ * confidence logits s_k of M held-out draft blocks, n_accept [M] their
+ * accepted prefix lengths (0..gamma), grid [G] candidate temperatures (> 0),
+ * n_bins equal-width ECE bins.  For k = 1..gamma in order, T_out[k-1] is the
+ * grid point minimising the ECE of prod_{i<=k} sigma(s_i / T_i) against
+ * 1[n >= k]; ece_out[k-1] is that minimum and curve [gamma, G] (may be NULL)
+ * the ECE of every grid point.  T_prefix [gamma] (may be NULL) replaces the
+ * chosen T_i in the products of the later positions.  Returns 0, or -1 on a
+ * bad argument (n_accept outside 0..gamma, a NaN logit, a grid point <= 0). */
+int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept, int G,
+                   const float *grid, int n_bins, const float *T_prefix, float *T_out,
+                   double *ece_out, double *curve);
 
 #ifdef __cplusplus
 }

@@ -173,6 +173,25 @@ def confidences(R: int, gamma: int, seed: int = 0, low: float = 0.05, high: floa
     return rng.uniform(low, high, size=(R, gamma)).astype(np.float32)
 
 
+def calibration_set(M: int, gamma: int, seed: int = 0, T_true=None, mean: float = 2.0,
+                    spread: float = 1.5):
+    """Held-out draft blocks for the sequential temperature-scaling fit: confidence
+    logits s [M, gamma] fp32 ~ N(mean, spread^2) and accepted prefix lengths
+    n [M] int32.  Acceptance model of the synthetic blocks: given that positions
+    1..k-1 were accepted, position k is accepted with probability
+    1 / (1 + exp(-s_k / T_true[k])) (T_true defaults to 1.5 everywhere, so a head
+    reporting sigma(s_k) is over-confident, as the pages find raw confidences)."""
+    rng = np.random.default_rng(seed + 7919)
+    s = rng.normal(mean, spread, size=(M, gamma)).astype(np.float32)
+    T = np.full(gamma, 1.5) if T_true is None else np.asarray(T_true, np.float64)
+    pass_prob = 1.0 / (1.0 + np.exp(-s.astype(np.float64) / T[None, :]))
+    u = rng.uniform(0.0, 1.0, size=(M, gamma))
+    passed = u < pass_prob
+    # accepted prefix length: index of the first rejection, gamma if none
+    first_fail = np.where(~passed, np.arange(gamma)[None, :], gamma).min(axis=1)
+    return s, first_fail.astype(np.int32)
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Host copy of a bf16 tensor as uint16 bit patterns (fp32 stays fp32)."""
     t = t.detach().cpu().contiguous()
