@@ -65,7 +65,7 @@ def lib():
         L.oracle_schedule.restype = i32
         L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 7
         L.oracle_verify.restype = i32
-        L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P]
+        L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P, ctypes.c_double, P]
         L.oracle_sts_fit.restype = i32
         _lib = L
     return _lib
@@ -214,10 +214,11 @@ def verify(T, tags, anchor, x, logq, lse, U, W1, W2t, *, A=None, seed=0, cycle=0
                 margin=margin, gap=gap)
 
 
-def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None):
+def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None, edge_eps=0.0):
     """[D] Module D: sequential temperature scaling, one grid search per position,
     left to right, minimising the ECE of the cumulative products prod_{i<=k} c_i
-    against the held-out outcome 1[n_accept >= k]."""
+    against the held-out outcome 1[n_accept >= k].  ``near_edge`` counts, per
+    position and grid point, the samples within ``edge_eps`` of a bin edge."""
     logit = np.ascontiguousarray(logit, dtype=np.float32)
     M, gamma = logit.shape
     n_accept = np.ascontiguousarray(n_accept, dtype=np.int32)
@@ -227,8 +228,10 @@ def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None):
     T = np.zeros(gamma, np.float32)
     ece = np.zeros(gamma)
     curve = np.zeros((gamma, G))
+    near = np.zeros((gamma, G), np.int32)
     rc = lib().oracle_sts_fit(M, gamma, _p(logit), _p(n_accept), G, _p(grid), int(n_bins), _p(Tp),
-                              _p(T), _p(ece), _p(curve))
+                              _p(T), _p(ece), _p(curve), float(edge_eps), _p(near))
     if rc != 0:
         raise ValueError(f"oracle_sts_fit failed ({rc})")
-    return dict(T=T, ece=ece, curve=curve, index=np.argmin(curve, axis=1).astype(np.int32))
+    return dict(T=T, ece=ece, curve=curve, index=np.argmin(curve, axis=1).astype(np.int32),
+                near_edge=near)

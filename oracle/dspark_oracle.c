@@ -511,7 +511,7 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
 /* ------------------------------------------------------------------------ */
 int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept, int G,
                    const float *grid, int n_bins, const float *T_prefix, float *T_out,
-                   double *ece_out, double *curve) {
+                   double *ece_out, double *curve, double edge_eps, int32_t *near_edge) {
     if (M < 1 || gamma < 1 || G < 1 || n_bins < 1) return -1;
     for (int g = 0; g < G; ++g)
         if (!(grid[g] > 0.0f) || !isfinite(grid[g])) return -1;
@@ -524,6 +524,7 @@ int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept
     double *bin_sum = (double *)malloc(sizeof(double) * (size_t)n_bins);
     if (!prefix || !bin_sum) { free(prefix); free(bin_sum); return -1; }
     for (int m = 0; m < M; ++m) prefix[m] = 1.0;
+    if (near_edge) memset(near_edge, 0, sizeof(int32_t) * (size_t)gamma * (size_t)G);
     for (int k = 1; k <= gamma; ++k) {
         int best = 0;
         double best_ece = 0.0;
@@ -537,6 +538,12 @@ int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept
                 if (b > n_bins - 1) b = n_bins - 1;
                 double y = n_accept[m] >= k ? 1.0 : 0.0;
                 bin_sum[b] += P - y;
+                if (near_edge) {
+                    /* samples within edge_eps of an interior bin edge j / n_bins */
+                    int j = (int)floor(P * n_bins + 0.5);
+                    if (j >= 1 && j <= n_bins - 1 && fabs(P - (double)j / n_bins) < edge_eps)
+                        ++near_edge[(size_t)(k - 1) * G + g];
+                }
             }
             double ece = 0.0;
             for (int b = 0; b < n_bins; ++b) ece += fabs(bin_sum[b]);

@@ -114,11 +114,14 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
  * grid point minimising the ECE of prod_{i<=k} sigma(s_i / T_i) against
  * 1[n >= k]; ece_out[k-1] is that minimum and curve [gamma, G] (may be NULL)
  * the ECE of every grid point.  T_prefix [gamma] (may be NULL) replaces the
- * chosen T_i in the products of the later positions.  Returns 0, or -1 on a
+ * chosen T_i in the products of the later positions.  near_edge [gamma, G]
+ * (may be NULL) counts the samples whose P lies within edge_eps of an interior
+ * bin edge: the only ones a perturbation of P below edge_eps can move to
+ * another bin (tests derive their tolerances from it).  Returns 0, or -1 on a
  * bad argument (n_accept outside 0..gamma, a NaN logit, a grid point <= 0). */
 int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept, int G,
                    const float *grid, int n_bins, const float *T_prefix, float *T_out,
-                   double *ece_out, double *curve);
+                   double *ece_out, double *curve, double edge_eps, int32_t *near_edge);
 
 #ifdef __cplusplus
 }

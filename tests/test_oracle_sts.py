@@ -74,6 +74,16 @@ def test_worked_example(orc):
     assert abs(out["curve"][1][0] - CONDITIONAL_T05) > 0.1
 
 
+def test_worked_example_near_edge(orc):
+    """Position 1 has P = 1/2 (logit 0) on the edge between bins 1 and 2 at every
+    temperature, and at T = 2 also 3/4, 3/4 and 1/4: four samples on edges.  No
+    product of position 2 (1/164, 81/6724, 81/164, 9/20, 3/8, ...) lies within
+    1e-4 of a multiple of 1/4."""
+    s, n = _worked_example()
+    out = orc.sts_fit(s, n, GRID3, n_bins=4, edge_eps=1e-4)
+    assert out["near_edge"].tolist() == [[1, 1, 4], [0, 0, 0]]
+
+
 def test_worked_example_forced_prefix(orc):
     """T_prefix replaces the chosen T_1 in position 2's products: with T_1 = 2
     the prefix is (3/4, 3/4, 1/4, 1/2) and, at T_2 = 2, P = (9/16, 3/16, 1/8, 3/8)
