@@ -95,6 +95,8 @@ typedef struct {
     float *lse;           /* out [R, gamma] log sum_v exp(U_k(v) + B_k(v))      */
     float *c;             /* out [R, gamma] confidences c_k                     */
     int32_t *err;         /* device error word (see conventions), or NULL       */
+    float *conf_logit;    /* out [R, gamma] w^T [h_k ; W_1[x_{k-1}]], the logit  */
+                          /* before 1/T_k (the input of dspark_sts_fit), or NULL */
 } dspark_draft_args;
 
 DSPARK_API size_t dspark_draft_markov_workspace_size(const dspark_draft_args *a);
@@ -243,6 +245,45 @@ typedef struct {
 
 DSPARK_API size_t dspark_verify_workspace_size(const dspark_verify_args *a);
 DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sequential temperature scaling.  [D] Module D: c_i is the probability     */
+/* that position i passes given that the positions before it passed, so the  */
+/* prefix of length k is accepted with probability                           */
+/* P_k = prod_{i<=k} sigma(s_i / T_i).  For k = 1..gamma in order, T_k is    */
+/* the grid temperature that minimises the expected calibration error of P_k */
+/* against the held-out outcome 1[n >= k], with T_1..T_{k-1} held fixed.     */
+/* ECE: n_bins equal-width bins of [0, 1], bin(P) = min(floor(P n_bins),      */
+/* n_bins - 1), ECE = (1/M) sum_b |sum_{m in b} (P_m - y_m)|.  The bin sums  */
+/* are exact fixed-point integers (units of 2^-31 of P), so results do not   */
+/* depend on the order of the additions.  Ties go to the lowest grid index.  */
+/* The fitted T is the draft's sts_T.  Device-side errors: a grid point that */
+/* is not a positive finite number is skipped (DSPARK_ERR_INVAL), a NaN logit */
+/* counts as 0 (DSPARK_ERR_NONFINITE), n outside 0..gamma is clamped          */
+/* (DSPARK_ERR_RANGE).                                                        */
+/* ------------------------------------------------------------------------ */
+#define DSPARK_STS_MAX_GAMMA 64
+#define DSPARK_STS_MAX_BINS 64
+typedef struct {
+    int32_t M;               /* held-out draft blocks                            */
+    int32_t gamma;           /* positions per block (<= DSPARK_STS_MAX_GAMMA)    */
+    int32_t G;               /* grid points                                      */
+    int32_t n_bins;          /* ECE bins (1..DSPARK_STS_MAX_BINS)                */
+    const float *logit;      /* [M, gamma] confidence logits s_k (conf_logit of  */
+                             /* the draft, taken with T = 1)                     */
+    const int32_t *n_accept; /* [M] accepted prefix length of each block, with   */
+                             /* all gamma positions verified                     */
+    const float *grid;       /* [G] candidate temperatures                       */
+    float *T;                /* out [gamma] fitted temperatures T_k              */
+    double *ece;             /* out [gamma] ECE of P_k at the fitted T_k         */
+    double *curve;           /* out [gamma, G] ECE at every grid point, or NULL  */
+    int32_t *err;            /* device error word, or NULL                       */
+} dspark_sts_args;
+
+/* Scratch: the [gamma, G, n_bins] bin sums (8 bytes each) and gamma counters.
+ * One launch per position on the given stream, after one memset. */
+DSPARK_API size_t dspark_sts_fit_workspace_size(const dspark_sts_args *a);
+DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Helpers                                                                    */

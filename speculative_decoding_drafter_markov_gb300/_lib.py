@@ -30,7 +30,7 @@ class DraftArgs(ctypes.Structure):
     _fields_ = [("R", i32), ("gamma", i32), ("V", i32), ("r", i32), ("d", i32), ("dtype", i32),
                 ("U", P), ("h", P), ("W1", P), ("W2t", P), ("w", P), ("sts_T", P), ("anchor", P),
                 ("seed", u64), ("cycle", u64),
-                ("x", P), ("logq", P), ("lse", P), ("c", P), ("err", P)]
+                ("x", P), ("logq", P), ("lse", P), ("c", P), ("err", P), ("conf_logit", P)]
 
 
 class RnnArgs(ctypes.Structure):
@@ -49,6 +49,11 @@ class VerifyArgs(ctypes.Structure):
                 ("lse", P), ("U", P), ("W1", P), ("W2t", P), ("A", P), ("seed", u64), ("cycle", u64),
                 ("n_accept", P), ("out_tokens", P), ("next_anchor", P), ("lse_p", P), ("logp", P),
                 ("err", P)]
+
+
+class StsArgs(ctypes.Structure):
+    _fields_ = [("M", i32), ("gamma", i32), ("G", i32), ("n_bins", i32), ("logit", P),
+                ("n_accept", P), ("grid", P), ("T", P), ("ece", P), ("curve", P), ("err", P)]
 
 
 class DSparkError(RuntimeError):
@@ -76,6 +81,8 @@ SYMBOLS = {
     "dspark_version": ([], ctypes.c_int),
     "dspark_philox": ([P, u64, i32, P, P], ctypes.c_int),
     "dspark_wait_selfcheck": ([P, i32, i32, u64, P, P], ctypes.c_int),
+    "dspark_sts_fit_workspace_size": ([ctypes.POINTER(StsArgs)], ctypes.c_size_t),
+    "dspark_sts_fit": ([ctypes.POINTER(StsArgs), P, P], ctypes.c_int),
 }
 
 
@@ -151,6 +158,7 @@ def _draft_struct(U, h, W1, W2t, w, anchor, seed, cycle, sts_T, out, err):
     a.w, a.sts_T, a.anchor = _ptr(w), _ptr(sts_T), _ptr(anchor)
     a.seed, a.cycle = int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1)
     a.x, a.logq, a.lse, a.c = _ptr(out["x"]), _ptr(out["logq"]), _ptr(out["lse"]), _ptr(out["c"])
+    a.conf_logit = _ptr(out.get("conf_logit"))
     a.err = _ptr(err)
     return a
 
@@ -338,3 +346,28 @@ def wait_selfcheck(flag, target, mode, limit_ns, err, stream=None):
     L = load()
     _check(L.dspark_wait_selfcheck(_ptr(flag), int(target), int(mode), int(limit_ns), _ptr(err),
                                    _stream(stream)))
+
+
+# --------------------------------------------------------------------- calibration
+def sts_fit(logit, n_accept, grid, *, n_bins=15, want_curve=True, ws=None, err=None, stream=None):
+    """Sequential temperature scaling of the confidences (include/dspark.h):
+    logit [M, gamma] fp32 confidence logits of held-out draft blocks (the draft's
+    ``conf_logit`` output), n_accept [M] int32 accepted prefix lengths, grid [G]
+    fp32 candidate temperatures.  Returns {"T": [gamma] fp32 (the draft's sts_T),
+    "ece": [gamma] fp64, "curve": [gamma, G] fp64 or None}."""
+    L = load()
+    M, gamma = logit.shape
+    dev = logit.device
+    if logit.dtype != torch.float32 or n_accept.dtype != torch.int32 or grid.dtype != torch.float32:
+        raise TypeError("logit and grid are float32, n_accept int32")
+    a = StsArgs()
+    a.M, a.gamma, a.G, a.n_bins = M, gamma, grid.numel(), int(n_bins)
+    out = {"T": torch.empty(gamma, dtype=torch.float32, device=dev),
+           "ece": torch.empty(gamma, dtype=torch.float64, device=dev),
+           "curve": torch.empty((gamma, grid.numel()), dtype=torch.float64, device=dev)
+           if want_curve else None}
+    a.logit, a.n_accept, a.grid = _ptr(logit), _ptr(n_accept), _ptr(grid)
+    a.T, a.ece, a.curve, a.err = _ptr(out["T"]), _ptr(out["ece"]), _ptr(out["curve"]), _ptr(err)
+    ws = _workspace(L.dspark_sts_fit_workspace_size(ctypes.byref(a)), dev, ws)
+    _check(L.dspark_sts_fit(ctypes.byref(a), _ptr(ws), _stream(stream)))
+    return out

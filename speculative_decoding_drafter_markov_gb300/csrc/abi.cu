@@ -69,6 +69,7 @@ dspark::DraftStep step_template(const dspark_draft_args *a, const float *A_rnn) 
     st.a_stride = a->gamma * a->r;
     st.h = a->h; st.d = a->d; st.w = a->w; st.sts_T = a->sts_T;
     st.x_out = a->x; st.logq = a->logq; st.lse = a->lse; st.c = a->c;
+    st.conf_logit = a->conf_logit;
     return st;
 }
 
@@ -118,6 +119,7 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
     rd.part = st.part; rd.nparts = st.nparts;
     rd.h = a->h; rd.W1 = a->W1; rd.w = a->w; rd.sts_T = a->sts_T;
     rd.x = a->x; rd.logq = a->logq; rd.lse = a->lse; rd.c = a->c; rd.err = a->err;
+    rd.conf_logit = a->conf_logit;
     if (use_tc && k_first == 1) {  // step 1 starts the step counters; later steps continue them
         cudaError_t e = cudaMemsetAsync(cleared, 0, cleared_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft counters");
@@ -363,6 +365,29 @@ DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_strea
     cudaError_t e = dspark::launch_verify(*a, w, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify");
     return ok();
+}
+
+DSPARK_API size_t dspark_sts_fit_workspace_size(const dspark_sts_args *a) {
+    if (!a || a->gamma < 1 || a->G < 1 || a->n_bins < 1) return 0;
+    return dspark::sts_ws_bytes(a->gamma, a->G, a->n_bins);
+}
+
+DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_t stream) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->M < 1 || a->gamma < 1 || a->G < 1 || a->n_bins < 1)
+        return fail(DSPARK_ERR_INVAL, "bad shape M=%d gamma=%d G=%d n_bins=%d", a->M, a->gamma, a->G,
+                    a->n_bins);
+    if (a->gamma > dspark::kStsMaxGamma || a->n_bins > dspark::kStsMaxBins)
+        return fail(DSPARK_ERR_UNSUPPORTED, "gamma=%d or n_bins=%d above %d", a->gamma, a->n_bins,
+                    dspark::kStsMaxGamma);
+    if (!a->logit || !a->n_accept || !a->grid || !a->T || !a->ece || !ws)
+        return fail(DSPARK_ERR_INVAL, "null pointer");
+    dspark::StsFit f{};
+    f.M = a->M; f.gamma = a->gamma; f.G = a->G; f.n_bins = a->n_bins;
+    f.logit = a->logit; f.n_accept = a->n_accept; f.grid = a->grid;
+    f.T = a->T; f.ece = a->ece; f.curve = a->curve; f.err = a->err;
+    cudaError_t e = dspark::launch_sts_fit(f, ws, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "sts fit");
 }
 
 DSPARK_API int dspark_wait_selfcheck(const int32_t *flag, int32_t target, int32_t mode, uint64_t limit_ns,

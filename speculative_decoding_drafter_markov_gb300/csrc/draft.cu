@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kReduceThreads) draft_reduce_kernel(const Draf
         p.logq[o] = s_z[0] - lse;
         const float T_k = p.sts_T ? p.sts_T[p.k - 1] : 1.0f;
         p.c[o] = 1.0f / (1.0f + expf(-s_dot[0] / T_k));
+        if (p.conf_logit) p.conf_logit[o] = s_dot[0];
     }
 }
 

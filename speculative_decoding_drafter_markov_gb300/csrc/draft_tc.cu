@@ -45,6 +45,7 @@ struct TcParams {
     int *counters;  // [n_mtiles]: partials published (per M-tile), zero at the start of the call
     int32_t *x;
     float *logq, *lse, *c;   // [R, gamma]
+    float *conf_logit;       // [R, gamma] or null
     int nparts;  // vocabulary ranges (CTAs per M-tile)
     int n_mtiles;
     int32_t *err;
@@ -82,7 +83,9 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, int k, int gro
         float sum = 0.f;
         for (int i = 0; i < tcp::kEpiThreads / 32; ++i) sum += red[i];
         const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
-        p.c[(size_t)grow * p.gamma + (k - 1)] = 1.0f / (1.0f + expf(-sum / T_k));
+        const size_t o = (size_t)grow * p.gamma + (k - 1);
+        p.c[o] = 1.0f / (1.0f + expf(-sum / T_k));
+        if (p.conf_logit) p.conf_logit[o] = sum;
     }
     tc::named_bar_sync(1, tcp::kEpiThreads);
 }
@@ -411,6 +414,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.h = static_cast<const __nv_bfloat16 *>(p.h); tp.w = p.w; tp.sts_T = p.sts_T;
     tp.counters = p.counters;
     tp.x = p.x_out; tp.logq = p.logq; tp.lse = p.lse; tp.c = p.c;
+    tp.conf_logit = p.conf_logit;
     tp.W1 = static_cast<const __nv_bfloat16 *>(p.W1);
     tp.x_prev = p.x_prev; tp.x_stride = p.x_stride;
     tp.A_op = p.A_op; tp.a_stride = p.a_stride;

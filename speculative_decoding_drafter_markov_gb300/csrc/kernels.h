@@ -34,6 +34,7 @@ struct DraftStep {
     const float *w, *sts_T;
     int32_t *x_out;
     float *logq, *lse, *c;
+    float *conf_logit;               // [R, gamma] or null
     int *counters;                   // [number of M-tiles], zero at the start of the call
     unsigned long long *winners;     // [gamma, R] packed race winners, zero at the start of the call
     int step_index;                  // 1 for the first step launched since the counters were zeroed
@@ -68,6 +69,7 @@ struct DraftReduce {
     const float *sts_T;              // [gamma] or null
     int32_t *x;
     float *logq, *lse, *c;           // [R, gamma]
+    float *conf_logit;               // [R, gamma] or null
     int32_t *err;
 };
 cudaError_t launch_draft_reduce(const DraftReduce &p, cudaStream_t s);
@@ -123,6 +125,22 @@ cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cu
 
 // ----- philox check ------------------------------------------------------------------
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out, cudaStream_t s);
+
+// ----- sequential temperature scaling (Module D) --------------------------------
+constexpr int kStsMaxGamma = DSPARK_STS_MAX_GAMMA;
+constexpr int kStsMaxBins = DSPARK_STS_MAX_BINS;
+struct StsFit {
+    int M, gamma, G, n_bins;
+    const float *logit;        // [M, gamma]
+    const int32_t *n_accept;   // [M]
+    const float *grid;         // [G]
+    float *T;                  // [gamma]
+    double *ece;               // [gamma]
+    double *curve;             // [gamma, G] or null
+    int32_t *err;
+};
+size_t sts_ws_bytes(int gamma, int G, int n_bins);
+cudaError_t launch_sts_fit(const StsFit &f, void *ws, cudaStream_t s);
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 

@@ -1,6 +1,7 @@
 """Comparison rules between the CUDA path and the oracle.
 
-Tolerances (absolute): log q, log p and confidences 1e-4; log-sum-exp 1e-3.
+Tolerances (absolute): log q, log p, confidences and confidence logits 1e-4;
+log-sum-exp 1e-3.
 Integer results (tokens, verify lengths, accepted counts) must match exactly,
 except a sampled token may differ where the oracle's two best Gumbel-perturbed
 scores are closer than 1e-3, and an acceptance decision may differ where the
@@ -14,6 +15,7 @@ import torch
 
 TOL_LOGQ = 1e-4
 TOL_C = 1e-4
+TOL_LOGIT = 1e-4
 TOL_LSE = 1e-3
 TOL_LOGP = 1e-4
 GAP_TOL = 1e-3
@@ -41,6 +43,8 @@ def compare_draft(gpu, ref, reqs, gamma):
             # lse_k and c_k only depend on x_{k-1}, which matched so far
             assert abs(gpu["lse"][rq, k] - ref["lse"][t, k]) <= TOL_LSE, (rq, k)
             assert abs(gpu["c"][rq, k] - ref["c"][t, k]) <= TOL_C, (rq, k)
+            if "conf_logit" in gpu:
+                assert abs(gpu["conf_logit"][rq, k] - ref["conf_logit"][t, k]) <= TOL_LOGIT, (rq, k)
             compared += 1
             if gpu["x"][rq, k] != ref["x"][t, k]:
                 assert ref["gap"][t, k] < GAP_TOL, (

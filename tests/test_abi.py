@@ -46,16 +46,19 @@ def test_struct_layouts_match_header(tmp_path):
     src = tmp_path / "sizes.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "dspark.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\","
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\","
         "sizeof(dspark_draft_args),sizeof(dspark_rnn_args),sizeof(dspark_sched_args),"
         "sizeof(dspark_verify_args),offsetof(dspark_draft_args,seed),"
-        "offsetof(dspark_sched_args,K_in),offsetof(dspark_verify_args,seed));return 0;}\n")
+        "offsetof(dspark_sched_args,K_in),offsetof(dspark_verify_args,seed),"
+        "offsetof(dspark_draft_args,conf_logit),sizeof(dspark_sts_args),"
+        "offsetof(dspark_sts_args,curve));return 0;}\n")
     exe = tmp_path / "sizes"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
     got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
     expect = [ctypes.sizeof(_lib.DraftArgs), ctypes.sizeof(_lib.RnnArgs),
               ctypes.sizeof(_lib.SchedArgs), ctypes.sizeof(_lib.VerifyArgs),
-              _lib.DraftArgs.seed.offset, _lib.SchedArgs.K_in.offset, _lib.VerifyArgs.seed.offset]
+              _lib.DraftArgs.seed.offset, _lib.SchedArgs.K_in.offset, _lib.VerifyArgs.seed.offset,
+              _lib.DraftArgs.conf_logit.offset, ctypes.sizeof(_lib.StsArgs), _lib.StsArgs.curve.offset]
     assert got == expect
 
 
@@ -105,3 +108,17 @@ def test_host_side_validation(lib):
     assert lib.dspark_verify(byref(v), None, None) == _lib.ERR_INVAL
     v.N = 21
     assert lib.dspark_verify(byref(v), None, None) == _lib.ERR_INVAL
+    # calibration fit: shapes and limits are checked on the host
+    t = _lib.StsArgs()
+    assert lib.dspark_sts_fit(None, None, None) == _lib.ERR_INVAL
+    t.M, t.gamma, t.G, t.n_bins = 0, 4, 8, 10
+    assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_INVAL
+    t.M = 16
+    t.n_bins = 65
+    assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_UNSUPPORTED
+    t.n_bins, t.gamma = 10, 65
+    assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_UNSUPPORTED
+    t.gamma = 4
+    assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_INVAL  # null tensors
+    # bin sums (8 B each) + counters, 256-byte aligned
+    assert lib.dspark_sts_fit_workspace_size(byref(t)) == 4 * 8 * 10 * 8 + 256

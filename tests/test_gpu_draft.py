@@ -14,15 +14,25 @@ from speculative_decoding_drafter_markov_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
+def _outputs(R, gamma):
+    """The draft's outputs, with the optional confidence logit requested."""
+    f32 = dict(dtype=torch.float32, device="cuda")
+    return {"x": torch.empty((R, gamma), dtype=torch.int32, device="cuda"),
+            "logq": torch.empty((R, gamma), **f32), "lse": torch.empty((R, gamma), **f32),
+            "c": torch.empty((R, gamma), **f32), "conf_logit": torch.empty((R, gamma), **f32)}
+
+
 def _gpu_draft(inp, seed, cycle, sts_T=None, rnn=False):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     sts = None if sts_T is None else torch.as_tensor(sts_T, device="cuda")
+    R, gamma, _ = inp["U"].shape
     if rnn:
         out = dsp.draft_rnn(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["W"], inp["w"],
-                            inp["anchor"], seed=seed, cycle=cycle, sts_T=sts, err=err)
+                            inp["anchor"], seed=seed, cycle=cycle, sts_T=sts, err=err,
+                            out=_outputs(R, gamma))
     else:
         out = dsp.draft_markov(inp["U"], inp["h"], inp["W1"], inp["W2t"], inp["w"], inp["anchor"],
-                               seed=seed, cycle=cycle, sts_T=sts, err=err)
+                               seed=seed, cycle=cycle, sts_T=sts, err=err, out=_outputs(R, gamma))
     torch.cuda.synchronize()
     assert int(err.item()) == 0, dsp.ERROR_NAMES[int(err.item())]
     return {k: host(v) for k, v in out.items()}
