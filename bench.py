@@ -12,7 +12,12 @@ Prints ONE JSON line (rank 0).  `value` is drafted-and-verified tokens per secon
 of device time, R * gamma / (T_draft + T_schedule + T_verify), summed over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dspark|reference]
-                  [--workload qwen4b|heavy|prod|rnn|tiny]
+                  [--workload qwen4b|heavy|prod|rnn|tiny|sts_fit]
+
+`--workload sts_fit` times the confidence calibration instead (Module D's
+sequential temperature scaling on a held-out set of draft blocks): one step is
+one full fit, and `value` is (block, position, temperature) evaluations per
+second.
 
 `--impl reference` times the CPU oracle (the plain single-threaded checker) on a
 bounded sample of requests of the same workload; it is the reference arm.
@@ -46,7 +51,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
-    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS) + ["sts_fit"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -509,9 +514,160 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- calibration fit
+# held-out set: 65,536 draft blocks of gamma = 16 (e.g. 512 requests x 128 cycles),
+# 256 temperatures on [0.05, 12.8], 15 ECE bins
+STS = {"M": 65536, "gamma": 16, "G": 256, "n_bins": 15}
+STS_METRIC = "STS calibration fit: (block, position, temperature) evaluations/s at 1 GB300"
+# special-function throughput on GB300, measured with a throughput probe of
+# independent chains: ex2.approx 32 and rcp.approx 16 results per SM per clock.
+# One evaluation takes one of each: 1/32 + 1/16 = 3/32 SM-cycles.
+EVALS_PER_SM_CLK = 32.0 / 3.0
+
+
+def _sts_inputs(seed):
+    s, n = W.calibration_set(STS["M"], STS["gamma"], seed=seed,
+                             T_true=np.linspace(1.2, 2.4, STS["gamma"]))
+    grid = np.linspace(0.05, 12.8, STS["G"]).astype(np.float32)
+    return s, n, grid
+
+
+def _sts_desc():
+    return (f"sts_fit: M={STS['M']} blocks x gamma={STS['gamma']} positions, G={STS['G']} "
+            f"temperatures, {STS['n_bins']} bins")
+
+
+def _sts_cpu(budget_s=12.0, M=4096):
+    """The oracle's fit on the first M blocks of the same set, per evaluation."""
+    import oracle as orc
+    orc.build()
+    s, n, grid = _sts_inputs(11)
+    s, n = s[:M], n[:M]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        orc.sts_fit(s, n, grid, n_bins=STS["n_bins"])
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 8:
+            break
+    evals = done * M * STS["gamma"] * STS["G"]
+    return {"value": evals / el, "unit": "eval/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} fits of the first {M} blocks of the set (gamma={STS['gamma']}, "
+                      f"G={STS['G']}), single-threaded C oracle, {el:.1f} s"}
+
+
+def run_sts_fit(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s, n, grid = _sts_inputs(11 + rank)
+    logit = torch.as_tensor(s, device=dev)
+    n_acc = torch.as_tensor(n, device=dev)
+    grid_d = torch.as_tensor(grid, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    fit = lambda: dsp.sts_fit(logit, n_acc, grid_d, n_bins=STS["n_bins"], ws=ws)
+    for _ in range(args.warmup):
+        flush.zero_()
+        fit()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for a, b in ev:
+        flush.zero_()  # the inputs (4.5 MB) fit in L2: flushed between timed fits
+        torch.cuda._sleep(2_000_000)
+        a.record(stream)
+        fit()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    times = [a.elapsed_time(b) for a, b in ev]
+    evals = STS["M"] * STS["gamma"] * STS["G"]
+    total_ms, value = aggregate_ranks(sum(times), args.steps * evals, world, dev)
+    fit_us = 1e3 * statistics.mean(times)
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    peak = sm * EVALS_PER_SM_CLK * mhz * 1e6 / 1e9  # G eval/s
+    achieved = evals / (fit_us * 1e-6) / 1e9
+    line = {
+        "metric": STS_METRIC, "value": value, "unit": "eval/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded held-out blocks with a known acceptance temperature)",
+        "config": {"workload": _sts_desc(),
+                   "l2": "256 MB buffer written between timed fits (the inputs fit in L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": f"sts_fit_kernel: one cooperative launch, {STS['gamma']} positions",
+                     "bound": "alu", "achieved": achieved, "peak": peak, "unit": "G eval/s",
+                     "frac": achieved / peak,
+                     "peak_kind": (f"MUFU: {sm} SMs x 32/3 evaluations per clock (one ex2 at "
+                                   f"32/clk, one rcp at 16/clk, measured) x {mhz:.0f} MHz (sampled)"),
+                     "timing": "CUDA events around the whole fit (memset + one cooperative launch)",
+                     "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        h_s = torch.as_tensor(s).pin_memory()
+        h_n = torch.as_tensor(n).pin_memory()
+        h_T = torch.empty(STS["gamma"], dtype=torch.float32).pin_memory()
+        h_e = torch.empty(STS["gamma"], dtype=torch.float64).pin_memory()
+        tot = 0.0
+        for i in range(args.steps + 2):
+            a, b = mk(), mk()
+            a.record(stream)
+            logit.copy_(h_s, non_blocking=True)
+            n_acc.copy_(h_n, non_blocking=True)
+            out = fit()
+            h_T.copy_(out["T"], non_blocking=True)
+            h_e.copy_(out["ece"], non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                tot += a.elapsed_time(b)
+        line["e2e"] = {"value": args.steps * evals / (tot / 1e3), "unit": "eval/s",
+                       "h2d_bytes_per_step": int(s.nbytes + n.nbytes),
+                       "d2h_bytes_per_step": STS["gamma"] * 12}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _sts_cpu()
+    return line, rank
+
+
+def run_sts_reference(args, world, rank):
+    if rank != 0:
+        return None
+    cpu = _sts_cpu(budget_s=max(1.0, 1.5 * args.steps))
+    evals = STS["M"] * STS["gamma"] * STS["G"]
+    return {"metric": STS_METRIC, "value": cpu["value"], "unit": "eval/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * evals / cpu["value"],
+            "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": _sts_desc(), "sample": cpu["sample"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": cpu["value"], "unit": "eval/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
+    if args.workload == "sts_fit":
+        if args.impl == "reference":
+            line = run_sts_reference(args, world, rank)
+        else:
+            line, rank = run_sts_fit(args, world, rank, local)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.impl == "reference":
         line = run_reference(args, world, rank)
         if line is not None:

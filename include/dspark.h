@@ -255,8 +255,10 @@ DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_strea
 /* against the held-out outcome 1[n >= k], with T_1..T_{k-1} held fixed.     */
 /* ECE: n_bins equal-width bins of [0, 1], bin(P) = min(floor(P n_bins),      */
 /* n_bins - 1), ECE = (1/M) sum_b |sum_{m in b} (P_m - y_m)|.  The bin sums  */
-/* are exact fixed-point integers (units of 2^-31 of P), so results do not   */
-/* depend on the order of the additions.  Ties go to the lowest grid index.  */
+/* are exact integers (P rounded to units of 2^-16 / n_bins), so results    */
+/* depend on the order of the additions; the rounding can move a P within  */
+/* 2^-17 / n_bins below a bin edge into the next bin.  Ties go to the lowest */
+/* grid index.                                                               */
 /* The fitted T is the draft's sts_T.  Device-side errors: a grid point that */
 /* is not a positive finite number is skipped (DSPARK_ERR_INVAL), a NaN logit */
 /* counts as 0 (DSPARK_ERR_NONFINITE), n outside 0..gamma is clamped          */
@@ -280,8 +282,9 @@ typedef struct {
     int32_t *err;            /* device error word, or NULL                       */
 } dspark_sts_args;
 
-/* Scratch: the [gamma, G, n_bins] bin sums (8 bytes each) and gamma counters.
- * One launch per position on the given stream, after one memset. */
+/* Scratch: the [gamma, G, n_bins] bin sums (8 bytes each), gamma counters and
+ * two [M] fp32 prefix-product buffers.  One launch per position on the given
+ * stream, after one memset. */
 DSPARK_API size_t dspark_sts_fit_workspace_size(const dspark_sts_args *a);
 DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_t stream);
 

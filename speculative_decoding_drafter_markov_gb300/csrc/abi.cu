@@ -368,8 +368,8 @@ DSPARK_API int dspark_verify(const dspark_verify_args *a, void *ws, dspark_strea
 }
 
 DSPARK_API size_t dspark_sts_fit_workspace_size(const dspark_sts_args *a) {
-    if (!a || a->gamma < 1 || a->G < 1 || a->n_bins < 1) return 0;
-    return dspark::sts_ws_bytes(a->gamma, a->G, a->n_bins);
+    if (!a || a->M < 1 || a->gamma < 1 || a->G < 1 || a->n_bins < 1) return 0;
+    return dspark::sts_ws_bytes(a->M, a->gamma, a->G, a->n_bins);
 }
 
 DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_t stream) {

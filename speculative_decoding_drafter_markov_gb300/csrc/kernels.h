@@ -139,7 +139,7 @@ struct StsFit {
     double *curve;             // [gamma, G] or null
     int32_t *err;
 };
-size_t sts_ws_bytes(int gamma, int G, int n_bins);
+size_t sts_ws_bytes(int M, int gamma, int G, int n_bins);
 cudaError_t launch_sts_fit(const StsFit &f, void *ws, cudaStream_t s);
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -120,5 +120,5 @@ def test_host_side_validation(lib):
     assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_UNSUPPORTED
     t.gamma = 4
     assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_INVAL  # null tensors
-    # bin sums (8 B each) + counters, 256-byte aligned
-    assert lib.dspark_sts_fit_workspace_size(byref(t)) == 4 * 8 * 10 * 8 + 256
+    # bin sums (8 B each) + counters + two prefix buffers, each 256-byte aligned
+    assert lib.dspark_sts_fit_workspace_size(byref(t)) == 4 * 8 * 10 * 8 + 256 + 2 * 256

@@ -17,7 +17,8 @@ positions are compared with the oracle following the kernel's choices
 EPS: per factor sigma(s/T), the exp argument carries (|x| + 2) 2^-23 relative
 error and the reciprocal 2 ulp, which gives at most ~5e-7 absolute error per
 factor (factors are <= 1).  A product of k factors is then within k * 5e-7.
-The test uses 2e-6 (gamma + 1).
+The kernel also rounds P to units of 2^-16 / n_bins before binning and
+summing, which adds at most 2^-17.  The test uses 2e-6 (gamma + 1) + 2^-17.
 """
 import numpy as np
 import pytest
@@ -46,7 +47,7 @@ def _check_parity(orc, s, n, grid, n_bins):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     gpu = _gpu_fit(s, n, grid, n_bins, err=err)
     assert int(err.item()) == 0
-    eps = 2e-6 * (gamma + 1)
+    eps = 2e-6 * (gamma + 1) + 2.0 ** -17
     ref = orc.sts_fit(s, n, grid, n_bins=n_bins, T_prefix=gpu["T"], edge_eps=eps)
     tol = eps + 2.0 * ref["near_edge"] / M + 1e-9
     diff = np.abs(gpu["curve"] - ref["curve"])
