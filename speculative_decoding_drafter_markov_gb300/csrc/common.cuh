@@ -216,7 +216,9 @@ __device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0,
 // of 4, words[j] the Philox word of entry v0 + j).  Written for instruction-level
 // parallelism: one max and one rescale per block, independent exponentials
 // summed in a fixed tree, independent filter tests; the rare candidates that pass
-// the filter are scored exactly in index order.
+// the filter are scored exactly in index order.  All 32 lanes of the warp call
+// it together (each with its own row): a column's exact scoring runs only when
+// some lane of the warp has a survivor there (a warp-uniform branch).
 template <int N>
 __device__ __forceinline__ void row_feed_block(RowState &s, const float (&z)[N], int v0,
                                                const uint32_t (&words)[N]) {
@@ -250,20 +252,38 @@ __device__ __forceinline__ void row_feed_block(RowState &s, const float (&z)[N],
         const float t = one_minus_uniform(words[j]);
         if (!(t >= e[j] * s.C)) pass |= 1u << j;
     }
-    if (pass) {
+    const unsigned any = __reduce_or_sync(0xffffffffu, pass);
+    if (any) {
 #pragma unroll
         for (int j = 0; j < N; ++j) {
-            if (pass & (1u << j)) {
-                const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
-                if (score > s.best) {
-                    s.best = score;
-                    s.idx = v0 + j;
-                    s.zbest = z[j];
-                    row_raise_thr(s, score);
+            if (any & (1u << j)) {
+                if (pass & (1u << j)) {
+                    const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
+                    if (score > s.best) {
+                        s.best = score;
+                        s.idx = v0 + j;
+                        s.zbest = z[j];
+                        row_raise_thr(s, score);
+                    }
                 }
             }
         }
     }
+}
+
+// A race winner as one 64-bit word whose unsigned order is the merge order
+// (higher score, then lower index): order-preserving score bits on top, the
+// complemented index below.  Zero means "no candidate".
+__device__ __forceinline__ unsigned long long pack_winner(float best, int idx) {
+    const uint32_t b = __float_as_uint(best);
+    const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)ob << 32) | (uint32_t)~(uint32_t)idx;
+}
+__device__ __forceinline__ int winner_index(unsigned long long w) { return (int)~(uint32_t)w; }
+__device__ __forceinline__ float winner_score(unsigned long long w) {
+    if (w == 0ull) return -INFINITY;
+    const uint32_t ob = (uint32_t)(w >> 32);
+    return __uint_as_float((ob & 0x80000000u) ? (ob & 0x7FFFFFFFu) : ~ob);
 }
 
 // Combine two states (b into a).  Ties of the race go to the lower index.

@@ -121,16 +121,6 @@ __device__ __forceinline__ int load_token(const TcParams &p, int grow, const int
     return x;
 }
 
-// The race winner of a row as one 64-bit word whose unsigned order is the
-// merge order (higher score, then lower index): order-preserving score bits
-// on top, the complemented index below.  Zero means "no candidate".
-__device__ __forceinline__ unsigned long long pack_winner(float best, int idx) {
-    const uint32_t b = __float_as_uint(best);
-    const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)ob << 32) | (uint32_t)~(uint32_t)idx;
-}
-__device__ __forceinline__ int winner_index(unsigned long long w) { return (int)~(uint32_t)w; }
-
 // the bias operand of the M-tile in the swizzled K-major layout: W_1[x_{k-1}]
 // (tokens in s.tok) or the split fp32 RNN operand; threads tid, tid + nthr, ...
 template <class P>
@@ -205,8 +195,8 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
 }
 
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
-// (m_tile, cv) owns requests m0 .. m0 + MV - 1 and vocabulary columns
-// [c0, c1), an equal share.  Per step: contraction + eq. (4) epilogue over the
+// (m_tile, cv) owns requests m0 .. m0 + MV - 1 and the vocabulary tiles
+// cv, cv + nparts, cv + 2 nparts, ... (about an equal share).  Per step: contraction + eq. (4) epilogue over the
 // columns, a merge into one partial per request (double-buffered by step
 // parity) and the race winner folded into a per-(step, request) 64-bit maximum.
 // Once every CTA of the M-tile has published (bounded wait; the launch is
@@ -217,7 +207,7 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
 // MMAs of the next step run.  The confidences of its rows are computed while
 // it waits for the other CTAs.
 template <class P>
-__global__ void __launch_bounds__(tcp::kThreads, 1)
+__global__ void __launch_bounds__(P::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
                   const TcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -226,9 +216,12 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
     const int m0 = m_tile * P::MV;
-    int c0, c1;
-    tcp::col_range(cv, p.nparts, p.V, c0, c1);
-    const int ntiles = (c1 - c0 + P::BN - 1) / P::BN;
+    // the CTA's vocabulary tiles: every nparts-th BN-wide tile, starting at tile
+    // cv, so the CTAs of an M-tile stream neighbouring pieces of each U row at
+    // the same time (DRAM page locality); the last tile may end at V
+    const int n_vtiles = (p.V + P::BN - 1) / P::BN;
+    const int c0 = cv * P::BN, c1 = p.V, tstride = p.nparts * P::BN;
+    const int ntiles = (n_vtiles - cv + p.nparts - 1) / p.nparts;
     const int kslabs = p.r / 64;
     int *ctr = p.counters + m_tile;
 
@@ -238,7 +231,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     P::ready(s);
 
     // 2. first bias operand, before the W_2 / U streams compete for bandwidth
-    gather_operand<P>(p, s, m0, threadIdx.x, tcp::kThreads);
+    gather_operand<P>(p, s, m0, threadIdx.x, P::kThreads);
     tc::fence_proxy_async_smem();
     __syncthreads();  // operand complete
 
@@ -248,7 +241,10 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             tc::prefetch_tmap(&tmU);
         }
         __syncwarp();
-        P::producer(s, &tmB, &tmU, c0, ntiles, kslabs, p.nsteps, p.k - 1, m0, p.err);
+        if (lane == 0) P::producer_w2(s, &tmB, c0, tstride, ntiles, kslabs, p.nsteps, p.err);
+        __syncwarp();
+    } else if (warp == tcp::kUWarp) {
+        if (lane == 0) P::producer_u(s, &tmU, c0, tstride, ntiles, p.nsteps, p.k - 1, m0, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, p.nsteps, p.err);
@@ -268,38 +264,51 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
 
             RowState st;
             row_init(st);
-            P::epilogue(s, step * ntiles, c0, ntiles, p.err,
-                        [&](int, int n0, const uint32_t *acc, const unsigned char *sU) {
-                if (!row_live) return;
-                // the row's best score so far, wherever in the CTA it was found, filters this thread
-                row_raise_thr(st, P::read_thr(s, row));
-                const float best0 = st.best;
-                const int vb = n0 + col0;
-                if (vb + P::CW <= c1) {
-                    // whole block in range: per 16 columns, the Philox words first (independent
-                    // chains), then the block
-#pragma unroll
-                    for (int h = 0; h < P::CW / 16; ++h) {
-                        uint32_t words[16];
-                        float z[16];
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int gg = 4 * h + g;
-                            const uint4 w4 = philox4x32_10(
-                                make_uint4((uint32_t)((vb >> 2) + gg), (uint32_t)k, (uint32_t)grow, c3), p.rk);
-                            words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
-                            const uint2 uu = P::u_quad(sU, row, col0 + 4 * gg);
-                            z[4 * g] = __uint_as_float(acc[4 * gg]) + tcp::bf16_lo(uu.x);
-                            z[4 * g + 1] = __uint_as_float(acc[4 * gg + 1]) + tcp::bf16_hi(uu.x);
-                            z[4 * g + 2] = __uint_as_float(acc[4 * gg + 2]) + tcp::bf16_lo(uu.y);
-                            z[4 * g + 3] = __uint_as_float(acc[4 * gg + 3]) + tcp::bf16_hi(uu.y);
-                        }
-                        row_feed_block<16>(st, z, vb + 16 * h, words);
+            // Filter thresholds shared by all CTAs: the step's winner word of a
+            // request (win[row], raised by every CTA) holds the exact score of
+            // some element of the row, so any value read from it is a valid
+            // threshold, however stale.  Once per tile one thread per request
+            // (the leader) forwards the CTA's best when it beats what it last saw
+            // and brings the global best into the CTA; its read is issued a tile
+            // ahead so the L2 latency stays off the tile loop.
+            const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
+            unsigned long long *gwin = win + (row_live ? grow : m0);
+            unsigned long long g_next = leader ? tc::ld_relaxed_gpu_u64(gwin) : 0ull, g_sent = 0ull;
+            P::epilogue(s, step * ntiles, c0, tstride, ntiles, p.err,
+                        [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *sU) {
+                if (leader && cofs == 0) {
+                    const unsigned long long g = g_next, loc = P::read_thr(s, row);
+                    if (loc > g && loc > g_sent) {
+                        atomicMax(gwin, loc);
+                        g_sent = loc;
                     }
-                } else if (vb < c1) {
+                    if (g > loc) P::publish_thr(s, row, g);
+                    g_next = tc::ld_relaxed_gpu_u64(gwin);
+                }
+                // the row's best score so far, wherever it was found, filters this thread
+                row_raise_thr(st, winner_score(P::read_thr(s, row)));
+                const float best0 = st.best;
+                const int cb = col0 + cofs, vb = n0 + cb;  // the chunk's first column: in the tile, in V
+                if (vb + 16 <= c1) {
+                    // whole chunk in range: the Philox words first (independent chains), then the block
+                    uint32_t words[16];
+                    float z[16];
 #pragma unroll
-                    for (int g = 0; g < P::CW / 4; ++g) {
-                        const int col = col0 + 4 * g;
+                    for (int g = 0; g < 4; ++g) {
+                        const uint4 w4 = philox4x32_10(
+                            make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)k, (uint32_t)grow, c3), p.rk);
+                        words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
+                        const uint2 uu = P::u_quad(sU, row, cb + 4 * g);
+                        z[4 * g] = __uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x);
+                        z[4 * g + 1] = __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x);
+                        z[4 * g + 2] = __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y);
+                        z[4 * g + 3] = __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y);
+                    }
+                    row_feed_block<16>(st, z, vb, words);
+                } else if (vb < c1 && row_live) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = cb + 4 * g;
                         const uint2 uu = P::u_quad(sU, row, col);
                         float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
                                       __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
                         row_feed4<false>(st, z, v0, c1, words);
                     }
                 }
-                if (st.best > best0) P::publish_thr(s, row, st.best);
+                if (row_live && st.best > best0) P::publish_thr(s, row, pack_winner(st.best, st.idx));
             });
 
             // merge the TPR threads of each request (fixed warp order) into this CTA's
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
             mg[3 * tcp::kEpiThreads + et] = st.zbest;
             reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + et] = st.idx;
             tc::named_bar_sync(1, tcp::kEpiThreads);
-            if (et < P::MV) s.thr[et] = P::ord_encode(-INFINITY);  // the next step starts afresh
+            if (et < P::MV) s.thr[et] = 0ull;  // the next step starts afresh
             if (et < P::MV && m0 + et < p.R) {
                 RowState f;
                 row_init(f);
@@ -397,7 +406,7 @@ __global__ void wait_selfcheck_kernel(const int *flag, int target, int mode, uin
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
 using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;   // Markov, R <= 64
-using DraftM128 = tcp::Pipe<128, 64, 8, 6, 1>;  // Markov, 128 requests per M-tile
+using DraftM128 = tcp::Pipe<128, 128, 6, 2, 1>; // Markov, 128 requests per M-tile
 using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -430,7 +439,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     // cooperative: the CTAs wait for one another at the end of the step
     void *args[] = {&tmB, &tmU, &tp};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(n_mtiles * nparts),
-                                       dim3(tcp::kThreads), args, (size_t)P::kBytes, s);
+                                       dim3(P::kThreads), args, (size_t)P::kBytes, s);
 }
 
 }  // namespace

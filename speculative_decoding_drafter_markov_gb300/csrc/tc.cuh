@@ -97,6 +97,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
     return v;
 }
 
+// relaxed L2 read of a word other CTAs of the launch raise (no ordering implied)
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *ptr) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr));
+    return v;
+}
+
 // bounded wait until *ctr >= target (a counter other CTAs of the launch raise)
 __device__ __forceinline__ bool wait_counter_ge(const int *ctr, int target, int32_t *err,
                                                 uint64_t limit_ns = kWaitLimitNs) {

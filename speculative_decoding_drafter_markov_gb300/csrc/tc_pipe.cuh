@@ -3,15 +3,18 @@
 // D = A . W_2^T[tile]^T on tcgen05, where A (the bias operand of each request:
 // W_1[x] or the RNN vector A_k, bf16, K-major, 128-byte swizzle) is resident in
 // shared memory and W_2^T streams through a ring of 64-wide K slabs.  One CTA
-// owns one M-tile of MV requests and a contiguous range of BN-wide vocabulary
-// tiles.  Warp roles (576 threads):
+// owns one M-tile of MV requests and a set of BN-wide vocabulary tiles
+// (a contiguous range, or every nparts-th tile).  Warp roles (576 threads):
 //   warps 0..15  epilogue: every warp reads its own block of the accumulator
 //                straight from TMEM (no staging) and runs the caller's
 //                functor on it; synchronisation is per warp, through mbarriers.
-//   warp 16      TMA producer: lane 0 streams the W_2^T slab ring (each slot
-//                freed by the MMA commit that consumed it), lane 1 the U ring
-//                (freed when all 16 epilogue warps have used a tile).
+//   warp 16      TMA producer of the W_2^T slab ring (each slot freed by the
+//                MMA commit that consumed it).
 //   warp 17      TMEM allocator and MMA issuer, NACC accumulators of BN columns.
+//   warp 18      (pipelines with a U ring) TMA producer of the U ring (a slot
+//                freed when all 16 epilogue warps have used its tile).  Each
+//                waiting role has a warp of its own: a lane blocked in an
+//                mbarrier wait would otherwise hold up a sibling lane's role.
 // MV = 128: quadrant q of the accumulator holds requests 32q..32q+31 and the
 // four warps of a quadrant split the BN columns.  MV = 64: A holds the 64
 // requests twice (rows i and 64 + i), so quadrants 0-1 and 2-3 hold the same
@@ -32,15 +35,16 @@ namespace tcp {
 
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = kEpiThreads + 64;
 constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
+constexpr int kUWarp = 18;
 
 template <int MV_, int BN_, int NS_, int SU_, int KSPLIT_>
 struct Pipe {
     static constexpr int MV = MV_, BN = BN_, NS = NS_, SU = SU_, KSPLIT = KSPLIT_;
     static constexpr bool DUAL = MV == 64;
     static constexpr bool WITH_U = SU > 0;
+    static constexpr int kThreads = kEpiThreads + (WITH_U ? 96 : 64);  // epilogue, producer(s), MMA
     static constexpr int kArows = 128;                  // MMA rows (A duplicated when DUAL)
     static constexpr int kSlabA = kArows * 128;         // one 64-wide K slab of A
     static constexpr int kABytes = 4 * KSPLIT * kSlabA; // r <= 256
@@ -56,10 +60,10 @@ struct Pipe {
     static constexpr int kOffBar = kOffU + SU * kUBytes;
     static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC + 1;
     static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
-    static constexpr int kOffTok = kOffThr + 4 * MV;        // per-request tokens / metadata
+    static constexpr int kOffTok = kOffThr + 8 * MV;        // per-request tokens / metadata
     static constexpr int kOffMisc = kOffTok + 4 * MV;
-    static constexpr int kOffRed = kOffMisc + 64;           // 80-float reduction scratch
-    static constexpr int kBytes = kOffRed + 320 + 1024;     // + alignment slack
+    static constexpr int kOffRed = kOffMisc + 64;           // 16-float reduction scratch
+    static constexpr int kBytes = kOffRed + 64 + 1024;      // + alignment slack
     // scratch for the per-CTA merge after the tile loop: the operand region,
     // which no MMA reads once the last accumulator has been consumed
     static constexpr int kMergeBytes = kEpiThreads * 5 * 4;
@@ -73,11 +77,11 @@ struct Pipe {
         unsigned char *smem, *sA;
         uint64_t *fullB, *emptyB, *fullU, *emptyU, *tfull, *tempty;
         uint64_t *aready;  // operand of the next step written (multi-step launches)
-        unsigned *thr;     // ordered-uint encoded row thresholds
+        unsigned long long *thr;  // per request: the best packed race winner the CTA knows
         int *tok;          // MV ints of per-request scratch
         uint32_t *tmem_slot;
         volatile int *abort_flag, *flag;
-        float *red;  // 80 floats
+        float *red;  // 16 floats
         uint32_t tmem_base;
     };
 
@@ -94,7 +98,7 @@ struct Pipe {
         s.tfull = bars + 2 * NS + 2 * SU;
         s.tempty = s.tfull + NACC;
         s.aready = s.tempty + NACC;
-        s.thr = reinterpret_cast<unsigned *>(s.smem + kOffThr);
+        s.thr = reinterpret_cast<unsigned long long *>(s.smem + kOffThr);
         s.tok = reinterpret_cast<int *>(s.smem + kOffTok);
         s.tmem_slot = reinterpret_cast<uint32_t *>(s.smem + kOffMisc);
         s.abort_flag = reinterpret_cast<volatile int *>(s.smem + kOffMisc + 4);
@@ -125,7 +129,7 @@ struct Pipe {
             *s.flag = 0;
             tc::fence_mbar_init();
         }
-        if (threadIdx.x < MV) s.thr[threadIdx.x] = ord_encode(-INFINITY);
+        if (threadIdx.x < MV) s.thr[threadIdx.x] = 0ull;
         if (warp == kMmaWarp) {
             tc::tmem_alloc(s.tmem_slot, kTmemCols);
             tc::tmem_relinquish();
@@ -137,15 +141,6 @@ struct Pipe {
     __device__ static void ready(State &s) {
         tc::tc_fence_after();
         s.tmem_base = *s.tmem_slot;
-    }
-
-    // order-preserving float <-> unsigned (for atomicMax on scores)
-    __device__ static unsigned ord_encode(float f) {
-        const unsigned b = __float_as_uint(f);
-        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    }
-    __device__ static float ord_decode(unsigned u) {
-        return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
     }
 
     // 16-byte chunk c (8 bf16 along K) of MMA row `row` of split part `part` of A
@@ -178,26 +173,32 @@ struct Pipe {
         return DUAL ? (q >= 2 ? BN / 2 : 0) + j * CW : j * CW;
     }
 
-    // warp 16 (all lanes call): lane 0 streams W_2^T slabs, lane 1 the U tiles,
-    // for `nsteps` consecutive draft steps over the same tile range (W_2^T does
-    // not depend on the step, so the next step's slabs stream in while the
-    // current one is merged); U of step i is position u_k0 + i.
-    __device__ static void producer(State &s, const CUtensorMap *tmB, const CUtensorMap *tmU, int col0,
-                                    int ntiles, int kslabs, int nsteps, int u_k0, int m0, int32_t *err) {
-        const int lane = threadIdx.x & 31;
-        if (lane == 0) {
+    // warp 16, lane 0: the W_2^T slabs of `nsteps` consecutive draft steps over
+    // the same tiles (W_2^T does not depend on the step, so the next step's
+    // slabs stream in while the current one is merged).  Tile t of the CTA
+    // starts at vocabulary column col0 + t * tstride.
+    __device__ static void producer_w2(State &s, const CUtensorMap *tmB, int col0, int tstride, int ntiles,
+                                       int kslabs, int nsteps, int32_t *err) {
+        {
             const int per_step = ntiles * kslabs, total = nsteps * per_step;
             int issued = 0;
             for (int g = 0; g < total; ++g) {
                 const int slot = g % NS, rem = g % per_step, t = rem / kslabs, j = rem - t * kslabs;
                 if (!tc::mbar_wait(&s.emptyB[slot], ((uint32_t)(g / NS) & 1u) ^ 1u, s.abort_flag, err)) break;
                 tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
-                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, col0 + t * BN);
+                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, col0 + t * tstride);
                 ++issued;
             }
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
                 tc::mbar_wait_drain(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, err);
-        } else if (lane == 1 && SU > 0) {
+        }
+    }
+
+    // warp 18, lane 0: the U tiles of the same steps and tiles; U of step i is
+    // position u_k0 + i of requests m0 ..
+    __device__ static void producer_u(State &s, const CUtensorMap *tmU, int col0, int tstride, int ntiles,
+                                      int nsteps, int u_k0, int m0, int32_t *err) {
+        if (SU > 0) {
             // U is read once: keep it from displacing W_2^T, which the next steps reuse
             const uint64_t pol = tc::policy_evict_first();
             constexpr int su = SU > 0 ? SU : 1;
@@ -207,7 +208,7 @@ struct Pipe {
                 const int st = g % su, step = g / ntiles, t = g - step * ntiles;
                 if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(g / su) & 1u) ^ 1u, s.abort_flag, err)) break;
                 unsigned char *dst = s.smem + kOffU + st * kUBytes;
-                const int n0 = col0 + t * BN;
+                const int n0 = col0 + t * tstride;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
                 for (int h = 0; h < BN / 64; ++h)
                     tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k0 + step, m0, pol);
@@ -277,12 +278,14 @@ struct Pipe {
     }
 
     // warps 0..15: per tile, load this warp's CW accumulator columns of its 32
-    // rows and call f(t, n0, acc, sU) (t: tile within this call; n0 = col0 +
-    // t BN: first vocabulary entry of the tile; sU: the tile's U, or null).
-    // Barrier phases continue from tile number tg0 (the tiles of earlier steps
-    // of the launch).  Per-warp flow, no CTA barrier.
+    // rows 16 at a time and call f(t, n0, cofs, acc, sU) on each chunk (t: tile
+    // within this call; n0 = col0 + t tstride: first vocabulary entry of the
+    // tile; cofs: the chunk's offset within the warp's CW columns; acc: its 16
+    // values; sU: the tile's U, or null).  The accumulator is released once its
+    // last chunk has been read.  Barrier phases continue from tile number tg0
+    // (the tiles of earlier steps of the launch).  Per-warp flow, no CTA barrier.
     template <class F>
-    __device__ static void epilogue(State &s, int tg0, int col0, int ntiles, int32_t *err, F &&f) {
+    __device__ static void epilogue(State &s, int tg0, int col0, int tstride, int ntiles, int32_t *err, F &&f) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const uint32_t taddr0 = s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)epi_col0();
         constexpr int su = SU > 0 ? SU : 1;
@@ -297,26 +300,30 @@ struct Pipe {
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc::tc_fence_after();
-            uint32_t acc[CW];
-            tc::tmem_ld16(taddr0 + (uint32_t)(b * BN), *reinterpret_cast<uint32_t(*)[16]>(acc));
-            if constexpr (CW == 32)
-                tc::tmem_ld16(taddr0 + (uint32_t)(b * BN + 16), *reinterpret_cast<uint32_t(*)[16]>(acc + 16));
-            tc::tmem_wait_ld();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
-            f(t, col0 + t * BN, acc, SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr);
+            const unsigned char *sU = SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr;
+#pragma unroll 1
+            for (int h = 0; h < CW / 16; ++h) {
+                uint32_t acc[16];
+                tc::tmem_ld16(taddr0 + (uint32_t)(b * BN + 16 * h), acc);
+                tc::tmem_wait_ld();
+                if (h == CW / 16 - 1) {
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
+                }
+                f(t, col0 + t * tstride, 16 * h, acc, sU);
+            }
             __syncwarp();
             if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
         }
     }
 
-    // raise row r's shared threshold to `score`
-    __device__ static void publish_thr(State &s, int r, float score) {
-        atomicMax(&s.thr[r], ord_encode(score));
+    // raise row r's shared threshold to the packed winner w (pack_winner)
+    __device__ static void publish_thr(State &s, int r, unsigned long long w) {
+        atomicMax(&s.thr[r], w);
     }
-    __device__ static float read_thr(const State &s, int r) {
-        return ord_decode(*reinterpret_cast<volatile unsigned *>(&s.thr[r]));
+    __device__ static unsigned long long read_thr(const State &s, int r) {
+        return *reinterpret_cast<volatile unsigned long long *>(&s.thr[r]);
     }
 
     // per-CTA merge scratch in the operand region (valid once every epilogue

@@ -37,7 +37,7 @@ struct VerifyTcParams {
 };
 
 template <class P>
-__global__ void __launch_bounds__(tcp::kThreads, 1)
+__global__ void __launch_bounds__(P::kThreads, 1)
     verify_phase2_tc(const __grid_constant__ CUtensorMap tmB, const VerifyTcParams p) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ int s_mode[P::MV], s_n[P::MV], s_row[P::MV], s_xn[P::MV];
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
 
     // bias operand of q_{n+1}: W_1[x_n] (x_0 = anchor) or the RNN vector A_{n+1}
     const int chunks_per_row = p.r / 8;
-    for (int e = threadIdx.x; e < P::MV * chunks_per_row; e += tcp::kThreads) {
+    for (int e = threadIdx.x; e < P::MV * chunks_per_row; e += P::kThreads) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int rq = m0 + row;
         const bool live = s_mode[row] == 1;
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
     if (warp == tcp::kProducerWarp) {
         if (lane == 0) tc::prefetch_tmap(&tmB);
         __syncwarp();
-        P::producer(s, &tmB, nullptr, t_begin * P::BN, ntiles, kslabs, 1, 0, m0, p.err);
+        if (lane == 0) P::producer_w2(s, &tmB, t_begin * P::BN, P::BN, ntiles, kslabs, 1, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
         if (lane == 0) P::mma(s, ntiles, kslabs, 1, p.err);
@@ -136,20 +136,21 @@ __global__ void __launch_bounds__(tcp::kThreads, 1)
         race_init(res);
         race_init(pr);
         const uint64_t pol = tc::policy_evict_first();  // target and base rows are read once
-        P::epilogue(s, 0, t_begin * P::BN, ntiles, p.err, [&](int, int n0, const uint32_t *acc, const unsigned char *) {
+        P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err, [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
             if (mode < 0) return;
-            const int vb = n0 + col0;
+            constexpr int CH = 16;  // columns per chunk
+            const int vb = n0 + col0 + cofs;
             // this block of the target row (and of U_{n+1}), 8 columns per load; V % 8 == 0
             // makes every 8-column chunk entirely in or out of range
-            uint4 tq[P::CW / 8], uq[P::CW / 8];
+            uint4 tq[CH / 8], uq[CH / 8];
 #pragma unroll
-            for (int c = 0; c < P::CW / 8; ++c) {
+            for (int c = 0; c < CH / 8; ++c) {
                 const bool in = vb + 8 * c < p.V;
                 tq[c] = in ? tc::ld_global_hint(trow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
                 uq[c] = (in && mode == 1) ? tc::ld_global_hint(urow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int g = 0; g < P::CW / 4; ++g) {
+            for (int g = 0; g < CH / 4; ++g) {
                 const int v0 = vb + 4 * g;
                 if (v0 >= p.V) break;
                 const uint4 &tt = tq[g >> 1];
@@ -306,7 +307,7 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     if (e != cudaSuccess) return e;
     // cooperative: the CTAs of an M-tile wait for one another before the final merge
     void *args[] = {&tmB, &tp};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(mt * nparts), dim3(tcp::kThreads),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(mt * nparts), dim3(P::kThreads),
                                        args, (size_t)P::kBytes, s);
 }
 
