@@ -140,7 +140,7 @@ __device__ __forceinline__ float log_exp_variate(float t) {
 // can only beat `best` if E_v < exp(z_v - best), and E_v >= t_v = 1 - u_v, so it
 // is skipped whenever t_v >= exp(z_v - m) * C.
 struct RowState {
-    float m;      // running max of z
+    float m;      // reference of the sum (the max of z, or below it; exp(z - m) stays finite)
     float mL;     // m * log2(e)
     float S;      // sum exp(z - m)
     float best;   // best race score z - ln E of this thread's elements
@@ -212,62 +212,81 @@ __device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0,
     }
 }
 
-// Feed N consecutive vocabulary entries v0..v0+N-1 (all below V; N a multiple
-// of 4, words[j] the Philox word of entry v0 + j).  Written for instruction-level
-// parallelism: one max and one rescale per block, independent exponentials
-// summed in a fixed tree, independent filter tests; the rare candidates that pass
-// the filter are scored exactly in index order.  All 32 lanes of the warp call
-// it together (each with its own row): a column's exact scoring runs only when
-// some lane of the warp has a survivor there (a warp-uniform branch).
-template <int N>
-__device__ __forceinline__ void row_feed_block(RowState &s, const float (&z)[N], int v0,
-                                               const uint32_t (&words)[N]) {
-    float mx[N];
+// Feed 16 consecutive vocabulary entries v0..v0+15 of one row (all below V;
+// words[j] the Philox word of entry v0 + j).  All 32 lanes of the warp call it
+// together, each with its own row.
+//
+// The sum of exponentials runs against a reference m that only has to keep
+// the terms finite: it is the first block's maximum and moves up only when a
+// block's sum leaves [0, 2^64] (a term far above m, or a non-finite logit), so
+// a block needs no max and no rescale.  Any reference gives the same
+// lse = m + ln S.  The race filter keeps element j when e_j C > t_j
+// (e_j C = exp(z_j - thr) slack); a block whose 16 differences are all
+// negative -- one AND of their sign bits -- skips the exact scoring, and the
+// exact scoring of a column runs only when some lane of the warp kept it.
+__device__ __forceinline__ void row_set_reference(RowState &s, const float (&z)[16]) {
+    float mx[16];
 #pragma unroll
-    for (int j = 0; j < N; ++j) mx[j] = z[j];
+    for (int j = 0; j < 16; ++j) mx[j] = z[j];
 #pragma unroll
-    for (int w = N / 2; w > 0; w >>= 1)
+    for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-    if (mx[0] > s.m) {
-        s.S *= ex2((s.m - mx[0]) * kLog2e);
-        s.m = mx[0];
-        s.mL = mx[0] * kLog2e;
-        row_refresh_C(s);
-    }
-    float e[N], sum[N];
+    const float M = fmaxf(s.m, mx[0]);
+    s.S = M == -INFINITY ? 0.f : s.S * ex2((s.m - M) * kLog2e);
+    s.m = M;
+    s.mL = M * kLog2e;
+    row_refresh_C(s);
+}
+
+__device__ __forceinline__ float block_exp_sum(const RowState &s, const float (&z)[16], float (&e)[16]) {
+    float sum[16];
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
+    for (int j = 0; j < 16; ++j) {
         e[j] = ex2(fmaf(z[j], kLog2e, -s.mL));
         sum[j] = e[j];
     }
 #pragma unroll
-    for (int w = N / 2; w > 0; w >>= 1)
+    for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) sum[j] += sum[j + w];
-    s.S += sum[0];
-    unsigned pass = 0;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-        const float t = one_minus_uniform(words[j]);
-        if (!(t >= e[j] * s.C)) pass |= 1u << j;
+    return sum[0];
+}
+
+__device__ __forceinline__ void row_feed16(RowState &s, const float (&z)[16], int v0, const uint32_t (&words)[16]) {
+    if (s.m == -INFINITY) row_set_reference(s, z);  // the row's first block in this thread
+    float e[16];
+    float sum = block_exp_sum(s, z, e);
+    if (!(sum <= 18446744073709551616.f)) {  // 2^64: move the reference up to this block's maximum
+        row_set_reference(s, z);
+        sum = block_exp_sum(s, z, e);
     }
-    const unsigned any = __reduce_or_sync(0xffffffffu, pass);
-    if (any) {
+    s.S += sum;
+    // race filter: d_j = e_j C - t_j (C capped so that e_j = 0 gives d_j = -t_j)
+    const float C = fminf(s.C, 3.0e38f);
+    float d[16];
+    uint32_t allneg = 0xFFFFFFFFu;
 #pragma unroll
-        for (int j = 0; j < N; ++j) {
-            if (any & (1u << j)) {
-                if (pass & (1u << j)) {
+    for (int j = 0; j < 16; ++j) {
+        d[j] = fmaf(e[j], C, -one_minus_uniform(words[j]));
+        allneg &= __float_as_uint(d[j]);
+    }
+    if (__any_sync(0xffffffffu, (int)allneg >= 0)) {
+        const float best0 = s.best;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (__any_sync(0xffffffffu, d[j] > 0.f)) {
+                if (d[j] > 0.f) {
                     const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
                     if (score > s.best) {
                         s.best = score;
                         s.idx = v0 + j;
                         s.zbest = z[j];
-                        row_raise_thr(s, score);
                     }
                 }
             }
         }
+        if (s.best > best0) row_raise_thr(s, s.best);
     }
 }
 

@@ -298,13 +298,18 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                         const uint4 w4 = philox4x32_10(
                             make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)k, (uint32_t)grow, c3), p.rk);
                         words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
-                        const uint2 uu = P::u_quad(sU, row, cb + 4 * g);
-                        z[4 * g] = __uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x);
-                        z[4 * g + 1] = __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x);
-                        z[4 * g + 2] = __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y);
-                        z[4 * g + 3] = __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y);
                     }
-                    row_feed_block<16>(st, z, vb, words);
+#pragma unroll
+                    for (int o = 0; o < 2; ++o) {
+                        const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
+                        const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            z[8 * o + 2 * i] = __uint_as_float(acc[8 * o + 2 * i]) + tcp::bf16_lo(u[i]);
+                            z[8 * o + 2 * i + 1] = __uint_as_float(acc[8 * o + 2 * i + 1]) + tcp::bf16_hi(u[i]);
+                        }
+                    }
+                    row_feed16(st, z, vb, words);
                 } else if (vb < c1 && row_live) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {

@@ -155,6 +155,12 @@ struct Pipe {
         if (DUAL) *reinterpret_cast<uint4 *>(a_chunk(s, row + 64, c, part)) = v;
     }
 
+    // eight columns col .. col + 7 (col a multiple of 8) of a U tile row
+    __device__ static uint4 u_oct(const unsigned char *sU, int row, int col) {
+        const int h = col >> 6, cc = col & 63;
+        return *reinterpret_cast<const uint4 *>(sU + h * kUBox + row * 128 + (((cc >> 3) ^ (row & 7)) << 4));
+    }
+
     // one quad of a U tile (64-column boxes, 128-byte swizzle)
     __device__ static uint2 u_quad(const unsigned char *sU, int row, int col) {
         const int h = col >> 6, cc = col & 63;
@@ -180,14 +186,22 @@ struct Pipe {
     __device__ static void producer_w2(State &s, const CUtensorMap *tmB, int col0, int tstride, int ntiles,
                                        int kslabs, int nsteps, int32_t *err) {
         {
-            const int per_step = ntiles * kslabs, total = nsteps * per_step;
-            int issued = 0;
+            const int total = nsteps * ntiles * kslabs;
+            int issued = 0, slot = 0, t = 0, j = 0;  // ring slot, tile and K slab of load `issued`
+            uint32_t phase = 0;
             for (int g = 0; g < total; ++g) {
-                const int slot = g % NS, rem = g % per_step, t = rem / kslabs, j = rem - t * kslabs;
-                if (!tc::mbar_wait(&s.emptyB[slot], ((uint32_t)(g / NS) & 1u) ^ 1u, s.abort_flag, err)) break;
+                if (!tc::mbar_wait(&s.emptyB[slot], phase ^ 1u, s.abort_flag, err)) break;
                 tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
                 tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, col0 + t * tstride);
                 ++issued;
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+                if (++j == kslabs) {
+                    j = 0;
+                    if (++t == ntiles) t = 0;
+                }
             }
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
                 tc::mbar_wait_drain(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, err);
@@ -203,16 +217,24 @@ struct Pipe {
             const uint64_t pol = tc::policy_evict_first();
             constexpr int su = SU > 0 ? SU : 1;
             const int total = nsteps * ntiles;
-            int issued = 0;
+            int issued = 0, st = 0, step = 0, t = 0;  // ring slot, step and tile of load `issued`
+            uint32_t phase = 0;
             for (int g = 0; g < total; ++g) {
-                const int st = g % su, step = g / ntiles, t = g - step * ntiles;
-                if (!tc::mbar_wait(&s.emptyU[st], ((uint32_t)(g / su) & 1u) ^ 1u, s.abort_flag, err)) break;
+                if (!tc::mbar_wait(&s.emptyU[st], phase ^ 1u, s.abort_flag, err)) break;
                 unsigned char *dst = s.smem + kOffU + st * kUBytes;
                 const int n0 = col0 + t * tstride;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
                 for (int h = 0; h < BN / 64; ++h)
                     tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k0 + step, m0, pol);
                 ++issued;
+                if (++st == su) {
+                    st = 0;
+                    phase ^= 1u;
+                }
+                if (++t == ntiles) {
+                    t = 0;
+                    ++step;
+                }
             }
             for (int g = issued - su < 0 ? 0 : issued - su; g < issued; ++g)
                 tc::mbar_wait_drain(&s.fullU[g % su], (uint32_t)(g / su) & 1u, err);
@@ -223,8 +245,12 @@ struct Pipe {
     // the epilogue has written its operand (phase i - 1 of `aready`).
     __device__ static void mma(State &s, int ntiles, int kslabs, int nsteps, int32_t *err) {
         constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
-        const uint32_t a_base = tc::smem_u32(s.sA);
-        int issued = 0;
+        // a descriptor moves with its operand: its low field is the shared
+        // address >> 4, which no address of this CTA carries out of
+        const uint64_t a_desc0 = tc::smem_desc_k128(tc::smem_u32(s.sA));
+        const uint64_t b_desc0 = tc::smem_desc_k128(tc::smem_u32(s.smem + kOffB));
+        int issued = 0, slot = 0, b = 0;  // W_2^T ring slot and accumulator of the next MMAs
+        uint32_t phase = 0, tphase = 0;
         bool ok = true;
         for (int step = 0; step < nsteps && ok; ++step) {
             if (step > 0) {
@@ -232,35 +258,40 @@ struct Pipe {
                 tc::tc_fence_after();
             }
             for (int tl = 0; tl < ntiles && ok; ++tl) {
-                const int t = step * ntiles + tl;
-                const int b = t % NACC;
-                if (!tc::mbar_wait(&s.tempty[b], ((uint32_t)(t / NACC) & 1u) ^ 1u, s.abort_flag, err)) {
+                if (!tc::mbar_wait(&s.tempty[b], tphase ^ 1u, s.abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
                 const uint32_t d = s.tmem_base + (uint32_t)(b * BN);
                 for (int j = 0; j < kslabs; ++j) {
-                    const int g = t * kslabs + j, slot = g % NS;
-                    if (!tc::mbar_wait(&s.fullB[slot], (uint32_t)(g / NS) & 1u, s.abort_flag, err)) {
+                    if (!tc::mbar_wait(&s.fullB[slot], phase, s.abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t b_slab = tc::smem_u32(s.smem + kOffB + slot * kSlabB);
+                    const uint64_t bd = b_desc0 + (uint64_t)((slot * kSlabB) >> 4);
+                    const uint64_t ad = a_desc0 + (uint64_t)((j * kSlabA) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = tc::smem_desc_k128(b_slab + kk * 32);
+                    for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
                         for (int part = 0; part < KSPLIT; ++part)
-                            tc::umma_bf16(d, tc::smem_desc_k128(a_base + (j + 4 * part) * kSlabA + kk * 32), bd,
-                                          idesc, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
-                    }
+                            tc::umma_bf16(d, ad + (uint64_t)((4 * part * kSlabA + kk * 32) >> 4),
+                                          bd + (uint64_t)((kk * 32) >> 4), idesc,
+                                          (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
                     tc::umma_commit(&s.emptyB[slot]);
+                    if (++slot == NS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 tc::umma_commit(&s.tfull[b]);
                 ++issued;
+                if (++b == NACC) {
+                    b = 0;
+                    tphase ^= 1u;
+                }
             }
         }
         if (issued > 0) {  // the last MMAs must finish before TMEM is freed
