@@ -124,11 +124,12 @@ DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, v
  * GPU that loads the library holds until the process exits.
  *
  * - Limit: the scratch is what dspark_draft_markov_workspace_size() returns
- *   for the same arguments -- 32 bytes per (request, vocabulary range), twice
- *   on the tensor-core path, plus 8 bytes per (request, step) and 256, each
- *   part rounded up to 256 bytes; the ranges are one per SM on the tensor-core
- *   path (bf16, r a multiple of 64 up to 256, V a multiple of 8: all the
- *   standard workloads, under 2 MiB) and ceil(V / 64) on the CUDA-core path --
+ *   for the same arguments -- 32 bytes per (request, vocabulary range), once
+ *   per step on the tensor-core path, plus 8 bytes per (request, step) and
+ *   256, each part rounded up to 256 bytes; the ranges are one per SM on the
+ *   tensor-core path (bf16, r a multiple of 64 up to 256, V a multiple of 8:
+ *   all the standard workloads, under 11 MiB) and ceil(V / 64) on the
+ *   CUDA-core path --
  *   and the array holds
  *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB).  Larger needs return
  *   DSPARK_ERR_UNSUPPORTED (message in dspark_last_error()) and launch nothing.

@@ -54,7 +54,7 @@ int check_draft(const dspark_draft_args *a) {
 
 // The step kernels' scratch: one partial per (request, vocabulary range) --
 // ceil(V / 64) ranges on the CUDA-core path; one per CTA on the tensor-core
-// path, twice (double-buffered by step parity) -- then the tensor-core step's
+// path, for each of the gamma steps -- then the tensor-core step's
 // per-M-tile completion counters and its [gamma, R] packed race winners, the
 // part cleared at the start of a call.
 constexpr size_t kCounterBytes = 256;
@@ -95,7 +95,7 @@ size_t partials_bytes(const dspark_draft_args *a, const float *A_rnn) {
     const dspark::DraftStep st = step_template(a, A_rnn);
     const bool tc = use_tc_path(st);
     const int np = step_nparts(st, tc);
-    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)a->R * np * (tc ? 2 : 1));
+    return dspark::align256(sizeof(dspark::DraftPartial) * (size_t)a->R * np * (tc ? a->gamma : 1));
 }
 
 size_t draft_ws_bytes(const dspark_draft_args *a, const float *A_rnn) {

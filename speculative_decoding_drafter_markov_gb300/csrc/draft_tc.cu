@@ -40,7 +40,7 @@ struct TcParams {
     const float *sts_T;      // [gamma] or null
     uint64_t seed, cycle;
     PhiloxRoundKeys rk;  // of seed
-    DraftPartial *part;  // [2][R][nparts]: step partials, double-buffered by step parity
+    DraftPartial *part;  // [gamma][R][nparts]: step partials, by counter index - 1
     unsigned long long *winners;  // [gamma][R] packed race winners, zero at the start of the call
     int *counters;  // [n_mtiles]: partials published (per M-tile), zero at the start of the call
     int32_t *x;
@@ -196,16 +196,17 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
 
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
 // (m_tile, cv) owns requests m0 .. m0 + MV - 1 and the vocabulary tiles
-// cv, cv + nparts, cv + 2 nparts, ... (about an equal share).  Per step: contraction + eq. (4) epilogue over the
-// columns, a merge into one partial per request (double-buffered by step
-// parity) and the race winner folded into a per-(step, request) 64-bit maximum.
-// Once every CTA of the M-tile has published (bounded wait; the launch is
-// cooperative, so all are resident) each reads the winners x_k of its rows and
-// gathers the next operand W_1[x_k] right away -- the producer has already
-// streamed the next step's first W_2^T slabs and U tiles -- and only then
-// finalises its share of rows (cv, cv + nparts, ...: lse_k, log q_k) while the
-// MMAs of the next step run.  The confidences of its rows are computed while
-// it waits for the other CTAs.
+// cv, cv + nparts, cv + 2 nparts, ... (about an equal share).  Per step:
+// contraction + eq. (4) epilogue over the columns, a merge into one partial
+// per request (kept per step) and the race winner folded into a per-(step,
+// request) 64-bit maximum.  Once every CTA of the M-tile has published
+// (bounded wait; the launch is cooperative, so all are resident) each reads
+// the winners x_k of its rows and gathers the next operand W_1[x_k] right away
+// -- the producer has already streamed the next step's first W_2^T slabs and U
+// tiles.  The confidences of its rows are computed while it waits for the
+// other CTAs.  Nothing else sits between two steps: the rows' lse_k and
+// log q_k (which need every CTA's partial) are finalised after the last step,
+// all (step, request) pairs of the M-tile spread over the CTAs' warps.
 template <class P>
 __global__ void __launch_bounds__(P::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         float *wsc = mg + 5 * tcp::kEpiThreads;  // 80 floats of finalise scratch
         for (int step = 0; step < p.nsteps; ++step) {
             const int k = p.k + step, q = p.step_index + step;
-            DraftPartial *part = p.part + (size_t)(q & 1) * p.R * p.nparts;
+            DraftPartial *part = p.part + (size_t)(q - 1) * p.R * p.nparts;
             unsigned long long *win = p.winners + (size_t)(q - 1) * p.R;
 
             RowState st;
@@ -380,9 +381,16 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 gather_operand<P>(p, s, m0, et, tcp::kEpiThreads);
                 P::operand_written(s, et);
             }
-            // finalise this CTA's share of the step's rows (scratch outside the operand)
-            for (int i = cv, n = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++n)
-                if (warp == n % tcp::kEpiWarps) finalise_row(p, part, m0 + i, k, lane);
+        }
+        // lse_k and log q_k of every step of the launch: (step, request) pairs of
+        // the M-tile over all its CTAs' warps, one pair per warp at a time
+        if (!*s.abort_flag) {
+            const int npairs = p.nsteps * P::MV;
+            for (int pi = cv * tcp::kEpiWarps + warp; pi < npairs; pi += p.nparts * tcp::kEpiWarps) {
+                const int si = pi / P::MV, i = pi - si * P::MV;
+                if (m0 + i < p.R)
+                    finalise_row(p, p.part + (size_t)(p.step_index + si - 1) * p.R * p.nparts, m0 + i, p.k + si, lane);
+            }
         }
     }
     P::teardown(s);
