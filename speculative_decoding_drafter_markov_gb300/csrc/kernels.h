@@ -114,6 +114,7 @@ struct VerifyWs {
     int32_t *row_of;       // [R, gamma + 1]
     VerifyPartial *part;   // [R, nparts]
     int *done;             // [kVerifyMaxMTiles] CTAs of an M-tile that published (tensor-core phase 2)
+    unsigned long long *win;  // [R] packed race winner of each request (tensor-core phase 2)
     int nparts;
 };
 constexpr int kVerifyMaxMTiles = 64;

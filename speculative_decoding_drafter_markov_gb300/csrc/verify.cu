@@ -39,6 +39,7 @@ __global__ void verify_init(int R, int gamma, VerifyWs w) {
     if (i < R) {
         w.first_rej[i] = kNone;
         w.ell[i] = -1;
+        w.win[i] = 0ull;
     }
 }
 
@@ -352,7 +353,8 @@ size_t verify_ws_bytes(int R, int gamma, int V, int N) {
     const int nparts = (V + kSliceV - 1) / kSliceV;
     return align256(sizeof(float) * (size_t)N) + align256(sizeof(int32_t) * (size_t)R) * 2 +
            align256(sizeof(int32_t) * (size_t)R * (gamma + 1)) +
-           align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles);
+           align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles) +
+           align256(sizeof(unsigned long long) * (size_t)R);
 }
 
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
@@ -370,11 +372,13 @@ VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
     w.part = reinterpret_cast<VerifyPartial *>(p);
     p += align256(sizeof(VerifyPartial) * (size_t)R * w.nparts);
     w.done = reinterpret_cast<int *>(p);
+    p += align256(sizeof(int) * kVerifyMaxMTiles);
+    w.win = reinterpret_cast<unsigned long long *>(p);
     return w;
 }
 
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s) {
-    const int n_init = a.R * (a.gamma + 1) > kVerifyMaxMTiles ? a.R * (a.gamma + 1) : kVerifyMaxMTiles;
+    const int n_init = a.R * (a.gamma + 1) > kVerifyMaxMTiles ? a.R * (a.gamma + 1) : kVerifyMaxMTiles;  // >= R
     verify_init<<<(n_init + 255) / 256, 256, 0, s>>>(a.R, a.gamma, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -127,76 +127,106 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         const int et = threadIdx.x;
         const int row = P::epi_row(), col0 = P::epi_col0();
         const int rq = m0 + row;
+        const bool row_live = rq < p.R;
         const int mode = s_mode[row], n = s_n[row];
         const float lsep = s_lsep[row] * kLog2e, lseq = s_lseq[row] * kLog2e;
         const __nv_bfloat16 *trow = p.T + (size_t)s_row[row] * p.V;
-        const __nv_bfloat16 *urow = p.U + ((size_t)rq * p.gamma + (mode == 1 ? n : 0)) * (size_t)p.V;
+        const __nv_bfloat16 *urow = p.U + ((size_t)(row_live ? rq : 0) * p.gamma + (mode == 1 ? n : 0)) * (size_t)p.V;
         const uint32_t c3 = philox_ctr3(p.cycle, 2);
-        Race res, pr;
-        race_init(res);
-        race_init(pr);
         const uint64_t pol = tc::policy_evict_first();  // target and base rows are read once
-        P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err, [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
-            if (mode < 0) return;
-            constexpr int CH = 16;  // columns per chunk
-            const int vb = n0 + col0 + cofs;
-            // this block of the target row (and of U_{n+1}), 8 columns per load; V % 8 == 0
-            // makes every 8-column chunk entirely in or out of range
-            uint4 tq[CH / 8], uq[CH / 8];
+        // One race per request: over the residual max(0, p - q) at a rejected
+        // position (mode 1), over p for the bonus (mode 0).  Filter thresholds are
+        // shared like the draft's: per request in shared memory inside the CTA and
+        // through the request's winner word (p.w.win) across CTAs, which a leader
+        // thread per request exchanges once per tile; any value read there is the
+        // exact score of some element of the request's race.
+        float best = -INFINITY, thr = -INFINITY, C = 3.0e38f;
+        int idx = -1;
+        const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
+        unsigned long long *gwin = p.w.win + (row_live ? rq : m0);
+        unsigned long long g_next = leader ? tc::ld_relaxed_gpu_u64(gwin) : 0ull, g_sent = 0ull;
+        P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err,
+                    [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
+            if (leader && cofs == 0) {
+                const unsigned long long g = g_next, loc = P::read_thr(s, row);
+                if (loc > g && loc > g_sent) {
+                    atomicMax(gwin, loc);
+                    g_sent = loc;
+                }
+                if (g > loc) P::publish_thr(s, row, g);
+                g_next = tc::ld_relaxed_gpu_u64(gwin);
+            }
+            {
+                const float t2 = winner_score(P::read_thr(s, row));
+                if (t2 > thr) {
+                    thr = t2;
+                    C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
+                }
+            }
+            const int vb = n0 + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
+            // the chunk of the target row (and of U_{n+1}), 8 columns per load
+            uint4 tq[2], uq[2];
 #pragma unroll
-            for (int c = 0; c < CH / 8; ++c) {
-                const bool in = vb + 8 * c < p.V;
+            for (int c = 0; c < 2; ++c) {
+                const bool in = mode >= 0 && vb + 8 * c < p.V;
                 tq[c] = in ? tc::ld_global_hint(trow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
                 uq[c] = (in && mode == 1) ? tc::ld_global_hint(urow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
+            uint32_t words[16];
 #pragma unroll
-            for (int g = 0; g < CH / 4; ++g) {
-                const int v0 = vb + 4 * g;
-                if (v0 >= p.V) break;
-                const uint4 &tt = tq[g >> 1];
-                const uint32_t t0 = (g & 1) ? tt.z : tt.x, t1 = (g & 1) ? tt.w : tt.y;
-                const float tv[4] = {tcp::bf16_lo(t0), tcp::bf16_hi(t0), tcp::bf16_lo(t1), tcp::bf16_hi(t1)};
-                const uint4 words =
-                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), p.rk);
-                // rejected position: race over the residual max(0, p - q) only (the race
-                // over p is its fallback for an empty residual and is run by the final
-                // kernel in that case); bonus position: race over p
-                float wv[4];
-                if (mode == 1) {
-                    const uint4 &uu = uq[g >> 1];
-                    const uint32_t u0 = (g & 1) ? uu.z : uu.x, u1 = (g & 1) ? uu.w : uu.y;
-                    const float zv[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(u0),
-                                         __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(u0),
-                                         __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(u1),
-                                         __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(u1)};
+            for (int g = 0; g < 4; ++g) {
+                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)n, (uint32_t)rq, c3), p.rk);
+                words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
+            }
+            // race weights: residual max(0, p - q) (mode 1), p (mode 0), 0 (no race or beyond V)
+            float wv[16], d[16];
+            uint32_t allneg = 0xFFFFFFFFu;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        wv[i] = fmaxf(ex2(fmaf(tv[i], kLog2e, -lsep)) - ex2(fmaf(zv[i], kLog2e, -lseq)), 0.f);
-                    race_feed4(res, wv, words, v0);
-                } else {
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t tt[4] = {tq[c].x, tq[c].y, tq[c].z, tq[c].w};
+                const uint32_t uu[4] = {uq[c].x, uq[c].y, uq[c].z, uq[c].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) wv[i] = ex2(fmaf(tv[i], kLog2e, -lsep));
-                    race_feed4(pr, wv, words, v0);
+                for (int i = 0; i < 8; ++i) {
+                    const int j = 8 * c + i;
+                    const float tv = (i & 1) ? tcp::bf16_hi(tt[i >> 1]) : tcp::bf16_lo(tt[i >> 1]);
+                    const float uv = (i & 1) ? tcp::bf16_hi(uu[i >> 1]) : tcp::bf16_lo(uu[i >> 1]);
+                    const float pv = ex2(fmaf(tv, kLog2e, -lsep));
+                    const float qv = ex2(fmaf(__uint_as_float(acc[j]) + uv, kLog2e, -lseq));
+                    const float w = mode == 1 ? fmaxf(pv - qv, 0.f) : pv;
+                    wv[j] = (mode >= 0 && vb + j < p.V) ? w : 0.f;
+                    d[j] = fmaf(wv[j], C, -one_minus_uniform(words[j]));
+                    allneg &= __float_as_uint(d[j]);
+                }
+            }
+            // exact scores ln w - ln E of the survivors, a column at a time when some lane kept it
+            if (__any_sync(0xffffffffu, (int)allneg >= 0)) {
+                const float best0 = best;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (__any_sync(0xffffffffu, d[j] > 0.f)) {
+                        if (d[j] > 0.f) {
+                            const float score = kLn2 * lg2(wv[j]) - log_exp_variate(one_minus_uniform(words[j]));
+                            if (score > best) {
+                                best = score;
+                                idx = vb + j;
+                            }
+                        }
+                    }
+                }
+                if (best > best0) {
+                    if (best > thr) {
+                        thr = best;
+                        C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
+                    }
+                    if (row_live) P::publish_thr(s, row, pack_winner(best, idx));
                 }
             }
         });
-        // merge the TPR threads of each request (fixed warp order) into this CTA's partial
-        float *mg = P::merge_scratch(s);
-        int *mgi = reinterpret_cast<int *>(mg);
-        mg[et] = res.best;
-        mgi[tcp::kEpiThreads + et] = res.idx;
-        mg[2 * tcp::kEpiThreads + et] = pr.best;
-        mgi[3 * tcp::kEpiThreads + et] = pr.idx;
+        // the CTA's best of each request into its winner word (ties: the lower index)
         tc::named_bar_sync(1, tcp::kEpiThreads);
         if (et < P::MV && m0 + et < p.R) {
-            float b1 = -INFINITY, b2 = -INFINITY;
-            int i1 = -1, i2 = -1;
-            for (int w = et >> 5; w < tcp::kEpiWarps; w += P::DUAL ? 2 : 4) {
-                const int src = w * 32 + (et & 31);
-                race_merge(b1, i1, mg[src], mgi[tcp::kEpiThreads + src]);
-                race_merge(b2, i2, mg[2 * tcp::kEpiThreads + src], mgi[3 * tcp::kEpiThreads + src]);
-            }
-            p.w.part[(size_t)(m0 + et) * p.nparts + cv] = VerifyPartial{b1, b2, i1, i2};
+            const unsigned long long loc = P::read_thr(s, et);
+            if (loc != 0ull) atomicMax(p.w.win + m0 + et, loc);
         }
 
         // Every CTA of the M-tile publishes, waits (bounded; the launch is cooperative,
@@ -211,46 +241,26 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         tc::named_bar_sync(1, tcp::kEpiThreads);
         if (*s.flag) {
             __threadfence();
-            for (int i = cv, n = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++n) {
-                if (warp != n % tcp::kEpiWarps) continue;
+            for (int i = cv, nn = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++nn) {
+                if (warp != nn % tcp::kEpiWarps) continue;
                 const int rq2 = m0 + i;
-                float b1 = -INFINITY, b2 = -INFINITY;
+                const unsigned long long wword = __ldcg(p.w.win + rq2);
+                const int iw = wword != 0ull ? winner_index(wword) : -1;
                 int i1 = -1, i2 = -1;
-                // a lane's slices four at a time, the loads of a batch in flight together
-                for (int q0 = lane; q0 < p.nparts; q0 += 4 * 32) {
-                    float4 vp[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q0 + 32 * q < p.nparts)
-                            vp[q] = __ldcg(reinterpret_cast<const float4 *>(p.w.part + (size_t)rq2 * p.nparts + q0 + 32 * q));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q0 + 32 * q < p.nparts) {
-                            race_merge(b1, i1, vp[q].x, __float_as_int(vp[q].z));
-                            race_merge(b2, i2, vp[q].y, __float_as_int(vp[q].w));
-                        }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float c1 = __shfl_xor_sync(0xffffffffu, b1, off);
-                    const int j1 = __shfl_xor_sync(0xffffffffu, i1, off);
-                    const float c2 = __shfl_xor_sync(0xffffffffu, b2, off);
-                    const int j2 = __shfl_xor_sync(0xffffffffu, i2, off);
-                    race_merge(b1, i1, c1, j1);
-                    race_merge(b2, i2, c2, j2);
-                }
+                const int ell = p.w.ell[rq2], fr = p.w.first_rej[rq2];
+                if (ell >= 0 && fr < ell) i1 = iw;
+                else i2 = iw;
                 // a rejected position whose residual max(0, p - q) came out empty (p equal
                 // to q to rounding everywhere) samples p with the same noise: this warp
                 // runs that race over the whole row
-                const int ell = p.w.ell[rq2], fr = p.w.first_rej[rq2];
-                if (ell >= 0 && fr < ell && i1 < 0 && i2 < 0) {
-                    const int row = p.w.row_of[rq2 * (p.gamma + 1) + fr];
+                if (ell >= 0 && fr < ell && i1 < 0) {
+                    const int row2 = p.w.row_of[rq2 * (p.gamma + 1) + fr];
                     Race fb;
                     race_init(fb);
-                    if (row >= 0) {
-                        const float lsep2 = p.w.lse_p[row] * kLog2e;
+                    if (row2 >= 0) {
+                        const float lsep2 = p.w.lse_p[row2] * kLog2e;
                         const uint32_t c3b = philox_ctr3(p.cycle, 2);
-                        const __nv_bfloat16 *trow2 = p.T + (size_t)row * p.V;
+                        const __nv_bfloat16 *trow2 = p.T + (size_t)row2 * p.V;
                         for (int v0 = 4 * lane; v0 < p.V; v0 += 128) {
                             const uint4 words =
                                 philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)fr, (uint32_t)rq2, c3b), p.rk);
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
 
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>
 using VerifyM64 = tcp::Pipe<64, 128, 9, 0, 1>;  // + static row metadata: within 227 KB
-using VerifyM128 = tcp::Pipe<128, 64, 10, 0, 1>;
+using VerifyM128 = tcp::Pipe<128, 128, 9, 0, 1>;
 using VerifyRnn = tcp::Pipe<128, 64, 10, 0, 2>;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
