@@ -277,10 +277,12 @@ class Cycle:
         return self.wl.R * self.wl.gamma
 
 
-# DRAM bytes (read + write) of one draft launch from the committed ncu capture
-# (profiles/draft_step_tc_qwen4b.md); only for the kernel version that capture
-# measured -- set to None whenever the draft kernel changes
-DRAFT_TRAFFIC_NCU = {"qwen4b": 263274240 + 4504064}
+# DRAM bytes (read + write) of one draft launch from the committed ncu captures
+# (profiles/draft_step_tc_qwen4b.md, profiles/draft_step_tc_heavy_prod.md); only
+# for the kernel version those captures measured -- drop an entry whenever the
+# draft kernel changes
+DRAFT_TRAFFIC_NCU = {"qwen4b": 238636544 + 3832832, "heavy": 1380381440 + 6754560,
+                     "prod": 2323365632 + 9620992}
 
 
 def draft_step_bytes(wl, with_w2=True):
@@ -297,8 +299,37 @@ def draft_cycle_bytes_strict(wl):
     return wl.gamma * draft_step_bytes(wl, with_w2=False) + wl.V * wl.r * es
 
 
+def bind_to_gpu_cpus(device_index):
+    """Restrict this process to the host CPUs NVML reports as local to the GPU,
+    so pinned host buffers (allocated after this) sit on the GPU's NUMA node.
+    Reads the device's affinity only; returns a short description."""
+    try:
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return "unchanged (nvmlInit failed)"
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            return "unchanged (no NVML handle)"
+        n_words = 16  # 64-bit words: up to 1024 CPUs
+        words = (ctypes.c_ulong * n_words)()
+        if lib.nvmlDeviceGetCpuAffinity(h, n_words, words) != 0:
+            return "unchanged (no CPU affinity)"
+        cpus = {64 * i + b for i in range(n_words) for b in range(64) if (words[i] >> b) & 1}
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return "unchanged (empty CPU set)"
+        os.sched_setaffinity(0, cpus)
+        return f"{len(cpus)} CPUs local to the GPU (NVML)"
+    except (OSError, AttributeError, RuntimeError) as e:
+        return f"unchanged ({type(e).__name__})"
+
+
 def run_dspark(args, world, rank, local):
     torch.cuda.set_device(local)
+    host_binding = bind_to_gpu_cpus(local)
     dev = torch.device("cuda", local)
     wl = W.WORKLOADS[args.workload]
     cyc = Cycle(wl, seed=1000 + rank, device=dev)
@@ -376,6 +407,7 @@ def run_dspark(args, world, rank, local):
                    "verify_rows": "all R*(gamma+1)" if not cyc.sched else "scheduled",
                    "l2": "256 MB buffer written between timed steps; U and T also exceed L2",
                    "host": "each timed cycle is enqueued behind a ~1 ms GPU spin (outside the span)",
+                   "host_binding": host_binding,
                    "parallelism": f"replicas x{world} (requests independent)"},
         "drafted_tok_s": world * drafted / (sum(t_draft) / 1e3),
         "verified_tok_s": world * verified / ((sum(t_sched) + sum(t_verify)) / 1e3),
@@ -411,41 +443,69 @@ def run_dspark(args, world, rank, local):
 
 
 def run_e2e(cyc, args, stream, flush):
-    """Same cycle through the public API from pinned host buffers: per step the
-    H2D copy of that cycle's inputs (base logits, hidden states, anchors, target
-    logits) and the D2H read of the results are inside the timed span."""
-    wl, i = cyc.wl, cyc.inp
-    host_in = {k: i[k].cpu().pin_memory() for k in ("U", "h", "anchor")}
+    """Same cycle through the public API from pinned host buffers: every step the
+    H2D copy of that step's inputs (base logits, hidden states, anchors, target
+    logits) and the D2H read of its results are inside the timed span.  The
+    copies run on a second stream into two device input buffers, so step s + 1's
+    inputs travel while step s computes (the double buffering a serving loop
+    would use); the span runs from before step 0's copy to after the last read."""
+    wl = cyc.wl
+    keys = ("U", "h", "anchor")
+    host_in = {k: cyc.inp[k].cpu().pin_memory() for k in keys}
     host_T = cyc.T.cpu().pin_memory()
     host_out = {k: torch.empty_like(v, device="cpu").pin_memory()
                 for k, v in (("out_tokens", cyc.vout["out_tokens"]),
                              ("n_accept", cyc.vout["n_accept"]), ("c", cyc.out["c"]))}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_T.numel() * 2
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    total = 0.0
+    # two device input sets: set 0 is the cycle's own, set 1 a copy of its shapes
+    sets = [(dict(cyc.inp), cyc.T),
+            ({**cyc.inp, **{k: torch.empty_like(cyc.inp[k]) for k in keys}}, torch.empty_like(cyc.T))]
+    copy_stream = torch.cuda.Stream()  # one stream: more streams measured no faster (~206 GB/s H2D)
     n = max(3, min(args.steps, 10))
-    for s in range(n + 2):
+    total = 0.0
+    for rep in range(2):  # the first pass warms up the copy path
+        mk = lambda: torch.cuda.Event(enable_timing=False)
+        copied = [mk() for _ in range(n)]
+        done = [mk() for _ in range(n)]
         flush.zero_()
+        torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
         a.record(stream)
-        for k, t in host_in.items():
-            i[k].copy_(t, non_blocking=True)
-        cyc.T.copy_(host_T, non_blocking=True)
-        cyc.draft(10_000 + s)
-        cyc.schedule(10_000 + s)
-        cyc.target()
-        cyc.verify(10_000 + s)
-        host_out["out_tokens"].copy_(cyc.vout["out_tokens"], non_blocking=True)
-        host_out["n_accept"].copy_(cyc.vout["n_accept"], non_blocking=True)
-        host_out["c"].copy_(cyc.out["c"], non_blocking=True)
+
+        def enqueue_copy(step):
+            inp, T = sets[step % 2]
+            copy_stream.wait_event(a)
+            if step >= 2:
+                copy_stream.wait_event(done[step - 2])  # that buffer's last reader
+            with torch.cuda.stream(copy_stream):
+                for k in keys:
+                    inp[k].copy_(host_in[k], non_blocking=True)
+                T.copy_(host_T, non_blocking=True)
+            copied[step].record(copy_stream)
+
+        enqueue_copy(0)
+        for step in range(n):
+            if step + 1 < n:
+                enqueue_copy(step + 1)
+            cyc.inp, cyc.T = sets[step % 2]
+            stream.wait_event(copied[step])
+            cyc.draft(10_000 + step)
+            cyc.schedule(10_000 + step)
+            cyc.target()
+            cyc.verify(10_000 + step)
+            host_out["out_tokens"].copy_(cyc.vout["out_tokens"], non_blocking=True)
+            host_out["n_accept"].copy_(cyc.vout["n_accept"], non_blocking=True)
+            host_out["c"].copy_(cyc.out["c"], non_blocking=True)
+            done[step].record(stream)
         b.record(stream)
         torch.cuda.synchronize()
-        if s >= 2:
-            total += a.elapsed_time(b)
+        total = a.elapsed_time(b)
+    cyc.inp, cyc.T = sets[0]
     return {"value": n * wl.R * wl.gamma / (total / 1e3), "unit": "tok/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipeline": "step s+1's H2D copies on a second stream during step s (two device input buffers)"}
 
 
 def _oracle_sample(wl, n_req, seed=0):
