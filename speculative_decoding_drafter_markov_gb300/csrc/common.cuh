@@ -39,6 +39,31 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// ---------------------------------------------------------------- paired fp32
+// Two independent fp32 operations in one instruction (the f32x2 forms of
+// sm_100-family GPUs); each lane rounds exactly like the scalar operation.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // ---------------------------------------------------------------- Philox
 struct PhiloxKey {
     uint32_t k0, k1;
@@ -240,17 +265,22 @@ __device__ __forceinline__ void row_set_reference(RowState &s, const float (&z)[
 }
 
 __device__ __forceinline__ float block_exp_sum(const RowState &s, const float (&z)[16], float (&e)[16]) {
-    float sum[16];
+    // arguments z log2(e) - m log2(e) two at a time; the pairwise sum tree adds
+    // j and j + 8, then j + 4, j + 2, j + 1, the same order as a scalar tree
+    const float2 L = make_float2(kLog2e, kLog2e), nm = make_float2(-s.mL, -s.mL);
+    float2 sum[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        e[j] = ex2(fmaf(z[j], kLog2e, -s.mL));
-        sum[j] = e[j];
+    for (int i = 0; i < 8; ++i) {
+        const float2 arg = fma2(make_float2(z[2 * i], z[2 * i + 1]), L, nm);
+        e[2 * i] = ex2(arg.x);
+        e[2 * i + 1] = ex2(arg.y);
+        sum[i] = make_float2(e[2 * i], e[2 * i + 1]);
     }
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+    for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-        for (int j = 0; j < w; ++j) sum[j] += sum[j + w];
-    return sum[0];
+        for (int i = 0; i < w; ++i) sum[i] = add2(sum[i], sum[i + w]);
+    return sum[0].x + sum[0].y;
 }
 
 __device__ __forceinline__ void row_feed16(RowState &s, const float (&z)[16], int v0, const uint32_t (&words)[16]) {
@@ -262,14 +292,20 @@ __device__ __forceinline__ void row_feed16(RowState &s, const float (&z)[16], in
         sum = block_exp_sum(s, z, e);
     }
     s.S += sum;
-    // race filter: d_j = e_j C - t_j (C capped so that e_j = 0 gives d_j = -t_j)
-    const float C = fminf(s.C, 3.0e38f);
+    // race filter: d_j = e_j C - t_j (C capped so that e_j = 0 gives d_j = -t_j);
+    // -t_j = (1 - 2^-24) - (1 + k' 2^-23) exactly (see one_minus_uniform)
+    const float Cc = fminf(s.C, 3.0e38f);
+    const float2 C2 = make_float2(Cc, Cc), c0 = make_float2(1.0f - 1.0f / 16777216.0f, 1.0f - 1.0f / 16777216.0f);
     float d[16];
     uint32_t allneg = 0xFFFFFFFFu;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        d[j] = fmaf(e[j], C, -one_minus_uniform(words[j]));
-        allneg &= __float_as_uint(d[j]);
+    for (int i = 0; i < 8; ++i) {
+        const float2 one_t = make_float2(__uint_as_float(((~words[2 * i]) >> 9) | 0x3F800000u),
+                                         __uint_as_float(((~words[2 * i + 1]) >> 9) | 0x3F800000u));
+        const float2 dd = fma2(make_float2(e[2 * i], e[2 * i + 1]), C2, sub2(c0, one_t));
+        d[2 * i] = dd.x;
+        d[2 * i + 1] = dd.y;
+        allneg &= __float_as_uint(dd.x) & __float_as_uint(dd.y);
     }
     if (__any_sync(0xffffffffu, (int)allneg >= 0)) {
         const float best0 = s.best;

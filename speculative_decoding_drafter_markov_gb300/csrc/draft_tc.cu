@@ -306,8 +306,11 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                         const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            z[8 * o + 2 * i] = __uint_as_float(acc[8 * o + 2 * i]) + tcp::bf16_lo(u[i]);
-                            z[8 * o + 2 * i + 1] = __uint_as_float(acc[8 * o + 2 * i + 1]) + tcp::bf16_hi(u[i]);
+                            const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
+                                                               __uint_as_float(acc[8 * o + 2 * i + 1])),
+                                                   make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
+                            z[8 * o + 2 * i] = zz.x;
+                            z[8 * o + 2 * i + 1] = zz.y;
                         }
                     }
                     row_feed16(st, z, vb, words);
