@@ -105,7 +105,7 @@ __device__ __forceinline__ bool wait_counter(const int *ctr, int target, int32_t
             set_err(err, DSPARK_ERR_TIMEOUT);
             return false;
         }
-        __nanosleep(128);
+        __nanosleep(32);
     }
     return true;
 }
@@ -332,9 +332,25 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 if (row_live && st.best > best0) P::publish_thr(s, row, pack_winner(st.best, st.idx));
             });
 
-            // merge the TPR threads of each request (fixed warp order) into this CTA's
-            // partial and fold its winner into the step's per-request maximum
+            // The next step needs only x_k: fold the CTA's winner of each request (its
+            // shared threshold word, which holds the best of all its threads) into the
+            // step's winner word and publish right away; the partials (m, S, ...) that
+            // lse_k and log q_k need after the last step follow off this path.  Only the
+            // last step publishes after its partials, since they are read right after.
             tc::named_bar_sync(1, tcp::kEpiThreads);  // every warp past its last accumulator
+            const bool last = step + 1 == p.nsteps;
+            if (!last) {
+                if (et < P::MV && m0 + et < p.R) {
+                    const unsigned long long wbest = s.thr[et];
+                    if (wbest != 0ull) atomicMax(win + m0 + et, wbest);
+                }
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                if (et == 0) {
+                    __threadfence();  // cumulative over the CTA's writes before the barrier
+                    atomicAdd(ctr, 1);
+                }
+            }
+            // merge the TPR threads of each request (fixed warp order) into this CTA's partial
             mg[et] = st.m;
             mg[tcp::kEpiThreads + et] = st.S;
             mg[2 * tcp::kEpiThreads + et] = st.best;
@@ -352,11 +368,24 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                               mg[3 * tcp::kEpiThreads + src], reinterpret_cast<int *>(mg)[4 * tcp::kEpiThreads + src]);
                 }
                 part[(size_t)(m0 + et) * p.nparts + cv] = make_partial(f.m, f.S, f.best, f.zbest, f.idx);
-                if (f.idx >= 0) atomicMax(win + m0 + et, pack_winner(f.best, f.idx));
+                if (last && f.idx >= 0) atomicMax(win + m0 + et, pack_winner(f.best, f.idx));
             }
-            __threadfence();
-            tc::named_bar_sync(1, tcp::kEpiThreads);
-            if (et == 0) atomicAdd(ctr, 1);
+            if (last) {
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                if (et == 0) {
+                    __threadfence();
+                    atomicAdd(ctr, 1);
+                }
+            } else if (et < P::MV && m0 + et < p.R) {
+                // pull the W_1 row of the request's best token so far into L2: the winning
+                // CTA's candidate is there when the next operand is gathered
+                const unsigned long long wnow = tc::ld_relaxed_gpu_u64(win + m0 + et);
+                const int xi = wnow != 0ull ? winner_index(wnow) : -1;
+                if (xi >= 0 && xi < p.V) {
+                    const char *rowp = reinterpret_cast<const char *>(p.W1 + (size_t)xi * p.r);
+                    for (int b = 0; b < p.r * 2; b += 128) tc::prefetch_l2(rowp + b);
+                }
+            }
 
             // while the other CTAs finish: confidences c_k of this CTA's rows
             // (local rows cv, cv + nparts, ...; x_{k-1} is still in s.tok)
