@@ -171,6 +171,20 @@ __device__ __forceinline__ uint4 ld_global_hint(const void *ptr, uint64_t policy
     return v;
 }
 
+// per-thread asynchronous 16-byte copy global -> shared through L2 (cp.async),
+// reading src_bytes (16, or 0 to write zeros) with an L2 cache policy
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most n of this thread's committed groups are still in flight
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
 // start pulling the line that holds `ptr` into L2
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));

@@ -22,6 +22,14 @@ namespace dspark {
 
 namespace {
 
+// Per-thread staging of the target and base rows: every epilogue thread copies
+// the 32 + 32 bytes of its next 16-column chunk with cp.async while it works on
+// the current one (two stages).  Stage s, piece k (0-1 target, 2-3 base, 16 B
+// each) of thread et sits at ((s 4 + k) kEpiThreads + et) 16: a warp's reads of
+// one piece are 32 consecutive 16-byte words (no bank conflicts).
+constexpr int kStagePieces = 4;
+constexpr int kStageBytes = 2 * kStagePieces * tcp::kEpiThreads * 16;
+
 struct VerifyTcParams {
     int R, V, r, gamma;
     const __nv_bfloat16 *T, *U, *W1;
@@ -35,6 +43,10 @@ struct VerifyTcParams {
     int32_t *err;
     dspark_verify_args a;  // outputs and the rest of the call (the outcome writer)
 };
+
+__device__ __forceinline__ void cp_async_stage(uint4 *dst, const __nv_bfloat16 *src, uint32_t bytes, uint64_t pol) {
+    tc::cp_async16(dst, src, bytes, pol);
+}
 
 template <class P>
 __global__ void __launch_bounds__(P::kThreads, 1)
@@ -142,11 +154,41 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         // exact score of some element of the request's race.
         float best = -INFINITY, thr = -INFINITY, C = 3.0e38f;
         int idx = -1;
+        // staging: chunk i of this thread lands in stage i % 2; the copy of chunk
+        // i + 1 is in flight while chunk i is processed
+        uint4 *stage = reinterpret_cast<uint4 *>((reinterpret_cast<uintptr_t>(s.smem) + P::kBytes - 1024 + 15) &
+                                                 ~static_cast<uintptr_t>(15));
+        const int c_end = min((t_begin + ntiles) * P::BN, p.V);  // end of this CTA's columns
+        auto stage_chunk = [&](int i, int vb) {
+            uint4 *dst = stage + (size_t)(i & 1) * kStagePieces * tcp::kEpiThreads + et;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const bool in = mode >= 0 && vb + 8 * c < c_end;
+                cp_async_stage(dst + c * tcp::kEpiThreads, in ? trow + vb + 8 * c : trow, in ? 16u : 0u, pol);
+                const bool inu = in && mode == 1;
+                cp_async_stage(dst + (2 + c) * tcp::kEpiThreads, inu ? urow + vb + 8 * c : urow, inu ? 16u : 0u,
+                               pol);
+            }
+            tc::cp_async_commit();
+        };
+        stage_chunk(0, t_begin * P::BN + col0);
+        int ci = 0;
         const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
         unsigned long long *gwin = p.w.win + (row_live ? rq : m0);
         unsigned long long g_next = leader ? tc::ld_relaxed_gpu_u64(gwin) : 0ull, g_sent = 0ull;
         P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err,
                     [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
+            const int vb = n0 + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
+            {
+                // the next chunk: the rest of this warp's block, else the next tile
+                const int vnext = cofs + 16 < P::CW ? vb + 16 : n0 + P::BN + col0;
+                if (vnext < c_end) {
+                    stage_chunk(ci + 1, vnext);
+                    tc::cp_async_wait<1>();
+                } else {
+                    tc::cp_async_wait<0>();
+                }
+            }
             if (leader && cofs == 0) {
                 const unsigned long long g = g_next, loc = P::read_thr(s, row);
                 if (loc > g && loc > g_sent) {
@@ -163,15 +205,17 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
                 }
             }
-            const int vb = n0 + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
-            // the chunk of the target row (and of U_{n+1}), 8 columns per load
+            // the chunk of the target row (and of U_{n+1}) from this thread's stage
             uint4 tq[2], uq[2];
+            {
+                const uint4 *src = stage + (size_t)(ci & 1) * kStagePieces * tcp::kEpiThreads + et;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const bool in = mode >= 0 && vb + 8 * c < p.V;
-                tq[c] = in ? tc::ld_global_hint(trow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
-                uq[c] = (in && mode == 1) ? tc::ld_global_hint(urow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < 2; ++c) {
+                    tq[c] = src[c * tcp::kEpiThreads];
+                    uq[c] = src[(2 + c) * tcp::kEpiThreads];
+                }
             }
+            ++ci;
             uint32_t words[16];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -286,10 +330,11 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     P::teardown(s);
 }
 
-// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>
-using VerifyM64 = tcp::Pipe<64, 128, 9, 0, 1>;  // + static row metadata: within 227 KB
-using VerifyM128 = tcp::Pipe<128, 128, 9, 0, 1>;
-using VerifyRnn = tcp::Pipe<128, 64, 10, 0, 2>;
+// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>;
+// with the 64 KB staging and the static row metadata, within 227 KB
+using VerifyM64 = tcp::Pipe<64, 128, 5, 0, 1>;
+using VerifyM128 = tcp::Pipe<128, 128, 5, 0, 1>;
+using VerifyRnn = tcp::Pipe<128, 64, 3, 0, 2>;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -313,12 +358,13 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.rk = philox_round_keys(a.seed);
     tp.a = a;
     auto kern = verify_phase2_tc<P>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
+    const int smem = P::kBytes + kStageBytes + 16;  // + 16: the stage starts on a 16-byte boundary
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // cooperative: the CTAs of an M-tile wait for one another before the final merge
     void *args[] = {&tmB, &tp};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(mt * nparts), dim3(P::kThreads),
-                                       args, (size_t)P::kBytes, s);
+                                       args, (size_t)smem, s);
 }
 
 }  // namespace
