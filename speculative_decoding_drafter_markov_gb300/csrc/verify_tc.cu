@@ -222,24 +222,43 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)n, (uint32_t)rq, c3), p.rk);
                 words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
             }
-            // race weights: residual max(0, p - q) (mode 1), p (mode 0), 0 (no race or beyond V)
+            // race weights: residual max(0, p - q) (mode 1), p (mode 0), 0 (no race or
+            // beyond V: the stage holds zeros there, so only mode < 0 needs a mask);
+            // paired fp32 operations, two columns at a time
             float wv[16], d[16];
             uint32_t allneg = 0xFFFFFFFFu;
+            const float2 L2e = make_float2(kLog2e, kLog2e), nlp = make_float2(-lsep, -lsep),
+                         nlq = make_float2(-lseq, -lseq), C2 = make_float2(C, C),
+                         c0 = make_float2(1.0f - 1.0f / 16777216.0f, 1.0f - 1.0f / 16777216.0f);
+            const bool live_w = mode >= 0 && vb < p.V;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const uint32_t tt[4] = {tq[c].x, tq[c].y, tq[c].z, tq[c].w};
                 const uint32_t uu[4] = {uq[c].x, uq[c].y, uq[c].z, uq[c].w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = 8 * c + i;
-                    const float tv = (i & 1) ? tcp::bf16_hi(tt[i >> 1]) : tcp::bf16_lo(tt[i >> 1]);
-                    const float uv = (i & 1) ? tcp::bf16_hi(uu[i >> 1]) : tcp::bf16_lo(uu[i >> 1]);
-                    const float pv = ex2(fmaf(tv, kLog2e, -lsep));
-                    const float qv = ex2(fmaf(__uint_as_float(acc[j]) + uv, kLog2e, -lseq));
-                    const float w = mode == 1 ? fmaxf(pv - qv, 0.f) : pv;
-                    wv[j] = (mode >= 0 && vb + j < p.V) ? w : 0.f;
-                    d[j] = fmaf(wv[j], C, -one_minus_uniform(words[j]));
-                    allneg &= __float_as_uint(d[j]);
+                for (int i = 0; i < 4; ++i) {
+                    const int j = 8 * c + 2 * i;
+                    const float2 pa = fma2(make_float2(tcp::bf16_lo(tt[i]), tcp::bf16_hi(tt[i])), L2e, nlp);
+                    const float2 z = add2(make_float2(__uint_as_float(acc[j]), __uint_as_float(acc[j + 1])),
+                                          make_float2(tcp::bf16_lo(uu[i]), tcp::bf16_hi(uu[i])));
+                    const float2 qa = fma2(z, L2e, nlq);
+                    const float2 pv = make_float2(ex2(pa.x), ex2(pa.y));
+                    const float2 qv = make_float2(ex2(qa.x), ex2(qa.y));
+                    float2 w = pv;
+                    if (mode == 1) {
+                        const float2 r = sub2(pv, qv);
+                        w = make_float2(fmaxf(r.x, 0.f), fmaxf(r.y, 0.f));
+                    }
+                    // columns at or beyond V (a ragged last chunk) read zeros, but p of a
+                    // zero logit is not zero: mask them
+                    wv[j] = live_w && vb + j < p.V ? w.x : 0.f;
+                    wv[j + 1] = live_w && vb + j + 1 < p.V ? w.y : 0.f;
+                    const float2 one_t = make_float2(__uint_as_float(((~words[j]) >> 9) | 0x3F800000u),
+                                                     __uint_as_float(((~words[j + 1]) >> 9) | 0x3F800000u));
+                    const float2 dd = fma2(make_float2(wv[j], wv[j + 1]), C2, sub2(c0, one_t));
+                    d[j] = dd.x;
+                    d[j + 1] = dd.y;
+                    allneg &= __float_as_uint(dd.x) & __float_as_uint(dd.y);
                 }
             }
             // exact scores ln w - ln E of the survivors, a column at a time when some lane kept it
