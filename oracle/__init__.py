@@ -67,6 +67,11 @@ def lib():
         L.oracle_verify.restype = i32
         L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P, ctypes.c_double, P]
         L.oracle_sts_fit.restype = i32
+        L.oracle_accept_stats.argtypes = [i32, i32, P, P, P, P, P, P]
+        L.oracle_accept_stats.restype = i32
+        d = ctypes.c_double
+        L.oracle_train_losses.argtypes = [i32, i32, i32, i32, P, P, P, P, d, d, d, P, P, P, P]
+        L.oracle_train_losses.restype = i32
         _lib = L
     return _lib
 
@@ -235,3 +240,50 @@ def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None, edge_eps=0.0):
         raise ValueError(f"oracle_sts_fit failed ({rc})")
     return dict(T=T, ece=ece, curve=curve, index=np.argmin(curve, axis=1).astype(np.int32),
                 near_edge=near)
+
+
+def accept_stats(n_accept, ell=None, gamma=None, *, into=None):
+    """[D] analysis 1: per-position conditional acceptance counts and the
+    acceptance-length histogram of one cycle's verification outcomes, added to
+    ``into`` (a dict from a previous call) or to fresh zero counters."""
+    n_accept = np.ascontiguousarray(n_accept, dtype=np.int32)
+    R = len(n_accept)
+    ell_a = None if ell is None else np.ascontiguousarray(ell, dtype=np.int32)
+    if gamma is None:
+        raise ValueError("gamma is required")
+    out = into if into is not None else dict(
+        reached=np.zeros(gamma, np.uint64), accepted=np.zeros(gamma, np.uint64),
+        tau_hist=np.zeros(gamma + 1, np.uint64), ell_hist=np.zeros(gamma + 1, np.uint64))
+    rc = lib().oracle_accept_stats(R, gamma, _p(n_accept), _p(ell_a), _p(out["reached"]), _p(out["accepted"]),
+                                   _p(out["tau_hist"]), _p(out["ell_hist"]))
+    if rc != 0:
+        raise ValueError("oracle_accept_stats: n_accept outside 0..min(ell, gamma)")
+    return out
+
+
+def train_losses(zd, zt, xs, s, gamma, *, a_ce=0.1, a_tv=0.9, a_conf=1.0, want_grad=False):
+    """[D] Module F, eqs. (8)-(12): per-row (lse_d, lse_t, ce, tv, c*, bce), the
+    losses (L_ce, L_tv, L_conf, L) averaged over the blocks, and optionally the
+    gradients with respect to the draft logits and the confidence logits."""
+    zd, dt = _elem(zd)
+    zt, dt2 = _elem(zt)
+    if dt != dt2:
+        raise TypeError("draft and target logits must share a dtype")
+    N, V = zd.shape
+    if N % gamma:
+        raise ValueError("rows must be blocks x gamma")
+    xs = np.ascontiguousarray(xs, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    row = np.zeros((N, 6))
+    loss = np.zeros(4)
+    gz = np.zeros((N, V)) if want_grad else None
+    gs = np.zeros(N) if want_grad else None
+    rc = lib().oracle_train_losses(N // gamma, gamma, V, dt, _p(zd), _p(zt), _p(xs), _p(s), float(a_ce),
+                                   float(a_tv), float(a_conf), _p(row), _p(loss), _p(gz), _p(gs))
+    if rc != 0:
+        raise ValueError("oracle_train_losses: token outside 0..V-1")
+    out = dict(lse_d=row[:, 0], lse_t=row[:, 1], ce=row[:, 2], tv=row[:, 3], cstar=row[:, 4], bce=row[:, 5],
+               L_ce=loss[0], L_tv=loss[1], L_conf=loss[2], L=loss[3])
+    if want_grad:
+        out.update(grad_z=gz, grad_s=gs)
+    return out

@@ -564,3 +564,104 @@ int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept
     free(bin_sum);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* [D] analysis 1: per-position conditional acceptance, counted over the     */
+/* instances whose first k - 1 positions were accepted; the acceptance       */
+/* length tau = n + 1 (the target's own token included).                      */
+/* ------------------------------------------------------------------------ */
+int oracle_accept_stats(int R, int gamma, const int32_t *n_accept, const int32_t *ell, uint64_t *reached,
+                        uint64_t *accepted, uint64_t *tau_hist, uint64_t *ell_hist) {
+    for (int r = 0; r < R; ++r) {
+        const int l = ell ? ell[r] : gamma;
+        if (l < 0) continue;
+        const int n = n_accept[r];
+        if (n < 0 || n > l || n > gamma || l > gamma) return -1;
+    }
+    for (int r = 0; r < R; ++r) {
+        const int l = ell ? ell[r] : gamma;
+        if (l < 0) continue;
+        const int n = n_accept[r];
+        for (int k = 1; k <= gamma; ++k) {
+            if (l >= k && n >= k - 1) reached[k - 1] += 1; /* position k was tested */
+            if (n >= k) accepted[k - 1] += 1;              /* and passed            */
+        }
+        tau_hist[n] += 1;
+        if (ell_hist) ell_hist[l] += 1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [D] Module F, eqs. (8)-(12): position-weighted cross-entropy, total        */
+/* variation and confidence BCE; the gradient with respect to the draft     */
+/* logits for the first two (the label c* of the third held fixed).          */
+/* ------------------------------------------------------------------------ */
+static double softplus(double t) { return t > 0.0 ? t + log1p(exp(-t)) : log1p(exp(t)); }
+
+int oracle_train_losses(int B, int gamma, int V, int dtype, const void *zd, const void *zt,
+                        const int32_t *xs, const float *s, double a_ce, double a_tv, double a_conf,
+                        double *row, double *loss, double *grad_z, double *grad_s) {
+    const int N = B * gamma;
+    for (int i = 0; i < N; ++i)
+        if (xs[i] < 0 || xs[i] >= V) return -1;
+    double L_ce = 0.0, L_tv = 0.0, L_conf = 0.0;
+    double *pd = (double *)malloc(sizeof(double) * (size_t)V);
+    double *pt = (double *)malloc(sizeof(double) * (size_t)V);
+    for (int i = 0; i < N; ++i) {
+        const int k = i % gamma + 1;
+        const double wk = exp(-(double)(k - 1) / (double)gamma);
+        /* the two softmaxes (max-shifted) */
+        double md = -INFINITY, mt = -INFINITY;
+        for (int v = 0; v < V; ++v) {
+            const double a = load_elem(zd, (size_t)i * V + v, dtype), b = load_elem(zt, (size_t)i * V + v, dtype);
+            if (a > md) md = a;
+            if (b > mt) mt = b;
+        }
+        double Sd = 0.0, St = 0.0;
+        for (int v = 0; v < V; ++v) {
+            pd[v] = exp(load_elem(zd, (size_t)i * V + v, dtype) - md);
+            pt[v] = exp(load_elem(zt, (size_t)i * V + v, dtype) - mt);
+            Sd += pd[v];
+            St += pt[v];
+        }
+        const double lse_d = md + log(Sd), lse_t = mt + log(St);
+        double tv = 0.0;
+        for (int v = 0; v < V; ++v) {
+            pd[v] /= Sd;
+            pt[v] /= St;
+            tv += fabs(pd[v] - pt[v]);
+        }
+        const double ce = lse_d - load_elem(zd, (size_t)i * V + xs[i], dtype);
+        const double cstar = 1.0 - 0.5 * tv;
+        const double si = (double)s[i];
+        const double bce = softplus(si) - cstar * si;
+        double *ro = row + (size_t)i * 6;
+        ro[0] = lse_d; ro[1] = lse_t; ro[2] = ce; ro[3] = tv; ro[4] = cstar; ro[5] = bce;
+        L_ce += wk * ce;
+        L_tv += wk * tv;
+        L_conf += wk * bce;
+        if (grad_z) {
+            double mean_sgn = 0.0; /* sum_u p^d_u sgn(p^d_u - p^t_u) */
+            for (int v = 0; v < V; ++v) {
+                const double dlt = pd[v] - pt[v];
+                mean_sgn += pd[v] * (dlt > 0.0 ? 1.0 : dlt < 0.0 ? -1.0 : 0.0);
+            }
+            for (int v = 0; v < V; ++v) {
+                const double dlt = pd[v] - pt[v];
+                const double sg = dlt > 0.0 ? 1.0 : dlt < 0.0 ? -1.0 : 0.0;
+                const double g_ce = pd[v] - (v == xs[i] ? 1.0 : 0.0);
+                const double g_tv = pd[v] * (sg - mean_sgn);
+                grad_z[(size_t)i * V + v] = wk / B * (a_ce * g_ce + a_tv * g_tv);
+            }
+        }
+        if (grad_s) grad_s[i] = a_conf * wk / B * (1.0 / (1.0 + exp(-si)) - cstar);
+    }
+    free(pd);
+    free(pt);
+    loss[0] = L_ce / B;
+    loss[1] = L_tv / B;
+    loss[2] = L_conf / B;
+    loss[3] = a_ce * loss[0] + a_tv * loss[1] + a_conf * loss[2];
+    return 0;
+}

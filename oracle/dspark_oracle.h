@@ -123,6 +123,44 @@ int oracle_sts_fit(int M, int gamma, const float *logit, const int32_t *n_accept
                    const float *grid, int n_bins, const float *T_prefix, float *T_out,
                    double *ece_out, double *curve, double edge_eps, int32_t *near_edge);
 
+/* Per-position acceptance diagnostics ([D] analysis 1: the per-position
+ * conditional acceptance rate, whose denominator counts only the instances
+ * whose positions 1..k-1 were all accepted; [D] offline results: the
+ * acceptance length tau).  For R requests of one cycle, n_accept [R] accepted
+ * drafted tokens and ell [R] verified drafted tokens (NULL = gamma for all;
+ * ell < 0 = request not verified this cycle, counted nowhere).  ADDS into
+ *   reached [gamma]: position k (index k-1) verified with 1..k-1 accepted,
+ *                    i.e. ell >= k and n >= k - 1;
+ *   accepted [gamma]: position k accepted, i.e. n >= k;
+ *   tau_hist [gamma + 1]: index n = tau - 1 (tau = n + 1 tokens per cycle);
+ *   ell_hist [gamma + 1] (may be NULL): index ell.
+ * Returns 0, or -1 if some n lies outside 0..min(ell, gamma) (nothing added). */
+int oracle_accept_stats(int R, int gamma, const int32_t *n_accept, const int32_t *ell, uint64_t *reached,
+                        uint64_t *accepted, uint64_t *tau_hist, uint64_t *ell_hist);
+
+/* Training losses of the drafter ([D] Module F, eqs. 8-12), for B blocks of
+ * gamma positions (row i = b gamma + k - 1), in fp64:
+ *   w_k = exp(-(k - 1) / gamma);
+ *   p^d_i = softmax(zd_i), p^t_i = softmax(zt_i) over V (zd draft logits,
+ *   zt target logits, dtype f32 or bf16);
+ *   ce_i = -log p^d_i(xs_i) (xs the target's token);
+ *   tv_i = || p^d_i - p^t_i ||_1;  cstar_i = 1 - tv_i / 2 (eq. 8);
+ *   c_i = sigma(s_i) (s the confidence logit);
+ *   bce_i = -[cstar_i log c_i + (1 - cstar_i) log(1 - c_i)], in the stable form
+ *           softplus(s_i) - cstar_i s_i;
+ *   L_ce = (1/B) sum_i w_k ce_i, L_tv = (1/B) sum_i w_k tv_i,
+ *   L_conf = (1/B) sum_i w_k bce_i  (eqs. 9-11, averaged over the blocks);
+ *   L = a_ce L_ce + a_tv L_tv + a_conf L_conf  (eq. 12).
+ * Outputs: row [N, 6] = (lse_d, lse_t, ce, tv, cstar, bce) per row and
+ * loss [4] = (L_ce, L_tv, L_conf, L).  If grad_z [N, V] is non-NULL it gets
+ * dL/dzd with cstar held fixed (a label): w_k / B times
+ *   a_ce (p^d - onehot(xs)) + a_tv p^d (sgn(p^d - p^t) - sum_u p^d_u sgn_u),
+ * sgn(0) = 0; grad_s [N] (may be NULL) gets dL/ds = a_conf w_k / B (c - cstar).
+ * Returns 0, or -1 on a token outside 0..V-1. */
+int oracle_train_losses(int B, int gamma, int V, int dtype, const void *zd, const void *zt,
+                        const int32_t *xs, const float *s, double a_ce, double a_tv, double a_conf,
+                        double *row, double *loss, double *grad_z, double *grad_s);
+
 #ifdef __cplusplus
 }
 #endif
