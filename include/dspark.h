@@ -290,6 +290,76 @@ DSPARK_API size_t dspark_sts_fit_workspace_size(const dspark_sts_args *a);
 DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Acceptance diagnostics ([D] analysis 1: the per-position conditional      */
+/* acceptance rate, whose denominator counts only the instances whose       */
+/* positions 1..k-1 were all accepted; [D] offline results: the acceptance  */
+/* length tau = accepted drafted tokens + the target's own token).           */
+/* For the R requests of one cycle -- n_accept from dspark_verify, ell the    */
+/* verified lengths (the scheduler's ell; NULL means gamma for all; ell < 0:  */
+/* not in this cycle's batch, counted nowhere) -- the call ADDS into caller-  */
+/* owned device counters, so consecutive cycles accumulate:                   */
+/*   reached [gamma]   position k (index k-1) verified with 1..k-1 accepted   */
+/*                     (ell >= k and n >= k - 1);                             */
+/*   accepted [gamma]  position k accepted (n >= k);                          */
+/*   tau_hist [gamma + 1]  requests by n (= tau - 1);                          */
+/*   ell_hist [gamma + 1]  requests by ell (may be NULL).                      */
+/* The conditional acceptance at position k is accepted / reached.  A request */
+/* with n outside 0..min(ell, gamma) is skipped and DSPARK_ERR_RANGE written  */
+/* to *err.  gamma <= DSPARK_DIAG_MAX_GAMMA.  No workspace; one launch.        */
+/* ------------------------------------------------------------------------ */
+#define DSPARK_DIAG_MAX_GAMMA 1024
+typedef struct {
+    int32_t R, gamma;
+    const int32_t *n_accept;      /* [R]                                      */
+    const int32_t *ell;           /* [R] or NULL                              */
+    unsigned long long *reached;  /* [gamma]      accumulated                 */
+    unsigned long long *accepted; /* [gamma]      accumulated                 */
+    unsigned long long *tau_hist; /* [gamma + 1]  accumulated                 */
+    unsigned long long *ell_hist; /* [gamma + 1]  accumulated, or NULL        */
+    int32_t *err;                 /* device error word, or NULL               */
+} dspark_accept_stats_args;
+
+DSPARK_API int dspark_accept_stats(const dspark_accept_stats_args *a, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Drafter training losses ([D] Module F, eqs. 8-12) over B blocks of gamma   */
+/* positions, row i = b gamma + k - 1, with w_k = exp(-(k - 1) / gamma):      */
+/*   p_d = softmax(zd_i), p_t = softmax(zt_i) over V;                          */
+/*   ce_i = -log p_d(xs_i); tv_i = ||p_d - p_t||_1; c*_i = 1 - tv_i / 2 (eq. 8);*/
+/*   bce_i = -[c* log c + (1 - c*) log(1 - c)], c = sigma(s_i), evaluated as   */
+/*           softplus(s_i) - c*_i s_i;                                         */
+/*   L_ce, L_tv, L_conf = (1/B) sum_i w_k (ce_i, tv_i, bce_i)  (eqs. 9-11);    */
+/*   L = a_ce L_ce + a_tv L_tv + a_conf L_conf  (eq. 12; the pages' defaults   */
+/*       are 0.1, 0.9, 1.0).                                                   */
+/* Outputs: row [N, 6] f32 = (lse_d, lse_t, ce, tv, c*, bce) per row (may be  */
+/* NULL); loss [4] f64 = (L_ce, L_tv, L_conf, L), overwritten; grad_z [N, V]  */
+/* f32 = dL/dzd with c* held fixed as a label (may be NULL: forward only):    */
+/* w_k / B [a_ce (p_d - onehot(xs)) + a_tv p_d (sgn(p_d - p_t) - sum_u p_d,u   */
+/* sgn_u)], sgn(0) = 0; grad_s [N] f32 = dL/ds = a_conf w_k / B (c - c*) (may */
+/* be NULL).  zd, zt: dtype f32 or bf16, 16-byte aligned rows (V a multiple  */
+/* of 8 for bf16, of 4 for f32).  Row sums run in fp32, the loss totals in   */
+/* fp64 (added in an unspecified order).  A token outside 0..V-1 writes       */
+/* DSPARK_ERR_RANGE to *err and that row's terms are skipped.  No workspace.  */
+/* One launch (two passes over each row, a third for grad_z; a row's second   */
+/* and third pass read it back from L2).                                     */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t B, gamma, V, dtype;
+    const void *zd;          /* [N, V] draft logits, N = B gamma                 */
+    const void *zt;          /* [N, V] target logits                             */
+    const int32_t *xs;       /* [N] target tokens                                */
+    const float *s;          /* [N] confidence logits                            */
+    float a_ce, a_tv, a_conf;
+    float *row;              /* out [N, 6] or NULL                               */
+    double *loss;            /* out [4]                                          */
+    float *grad_z;           /* out [N, V] or NULL                               */
+    float *grad_s;           /* out [N] or NULL                                  */
+    int32_t *err;            /* device error word, or NULL                       */
+} dspark_train_loss_args;
+
+DSPARK_API int dspark_train_losses(const dspark_train_loss_args *a, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Helpers                                                                    */
 /* ------------------------------------------------------------------------ */
 /* Message of the last failing call on this host thread ("" if none). */

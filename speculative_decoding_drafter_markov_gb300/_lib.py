@@ -56,6 +56,17 @@ class StsArgs(ctypes.Structure):
                 ("n_accept", P), ("grid", P), ("T", P), ("ece", P), ("curve", P), ("err", P)]
 
 
+class AcceptStatsArgs(ctypes.Structure):
+    _fields_ = [("R", i32), ("gamma", i32), ("n_accept", P), ("ell", P), ("reached", P), ("accepted", P),
+                ("tau_hist", P), ("ell_hist", P), ("err", P)]
+
+
+class TrainLossArgs(ctypes.Structure):
+    _fields_ = [("B", i32), ("gamma", i32), ("V", i32), ("dtype", i32), ("zd", P), ("zt", P), ("xs", P),
+                ("s", P), ("a_ce", ctypes.c_float), ("a_tv", ctypes.c_float), ("a_conf", ctypes.c_float),
+                ("row", P), ("loss", P), ("grad_z", P), ("grad_s", P), ("err", P)]
+
+
 class DSparkError(RuntimeError):
     def __init__(self, code, msg):
         super().__init__(f"dspark error {ERROR_NAMES.get(code, code)}: {msg}")
@@ -83,6 +94,8 @@ SYMBOLS = {
     "dspark_wait_selfcheck": ([P, i32, i32, u64, P, P], ctypes.c_int),
     "dspark_sts_fit_workspace_size": ([ctypes.POINTER(StsArgs)], ctypes.c_size_t),
     "dspark_sts_fit": ([ctypes.POINTER(StsArgs), P, P], ctypes.c_int),
+    "dspark_accept_stats": ([ctypes.POINTER(AcceptStatsArgs), P], ctypes.c_int),
+    "dspark_train_losses": ([ctypes.POINTER(TrainLossArgs), P], ctypes.c_int),
 }
 
 
@@ -370,4 +383,61 @@ def sts_fit(logit, n_accept, grid, *, n_bins=15, want_curve=True, ws=None, err=N
     a.T, a.ece, a.curve, a.err = _ptr(out["T"]), _ptr(out["ece"]), _ptr(out["curve"]), _ptr(err)
     ws = _workspace(L.dspark_sts_fit_workspace_size(ctypes.byref(a)), dev, ws)
     _check(L.dspark_sts_fit(ctypes.byref(a), _ptr(ws), _stream(stream)))
+    return out
+
+
+# --------------------------------------------------------------------- diagnostics
+def accept_stats_counters(gamma, device):
+    """Zeroed device counters for accept_stats (uint64 stored as int64)."""
+    z = lambda n: torch.zeros(n, dtype=torch.int64, device=device)
+    return {"reached": z(gamma), "accepted": z(gamma), "tau_hist": z(gamma + 1), "ell_hist": z(gamma + 1)}
+
+
+def accept_stats(n_accept, gamma, *, ell=None, counters=None, err=None, stream=None):
+    """Per-position conditional acceptance counts and the acceptance-length
+    histogram of one cycle (include/dspark.h), added into ``counters`` (a dict
+    from accept_stats_counters; created when None).  n_accept [R] int32 from
+    verify, ell [R] int32 verified lengths or None (gamma for all)."""
+    L = load()
+    dev = n_accept.device
+    if n_accept.dtype != torch.int32 or (ell is not None and ell.dtype != torch.int32):
+        raise TypeError("n_accept and ell are int32")
+    c = counters if counters is not None else accept_stats_counters(gamma, dev)
+    a = AcceptStatsArgs()
+    a.R, a.gamma = n_accept.numel(), int(gamma)
+    a.n_accept, a.ell = _ptr(n_accept), _ptr(ell)
+    a.reached, a.accepted, a.tau_hist = _ptr(c["reached"]), _ptr(c["accepted"]), _ptr(c["tau_hist"])
+    a.ell_hist, a.err = _ptr(c.get("ell_hist")), _ptr(err)
+    _check(L.dspark_accept_stats(ctypes.byref(a), _stream(stream)))
+    return c
+
+
+# --------------------------------------------------------------------- training losses
+def train_losses(zd, zt, xs, s, gamma, *, a_ce=0.1, a_tv=0.9, a_conf=1.0, want_row=True, want_grad=False,
+                 err=None, stream=None):
+    """The drafter's training losses (include/dspark.h; eqs. 8-12): zd, zt [N, V]
+    draft and target logits (bf16 or fp32, N = B gamma), xs [N] int32 target
+    tokens, s [N] fp32 confidence logits.  Returns {"loss": [4] fp64
+    (L_ce, L_tv, L_conf, L), "row": [N, 6] fp32 or None, "grad_z": [N, V] fp32
+    or None, "grad_s": [N] fp32 or None}."""
+    L = load()
+    N, V = zd.shape
+    dev = zd.device
+    if zt.shape != zd.shape or zt.dtype != zd.dtype:
+        raise TypeError("zd and zt must match in shape and dtype")
+    if xs.dtype != torch.int32 or s.dtype != torch.float32:
+        raise TypeError("xs is int32 and s float32")
+    if N % gamma:
+        raise ValueError("rows must be blocks x gamma")
+    a = TrainLossArgs()
+    a.B, a.gamma, a.V, a.dtype = N // gamma, int(gamma), V, _dtype_code(zd)
+    a.zd, a.zt, a.xs, a.s = _ptr(zd), _ptr(zt), _ptr(xs), _ptr(s)
+    a.a_ce, a.a_tv, a.a_conf = float(a_ce), float(a_tv), float(a_conf)
+    out = {"loss": torch.empty(4, dtype=torch.float64, device=dev),
+           "row": torch.empty((N, 6), dtype=torch.float32, device=dev) if want_row else None,
+           "grad_z": torch.empty((N, V), dtype=torch.float32, device=dev) if want_grad else None,
+           "grad_s": torch.empty(N, dtype=torch.float32, device=dev) if want_grad else None}
+    a.row, a.loss, a.grad_z, a.grad_s = _ptr(out["row"]), _ptr(out["loss"]), _ptr(out["grad_z"]), _ptr(out["grad_s"])
+    a.err = _ptr(err)
+    _check(L.dspark_train_losses(ctypes.byref(a), _stream(stream)))
     return out

@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdspark.so")
-SOURCES = ["abi.cu", "draft.cu", "draft_tc.cu", "gemm_lt.cu", "sched.cu", "sts.cu", "verify.cu",
-           "verify_tc.cu"]
+SOURCES = ["abi.cu", "diag.cu", "draft.cu", "draft_tc.cu", "gemm_lt.cu", "sched.cu", "sts.cu",
+           "train_loss.cu", "verify.cu", "verify_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 TU_FLAGS = {}
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

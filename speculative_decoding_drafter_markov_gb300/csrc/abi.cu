@@ -390,6 +390,34 @@ DSPARK_API int dspark_sts_fit(const dspark_sts_args *a, void *ws, dspark_stream_
     return e == cudaSuccess ? ok() : cuda_fail(e, "sts fit");
 }
 
+DSPARK_API int dspark_accept_stats(const dspark_accept_stats_args *a, dspark_stream_t stream) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->R < 0 || a->gamma < 1) return fail(DSPARK_ERR_INVAL, "bad shape R=%d gamma=%d", a->R, a->gamma);
+    if (a->gamma > DSPARK_DIAG_MAX_GAMMA)
+        return fail(DSPARK_ERR_UNSUPPORTED, "gamma=%d above %d", a->gamma, DSPARK_DIAG_MAX_GAMMA);
+    if ((a->R > 0 && !a->n_accept) || !a->reached || !a->accepted || !a->tau_hist)
+        return fail(DSPARK_ERR_INVAL, "null pointer");
+    if (a->R == 0) return ok();
+    cudaError_t e = dspark::launch_accept_stats(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "accept stats");
+}
+
+DSPARK_API int dspark_train_losses(const dspark_train_loss_args *a, dspark_stream_t stream) {
+    if (!a) return fail(DSPARK_ERR_INVAL, "null argument struct");
+    if (a->B < 1 || a->gamma < 1 || a->V < 1)
+        return fail(DSPARK_ERR_INVAL, "bad shape B=%d gamma=%d V=%d", a->B, a->gamma, a->V);
+    if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16) return fail(DSPARK_ERR_INVAL, "bad dtype %d", a->dtype);
+    if ((long long)a->B * a->gamma > 0x7fffffffll) return fail(DSPARK_ERR_UNSUPPORTED, "too many rows");
+    const int vec = a->dtype == DSPARK_BF16 ? 8 : 4;
+    if (a->V % vec) return fail(DSPARK_ERR_UNSUPPORTED, "V=%d not a multiple of %d", a->V, vec);
+    if (!a->zd || !a->zt || !a->xs || !a->s || !a->loss) return fail(DSPARK_ERR_INVAL, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(a->zd) | reinterpret_cast<uintptr_t>(a->zt) |
+         reinterpret_cast<uintptr_t>(a->grad_z)) & 15u)
+        return fail(DSPARK_ERR_INVAL, "logit and gradient rows must be 16-byte aligned");
+    cudaError_t e = dspark::launch_train_losses(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "train losses");
+}
+
 DSPARK_API int dspark_wait_selfcheck(const int32_t *flag, int32_t target, int32_t mode, uint64_t limit_ns,
                                      int32_t *err, dspark_stream_t stream) {
     if (!flag || !err) return fail(DSPARK_ERR_INVAL, "null pointer");

@@ -124,6 +124,10 @@ cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaSt
 bool verify_tc_supported(const dspark_verify_args &a);
 cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s);
 
+// ----- acceptance diagnostics and training losses ------------------------------------
+cudaError_t launch_accept_stats(const dspark_accept_stats_args &a, cudaStream_t s);
+cudaError_t launch_train_losses(const dspark_train_loss_args &a, cudaStream_t s);
+
 // ----- philox check ------------------------------------------------------------------
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t seed, int n, uint32_t *out, cudaStream_t s);
 

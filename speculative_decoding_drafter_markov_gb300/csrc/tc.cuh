@@ -153,6 +153,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
+// L2 policy for data read again soon (keep it over evict-first data)
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
                                                  int c1, int c2, uint64_t policy) {
     asm volatile(

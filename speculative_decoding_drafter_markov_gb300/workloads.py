@@ -120,6 +120,26 @@ def draft_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
     return out
 
 
+def train_loss_inputs(B: int, gamma: int, V: int, dtype=torch.bfloat16, seed: int = 0, device="cpu",
+                      sigma: float = 0.7) -> dict:
+    """Inputs of the drafter's training losses for B blocks of gamma positions:
+    draft logits zd = N(0, 3^2) plus a planted peak of U(5, 9) on one token per
+    row (the draft workloads' base logits), target logits zt = zd + N(0, sigma^2),
+    target tokens xs = the peak token in 80 % of the rows and a uniform token
+    otherwise, confidence logits s ~ N(1, 1)."""
+    g = _gen(seed, device)
+    N = B * gamma
+    zd = torch.randn((N, V), generator=g, device=device) * 3.0
+    tok = torch.randint(0, V, (N,), generator=g, device=device)
+    zd[torch.arange(N, device=device), tok] += 5.0 + 4.0 * torch.rand((N,), generator=g, device=device)
+    zt = zd + torch.randn((N, V), generator=g, device=device) * sigma
+    other = torch.randint(0, V, (N,), generator=g, device=device)
+    keep = torch.rand((N,), generator=g, device=device) < 0.8
+    xs = torch.where(keep, tok, other).to(torch.int32)
+    s = torch.randn((N,), generator=g, device=device) + 1.0
+    return {"zd": zd.to(dtype).contiguous(), "zt": zt.to(dtype).contiguous(), "xs": xs, "s": s}
+
+
 def tags_from_ell(ell) -> np.ndarray:
     """Flattened batch layout: rows grouped by request, positions 0..ell_r."""
     ell = np.asarray(ell, dtype=np.int64)

@@ -122,3 +122,28 @@ def test_host_side_validation(lib):
     assert lib.dspark_sts_fit(byref(t), None, None) == _lib.ERR_INVAL  # null tensors
     # bin sums (8 B each) + counters + two prefix buffers, each 256-byte aligned
     assert lib.dspark_sts_fit_workspace_size(byref(t)) == 4 * 8 * 10 * 8 + 256 + 2 * 256
+    # acceptance diagnostics: shapes, limits and pointers are checked on the host
+    d = _lib.AcceptStatsArgs()
+    assert lib.dspark_accept_stats(None, None) == _lib.ERR_INVAL
+    d.R, d.gamma = 4, 0
+    assert lib.dspark_accept_stats(byref(d), None) == _lib.ERR_INVAL
+    d.gamma = 1025
+    assert lib.dspark_accept_stats(byref(d), None) == _lib.ERR_UNSUPPORTED
+    d.gamma = 8
+    assert lib.dspark_accept_stats(byref(d), None) == _lib.ERR_INVAL  # null counters
+    d.reached = d.accepted = d.tau_hist = ctypes.c_void_p(16)
+    d.R = 0
+    assert lib.dspark_accept_stats(byref(d), None) == _lib.OK  # nothing to count: no launch
+    # training losses
+    tl = _lib.TrainLossArgs()
+    assert lib.dspark_train_losses(None, None) == _lib.ERR_INVAL
+    tl.B, tl.gamma, tl.V, tl.dtype = 2, 4, 100, _lib.BF16
+    assert lib.dspark_train_losses(byref(tl), None) == _lib.ERR_UNSUPPORTED  # V % 8 for bf16
+    tl.V = 96
+    assert lib.dspark_train_losses(byref(tl), None) == _lib.ERR_INVAL  # null tensors
+    tl.dtype = 7
+    assert lib.dspark_train_losses(byref(tl), None) == _lib.ERR_INVAL
+    tl.dtype = _lib.F32
+    tl.zd = tl.zt = tl.xs = tl.s = tl.loss = ctypes.c_void_p(16)
+    tl.grad_z = ctypes.c_void_p(24)
+    assert lib.dspark_train_losses(byref(tl), None) == _lib.ERR_INVAL  # misaligned gradient rows
