@@ -12,12 +12,16 @@ Prints ONE JSON line (rank 0).  `value` is drafted-and-verified tokens per secon
 of device time, R * gamma / (T_draft + T_schedule + T_verify), summed over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dspark|reference]
-                  [--workload qwen4b|heavy|prod|rnn|tiny|sts_fit]
+                  [--workload qwen4b|heavy|prod|rnn|tiny|sts_fit|train_loss]
 
 `--workload sts_fit` times the confidence calibration instead (Module D's
 sequential temperature scaling on a held-out set of draft blocks): one step is
 one full fit, and `value` is (block, position, temperature) evaluations per
 second.
+
+`--workload train_loss` times the drafter's training losses and their gradient
+(Module F, eqs. 8-12) on 64 blocks x 8 positions over V = 151936 (bf16 logits):
+one step is one call, and `value` is positions per second.
 
 `--impl reference` times the CPU oracle (the plain single-threaded checker) on a
 bounded sample of requests of the same workload; it is the reference arm.
@@ -51,7 +55,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
-    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS) + ["sts_fit"])
+    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS) + ["sts_fit", "train_loss"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -435,11 +439,35 @@ def run_dspark(args, world, rank, local):
         "gpu_launches": args.steps * cyc.launches_per_cycle,
         "clocks": clk,
     }
+    line["diagnostics"] = acceptance_diagnostics(cyc)
     if not args.no_e2e:
         line["e2e"] = run_e2e(cyc, args, stream, flush)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
     return line, rank
+
+
+def acceptance_diagnostics(cyc, cycles=16):
+    """Per-position conditional acceptance and the acceptance-length histogram of
+    `cycles` further decoding cycles (untimed), counted on the GPU by
+    dspark_accept_stats from each cycle's verification outcome."""
+    wl = cyc.wl
+    counters = None
+    for c in range(cycles):
+        cyc.draft(20_000 + c)
+        cyc.schedule(20_000 + c)
+        cyc.target()
+        cyc.verify(20_000 + c)
+        ell = cyc.sched_out["ell"] if cyc.sched else None
+        counters = dsp.accept_stats(cyc.vout["n_accept"], wl.gamma, ell=ell, counters=counters)
+    torch.cuda.synchronize()
+    reached = counters["reached"].cpu().numpy()
+    accepted = counters["accepted"].cpu().numpy()
+    tau = counters["tau_hist"].cpu().numpy()
+    cond = [round(float(a) / float(r), 4) if r > 0 else None for a, r in zip(accepted, reached)]
+    return {"cycles": cycles, "conditional_acceptance": cond, "reached": reached.tolist(),
+            "tau_hist": tau.tolist(),
+            "mean_tau": float((tau * np.arange(1, len(tau) + 1)).sum() / max(1, tau.sum()))}
 
 
 def run_e2e(cyc, args, stream, flush):
@@ -715,14 +743,139 @@ def run_sts_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+TRAIN = {"B": 64, "gamma": 8, "V": 151936}
+TRAIN_METRIC = "drafter training losses + gradient: positions/s at 1 GB300; % of HBM roofline"
+
+
+def _train_desc():
+    return (f"train_loss: B={TRAIN['B']} blocks x gamma={TRAIN['gamma']} positions, V={TRAIN['V']}, "
+            f"bf16 draft and target logits, fp32 gradient")
+
+
+def _train_bytes():
+    N, V = TRAIN["B"] * TRAIN["gamma"], TRAIN["V"]
+    return 2 * N * V * 2 + N * V * 4 + N * (4 + 4 + 4 + 24)  # logits read once, gradient written
+
+
+def _train_cpu(budget_s=12.0, n_blocks=1):
+    """The oracle (losses + gradient) on the first n_blocks blocks, per position."""
+    import oracle as orc
+    orc.build()
+    inp = W.train_loss_inputs(n_blocks, TRAIN["gamma"], TRAIN["V"], seed=21, device="cpu")
+    zd, zt = W.bf16_bits(inp["zd"]), W.bf16_bits(inp["zt"])
+    xs, sv = inp["xs"].numpy(), inp["s"].numpy()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        orc.train_losses(zd, zt, xs, sv, TRAIN["gamma"], want_grad=True)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 50:
+            break
+    pos = done * n_blocks * TRAIN["gamma"]
+    return {"value": pos / el, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} calls on {n_blocks} block(s) of the workload (gamma={TRAIN['gamma']}, "
+                      f"V={TRAIN['V']}, losses and gradient), single-threaded C oracle, {el:.1f} s"}
+
+
+def run_train_loss(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g = TRAIN["gamma"]
+    inp = W.train_loss_inputs(TRAIN["B"], g, TRAIN["V"], seed=21 + rank, device=dev)
+    N = TRAIN["B"] * g
+    grad = torch.empty((N, TRAIN["V"]), dtype=torch.float32, device=dev)
+    loss = torch.empty(4, dtype=torch.float64, device=dev)
+    call = lambda: dsp.train_losses(inp["zd"], inp["zt"], inp["xs"], inp["s"], g, want_grad=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for a, b in ev:
+        flush.zero_()
+        torch.cuda._sleep(2_000_000)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    times = [a.elapsed_time(b) for a, b in ev]
+    total_ms, value = aggregate_ranks(sum(times), args.steps * N, world, dev)
+    call_us = 1e3 * statistics.mean(times)
+    achieved = _train_bytes() / (call_us * 1e-6) / 1e9
+    peak, _, peak_src = _peaks()
+    line = {
+        "metric": TRAIN_METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->f32",
+        "data": "synthetic (seeded draft and target logits of the draft workloads' distribution)",
+        "config": {"workload": _train_desc(),
+                   "l2": "256 MB buffer written between timed calls; the logits (311 MB) exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "train_loss_kernel: one launch (memset of the 4 totals before it)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": _train_bytes(),
+                     "bytes_rule": "draft and target logits read once, fp32 gradient written once",
+                     "timing": "CUDA events around the whole call", "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        h_d, h_t = inp["zd"].cpu().pin_memory(), inp["zt"].cpu().pin_memory()
+        h_loss = torch.empty(4, dtype=torch.float64).pin_memory()
+        tot = 0.0
+        for i in range(args.steps + 2):
+            a, b = mk(), mk()
+            a.record(stream)
+            inp["zd"].copy_(h_d, non_blocking=True)
+            inp["zt"].copy_(h_t, non_blocking=True)
+            out = call()
+            h_loss.copy_(out["loss"], non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                tot += a.elapsed_time(b)
+        line["e2e"] = {"value": args.steps * N / (tot / 1e3), "unit": "positions/s",
+                       "h2d_bytes_per_step": int(h_d.numel() * 2 + h_t.numel() * 2), "d2h_bytes_per_step": 32}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _train_cpu()
+    return line, rank
+
+
+def run_train_reference(args, world, rank):
+    if rank != 0:
+        return None
+    cpu = _train_cpu(budget_s=max(1.0, 1.5 * args.steps))
+    N = TRAIN["B"] * TRAIN["gamma"]
+    return {"metric": TRAIN_METRIC, "value": cpu["value"], "unit": "positions/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * N / cpu["value"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": {"workload": _train_desc(), "sample": cpu["sample"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": cpu["value"], "unit": "positions/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
-    if args.workload == "sts_fit":
+    if args.workload in ("sts_fit", "train_loss"):
+        sts = args.workload == "sts_fit"
         if args.impl == "reference":
-            line = run_sts_reference(args, world, rank)
+            line = run_sts_reference(args, world, rank) if sts else run_train_reference(args, world, rank)
         else:
-            line, rank = run_sts_fit(args, world, rank, local)
+            line, rank = (run_sts_fit if sts else run_train_loss)(args, world, rank, local)
         if line is not None and rank == 0:
             print(json.dumps(line), flush=True)
         if world > 1:

@@ -162,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) train_loss_kernel(const dspark_tr
                     widen<T>(raw_t[q], xt);
 #pragma unroll
                     for (int j = 0; j < kVec; ++j) {
-                        const float pd = ex2(fmaf(xd[j], kLog2e, -ld2)), pt = ex2(fmaf(xt[j], kLog2e, -lt2));
-                        const float dl = pd - pt;
-                        tv += fabsf(dl);
-                        msg += dl > 0.f ? pd : (dl < 0.f ? -pd : 0.f);
+                        const float ad = fmaf(xd[j], kLog2e, -ld2), at = fmaf(xt[j], kLog2e, -lt2);
+                        const float pd = ex2(ad), pt = ex2(at);
+                        tv += fabsf(pd - pt);
+                        msg += ad > at ? pd : (ad < at ? -pd : 0.f);  // the sign pass 3 uses
                     }
                 }
             }
@@ -205,9 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1) train_loss_kernel(const dspark_tr
                 float g[kVec];
 #pragma unroll
                 for (int j = 0; j < kVec; ++j) {
-                    const float pd = ex2(fmaf(xd[j], kLog2e, -ld2)), pt = ex2(fmaf(xt[j], kLog2e, -lt2));
-                    const float dl = pd - pt;
-                    const float sg = dl > 0.f ? 1.f : (dl < 0.f ? -1.f : 0.f);
+                    // sgn(p_d - p_t) = sgn(log p_d - log p_t): the target's exponential is not needed
+                    const float ad = fmaf(xd[j], kLog2e, -ld2), at = fmaf(xt[j], kLog2e, -lt2);
+                    const float pd = ex2(ad);
+                    const float sg = ad > at ? 1.f : (ad < at ? -1.f : 0.f);
                     const int v = c * kVec + j;
                     g[j] = gce * (pd - (v == xs ? 1.f : 0.f)) + gtv * pd * (sg - msg);
                 }
