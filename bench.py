@@ -19,6 +19,13 @@ sequential temperature scaling on a held-out set of draft blocks): one step is
 one full fit, and `value` is (block, position, temperature) evaluations per
 second.
 
+`--workload sched_profile` profiles SPS(B) from a stand-in target forward (two bf16
+GEMM layers at d = 2560, timed over B = 16..8704) and runs the prefix scheduler on
+that measured table for R = 16..512 requests of gamma = 16 (with and without the
+early-stop break): `value` is the expected throughput Theta of the no-break
+schedule at R = 256, and the line carries the verify budget per request against
+load (the production section's Figure 8 mechanism, reproduced qualitatively).
+
 `--workload train_loss` times the drafter's training losses and their gradient
 (Module F, eqs. 8-12) on 64 blocks x 8 positions over V = 151936 (bf16 logits):
 one step is one call, and `value` is positions per second.
@@ -55,7 +62,8 @@ def _args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
-    ap.add_argument("--workload", default="qwen4b", choices=sorted(W.WORKLOADS) + ["sts_fit", "train_loss"])
+    ap.add_argument("--workload", default="qwen4b",
+                    choices=sorted(W.WORKLOADS) + ["sts_fit", "train_loss", "sched_profile"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -867,9 +875,68 @@ def run_train_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+SCHED_PROFILE = {"gamma": 16, "R": [16, 32, 64, 128, 256, 512], "d": 2560, "layers": 2, "step": 8}
+SCHED_METRIC = "scheduler on a profiled SPS(B) table: expected throughput Theta (tok/s) at R=256, gamma=16"
+
+
+def run_sched_profile(args, world, rank, local):
+    """Profile SPS(B) from the stand-in target forward, then schedule on it."""
+    from speculative_decoding_drafter_markov_gb300 import sps as sps_mod
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = SCHED_PROFILE
+    g = cfg["gamma"]
+    B_min, B_max = min(cfg["R"]), max(cfg["R"]) * (g + 1)
+    fwd = W.stand_in_target(d=cfg["d"], layers=cfg["layers"], max_B=B_max, device=dev, seed=rank)
+    t0 = time.perf_counter()
+    table = sps_mod.profile_sps(fwd, B_min, B_max, step=cfg["step"], reps=3)
+    prof_s = time.perf_counter() - t0
+    t_d = torch.as_tensor(table, device=dev)
+    curve = []
+    for R in cfg["R"]:
+        c_d = torch.as_tensor(W.confidences(R, g, seed=1000 + R), device=dev)
+        brk = dsp.schedule(c_d, t_d, B_min, mode=dsp.SCHED_SYNC)
+        nob = dsp.schedule(c_d, t_d, B_min, mode=dsp.SCHED_ASYNC, K_in=brk["K_out"])
+        torch.cuda.synchronize()
+        curve.append({"R": R, "ell_break": float(brk["ell"].float().mean()),
+                      "ell_nobreak": float(nob["ell"].float().mean()),
+                      "theta_break": float(brk["theta_best"][0]), "theta_nobreak": float(nob["theta_best"][0])})
+    at = next(p for p in curve if p["R"] == 256)
+    # where the measured curve falls: the largest one-step drops of SPS(B)
+    drops = np.argsort(table[1:] / table[:-1])[:4]
+    line = {
+        "metric": SCHED_METRIC, "value": at["theta_nobreak"], "unit": "tok/s", "n_gpus": world,
+        "steps": 1, "warmup": 0, "ms_per_step": 1e3 * prof_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic confidences; SPS(B) measured on this GPU",
+        "config": {"workload": (f"sched_profile: stand-in target {cfg['layers']} x (bf16 GEMM [B,{cfg['d']}]x"
+                                f"[{cfg['d']},{3 * cfg['d']}] + [B,{3 * cfg['d']}]x[{3 * cfg['d']},{cfg['d']}]), "
+                                f"B={B_min}..{B_max} every {cfg['step']}; R={cfg['R']}, gamma={g}"),
+                   "parallelism": f"replicas x{world}"},
+        "theta_break_at_256": at["theta_break"],
+        "budget_vs_load": curve,
+        "sps_table": {"B_min": B_min, "B_max": B_max, "sps_at_B_min": float(table[0]),
+                      "sps_at_B_max": float(table[-1]),
+                      "largest_drops_at_B": [int(B_min + 1 + i) for i in drops],
+                      "profile_seconds": prof_s},
+        "gpu_launches": 2 * len(cfg["R"]),
+    }
+    return line, rank
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
+    if args.workload == "sched_profile":
+        if args.impl == "reference":
+            line = None if rank != 0 else {"impl": "reference", "unavailable":
+                                           "the profiled table is a measurement of this GPU; no CPU counterpart"}
+        else:
+            line, rank = run_sched_profile(args, world, rank, local)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.workload in ("sts_fit", "train_loss"):
         sts = args.workload == "sts_fit"
         if args.impl == "reference":

@@ -140,6 +140,23 @@ def train_loss_inputs(B: int, gamma: int, V: int, dtype=torch.bfloat16, seed: in
     return {"zd": zd.to(dtype).contiguous(), "zt": zt.to(dtype).contiguous(), "xs": xs, "s": s}
 
 
+def stand_in_target(d: int = 2560, layers: int = 2, max_B: int = 8704, device="cuda", seed: int = 0):
+    """A stand-in for the target model's forward at verify batch B, whose timing
+    gives a profiled SPS(B) table: per layer two bf16 GEMMs, [B, d] x [d, 3d] and
+    [B, 3d] x [3d, d] (an MLP block); the values computed are not used."""
+    g = _gen(seed, device)
+    x = (torch.randn((max_B, d), generator=g, device=device) * 0.1).to(torch.bfloat16)
+    ws = [((torch.randn((d, 3 * d), generator=g, device=device) * 0.02).to(torch.bfloat16),
+           (torch.randn((3 * d, d), generator=g, device=device) * 0.02).to(torch.bfloat16)) for _ in range(layers)]
+
+    def forward(B: int):
+        y = x[:B]
+        for w1, w2 in ws:
+            y = torch.matmul(torch.matmul(y, w1), w2)
+        return y
+    return forward
+
+
 def tags_from_ell(ell) -> np.ndarray:
     """Flattened batch layout: rows grouped by request, positions 0..ell_r."""
     ell = np.asarray(ell, dtype=np.int64)
