@@ -31,6 +31,7 @@ struct TcParams {
     int nsteps;  // steps k .. k + nsteps - 1 (Markov head; 1 for the RNN head)
     int step_index;  // counter index of step k (1 for the first step since the counters were zeroed)
     const __nv_bfloat16 *W1;
+    const __nv_bfloat16 *W2t;  // [V, r] (the W_2^T tiles of the first step are pulled into L2 early)
     const int32_t *x_prev;  // token x_{k-1} of row i at x_prev[i * x_stride]
     int x_stride;
     const float *A_op;  // RNN: operand of row i at A_op[i * a_stride], else null
@@ -226,6 +227,15 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     const int kslabs = p.r / 64;
     int *ctr = p.counters + m_tile;
 
+    // 0. the first step reads this CTA's W_2^T tiles from DRAM: start them towards L2
+    //    now, while the tokens and the first operand are gathered (one M-tile only:
+    //    with several, the M-tiles' CTAs would pull the same tiles; measured no gain)
+    if (threadIdx.x == P::MV && p.n_mtiles == 1) {
+        for (int t = 0; t < ntiles; ++t) {
+            const int n0 = c0 + t * tstride, rows = min(P::BN, p.V - n0);
+            tc::prefetch_l2_bulk(p.W2t + (size_t)n0 * p.r, (uint32_t)(rows * p.r * 2));
+        }
+    }
     // 1. the M-tile's tokens x_{k-1} (one load per row, all in flight together)
     if (threadIdx.x < P::MV) s.tok[threadIdx.x] = load_token(p, m0 + threadIdx.x, p.x_prev, p.x_stride);
     __syncthreads();  // tokens, barriers, thresholds, TMEM
@@ -470,6 +480,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.x = p.x_out; tp.logq = p.logq; tp.lse = p.lse; tp.c = p.c;
     tp.conf_logit = p.conf_logit;
     tp.W1 = static_cast<const __nv_bfloat16 *>(p.W1);
+    tp.W2t = static_cast<const __nv_bfloat16 *>(p.W2t);
     tp.x_prev = p.x_prev; tp.x_stride = p.x_stride;
     tp.A_op = p.A_op; tp.a_stride = p.a_stride;
     tp.seed = p.seed; tp.cycle = p.cycle;

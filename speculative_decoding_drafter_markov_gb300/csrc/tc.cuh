@@ -192,6 +192,11 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
+// start pulling `bytes` bytes at `ptr` into L2 (16-byte aligned, a multiple of 16)
+__device__ __forceinline__ void prefetch_l2_bulk(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 // start pulling the line that holds `ptr` into L2
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
