@@ -48,7 +48,7 @@ __device__ __forceinline__ void cp_async_stage(uint4 *dst, const __nv_bfloat16 *
     tc::cp_async16(dst, src, bytes, pol);
 }
 
-template <class P>
+template <class P, bool STAGE>
 __global__ void __launch_bounds__(P::kThreads, 1)
     verify_phase2_tc(const __grid_constant__ CUtensorMap tmB, const VerifyTcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -154,8 +154,9 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         // exact score of some element of the request's race.
         float best = -INFINITY, thr = -INFINITY, C = 3.0e38f;
         int idx = -1;
-        // staging: chunk i of this thread lands in stage i % 2; the copy of chunk
-        // i + 1 is in flight while chunk i is processed
+        // staging (STAGE): chunk i of this thread lands in stage i % 2; the copy of
+        // chunk i + 1 is in flight while chunk i is processed.  Without it, plain
+        // loads at the start of each chunk.
         uint4 *stage = reinterpret_cast<uint4 *>((reinterpret_cast<uintptr_t>(s.smem) + P::kBytes - 1024 + 15) &
                                                  ~static_cast<uintptr_t>(15));
         const int c_end = min((t_begin + ntiles) * P::BN, p.V);  // end of this CTA's columns
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
             }
             tc::cp_async_commit();
         };
-        stage_chunk(0, t_begin * P::BN + col0);
+        if (STAGE) stage_chunk(0, t_begin * P::BN + col0);
         int ci = 0;
         const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
         unsigned long long *gwin = p.w.win + (row_live ? rq : m0);
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err,
                     [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
             const int vb = n0 + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
-            {
+            if (STAGE) {
                 // the next chunk: the rest of this warp's block, else the next tile
                 const int vnext = cofs + 16 < P::CW ? vb + 16 : n0 + P::BN + col0;
                 if (vnext < c_end) {
@@ -205,14 +206,22 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
                 }
             }
-            // the chunk of the target row (and of U_{n+1}) from this thread's stage
+            // the chunk of the target row (and of U_{n+1}): this thread's stage, or
+            // 16-byte loads (zeros beyond the CTA's columns)
             uint4 tq[2], uq[2];
-            {
+            if (STAGE) {
                 const uint4 *src = stage + (size_t)(ci & 1) * kStagePieces * tcp::kEpiThreads + et;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     tq[c] = src[c * tcp::kEpiThreads];
                     uq[c] = src[(2 + c) * tcp::kEpiThreads];
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const bool in = mode >= 0 && vb + 8 * c < c_end;
+                    tq[c] = in ? tc::ld_global_hint(trow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                    uq[c] = (in && mode == 1) ? tc::ld_global_hint(urow + vb + 8 * c, pol) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             ++ci;
@@ -349,15 +358,17 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     P::teardown(s);
 }
 
-// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>;
-// with the 64 KB staging and the static row metadata, within 227 KB
-using VerifyM64 = tcp::Pipe<64, 128, 5, 0, 1>;
+// Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>.
+// The 128-request configuration stages its rows (64 KB, with a shorter W_2^T ring);
+// measured against plain loads it was faster there and slower for 64 requests and
+// the RNN operand.  With the static row metadata, all within 227 KB.
+using VerifyM64 = tcp::Pipe<64, 128, 9, 0, 1>;
 using VerifyM128 = tcp::Pipe<128, 128, 5, 0, 1>;
-using VerifyRnn = tcp::Pipe<128, 64, 3, 0, 2>;
+using VerifyRnn = tcp::Pipe<128, 64, 10, 0, 2>;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <class P>
+template <class P, bool STAGE>
 cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
     int nparts = 0, mt = 0;
     tc_grid_shape(a.R, a.V, P::MV, P::BN, &nparts, &mt);
@@ -376,8 +387,8 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
     tp.rk = philox_round_keys(a.seed);
     tp.a = a;
-    auto kern = verify_phase2_tc<P>;
-    const int smem = P::kBytes + kStageBytes + 16;  // + 16: the stage starts on a 16-byte boundary
+    auto kern = verify_phase2_tc<P, STAGE>;
+    const int smem = P::kBytes + (STAGE ? kStageBytes + 16 : 0);  // + 16: the stage starts on a 16-byte boundary
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // cooperative: the CTAs of an M-tile wait for one another before the final merge
@@ -396,9 +407,9 @@ bool verify_tc_supported(const dspark_verify_args &a) {
 }
 
 cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
-    if (a.A) return launch_cfg<VerifyRnn>(a, w, s);
-    if (a.R <= 64) return launch_cfg<VerifyM64>(a, w, s);
-    return launch_cfg<VerifyM128>(a, w, s);
+    if (a.A) return launch_cfg<VerifyRnn, false>(a, w, s);
+    if (a.R <= 64) return launch_cfg<VerifyM64, false>(a, w, s);
+    return launch_cfg<VerifyM128, true>(a, w, s);
 }
 
 }  // namespace dspark
