@@ -293,8 +293,8 @@ class Cycle:
 # (profiles/draft_step_tc_qwen4b.md, profiles/draft_step_tc_heavy_prod.md); only
 # for the kernel version those captures measured -- drop an entry whenever the
 # draft kernel changes
-DRAFT_TRAFFIC_NCU = {"qwen4b": 238636544 + 3832832, "heavy": 1380381440 + 6754560,
-                     "prod": 2323365632 + 9620992}
+DRAFT_TRAFFIC_NCU = {"qwen4b": 239431936 + 4006912, "heavy": 1382179584 + 6979840,
+                     "prod": 2328975104 + 9806848}
 
 
 # Philox-4x32-10 throughput of this GPU's integer-multiply pipe: 20 32x32->64
