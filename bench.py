@@ -295,6 +295,9 @@ class Cycle:
 # draft kernel changes
 DRAFT_TRAFFIC_NCU = {"qwen4b": 239431936 + 4006912, "heavy": 1382179584 + 6979840,
                      "prod": 2328975104 + 9806848}
+# the same for the training-loss launch at the train_loss workload
+# (profiles/train_loss_resident_train_loss.md)
+TRAIN_TRAFFIC_NCU = 311273216 + 252015616
 
 
 # Philox-4x32-10 throughput of this GPU's integer-multiply pipe: 20 32x32->64
@@ -852,12 +855,15 @@ def run_train_loss(args, world, rank, local):
         "config": {"workload": _train_desc(),
                    "l2": "256 MB buffer written between timed calls; the logits (311 MB) exceed L2",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"kernel": "train_loss_kernel: one launch (memset of the 4 totals before it)",
+        "roofline": {"kernel": "train_loss_resident: one launch, clusters of 8 CTAs each holding 1/8 of a row "
+                               "pair in shared memory (memset of the 4 totals before it)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_src} copy bandwidth",
                      "algorithmic_bytes_per_launch": _train_bytes(),
                      "bytes_rule": "draft and target logits read once, fp32 gradient written once",
-                     "timing": "CUDA events around the whole call", "traffic": None},
+                     "timing": "CUDA events around the whole call", "traffic": TRAIN_TRAFFIC_NCU,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
+                                       "(part of the gradient is still in L2 when the launch ends)"},
         "gpu_launches": args.steps,
         "clocks": clk,
     }

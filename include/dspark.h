@@ -340,8 +340,10 @@ DSPARK_API int dspark_accept_stats(const dspark_accept_stats_args *a, dspark_str
 /* of 8 for bf16, of 4 for f32).  Row sums run in fp32, the loss totals in   */
 /* fp64 (added in an unspecified order).  A token outside 0..V-1 writes       */
 /* DSPARK_ERR_RANGE to *err and that row's terms are skipped.  No workspace.  */
-/* One launch (two passes over each row, a third for grad_z; a row's second   */
-/* and third pass read it back from L2).                                     */
+/* One launch.  Each row is swept three times (twice without grad_z).  For  */
+/* V <= ~226K (bf16) or ~113K (f32) a cluster of 8 CTAs holds the row pair   */
+/* in shared memory, 1/8 each, and HBM sees it once; for larger V the second */
+/* and third sweeps read the row back from L2.                               */
 /* ------------------------------------------------------------------------ */
 typedef struct {
     int32_t B, gamma, V, dtype;

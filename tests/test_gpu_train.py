@@ -102,6 +102,27 @@ def test_full_size_sampled_blocks(orc):
     _check(orc, inp, gamma, rows=rows)
 
 
+def test_many_rows_per_cluster(orc):
+    # 160 rows over the resident kernel's clusters of 8 CTAs: every cluster
+    # reloads its slices several times; every element checked
+    inp = W.train_loss_inputs(40, 4, 4104, dtype=torch.bfloat16, seed=6, device="cuda")
+    _check(orc, inp, 4)
+
+
+def test_tiny_vocab_empty_slices(orc):
+    # V = 16 over 8 CTAs: slices are rounded to 16 bytes, so six CTAs hold nothing
+    inp = W.train_loss_inputs(2, 3, 16, dtype=torch.bfloat16, seed=7, device="cuda")
+    _check(orc, inp, 3)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_streaming_kernel(orc, dtype):
+    # V = 262144: a CTA's slice pair (128 KB for bf16, 256 KB for f32) leaves no
+    # room for a second CTA on the SM, so the rows stream through L2 instead
+    inp = W.train_loss_inputs(1, 2, 262144, dtype=dtype, seed=8, device="cuda")
+    _check(orc, inp, 2)
+
+
 def test_bad_token_reported():
     inp = W.train_loss_inputs(1, 2, 64, dtype=torch.float32, seed=5, device="cuda")
     inp["xs"][1] = 64
