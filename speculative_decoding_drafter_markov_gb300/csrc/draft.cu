@@ -199,20 +199,22 @@ __global__ void __launch_bounds__(256) rnn_hproj_kernel(int M, int d, int r, con
 // + Hpre_k, then s_k = sigma(G_g) s_{k-1} + (1 - sigma(G_g)) tanh(G_c) and the
 // bias operand A_k = tanh(G_o).  CTA (ib, qb) computes entries i0 .. i0 + IB - 1
 // of the three gates for requests q0 .. q0 + RB - 1: the 3 IB rows of W and the
-// RB vectors z are staged in shared memory as fp32 (rows padded by one word,
-// so the lanes of a warp read distinct banks), one thread per (request, i).
-// Rows are padded by 4 words: 16-byte aligned for vector reads, and the 8
-// weight rows of a warp start 4 banks apart.
+// RB vectors z are staged in shared memory as fp32, and kRnnKS adjacent lanes
+// share each (request, i), lane ks taking the 16-byte groups 4 ks, 4 ks + 16, ...
+// of the 2r inputs (short dependence chains, four times the threads), then a
+// two-step shuffle sum.  Rows are padded by 16 words: 16-byte aligned, and two
+// weight rows read by one quarter-warp sit 64 bytes apart in the banks.
 // The state is double-buffered (s_in -> s_out) since every CTA reads whole
 // rows of s_{k-1}.
 constexpr int kRnnIB = 8;
+constexpr int kRnnKS = 4;
 
 template <typename T, int RB>
-__global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) {
+__global__ void __launch_bounds__(RB * kRnnIB * kRnnKS, 1) rnn_step_kernel(const RnnStep p) {
     extern __shared__ float sh[];
-    const int r = p.r, K = 2 * r, ld = K + 4;
-    float *Ws = sh;                    // [3 IB][K + 1]: rows g r + i0 + ii, g = gate
-    float *Zs = sh + 3 * kRnnIB * ld;  // [RB][K + 1]
+    const int r = p.r, K = 2 * r, ld = K + 16;
+    float *Ws = sh;                    // [3 IB][ld]: rows g r + i0 + ii, g = gate
+    float *Zs = sh + 3 * kRnnIB * ld;  // [RB][ld]
     const int i0 = blockIdx.x * kRnnIB, q0 = blockIdx.y * RB;
     const int ldw = 2 * r + p.d;
     const T *W = static_cast<const T *>(p.W);
@@ -281,14 +283,24 @@ __global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) 
             Zs[q * ld + j] = v;
         }
     }
-    __syncthreads();
-    const int q = threadIdx.x / kRnnIB, ii = threadIdx.x - q * kRnnIB;
+    // this thread's (request, entry, input share); the h-projection terms are
+    // loaded now, off the dependence chain of the dot products
+    const int ks = threadIdx.x % kRnnKS, qi = threadIdx.x / kRnnKS;
+    const int q = qi / kRnnIB, ii = qi - q * kRnnIB;
     const int rq = q0 + q, i = i0 + ii;
+    const bool out = ks == 0 && rq < p.R && i < r;
+    float hg = 0.f, hc = 0.f, ho = 0.f;
+    if (out) {
+        const float *hp = p.Hpre + ((size_t)rq * p.gamma + (p.k - 1)) * (size_t)(3 * r);
+        hg = hp[i];
+        hc = hp[r + i];
+        ho = hp[2 * r + i];
+    }
+    __syncthreads();
     const float *z = Zs + q * ld;
     const float *wg = Ws + ii * ld, *wc = Ws + (kRnnIB + ii) * ld, *wo = Ws + (2 * kRnnIB + ii) * ld;
     float gg = 0.f, gc = 0.f, go = 0.f;
-    int j = 0;
-    for (; j + 4 <= K; j += 4) {
+    for (int j = 4 * ks; j + 4 <= K; j += 4 * kRnnKS) {
         const float4 zv = *reinterpret_cast<const float4 *>(z + j);
         const float4 a = *reinterpret_cast<const float4 *>(wg + j);
         const float4 b = *reinterpret_cast<const float4 *>(wc + j);
@@ -297,17 +309,23 @@ __global__ void __launch_bounds__(RB * kRnnIB) rnn_step_kernel(const RnnStep p) 
         gc = fmaf(b.x, zv.x, gc); gc = fmaf(b.y, zv.y, gc); gc = fmaf(b.z, zv.z, gc); gc = fmaf(b.w, zv.w, gc);
         go = fmaf(c.x, zv.x, go); go = fmaf(c.y, zv.y, go); go = fmaf(c.z, zv.z, go); go = fmaf(c.w, zv.w, go);
     }
-    for (; j < K; ++j) {
-        const float zj = z[j];
-        gg = fmaf(wg[j], zj, gg);
-        gc = fmaf(wc[j], zj, gc);
-        go = fmaf(wo[j], zj, go);
+    if (ks == 0)
+        for (int j = K & ~3; j < K; ++j) {  // K % 4 trailing inputs
+            const float zj = z[j];
+            gg = fmaf(wg[j], zj, gg);
+            gc = fmaf(wc[j], zj, gc);
+            go = fmaf(wo[j], zj, go);
+        }
+#pragma unroll
+    for (int off = 1; off < kRnnKS; off <<= 1) {
+        gg += __shfl_xor_sync(0xffffffffu, gg, off);
+        gc += __shfl_xor_sync(0xffffffffu, gc, off);
+        go += __shfl_xor_sync(0xffffffffu, go, off);
     }
-    if (rq < p.R && i < r) {
-        const float *hp = p.Hpre + ((size_t)rq * p.gamma + (p.k - 1)) * (size_t)(3 * r);
-        gg += hp[i];
-        gc += hp[r + i];
-        go += hp[2 * r + i];
+    if (out) {
+        gg += hg;
+        gc += hc;
+        go += ho;
         const float g = 1.0f / (1.0f + expf(-gg));
         p.s_out[(size_t)rq * r + i] = g * z[i] + (1.0f - g) * tanhf(gc);
         p.A[((size_t)rq * p.gamma + (p.k - 1)) * (size_t)r + i] = tanhf(go);
@@ -357,20 +375,19 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
 
 template <typename T, int RB>
 static cudaError_t launch_rnn_step_t(const RnnStep &p, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 4);
+    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 16);
     auto kern = rnn_step_kernel<T, RB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((p.r + kRnnIB - 1) / kRnnIB, (p.R + RB - 1) / RB);
-    kern<<<grid, RB * kRnnIB, smem, s>>>(p);
+    kern<<<grid, RB * kRnnIB * kRnnKS, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s) {
-    // 32 requests per CTA up to r = 256 (120 KB of shared memory), 16 above
-    if (p.dtype == DSPARK_BF16)
-        return p.r <= 256 ? launch_rnn_step_t<__nv_bfloat16, 32>(p, s) : launch_rnn_step_t<__nv_bfloat16, 16>(p, s);
-    return p.r <= 256 ? launch_rnn_step_t<float, 32>(p, s) : launch_rnn_step_t<float, 16>(p, s);
+    // 16 requests per CTA (512 threads; 82 KB of shared memory at r = 256)
+    if (p.dtype == DSPARK_BF16) return launch_rnn_step_t<__nv_bfloat16, 16>(p, s);
+    return launch_rnn_step_t<float, 16>(p, s);
 }
 
 }  // namespace dspark

@@ -37,7 +37,7 @@ def _table(R, gamma, kind, seed=0):
 
 
 @pytest.mark.parametrize("R,gamma", [(1, 1), (4, 4), (7, 3), (64, 8), (256, 16), (512, 16),
-                                     (8192, 1), (3, 5)])
+                                     (8192, 1), (3, 5), (2, 700), (3, 1000), (1, 8192)])
 @pytest.mark.parametrize("kind", ["smooth", "steep", "saw"])
 def test_sync(orc, R, gamma, kind):
     c = W.confidences(R, gamma, seed=R * 31 + gamma)
