@@ -91,6 +91,41 @@ __device__ __forceinline__ void confidence_row(const TcParams &p, int k, int gro
     tc::named_bar_sync(1, tcp::kEpiThreads);
 }
 
+// The same for one request by one warp (lanes over 16-byte chunks, four in
+// flight, then a fixed shuffle tree; lane 0 writes): the confidences deferred
+// to the end of the launch.
+__device__ __forceinline__ void confidence_warp(const TcParams &p, int k, int grow, int xp, int lane) {
+    const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
+    const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
+    float dot = 0.f;
+    if ((p.d & 7) == 0) {
+        const int hc = p.d / 8, nc = hc + p.r / 8;
+#pragma unroll 4
+        for (int ch = lane; ch < nc; ch += 32) {
+            const uint4 raw = ch < hc ? *reinterpret_cast<const uint4 *>(h + ch * 8)
+                                      : *reinterpret_cast<const uint4 *>(e + (ch - hc) * 8);
+            const float *wv = p.w + ch * 8;
+            const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dot = fmaf(wv[2 * i], tcp::bf16_lo(v[i]), dot);
+                dot = fmaf(wv[2 * i + 1], tcp::bf16_hi(v[i]), dot);
+            }
+        }
+    } else {
+        for (int j = lane; j < p.d + p.r; j += 32)
+            dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) {
+        const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
+        const size_t o = (size_t)grow * p.gamma + (k - 1);
+        p.c[o] = 1.0f / (1.0f + expf(-dot / T_k));
+        if (p.conf_logit) p.conf_logit[o] = dot;
+    }
+}
+
 __device__ __forceinline__ int ld_acquire(const int *ptr) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -204,10 +239,12 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
 // (bounded wait; the launch is cooperative, so all are resident) each reads
 // the winners x_k of its rows and gathers the next operand W_1[x_k] right away
 // -- the producer has already streamed the next step's first W_2^T slabs and U
-// tiles.  The confidences of its rows are computed while it waits for the
-// other CTAs.  Nothing else sits between two steps: the rows' lse_k and
-// log q_k (which need every CTA's partial) are finalised after the last step,
-// all (step, request) pairs of the M-tile spread over the CTAs' warps.
+// tiles.  While it waits for the other CTAs, CTA cv computes the confidence
+// of row cv (one row per CTA hides behind the wait; the rows beyond the
+// M-tile's CTA count, with more requests than CTAs, are deferred).  Nothing
+// else sits between two steps: the rows' lse_k and log q_k (which need every
+// CTA's partial) and the deferred confidences (x_{k-1} from the per-step
+// winner words) are computed after the last step, spread over the CTAs' warps.
 template <class P>
 __global__ void __launch_bounds__(P::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
@@ -267,7 +304,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         const bool row_live = grow < p.R;
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         float *mg = P::merge_scratch(s);
-        float *wsc = mg + 5 * tcp::kEpiThreads;  // 80 floats of finalise scratch
         for (int step = 0; step < p.nsteps; ++step) {
             const int k = p.k + step, q = p.step_index + step;
             DraftPartial *part = p.part + (size_t)(q - 1) * p.R * p.nparts;
@@ -397,9 +433,9 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 }
             }
 
-            // while the other CTAs finish: confidences c_k of this CTA's rows
-            // (local rows cv, cv + nparts, ...; x_{k-1} is still in s.tok)
-            for (int i = cv; i < P::MV && m0 + i < p.R; i += p.nparts) confidence_row(p, k, m0 + i, s.tok[i], et, s.red);
+            // while the other CTAs finish: the confidence c_k of local row cv
+            // (x_{k-1} is still in s.tok)
+            if (cv < P::MV && m0 + cv < p.R) confidence_row(p, k, m0 + cv, s.tok[cv], et, s.red);
 
             // wait (bounded) until every CTA of the M-tile has published this step
             if (et == 0) *s.flag = !*s.abort_flag && wait_counter(ctr, q * p.nparts, p.err) ? 1 : 0;
@@ -432,6 +468,22 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 const int si = pi / P::MV, i = pi - si * P::MV;
                 if (m0 + i < p.R)
                     finalise_row(p, p.part + (size_t)(p.step_index + si - 1) * p.R * p.nparts, m0 + i, p.k + si, lane);
+            }
+            // deferred confidences: local rows nparts .. MV - 1 of every step; x_{k-1}
+            // is the launch's input token for its first step, else the previous
+            // step's winner (as the operand took it)
+            const int nrest = P::MV - p.nparts;
+            for (int pi = cv * tcp::kEpiWarps + warp; pi < p.nsteps * nrest; pi += p.nparts * tcp::kEpiWarps) {
+                const int si = pi / nrest, gr = m0 + p.nparts + (pi - si * nrest);
+                if (gr >= p.R) continue;
+                int xp;
+                if (si == 0) {
+                    xp = load_token(p, gr, p.x_prev, p.x_stride);
+                } else {
+                    xp = winner_index(__ldcg(p.winners + (size_t)(p.step_index + si - 2) * p.R + gr));
+                    if (xp < 0 || xp >= p.V) xp = 0;
+                }
+                confidence_warp(p, p.k + si, gr, xp, lane);
             }
         }
     }
