@@ -293,8 +293,8 @@ class Cycle:
 # (profiles/draft_step_tc_qwen4b.md, profiles/draft_step_tc_heavy_prod.md); only
 # for the kernel version those captures measured -- drop an entry whenever the
 # draft kernel changes
-DRAFT_TRAFFIC_NCU = {"qwen4b": 239431936 + 4006912, "heavy": 1382179584 + 6979840,
-                     "prod": 2328975104 + 9806848}
+DRAFT_TRAFFIC_NCU = {"qwen4b": 239669504 + 3837696, "heavy": 1376131840 + 6041856,
+                     "prod": 2314692352 + 7125248}
 # the same for the training-loss launch at the train_loss workload
 # (profiles/train_loss_resident_train_loss.md)
 TRAIN_TRAFFIC_NCU = 311273216 + 252015616
