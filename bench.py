@@ -245,9 +245,10 @@ class Cycle:
                                            inp["W2t"], A=self.out.get("A"))
         self.vws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         # library kernels per cycle: the gamma Markov draft steps (one launch) or,
-        # RNN head, the h projection then per step the state update and the step;
-        # schedule + build_tags; verify (init, phase 1, phase 2 with the final merge)
-        n_draft = 1 + 2 * gm if self.rnn else 1
+        # RNN head, the h projection, the first step's state update, then one
+        # launch per step (which ends with the next step's update); schedule +
+        # build_tags; verify (init, phase 1, phase 2 with the final merge)
+        n_draft = 2 + gm if self.rnn else 1
         self.launches_per_cycle = n_draft + 3 + (2 if self.sched else 0)
 
     def draft(self, cycle):

@@ -134,22 +134,35 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         cudaError_t e = launch_draft_step_tc(st, s);
         return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft steps (tensor cores)");
     }
+    // the RNN state update of step k: s_{k-1} in buffer (k - 1) % 2, s_k into buffer k % 2
+    auto rnn_update = [&](int k) {
+        RnnStep rs = *rnn;
+        if ((k & 1) == 0) {
+            rs.s_in = rnn->s_out;
+            rs.s_out = const_cast<float *>(rnn->s_in);
+        }
+        rs.k = k;
+        rs.x_prev = k == 1 ? a->anchor : a->x + (k - 2);
+        rs.x_stride = k == 1 ? 1 : a->gamma;
+        rs.x_win = nullptr;
+        return rs;
+    };
     for (int k = k_first; k <= k_last; ++k) {
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
         const int xs = k == 1 ? 1 : a->gamma;
         if (rnn) {
-            // state double buffer: s_{k-1} in buffer (k - 1) % 2, s_k into buffer k % 2
-            RnnStep rs = *rnn;
-            if ((k & 1) == 0) {
-                rs.s_in = rnn->s_out;
-                rs.s_out = const_cast<float *>(rnn->s_in);
+            // on the tensor cores the update of step k > k_first ran at the end of the
+            // previous step's launch, from that step's race winners
+            if (!use_tc || k == k_first) {
+                cudaError_t e = launch_rnn_step(rnn_update(k), s);
+                if (e != cudaSuccess) return cuda_fail(e, "rnn step");
             }
-            rs.k = k;
-            rs.x_prev = xp;
-            rs.x_stride = xs;
-            cudaError_t e = launch_rnn_step(rs, s);
-            if (e != cudaSuccess) return cuda_fail(e, "rnn step");
             st.A_op = A_rnn + (size_t)(k - 1) * a->r;
+            st.rnn_next_on = use_tc && k < k_last;
+            if (st.rnn_next_on) {
+                st.rnn_next = rnn_update(k + 1);
+                st.rnn_next.x_win = st.winners + (size_t)(k - 1) * a->R;  // step k's winners (counter index k)
+            }
         }
         st.k = k;
         st.step_index = k;

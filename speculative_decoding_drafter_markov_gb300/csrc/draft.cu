@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rnn_step.cuh"
 
 namespace dspark {
 
@@ -195,141 +196,17 @@ __global__ void __launch_bounds__(256) rnn_hproj_kernel(int M, int d, int r, con
         }
 }
 
-// One step of eq. (6) after the h_k part: G = W[:, :2r] [s_{k-1}; W_1[x_{k-1}]]
-// + Hpre_k, then s_k = sigma(G_g) s_{k-1} + (1 - sigma(G_g)) tanh(G_c) and the
-// bias operand A_k = tanh(G_o).  CTA (ib, qb) computes entries i0 .. i0 + IB - 1
-// of the three gates for requests q0 .. q0 + RB - 1: the 3 IB rows of W and the
-// RB vectors z are staged in shared memory as fp32, and kRnnKS adjacent lanes
-// share each (request, i), lane ks taking the 16-byte groups 4 ks, 4 ks + 16, ...
-// of the 2r inputs (short dependence chains, four times the threads), then a
-// two-step shuffle sum.  Rows are padded by 16 words: 16-byte aligned, and two
-// weight rows read by one quarter-warp sit 64 bytes apart in the banks.
+// One step of eq. (6) after the h_k part, one tile (rnn_step.cuh) per CTA.
 // The state is double-buffered (s_in -> s_out) since every CTA reads whole
 // rows of s_{k-1}.
-constexpr int kRnnIB = 8;
-constexpr int kRnnKS = 4;
+struct CtaSync {
+    __device__ void operator()() const { __syncthreads(); }
+};
 
-template <typename T, int RB>
-__global__ void __launch_bounds__(RB * kRnnIB * kRnnKS, 1) rnn_step_kernel(const RnnStep p) {
+template <typename T>
+__global__ void __launch_bounds__(rnn::kThreads, 1) rnn_step_kernel(const RnnStep p) {
     extern __shared__ float sh[];
-    const int r = p.r, K = 2 * r, ld = K + 16;
-    float *Ws = sh;                    // [3 IB][ld]: rows g r + i0 + ii, g = gate
-    float *Zs = sh + 3 * kRnnIB * ld;  // [RB][ld]
-    const int i0 = blockIdx.x * kRnnIB, q0 = blockIdx.y * RB;
-    const int ldw = 2 * r + p.d;
-    const T *W = static_cast<const T *>(p.W);
-    const T *W1 = static_cast<const T *>(p.W1);
-    __shared__ int s_xp[RB];
-    if (threadIdx.x < RB) {
-        const int rq = q0 + threadIdx.x;
-        int xp = rq < p.R ? p.x_prev[(size_t)rq * p.x_stride] : 0;
-        if (xp < 0 || xp >= p.V) {
-            if (rq < p.R) set_err(p.err, DSPARK_ERR_RANGE);
-            xp = 0;
-        }
-        s_xp[threadIdx.x] = xp;
-    }
-    __syncthreads();
-    constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
-    if (r % kVec == 0 && ldw % kVec == 0) {
-        // 16-byte loads, several in flight per thread (the loops are unrolled)
-        const int cpr = K / kVec;  // chunks per staged row
-#pragma unroll 4
-        for (int e = threadIdx.x; e < 3 * kRnnIB * cpr; e += blockDim.x) {
-            const int row = e / cpr, c = e - row * cpr;
-            const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
-            float *dst = Ws + row * ld + c * kVec;
-            if (i < r) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(W + (size_t)(g * r + i) * ldw + c * kVec);
-                const T *vals = reinterpret_cast<const T *>(&raw);
-#pragma unroll
-                for (int k = 0; k < kVec; ++k) dst[k] = to_f32(vals[k]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < kVec; ++k) dst[k] = 0.f;
-            }
-        }
-#pragma unroll 4
-        for (int e = threadIdx.x; e < RB * cpr; e += blockDim.x) {
-            const int q = e / cpr, c = e - q * cpr, rq = q0 + q, j = c * kVec;
-            float *dst = Zs + q * ld + j;
-            if (rq >= p.R) {
-#pragma unroll
-                for (int k = 0; k < kVec; ++k) dst[k] = 0.f;
-            } else if (j < r) {
-                const float *src = p.s_in + (size_t)rq * r + j;
-#pragma unroll
-                for (int k = 0; k < kVec; k += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(src + k);
-                    dst[k] = f.x; dst[k + 1] = f.y; dst[k + 2] = f.z; dst[k + 3] = f.w;
-                }
-            } else {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(W1 + (size_t)s_xp[q] * r + (j - r));
-                const T *vals = reinterpret_cast<const T *>(&raw);
-#pragma unroll
-                for (int k = 0; k < kVec; ++k) dst[k] = to_f32(vals[k]);
-            }
-        }
-    } else {
-        for (int e = threadIdx.x; e < 3 * kRnnIB * K; e += blockDim.x) {
-            const int row = e / K, j = e - row * K;
-            const int g = row / kRnnIB, i = i0 + (row - g * kRnnIB);
-            Ws[row * ld + j] = i < r ? to_f32(W[(size_t)(g * r + i) * ldw + j]) : 0.f;
-        }
-        for (int e = threadIdx.x; e < RB * K; e += blockDim.x) {
-            const int q = e / K, j = e - q * K, rq = q0 + q;
-            float v = 0.f;
-            if (rq < p.R) v = j < r ? p.s_in[(size_t)rq * r + j] : to_f32(W1[(size_t)s_xp[q] * r + (j - r)]);
-            Zs[q * ld + j] = v;
-        }
-    }
-    // this thread's (request, entry, input share); the h-projection terms are
-    // loaded now, off the dependence chain of the dot products
-    const int ks = threadIdx.x % kRnnKS, qi = threadIdx.x / kRnnKS;
-    const int q = qi / kRnnIB, ii = qi - q * kRnnIB;
-    const int rq = q0 + q, i = i0 + ii;
-    const bool out = ks == 0 && rq < p.R && i < r;
-    float hg = 0.f, hc = 0.f, ho = 0.f;
-    if (out) {
-        const float *hp = p.Hpre + ((size_t)rq * p.gamma + (p.k - 1)) * (size_t)(3 * r);
-        hg = hp[i];
-        hc = hp[r + i];
-        ho = hp[2 * r + i];
-    }
-    __syncthreads();
-    const float *z = Zs + q * ld;
-    const float *wg = Ws + ii * ld, *wc = Ws + (kRnnIB + ii) * ld, *wo = Ws + (2 * kRnnIB + ii) * ld;
-    float gg = 0.f, gc = 0.f, go = 0.f;
-    for (int j = 4 * ks; j + 4 <= K; j += 4 * kRnnKS) {
-        const float4 zv = *reinterpret_cast<const float4 *>(z + j);
-        const float4 a = *reinterpret_cast<const float4 *>(wg + j);
-        const float4 b = *reinterpret_cast<const float4 *>(wc + j);
-        const float4 c = *reinterpret_cast<const float4 *>(wo + j);
-        gg = fmaf(a.x, zv.x, gg); gg = fmaf(a.y, zv.y, gg); gg = fmaf(a.z, zv.z, gg); gg = fmaf(a.w, zv.w, gg);
-        gc = fmaf(b.x, zv.x, gc); gc = fmaf(b.y, zv.y, gc); gc = fmaf(b.z, zv.z, gc); gc = fmaf(b.w, zv.w, gc);
-        go = fmaf(c.x, zv.x, go); go = fmaf(c.y, zv.y, go); go = fmaf(c.z, zv.z, go); go = fmaf(c.w, zv.w, go);
-    }
-    if (ks == 0)
-        for (int j = K & ~3; j < K; ++j) {  // K % 4 trailing inputs
-            const float zj = z[j];
-            gg = fmaf(wg[j], zj, gg);
-            gc = fmaf(wc[j], zj, gc);
-            go = fmaf(wo[j], zj, go);
-        }
-#pragma unroll
-    for (int off = 1; off < kRnnKS; off <<= 1) {
-        gg += __shfl_xor_sync(0xffffffffu, gg, off);
-        gc += __shfl_xor_sync(0xffffffffu, gc, off);
-        go += __shfl_xor_sync(0xffffffffu, go, off);
-    }
-    if (out) {
-        gg += hg;
-        gc += hc;
-        go += ho;
-        const float g = 1.0f / (1.0f + expf(-gg));
-        p.s_out[(size_t)rq * r + i] = g * z[i] + (1.0f - g) * tanhf(gc);
-        p.A[((size_t)rq * p.gamma + (p.k - 1)) * (size_t)r + i] = tanhf(go);
-    }
+    rnn::step_tile<T>(p, sh, blockIdx.x * rnn::kIB, blockIdx.y * rnn::kRB, threadIdx.x, CtaSync{});
 }
 
 }  // namespace
@@ -373,21 +250,21 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
     return cudaGetLastError();
 }
 
-template <typename T, int RB>
+template <typename T>
 static cudaError_t launch_rnn_step_t(const RnnStep &p, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (size_t)(3 * kRnnIB + RB) * (2 * p.r + 16);
-    auto kern = rnn_step_kernel<T, RB>;
+    const size_t smem = rnn::tile_smem_bytes(p.r);
+    auto kern = rnn_step_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((p.r + kRnnIB - 1) / kRnnIB, (p.R + RB - 1) / RB);
-    kern<<<grid, RB * kRnnIB * kRnnKS, smem, s>>>(p);
+    const dim3 grid((p.r + rnn::kIB - 1) / rnn::kIB, (p.R + rnn::kRB - 1) / rnn::kRB);
+    kern<<<grid, rnn::kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s) {
-    // 16 requests per CTA (512 threads; 82 KB of shared memory at r = 256)
-    if (p.dtype == DSPARK_BF16) return launch_rnn_step_t<__nv_bfloat16, 16>(p, s);
-    return launch_rnn_step_t<float, 16>(p, s);
+    // 16 requests x 8 entries per CTA (512 threads; 83 KB of shared memory at r = 256)
+    if (p.dtype == DSPARK_BF16) return launch_rnn_step_t<__nv_bfloat16>(p, s);
+    return launch_rnn_step_t<float>(p, s);
 }
 
 }  // namespace dspark

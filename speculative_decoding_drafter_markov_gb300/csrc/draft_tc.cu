@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rnn_step.cuh"
 #include "tc.cuh"
 #include "tc_pipe.cuh"
 
@@ -50,6 +51,8 @@ struct TcParams {
     int nparts;  // vocabulary ranges (CTAs per M-tile)
     int n_mtiles;
     int32_t *err;
+    RnnStep rnn_next;  // RNN head: the state update of step k + 1, run at the end of the launch
+    int rnn_next_on;
 };
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
@@ -125,6 +128,11 @@ __device__ __forceinline__ void confidence_warp(const TcParams &p, int k, int gr
         if (p.conf_logit) p.conf_logit[o] = dot;
     }
 }
+
+// barrier of the 16 epilogue warps
+struct EpiSync {
+    __device__ void operator()() const { tc::named_bar_sync(1, tcp::kEpiThreads); }
+};
 
 __device__ __forceinline__ int ld_acquire(const int *ptr) {
     int v;
@@ -486,6 +494,24 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 confidence_warp(p, p.k + si, gr, xp, lane);
             }
         }
+        // RNN head: the state update of step k + 1 (x_k from this step's winner
+        // words, final for every CTA past the last wait), tiles of 16 requests x
+        // 8 entries over all CTAs, staged in the operand region, which no MMA
+        // reads any more; the next launch gathers A_{k+1} from global memory
+        if constexpr (P::KSPLIT == 2) {
+            static_assert(P::kABytes - P::kMergeBytes >= (int)rnn::tile_smem_bytes(256) &&
+                              rnn::kThreads == tcp::kEpiThreads,
+                          "state-update tile in the operand region");
+            if (p.rnn_next_on && p.r <= 256 && !*s.abort_flag) {
+                tc::named_bar_sync(1, tcp::kEpiThreads);
+                float *sh = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) +
+                                                      P::kMergeBytes);
+                const int ni = (p.r + rnn::kIB - 1) / rnn::kIB, nq = (p.R + rnn::kRB - 1) / rnn::kRB;
+                for (int t = blockIdx.x; t < ni * nq; t += gridDim.x)
+                    rnn::step_tile<__nv_bfloat16>(p.rnn_next, sh, (t % ni) * rnn::kIB, (t / ni) * rnn::kRB, et,
+                                                  EpiSync{});
+            }
+        }
     }
     P::teardown(s);
 }
@@ -541,6 +567,8 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.winners = p.winners;
     tp.n_mtiles = n_mtiles;
     tp.err = p.err;
+    tp.rnn_next = p.rnn_next;
+    tp.rnn_next_on = P::KSPLIT == 2 && p.rnn_next_on;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;

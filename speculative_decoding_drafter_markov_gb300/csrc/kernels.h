@@ -13,6 +13,20 @@ namespace dspark {
 // ----- draft step (eqs. 4, 5): vocabulary-sliced partials of one step k ---------
 // The bias operand of row i is either W1[x_prev[i * x_stride]] (Markov head) or
 // the fp32 vector A_op + i * a_stride (RNN head).
+struct RnnStep {
+    int R, V, r, d, gamma, k, dtype;
+    const void *W;                   // [3r, 2r + d]
+    const void *W1;
+    const int32_t *x_prev;           // x_{k-1} of request i at x_prev[i * x_stride], unless
+    int x_stride;
+    const unsigned long long *x_win; // set: x_{k-1} = the packed race winner x_win[i] of step k-1
+    const float *Hpre;               // [R * gamma, 3r]
+    const float *s_in;               // [R, r] state s_{k-1}
+    float *s_out;                    // [R, r] state s_k (a different buffer)
+    float *A;                        // [R, gamma, r]
+    int32_t *err;
+};
+
 struct DraftStep {
     int R, V, r, gamma, k;          // k = 1..gamma
     int dtype;
@@ -39,6 +53,10 @@ struct DraftStep {
     unsigned long long *winners;     // [gamma, R] packed race winners, zero at the start of the call
     int step_index;                  // 1 for the first step launched since the counters were zeroed
     int nsteps;                      // tensor-core Markov step: steps k .. k + nsteps - 1 in one launch
+    // tensor-core RNN step: when set, the launch ends with the state update of
+    // step k + 1 (rnn_next.x_win = this step's winners)
+    RnnStep rnn_next;
+    int rnn_next_on;
 };
 int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
@@ -80,18 +98,6 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
                              float *Hpre, cudaStream_t s);
 // One recurrent step: gates from [s; W1[x_{k-1}]] and Hpre; updates state in
 // place, writes A[:, k-1, :] = tanh(W_o z_k).
-struct RnnStep {
-    int R, V, r, d, gamma, k, dtype;
-    const void *W;                   // [3r, 2r + d]
-    const void *W1;
-    const int32_t *x_prev;
-    int x_stride;
-    const float *Hpre;               // [R * gamma, 3r]
-    const float *s_in;               // [R, r] state s_{k-1}
-    float *s_out;                    // [R, r] state s_k (a different buffer)
-    float *A;                        // [R, gamma, r]
-    int32_t *err;
-};
 cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s);
 // Hpre [M, 3r] = h [M, d] W[:, 2r:]^T on the tensor cores (bf16), through cuBLASLt
 bool hproj_lt_available();
