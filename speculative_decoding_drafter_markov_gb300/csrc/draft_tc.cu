@@ -494,10 +494,11 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 confidence_warp(p, p.k + si, gr, xp, lane);
             }
         }
-        // RNN head: the state update of step k + 1 (x_k from this step's winner
-        // words, final for every CTA past the last wait), tiles of 16 requests x
-        // 8 entries over all CTAs, staged in the operand region, which no MMA
-        // reads any more; the next launch gathers A_{k+1} from global memory
+        // RNN head: the state update of step k + 1 for the M-tile's requests (x_k
+        // from this step's winner words, final for the M-tile once its CTAs are
+        // past the last wait), tiles of 16 requests x 8 entries over the M-tile's
+        // CTAs, staged in the operand region, which no MMA reads any more; the
+        // next launch gathers A_{k+1} from global memory
         if constexpr (P::KSPLIT == 2) {
             static_assert(P::kABytes - P::kMergeBytes >= (int)rnn::tile_smem_bytes(256) &&
                               rnn::kThreads == tcp::kEpiThreads,
@@ -506,9 +507,10 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 tc::named_bar_sync(1, tcp::kEpiThreads);
                 float *sh = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) +
                                                       P::kMergeBytes);
-                const int ni = (p.r + rnn::kIB - 1) / rnn::kIB, nq = (p.R + rnn::kRB - 1) / rnn::kRB;
-                for (int t = blockIdx.x; t < ni * nq; t += gridDim.x)
-                    rnn::step_tile<__nv_bfloat16>(p.rnn_next, sh, (t % ni) * rnn::kIB, (t / ni) * rnn::kRB, et,
+                const int ni = (p.r + rnn::kIB - 1) / rnn::kIB;
+                const int nq = (min(P::MV, p.R - m0) + rnn::kRB - 1) / rnn::kRB;
+                for (int t = cv; t < ni * nq; t += p.nparts)
+                    rnn::step_tile<__nv_bfloat16>(p.rnn_next, sh, (t % ni) * rnn::kIB, m0 + (t / ni) * rnn::kRB, et,
                                                   EpiSync{});
             }
         }

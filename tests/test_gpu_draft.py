@@ -134,7 +134,8 @@ def test_markov_full_size_sampled(orc, name, reqs):
 RNN_SMALL = [
     W.small("rnn", R=5, gamma=4, V=900, r=16, d=24),
     W.small("rnn", R=3, gamma=3, V=257, r=8, d=8, dtype="f32"),
-    W.small("rnn", R=70, gamma=3, V=2000, r=64, d=24),   # tensor cores, 2 M-tiles
+    W.small("rnn", R=70, gamma=3, V=2000, r=64, d=24),   # tensor cores, one M-tile of 128
+    W.small("rnn", R=150, gamma=3, V=2000, r=64, d=24),  # tensor cores, 2 M-tiles (the second ragged)
 ]
 
 
