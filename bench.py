@@ -294,8 +294,8 @@ class Cycle:
 # (profiles/draft_step_tc_qwen4b.md, profiles/draft_step_tc_heavy_prod.md); only
 # for the kernel version those captures measured -- drop an entry whenever the
 # draft kernel changes
-DRAFT_TRAFFIC_NCU = {"qwen4b": 239669504 + 3837696, "heavy": 1376131840 + 6041856,
-                     "prod": 2314692352 + 7125248}
+DRAFT_TRAFFIC_NCU = {"qwen4b": 238429440 + 3288320, "heavy": 1375298816 + 6294784,
+                     "prod": 2296707328 + 6909696}
 # the same for the training-loss launch at the train_loss workload
 # (profiles/train_loss_resident_train_loss.md)
 TRAIN_TRAFFIC_NCU = 311273216 + 252015616
