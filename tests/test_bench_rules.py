@@ -1,0 +1,43 @@
+"""The bench's roofline byte counts against the per-step figures of the hot-path
+measurement table: U_k + W_2 per draft step is 97.2 MB (qwen4b), 155.6 MB (heavy),
+198.6 MB (prod, V = 129280) and 116.7 MB (rnn).  The bench adds the gathered W_1
+rows, h_k and w, which must stay a small correction; the strict per-cycle count
+reads W_2 once for all gamma steps."""
+import pytest
+
+import bench
+from speculative_decoding_drafter_markov_gb300 import workloads as W
+
+TABLE_MB = {"qwen4b": 97.2, "heavy": 155.6, "prod": 198.6, "rnn": 116.7}
+
+
+@pytest.mark.parametrize("name", sorted(TABLE_MB))
+def test_step_bytes_match_the_table(name):
+    wl = W.WORKLOADS[name]
+    step = bench.draft_step_bytes(wl)
+    extras = (wl.R * wl.r + wl.R * wl.d) * 2 + (wl.d + wl.r) * 4  # W_1 rows, h_k (bf16), w (fp32)
+    assert abs((step - extras) / 1e6 - TABLE_MB[name]) < 0.05
+    assert extras / step < 0.03  # h_k dominates: 2.2 % at prod (d = 4096, R = 512)
+
+
+@pytest.mark.parametrize("name", sorted(TABLE_MB))
+def test_strict_cycle_reads_w2_once(name):
+    wl = W.WORKLOADS[name]
+    w2 = wl.V * wl.r * 2
+    per_step = bench.draft_step_bytes(wl)
+    assert bench.draft_cycle_bytes_strict(wl) == wl.gamma * (per_step - w2) + w2
+
+
+def test_qwen4b_figures_quoted_by_the_bench():
+    wl = W.WORKLOADS["qwen4b"]
+    assert wl.gamma * bench.draft_step_bytes(wl) == 780886016  # per launch, W_2 counted each step
+    assert bench.draft_cycle_bytes_strict(wl) == 236347392
+
+
+def test_training_loss_bytes():
+    B, gamma, V = bench.TRAIN["B"], bench.TRAIN["gamma"], bench.TRAIN["V"]
+    N = B * gamma
+    logits_once = 2 * N * V * 2  # draft and target rows, bf16
+    gradient_once = N * V * 4    # fp32
+    assert logits_once + gradient_once <= bench._train_bytes() < (logits_once + gradient_once) * 1.0001
+    assert abs(bench._train_bytes() / 1e6 - 622.3) < 0.1
