@@ -336,6 +336,29 @@ def draft_cycle_bytes_strict(wl):
     return wl.gamma * draft_step_bytes(wl, with_w2=False) + wl.V * wl.r * es
 
 
+def verify_cycle_bytes(wl, rows, rejected):
+    """Algorithmic bytes of one verification: the target rows of the batch read
+    once (phase 1: log-sum-exp and acceptance), then per request the target row
+    at its rejected or bonus position, the base row U_{n+1} for each rejected
+    request (the residual needs q) and W_2 once (phase 2)."""
+    es = 4 if wl.dtype == "f32" else 2
+    return (rows * wl.V + wl.R * wl.V + rejected * wl.V + wl.V * wl.r) * es
+
+
+def _verify_roofline(wl, verified, rejected, steps, t_verify_ms, hbm):
+    """The verification stage (init, phase 1, phase 2) against the HBM copy
+    bandwidth, from the mean rows and rejected requests per cycle."""
+    rows = wl.R + verified / steps
+    nbytes = verify_cycle_bytes(wl, rows, rejected / steps)
+    us = 1e3 * statistics.mean(t_verify_ms)
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "algorithmic_bytes_per_cycle": nbytes, "rows_per_cycle": rows,
+            "bytes_rule": "target rows once; per request its rejected/bonus target row; U_{n+1} rows of "
+                          "rejected requests; W_2 once",
+            "timing": "CUDA events around the whole verify call"}
+
+
 def bind_to_gpu_cpus(device_index):
     """Restrict this process to the host CPUs NVML reports as local to the GPU,
     so pinned host buffers (allocated after this) sit on the GPU's NUMA node.
@@ -395,6 +418,7 @@ def run_dspark(args, world, rank, local):
     events = [{"a": mk(), "b": mk(), "d": mk(), "s": mk(), "g": mk()} for _ in range(args.steps)]
     clocks = ClockSampler(local)
     accepted_dev = torch.zeros((), dtype=torch.int64, device=dev)  # sum of (n_accept + 1)
+    rejected_dev = torch.zeros((), dtype=torch.int64, device=dev)  # requests with n_accept < l
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -410,6 +434,7 @@ def run_dspark(args, world, rank, local):
         one_cycle(args.warmup + s, ev)
         ev["b"].record(stream)
         accepted_dev += cyc.vout["n_accept"].sum() + wl.R  # outside the timed span
+        rejected_dev += (cyc.vout["n_accept"] < (cyc.sched_out["ell"] if cyc.sched else gm)).sum()
         if cyc.sched:
             torch.cuda.synchronize()
             verified += cyc.verified_tokens()
@@ -427,6 +452,7 @@ def run_dspark(args, world, rank, local):
     drafted = args.steps * wl.R * gm
     total_ms, value = aggregate_ranks(sum(t_cycle), drafted, world, dev)
     accepted = int(accepted_dev.item())
+    rejected = int(rejected_dev.item())
 
     hbm, tc, peak_kind = _peaks()
     draft_us = 1e3 * statistics.mean(t_draft)
@@ -455,7 +481,8 @@ def run_dspark(args, world, rank, local):
                      "draft_step": draft_us / gm,
                      "schedule": 1e3 * statistics.mean(t_sched),
                      "verify": 1e3 * statistics.mean(t_verify)},
-        "roofline": {"kernel": (f"draft: h projection + {gm} x (state update, draft_step_tc)"
+        "roofline": {"kernel": (f"draft: h projection, step 1 state update, {gm} x draft_step_tc "
+                                "(each ending with the next step's state update)"
                                 if cyc.rnn else
                                 f"draft_step_tc: the {gm} draft steps of a cycle in one launch "
                                 "(fused contraction + epilogue + row merge per step)"),
@@ -470,6 +497,7 @@ def run_dspark(args, world, rank, local):
                                        "frac": strict / hbm,
                                        "algorithmic_bytes_per_launch": draft_cycle_bytes_strict(wl)},
         "roofline_philox": philox_roofline(wl, draft_us, clk),
+        "roofline_verify": _verify_roofline(wl, verified, rejected, args.steps, t_verify, hbm),
         "gpu_launches": args.steps * cyc.launches_per_cycle,
         "clocks": clk,
     }

@@ -41,3 +41,26 @@ def test_training_loss_bytes():
     gradient_once = N * V * 4    # fp32
     assert logits_once + gradient_once <= bench._train_bytes() < (logits_once + gradient_once) * 1.0001
     assert abs(bench._train_bytes() / 1e6 - 622.3) < 0.1
+
+
+def test_verify_bytes_follow_the_table():
+    # every drafted token verified at qwen4b: 576 target rows (175 MB), then per
+    # request a target row and, when it rejected, its U row, plus W_2 -- at most
+    # the table's 116.7 MB of residual rows
+    wl = W.WORKLOADS["qwen4b"]
+    rows = wl.R * (wl.gamma + 1)
+    lo = bench.verify_cycle_bytes(wl, rows, 0)
+    hi = bench.verify_cycle_bytes(wl, rows, wl.R)
+    assert abs(rows * wl.V * 2 / 1e6 - 175.0) < 0.1
+    assert abs((hi - rows * wl.V * 2) / 1e6 - 116.7) < 0.1
+    assert hi - lo == wl.R * wl.V * 2
+
+
+def test_verify_roofline_arithmetic():
+    wl = W.WORKLOADS["qwen4b"]
+    steps, rejected, verified = 4, 4 * 60, 4 * wl.R * wl.gamma
+    r = bench._verify_roofline(wl, verified, rejected, steps, [0.0829] * steps, 6761.6)
+    nbytes = bench.verify_cycle_bytes(wl, wl.R * (wl.gamma + 1), 60)
+    assert r["algorithmic_bytes_per_cycle"] == nbytes
+    assert abs(r["achieved"] - nbytes / 82.9e-6 / 1e9) < 1e-6 * r["achieved"]
+    assert abs(r["frac"] - r["achieved"] / 6761.6) < 1e-12
