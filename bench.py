@@ -347,10 +347,13 @@ def verify_cycle_bytes(wl, rows, rejected):
 
 def _verify_roofline(wl, verified, rejected, steps, t_verify_ms, hbm):
     """The verification stage (init, phase 1, phase 2) against the HBM copy
-    bandwidth, from the mean rows and rejected requests per cycle."""
+    bandwidth, from the mean rows and rejected requests per cycle (None when the
+    timings are unusable)."""
     rows = wl.R + verified / steps
     nbytes = verify_cycle_bytes(wl, rows, rejected / steps)
-    us = 1e3 * statistics.mean(t_verify_ms)
+    us = 1e3 * statistics.mean(t_verify_ms) if t_verify_ms else 0.0
+    if not us > 0.0 or not hbm:
+        return None
     achieved = nbytes / (us * 1e-6) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "algorithmic_bytes_per_cycle": nbytes, "rows_per_cycle": rows,

@@ -64,3 +64,9 @@ def test_verify_roofline_arithmetic():
     assert r["algorithmic_bytes_per_cycle"] == nbytes
     assert abs(r["achieved"] - nbytes / 82.9e-6 / 1e9) < 1e-6 * r["achieved"]
     assert abs(r["frac"] - r["achieved"] / 6761.6) < 1e-12
+
+
+def test_verify_roofline_without_timings():
+    wl = W.WORKLOADS["qwen4b"]
+    assert bench._verify_roofline(wl, 8, 1, 1, [], 6761.6) is None
+    assert bench._verify_roofline(wl, 8, 1, 1, [0.0], 6761.6) is None
