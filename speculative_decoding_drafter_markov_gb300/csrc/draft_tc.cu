@@ -56,17 +56,15 @@ struct TcParams {
 };
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
-// xp = x_{k-1}).  This thread's share of the dot product: 16-byte chunks t,
-// t + nthr, ... of [h_k ; e] (elements when d % 8 != 0), four loads in flight,
-// summed in order.
-__device__ __forceinline__ float confidence_share(const TcParams &p, int k, int grow, int xp, int t, int nthr) {
+// xp = x_{k-1}), by all epilogue threads, reduced in a fixed order through
+// `red` (16 floats of shared memory).
+__device__ __forceinline__ void confidence_row(const TcParams &p, int k, int grow, int xp, int et, float *red) {
     const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
     const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
     float dot = 0.f;
     if ((p.d & 7) == 0) {
         const int hc = p.d / 8, nc = hc + p.r / 8;
-#pragma unroll 4
-        for (int ch = t; ch < nc; ch += nthr) {
+        for (int ch = et; ch < nc; ch += tcp::kEpiThreads) {
             const uint4 raw = ch < hc ? *reinterpret_cast<const uint4 *>(h + ch * 8)
                                       : *reinterpret_cast<const uint4 *>(e + (ch - hc) * 8);
             const float *wv = p.w + ch * 8;  // w = [w_h ; w_e] lines up with [h ; e]
@@ -78,40 +76,57 @@ __device__ __forceinline__ float confidence_share(const TcParams &p, int k, int 
             }
         }
     } else {
-        for (int j = t; j < p.d + p.r; j += nthr)
+        for (int j = et; j < p.d + p.r; j += tcp::kEpiThreads)
             dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    return dot;  // the warp's sum, in every lane
-}
-
-// c_k and the confidence logit from the finished dot product (one thread)
-__device__ __forceinline__ void confidence_store(const TcParams &p, int k, int grow, float logit) {
-    const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
-    const size_t o = (size_t)grow * p.gamma + (k - 1);
-    p.c[o] = 1.0f / (1.0f + expf(-logit / T_k));
-    if (p.conf_logit) p.conf_logit[o] = logit;
-}
-
-// by all epilogue threads, the warps' sums reduced in a fixed order through
-// `red` (16 floats of shared memory)
-__device__ __forceinline__ void confidence_row(const TcParams &p, int k, int grow, int xp, int et, float *red) {
-    const float dot = confidence_share(p, k, grow, xp, et, tcp::kEpiThreads);
     if ((et & 31) == 0) red[et >> 5] = dot;
     tc::named_bar_sync(1, tcp::kEpiThreads);
     if (et == 0) {
         float sum = 0.f;
         for (int i = 0; i < tcp::kEpiThreads / 32; ++i) sum += red[i];
-        confidence_store(p, k, grow, sum);
+        const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
+        const size_t o = (size_t)grow * p.gamma + (k - 1);
+        p.c[o] = 1.0f / (1.0f + expf(-sum / T_k));
+        if (p.conf_logit) p.conf_logit[o] = sum;
     }
     tc::named_bar_sync(1, tcp::kEpiThreads);
 }
 
-// by one warp (lane 0 writes): the confidences deferred to the end of the launch
+// The same for one request by one warp (lanes over 16-byte chunks, four in
+// flight, then a fixed shuffle tree; lane 0 writes): the confidences deferred
+// to the end of the launch.
 __device__ __forceinline__ void confidence_warp(const TcParams &p, int k, int grow, int xp, int lane) {
-    const float dot = confidence_share(p, k, grow, xp, lane, 32);
-    if (lane == 0) confidence_store(p, k, grow, dot);
+    const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
+    const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
+    float dot = 0.f;
+    if ((p.d & 7) == 0) {
+        const int hc = p.d / 8, nc = hc + p.r / 8;
+#pragma unroll 4
+        for (int ch = lane; ch < nc; ch += 32) {
+            const uint4 raw = ch < hc ? *reinterpret_cast<const uint4 *>(h + ch * 8)
+                                      : *reinterpret_cast<const uint4 *>(e + (ch - hc) * 8);
+            const float *wv = p.w + ch * 8;
+            const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dot = fmaf(wv[2 * i], tcp::bf16_lo(v[i]), dot);
+                dot = fmaf(wv[2 * i + 1], tcp::bf16_hi(v[i]), dot);
+            }
+        }
+    } else {
+        for (int j = lane; j < p.d + p.r; j += 32)
+            dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) {
+        const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
+        const size_t o = (size_t)grow * p.gamma + (k - 1);
+        p.c[o] = 1.0f / (1.0f + expf(-dot / T_k));
+        if (p.conf_logit) p.conf_logit[o] = dot;
+    }
 }
 
 // barrier of the 16 epilogue warps
