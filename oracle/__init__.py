@@ -44,35 +44,39 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def bind(L):
+    """Declare the argument types of the oracle's C functions on a loaded library."""
+    P = ctypes.c_void_p
+    i32, u64, u32 = ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32
+    L.oracle_philox4x32_10.argtypes = [P, P, P]
+    L.oracle_philox4x32_10.restype = None
+    L.oracle_uniform.argtypes = [u32]
+    L.oracle_uniform.restype = ctypes.c_double
+    L.oracle_philox_word.argtypes = [u64, u32, u32, u32, u64, u32, u32]
+    L.oracle_philox_word.restype = u32
+    L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 7
+    L.oracle_draft_markov.restype = i32
+    L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 8
+    L.oracle_draft_rnn.restype = i32
+    L.oracle_schedule.argtypes = [i32, i32, P, P, i32, i32, i32, i32, P, P, P, P]
+    L.oracle_schedule.restype = i32
+    L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 7
+    L.oracle_verify.restype = i32
+    L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P, ctypes.c_double, P]
+    L.oracle_sts_fit.restype = i32
+    L.oracle_accept_stats.argtypes = [i32, i32, P, P, P, P, P, P]
+    L.oracle_accept_stats.restype = i32
+    d = ctypes.c_double
+    L.oracle_train_losses.argtypes = [i32, i32, i32, i32, P, P, P, P, d, d, d, P, P, P, P]
+    L.oracle_train_losses.restype = i32
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB)
-        P = ctypes.c_void_p
-        i32, u64, u32 = ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32
-        L.oracle_philox4x32_10.argtypes = [P, P, P]
-        L.oracle_philox4x32_10.restype = None
-        L.oracle_uniform.argtypes = [u32]
-        L.oracle_uniform.restype = ctypes.c_double
-        L.oracle_philox_word.argtypes = [u64, u32, u32, u32, u64, u32, u32]
-        L.oracle_philox_word.restype = u32
-        L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 7
-        L.oracle_draft_markov.restype = i32
-        L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 8
-        L.oracle_draft_rnn.restype = i32
-        L.oracle_schedule.argtypes = [i32, i32, P, P, i32, i32, i32, i32, P, P, P, P]
-        L.oracle_schedule.restype = i32
-        L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 7
-        L.oracle_verify.restype = i32
-        L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P, ctypes.c_double, P]
-        L.oracle_sts_fit.restype = i32
-        L.oracle_accept_stats.argtypes = [i32, i32, P, P, P, P, P, P]
-        L.oracle_accept_stats.restype = i32
-        d = ctypes.c_double
-        L.oracle_train_losses.argtypes = [i32, i32, i32, i32, P, P, P, P, d, d, d, P, P, P, P]
-        L.oracle_train_losses.restype = i32
-        _lib = L
+        _lib = bind(ctypes.CDLL(_LIB))
     return _lib
 
 
