@@ -62,7 +62,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
-    ap.add_argument("--workload", default="qwen4b",
+    ap.add_argument("--workload", default="prod",
                     choices=sorted(W.WORKLOADS) + ["sts_fit", "train_loss", "sched_profile"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -290,15 +290,43 @@ class Cycle:
         return self.wl.R * self.wl.gamma
 
 
-# DRAM bytes (read + write) of one draft launch from the committed ncu captures
-# (profiles/draft_step_tc_qwen4b.md, profiles/draft_step_tc_heavy_prod.md); only
-# for the kernel version those captures measured -- drop an entry whenever the
-# draft kernel changes
-DRAFT_TRAFFIC_NCU = {"qwen4b": 238429440 + 3288320, "heavy": 1375298816 + 6294784,
-                     "prod": 2296707328 + 6909696}
-# the same for the training-loss launch at the train_loss workload
-# (profiles/train_loss_resident_train_loss.md)
-TRAIN_TRAFFIC_NCU = 311273216 + 252015616
+# DRAM bytes (read + write) of one launch as ncu measured them, recorded with
+# the SHA-256 of the kernel's sources at the time of the capture: a figure is
+# used only while the sources still hash the same (else the traffic is null)
+NCU_DRAM_FILE = os.path.join(ROOT, "profiles", "ncu_dram_bytes.txt")
+KERNEL_SOURCES = {
+    "draft_step_tc": ["draft_tc.cu", "tc_pipe.cuh", "tc.cuh", "common.cuh", "kernels.h", "rnn_step.cuh"],
+    "train_loss_resident": ["train_loss.cu", "common.cuh"],
+    "verify_phase2_tc": ["verify_tc.cu", "verify_common.cuh", "tc_pipe.cuh", "tc.cuh", "common.cuh",
+                         "kernels.h"],
+}
+
+
+def kernel_source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_drafter_markov_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """(bytes per launch, note): the recorded ncu DRAM bytes of `kernel` at
+    `workload` if they were taken on the current sources, else (None, why)."""
+    want = kernel_source_hash(kernel)
+    try:
+        lines = open(NCU_DRAM_FILE).read().splitlines()
+    except OSError:
+        return None, "no ncu record"
+    for line in lines:
+        f = line.split()
+        if len(f) >= 5 and not line.startswith("#") and f[0] == kernel and f[1] == workload:
+            if f[2] == want:
+                return int(f[3]) + int(f[4]), f"ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch ({f[5] if len(f) > 5 else 'full size'})"
+            return None, "kernel changed since the last ncu capture"
+    return None, "no ncu capture at this workload"
 
 
 # Philox-4x32-10 throughput of this GPU's integer-multiply pipe: 20 32x32->64
@@ -336,13 +364,15 @@ def draft_cycle_bytes_strict(wl):
     return wl.gamma * draft_step_bytes(wl, with_w2=False) + wl.V * wl.r * es
 
 
-def verify_cycle_bytes(wl, rows, rejected):
+def verify_cycle_bytes(wl, rows, rejected, reread=True):
     """Algorithmic bytes of one verification: the target rows of the batch read
-    once (phase 1: log-sum-exp and acceptance), then per request the target row
-    at its rejected or bonus position, the base row U_{n+1} for each rejected
-    request (the residual needs q) and W_2 once (phase 2)."""
+    once (phase 1: log-sum-exp and acceptance), then the base row U_{n+1} of
+    each rejected request (the residual needs q) and W_2 once (phase 2).  With
+    `reread`, phase 2 also reads each request's target row at its rejected or
+    bonus position a second time: the residual max(0, p - q) needs that row's
+    log-sum-exp, which only phase 1's full pass over the row gives."""
     es = 4 if wl.dtype == "f32" else 2
-    return (rows * wl.V + wl.R * wl.V + rejected * wl.V + wl.V * wl.r) * es
+    return (rows * wl.V + (wl.R * wl.V if reread else 0) + rejected * wl.V + wl.V * wl.r) * es
 
 
 def _verify_roofline(wl, verified, rejected, steps, t_verify_ms, hbm):
@@ -355,10 +385,14 @@ def _verify_roofline(wl, verified, rejected, steps, t_verify_ms, hbm):
     if not us > 0.0 or not hbm:
         return None
     achieved = nbytes / (us * 1e-6) / 1e9
+    strict = verify_cycle_bytes(wl, rows, rejected / steps, reread=False) / (us * 1e-6) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "algorithmic_bytes_per_cycle": nbytes, "rows_per_cycle": rows,
-            "bytes_rule": "target rows once; per request its rejected/bonus target row; U_{n+1} rows of "
-                          "rejected requests; W_2 once",
+            "bytes_rule": "target rows once (phase 1); phase 2 reads each request's rejected/bonus target "
+                          "row again (its residual needs the row's log-sum-exp first), the U_{n+1} rows of "
+                          "rejected requests and W_2 once",
+            "frac_strict": strict / hbm,
+            "strict_rule": "as bytes_rule without phase 2's second read of the target rows",
             "timing": "CUDA events around the whole verify call"}
 
 
@@ -464,6 +498,7 @@ def run_dspark(args, world, rank, local):
         bytes_launch += 3 * wl.r * (2 * wl.r + wl.d) * 2
     achieved = bytes_launch / (draft_us * 1e-6) / 1e9
     strict = draft_cycle_bytes_strict(wl) / (draft_us * 1e-6) / 1e9
+    draft_traffic = ncu_traffic("draft_step_tc", wl.name) if not cyc.rnn else (None, "RNN head: several launches")
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -494,8 +529,7 @@ def run_dspark(args, world, rank, local):
                      "algorithmic_bytes_per_launch": bytes_launch,
                      "bytes_rule": "per step: U_k + W_2 + W_1 rows + h_k + w; x gamma steps",
                      "timing": "CUDA events around the whole draft call",
-                     "traffic": DRAFT_TRAFFIC_NCU.get(wl.name),
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"},
+                     "traffic": draft_traffic[0], "traffic_source": draft_traffic[1]},
         "roofline_w2_once_per_cycle": {"achieved": strict, "peak": hbm, "unit": "GB/s",
                                        "frac": strict / hbm,
                                        "algorithmic_bytes_per_launch": draft_cycle_bytes_strict(wl)},
@@ -635,7 +669,8 @@ def cpu_baseline(wl, budget_s=12.0):
         el = time.perf_counter() - t0
         if el >= budget_s or done >= 64:
             break
-    return {"value": done * wl.gamma / el, "unit": "tok/s", "cores": 1, "kind": "oracle",
+    return {"value": done * wl.gamma / el, "unit": "tok/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": f"{done} request-cycles of {wl.name} (full V={wl.V}, gamma={wl.gamma}, "
                       f"verify all), single-threaded C oracle, {el:.1f} s"}
 
@@ -661,7 +696,8 @@ def run_reference(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": _workload_desc(wl), "sample": "1 request per step"},
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "host_cores": os.cpu_count(),
+                             "kind": "oracle",
                              "sample": f"1 request per step of {wl.name}, {args.steps} steps"},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -879,6 +915,7 @@ def run_train_loss(args, world, rank, local):
     call_us = 1e3 * statistics.mean(times)
     achieved = _train_bytes() / (call_us * 1e-6) / 1e9
     peak, _, peak_src = _peaks()
+    train_traffic = ncu_traffic("train_loss_resident", "train_loss")
     line = {
         "metric": TRAIN_METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -893,9 +930,8 @@ def run_train_loss(args, world, rank, local):
                      "frac": achieved / peak, "peak_kind": f"{peak_src} copy bandwidth",
                      "algorithmic_bytes_per_launch": _train_bytes(),
                      "bytes_rule": "draft and target logits read once, fp32 gradient written once",
-                     "timing": "CUDA events around the whole call", "traffic": TRAIN_TRAFFIC_NCU,
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
-                                       "(part of the gradient is still in L2 when the launch ends)"},
+                     "timing": "CUDA events around the whole call", "traffic": train_traffic[0],
+                     "traffic_source": train_traffic[1]},
         "gpu_launches": args.steps,
         "clocks": clk,
     }

@@ -134,8 +134,10 @@ DSPARK_API int dspark_draft_markov_step(const dspark_draft_args *a, int32_t k, v
  *   DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB).  Larger needs return
  *   DSPARK_ERR_UNSUPPORTED (message in dspark_last_error()) and launch nothing.
  * - The first call on each device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any
- *   stream capture on the device.
+ *   that device current) and caches it with the id of the device's current
+ *   context; a call in another context of the device (after cudaDeviceReset,
+ *   for instance, which unloads the module) looks it up again.  Make the first
+ *   call in each context before any stream capture on the device.
  * - Every call on a device shares the one array.  Each call first clears the
  *   part that must start at zero (completion counters, with an asynchronous
  *   memset on the stream) and every step overwrites the rest before reading

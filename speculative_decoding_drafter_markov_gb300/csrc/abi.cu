@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cuda.h>
+
 #include <mutex>
 #include <string>
 
@@ -219,7 +221,34 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[DSPARK_NOALLOC_
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices];  // device address of the array, per device
+// device address of the array per device, and the id of the context it was
+// looked up in: a new context (e.g. after cudaDeviceReset) loads the module
+// again, so the address is looked up again there
+void *g_noalloc_ptr[kMaxDevices];
+unsigned long long g_noalloc_ctx[kMaxDevices];
+
+// driver entry points for the current context and its process-unique id
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+void *driver_fn(const char *name) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return ptr;
+}
+
+// id of the calling thread's current context (0: none yet, or unknown)
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+    static CtxGetIdFn get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 int noalloc_scratch(void **out) {
     int dev = 0;
@@ -227,11 +256,13 @@ int noalloc_scratch(void **out) {
     if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(DSPARK_ERR_UNSUPPORTED, "noalloc: device %d", dev);
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    const unsigned long long ctx = current_ctx_id();
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current if needed
         if (e != cudaSuccess) return cuda_fail(e, "noalloc: cudaGetSymbolAddress");
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = current_ctx_id();
     }
     *out = g_noalloc_ptr[dev];
     return DSPARK_OK;

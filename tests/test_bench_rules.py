@@ -70,3 +70,23 @@ def test_verify_roofline_without_timings():
     wl = W.WORKLOADS["qwen4b"]
     assert bench._verify_roofline(wl, 8, 1, 1, [], 6761.6) is None
     assert bench._verify_roofline(wl, 8, 1, 1, [0.0], 6761.6) is None
+
+
+def test_verify_strict_bytes_drop_the_second_read():
+    wl = W.WORKLOADS["prod"]
+    rows = wl.R * 5
+    assert (bench.verify_cycle_bytes(wl, rows, 100) - bench.verify_cycle_bytes(wl, rows, 100, reread=False)
+            == wl.R * wl.V * 2)
+    r = bench._verify_roofline(wl, 4 * wl.R * 4, 400, 4, [0.2] * 4, 6761.6)
+    assert r["frac_strict"] < r["frac"]
+
+
+def test_traffic_record_keyed_by_source_hash(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash("draft_step_tc")
+    rec = tmp_path / "rec.txt"
+    rec.write_text(f"# comment\ndraft_step_tc prod {h} 100 20 full-size\n"
+                   "draft_step_tc heavy 0000000000000000 5 5 full-size\n")
+    monkeypatch.setattr(bench, "NCU_DRAM_FILE", str(rec))
+    assert bench.ncu_traffic("draft_step_tc", "prod")[0] == 120
+    assert bench.ncu_traffic("draft_step_tc", "heavy")[0] is None  # stale: another kernel build
+    assert bench.ncu_traffic("draft_step_tc", "qwen4b")[0] is None  # never captured

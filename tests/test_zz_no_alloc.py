@@ -37,7 +37,10 @@ def _call_noalloc(inp, out, err, seed, cycle):
 
 
 @pytest.mark.parametrize("wl", [W.small("qwen4b", R=40, gamma=4, V=5000, r=64, d=32),
-                                W.WORKLOADS["qwen4b"]], ids=lambda w: w.name)
+                                W.WORKLOADS["qwen4b"],
+                                # CUDA-core path: fp32, ragged V and r
+                                W.small("qwen4b", R=10, gamma=3, V=1001, r=24, d=40, dtype="f32")],
+                         ids=lambda w: f"{w.name}-{w.dtype}")
 def test_noalloc_matches_workspace_version(wl):
     inp = W.draft_inputs(wl, seed=3, device="cuda")
     for call, (seed, cycle) in enumerate([(11, 0), (11, 1)]):  # two calls in a row
