@@ -54,13 +54,13 @@ def bind(L):
     L.oracle_uniform.restype = ctypes.c_double
     L.oracle_philox_word.argtypes = [u64, u32, u32, u32, u64, u32, u32]
     L.oracle_philox_word.restype = u32
-    L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 7
+    L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 8
     L.oracle_draft_markov.restype = i32
-    L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 8
+    L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 9
     L.oracle_draft_rnn.restype = i32
     L.oracle_schedule.argtypes = [i32, i32, P, P, i32, i32, i32, i32, P, P, P, P]
     L.oracle_schedule.restype = i32
-    L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 7
+    L.oracle_verify.argtypes = [i32] * 6 + [P] * 10 + [u64, u64, P, i32] + [P] * 8
     L.oracle_verify.restype = i32
     L.oracle_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P, P, ctypes.c_double, P]
     L.oracle_sts_fit.restype = i32
@@ -129,13 +129,14 @@ def draft_markov(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, reqs=
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
     gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma))
+    runner = np.full((n, gamma), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_markov(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(w),
                                    _p(sts), _p(anchor), seed, cycle, _p(rl), n, _p(x), _p(logq),
-                                   _p(lse), _p(c), _p(gap), _p(z), _p(logit))
+                                   _p(lse), _p(c), _p(gap), _p(runner), _p(z), _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_markov failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, conf_logit=logit)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out
@@ -161,14 +162,15 @@ def draft_rnn(U, h, W1, W2t, W, w, anchor, *, s0=None, seed=0, cycle=0, sts_T=No
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
     gap = np.zeros((n, gamma)); A = np.zeros((n, gamma, r)); logit = np.zeros((n, gamma))
+    runner = np.full((n, gamma), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_rnn(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(W),
                                 _p(s0a), _p(w), _p(sts), _p(anchor), seed, cycle, _p(rl), n,
-                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(z), _p(A),
-                                _p(logit))
+                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(runner), _p(z),
+                                _p(A), _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_rnn failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, A=A, conf_logit=logit)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, A=A, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out
@@ -214,13 +216,15 @@ def verify(T, tags, anchor, x, logq, lse, U, W1, W2t, *, A=None, seed=0, cycle=0
     nxt = np.full(R, -1, np.int32)
     lse_p = np.full(N, np.nan); logp = np.full(N, np.nan); margin = np.full(N, np.nan)
     gap = np.full(R, np.nan)
+    runner = np.full(R, -1, np.int32)
     rc = lib().oracle_verify(R, gamma, V, r, dt, N, _p(T), _p(tags), _p(anchor), _p(x), _p(logq),
                              _p(lse), _p(U), _p(W1), _p(W2t), _p(Aa), seed, cycle, _p(rl), n,
-                             _p(n_acc), _p(out), _p(nxt), _p(lse_p), _p(logp), _p(margin), _p(gap))
+                             _p(n_acc), _p(out), _p(nxt), _p(lse_p), _p(logp), _p(margin), _p(gap),
+                             _p(runner))
     if rc != 0:
         raise ValueError(f"oracle_verify failed ({rc})")
     return dict(n_accept=n_acc, out_tokens=out, next_anchor=nxt, lse_p=lse_p, logp=logp,
-                margin=margin, gap=gap)
+                margin=margin, gap=gap, runner=runner)
 
 
 def sts_fit(logit, n_accept, grid, *, n_bins=15, T_prefix=None, edge_eps=0.0):

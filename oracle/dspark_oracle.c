@@ -87,7 +87,7 @@ static double gumbel(uint64_t seed, uint32_t step, uint32_t req, uint64_t cycle,
 /* ------------------------------------------------------------------------ */
 static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, uint32_t req,
                         uint64_t cycle, int32_t *x_out, double *logq_out, double *lse_out,
-                        double *gap_out) {
+                        double *gap_out, int32_t *runner_out) {
     double m = -INFINITY;
     for (int v = 0; v < V; ++v)
         if (z[v] > m) m = z[v];
@@ -96,21 +96,24 @@ static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, ui
     double lse = m + log(S);
 
     double best = -INFINITY, second = -INFINITY;
-    int arg = -1;
+    int arg = -1, arg2 = -1;
     for (int v = 0; v < V; ++v) {
         double score = z[v] + gumbel(seed, step, req, cycle, 0, v);
         if (score > best) {
             second = best;
+            arg2 = arg;
             best = score;
             arg = v;
         } else if (score > second) {
             second = score;
+            arg2 = v;
         }
     }
     *x_out = arg;
     *logq_out = z[arg] - lse;
     *lse_out = lse;
     if (gap_out) *gap_out = best - second;
+    if (runner_out) *runner_out = arg2;
 }
 
 /* [D] eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]]); the optional per-step
@@ -134,7 +137,7 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        double *z_out, double *logit) {
+                        int32_t *runner, double *z_out, double *logit) {
     int n = reqs ? n_reqs : R;
     double *e = (double *)malloc(sizeof(double) * (size_t)r);
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
@@ -157,7 +160,7 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
             }
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
-                        gap ? &gap[o] : NULL);
+                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL);
             const void *h_k = dtype == ORACLE_F32
                                   ? (const void *)((const float *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d)
                                   : (const void *)((const uint16_t *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d);
@@ -185,8 +188,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, double *z_out, double *A_out,
-                     double *logit) {
+                     double *lse, double *c, double *gap, int32_t *runner, double *z_out,
+                     double *A_out, double *logit) {
     int n = reqs ? n_reqs : R;
     int zlen = 2 * r + d;
     double *s = (double *)malloc(sizeof(double) * (size_t)r);
@@ -231,7 +234,7 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
             }
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
-                        gap ? &gap[o] : NULL);
+                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL);
             /* eq. (7) reads the embedding W_1[x_{k-1}], i.e. the middle block of z_k */
             const void *h_k = dtype == ORACLE_F32 ? (const void *)((const float *)h + hrow)
                                                   : (const void *)((const uint16_t *)h + hrow);
@@ -385,7 +388,7 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
                   const void *W2t, const float *A, uint64_t seed, uint64_t cycle,
                   const int32_t *reqs, int n_reqs, int32_t *n_accept, int32_t *out_tokens,
                   int32_t *next_anchor, double *lse_p, double *logp, double *margin,
-                  double *gap) {
+                  double *gap, int32_t *runner) {
     /* rows of each request: first row index and count */
     int32_t *first = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
     int32_t *count = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
@@ -469,16 +472,18 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
                 for (int v = 0; v < V; ++v) w[v] = exp(load_elem(T, row * (size_t)V + v, dtype) - lp);
         }
         double best = -INFINITY, second = -INFINITY;
-        int y = -1;
+        int y = -1, y2 = -1;
         for (int v = 0; v < V; ++v) {
             if (!(w[v] > 0.0)) continue;
             double score = log(w[v]) + gumbel(seed, (uint32_t)n_r, (uint32_t)rq, cycle, 2, v);
             if (score > best) {
                 second = best;
+                y2 = y;
                 best = score;
                 y = v;
             } else if (score > second) {
                 second = score;
+                y2 = v;
             }
         }
         n_accept[rq] = n_r;
@@ -490,6 +495,7 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
         }
         next_anchor[rq] = y;
         if (gap) gap[rq] = best - second;
+        if (runner) runner[rq] = y2;
     }
     free(first); free(count); free(w); free(b);
     return status;

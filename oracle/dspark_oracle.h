@@ -59,14 +59,16 @@ uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t re
  *   U [R, gamma, V], h [R, gamma, d], W1 [V, r], W2t [V, r] (row v = column v
  *   of W_2), w [d + r] f32, sts_T [gamma] f32 or NULL, anchor [R].
  * Outputs: x [n, gamma], logq, lse, c [n, gamma], gap [n, gamma] = gap
- * between the two largest Gumbel-perturbed scores, z [n, gamma, V] logits,
+ * between the two largest Gumbel-perturbed scores, runner [n, gamma] = the
+ * index of the second largest (the token a near tie could swap in),
+ * z [n, gamma, V] logits,
  * logit [n, gamma] = w^T [h_k ; W_1[x_{k-1}]] (the confidence logit). */
 int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const void *U, const void *h, const void *W1, const void *W2t,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        double *z, double *logit);
+                        int32_t *runner, double *z, double *logit);
 
 /* RNN-head draft (eq. 6).  W [3r, 2r + d]: rows [0, r) gate, [r, 2r) candidate,
  * [2r, 3r) output.  s0 [R, r] f32 or NULL (zero).  Extra output: A [n, gamma, r],
@@ -76,8 +78,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, double *z, double *A,
-                     double *logit);
+                     double *lse, double *c, double *gap, int32_t *runner, double *z,
+                     double *A, double *logit);
 
 /* Hardware-aware prefix scheduler (Module E, Algorithm 1; production async
  * variant).  c [R, gamma] f32; sps[i] = SPS(B_min + i) for i < B_count.
@@ -97,7 +99,8 @@ int oracle_schedule(int R, int gamma, const float *c, const double *sps, int B_m
  * [R] / [R, gamma + 1] / [N] arrays, written only for those requests.
  *   n_accept [R], out_tokens [R, gamma + 1] (-1 padded), next_anchor [R],
  *   lse_p [N], logp [N] (NaN on rows without a test), margin [N] =
- *   (log p - log q) - log u, gap [R] = top-two score gap of the final sample.
+ *   (log p - log q) - log u, gap [R] = top-two score gap of the final sample,
+ *   runner [R] = the index with the second largest score of that sample.
  * Returns 0, or -1 on malformed tags. */
 int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *T,
                   const int32_t *tags, const int32_t *anchor, const int32_t *x,
@@ -105,7 +108,7 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
                   const void *W2t, const float *A, uint64_t seed, uint64_t cycle,
                   const int32_t *reqs, int n_reqs, int32_t *n_accept, int32_t *out_tokens,
                   int32_t *next_anchor, double *lse_p, double *logp, double *margin,
-                  double *gap);
+                  double *gap, int32_t *runner);
 
 /* Sequential temperature scaling ([D] Module D).  logit [M, gamma] f32
  * confidence logits s_k of M held-out draft blocks, n_accept [M] their

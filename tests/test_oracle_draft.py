@@ -125,3 +125,22 @@ def test_bad_anchor_rejected(orc):
     anchor[1] = V
     with pytest.raises(ValueError):
         orc.draft_markov(U, h, W1, W2t, w, anchor)
+
+
+def test_sample_gap_and_runner_up_by_brute_force(orc):
+    """The reported token is the argmax of z + g, the runner-up the second place and
+    the gap their difference, with g = -log(-log u) of the stream-0 Philox words
+    recomputed here word by word."""
+    R, gamma, V, r, d = 2, 3, 40, 4, 2
+    U, h, W1, W2t, w, anchor = _inputs(R, gamma, V, r, d, seed=4, scale=1.0)
+    seed, cycle = 77, 5
+    out = orc.draft_markov(U, h, W1, W2t, w, anchor, seed=seed, cycle=cycle, want_z=True)
+    for rq in range(R):
+        for k in range(gamma):
+            g = np.array([-np.log(-np.log(orc.uniform(orc.philox_word(seed, v // 4, k + 1, rq, cycle, 0, v % 4))))
+                          for v in range(V)])
+            score = out["z"][rq, k] + g
+            order = np.argsort(-score, kind="stable")
+            assert out["x"][rq, k] == order[0]
+            assert out["runner"][rq, k] == order[1]
+            assert out["gap"][rq, k] == pytest.approx(score[order[0]] - score[order[1]], abs=1e-12)

@@ -212,3 +212,20 @@ def test_malformed_tags_rejected(orc):
                 [[0, 0], [0, 1], [1, 1], [1, 2]]):  # request 1 without position 0
         with pytest.raises(ValueError):
             orc.verify(T, np.array(bad, np.int32), np.zeros(R, np.int32), x, lq, lq, U, W1, W2t)
+
+
+def test_final_sample_runner_up_by_brute_force(orc):
+    # l = 0: the final token is the Gumbel-max of log p_0 with stream-2 noise at position 0
+    R, V = 3, 30
+    rng = np.random.default_rng(12)
+    U = rng.standard_normal((R, 1, V)).astype(np.float32)
+    T_rows = rng.standard_normal((R, 2, V)).astype(np.float32)
+    seed, cycle = 5, 9
+    _, v = _draft_then_verify(orc, U, T_rows, np.zeros(R, np.int64), seed=seed, cycle=cycle)
+    for rq in range(R):
+        logp = T_rows[rq, 0].astype(np.float64) - special.logsumexp(T_rows[rq, 0].astype(np.float64))
+        g = np.array([-np.log(-np.log(orc.uniform(orc.philox_word(seed, u // 4, 0, rq, cycle, 2, u % 4))))
+                      for u in range(V)])
+        order = np.argsort(-(logp + g), kind="stable")
+        assert v["out_tokens"][rq, 0] == order[0]
+        assert v["runner"][rq] == order[1]
