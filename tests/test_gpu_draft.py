@@ -1,12 +1,15 @@
 """GPU parity of the draft calls (Markov and RNN heads) against the oracle.
 
 Small cases run the oracle on every request; the standard full-size workloads
-(the launch configuration the benchmark times) run it on sampled requests.
+(the launch configuration the benchmark times) run it on every request of
+qwen4b and on 64 requests spread over the batch elsewhere, split over the host
+cores.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle_pool
 from parity import compare_draft, host
 from speculative_decoding_drafter_markov_gb300 import _lib as dsp
 from speculative_decoding_drafter_markov_gb300 import workloads as W
@@ -39,12 +42,14 @@ def _gpu_draft(inp, seed, cycle, sts_T=None, rnn=False):
 
 
 def _oracle_draft(orc, inp, seed, cycle, reqs=None, sts_T=None, rnn=False):
+    """The oracle's draft of `reqs` (all when None), the requests split over host threads."""
     args = [host(inp[k]) for k in ("U", "h", "W1", "W2t")]
+    reqs = list(range(inp["U"].shape[0])) if reqs is None else list(reqs)
     if rnn:
-        return orc.draft_rnn(*args, host(inp["W"]), host(inp["w"]), host(inp["anchor"]), seed=seed,
-                             cycle=cycle, sts_T=sts_T, reqs=reqs)
-    return orc.draft_markov(*args, host(inp["w"]), host(inp["anchor"]), seed=seed, cycle=cycle,
-                            sts_T=sts_T, reqs=reqs)
+        return oracle_pool.draft(orc.draft_rnn, reqs, *args, host(inp["W"]), host(inp["w"]),
+                                 host(inp["anchor"]), seed=seed, cycle=cycle, sts_T=sts_T)
+    return oracle_pool.draft(orc.draft_markov, reqs, *args, host(inp["w"]), host(inp["anchor"]),
+                             seed=seed, cycle=cycle, sts_T=sts_T)
 
 
 def _to_cuda(inp):
@@ -118,9 +123,15 @@ def test_step_calls_match_one_call(wl):
         assert np.array_equal(host(out[k]), whole[k]), k
 
 
-@pytest.mark.parametrize("name,reqs", [("qwen4b", [0, 37, 63]), ("heavy", [5, 200]),
-                                       ("prod", [511])])
-def test_markov_full_size_sampled(orc, name, reqs):
+# full-size cases: every request at qwen4b, 64 requests spread over the batch
+# elsewhere (the first and last included)
+FULL_REQS = {"qwen4b": list(range(64)), "heavy": list(range(0, 256, 4)) + [255],
+             "prod": list(range(0, 512, 8)) + [511], "rnn": list(range(0, 128, 2)) + [127]}
+
+
+@pytest.mark.parametrize("name", ["qwen4b", "heavy", "prod"])
+def test_markov_full_size_sampled(orc, name):
+    reqs = FULL_REQS[name]
     wl = W.WORKLOADS[name]
     inp = W.draft_inputs(wl, seed=1, device="cuda")
     gpu = _gpu_draft(inp, 2024, 3)
@@ -157,9 +168,14 @@ def test_rnn_full_size_sampled(orc):
     wl = W.WORKLOADS["rnn"]
     inp = W.draft_inputs(wl, seed=1, device="cuda")
     gpu = _gpu_draft(inp, 11, 0, rnn=True)
-    reqs = [0, 127]
+    reqs = FULL_REQS["rnn"]
     ref = _oracle_draft(orc, inp, 11, 0, reqs=reqs, rnn=True)
     compare_draft(gpu, ref, reqs, wl.gamma)
+    for t, rq in enumerate(reqs):  # the bias operand A_k until the first flip
+        for k in range(wl.gamma):
+            np.testing.assert_allclose(gpu["A"][rq, k], ref["A"][t, k], atol=1e-4)
+            if gpu["x"][rq, k] != ref["x"][t, k]:
+                break
 
 
 def test_bad_anchor_reports_range():

@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle_pool
 from parity import compare_verify, host
 from speculative_decoding_drafter_markov_gb300 import _lib as dsp
 from speculative_decoding_drafter_markov_gb300 import workloads as W
@@ -17,12 +18,13 @@ def _case(orc, wl, seed, cycle, ell, reqs=None, device="cpu", rnn=False):
     seeded synthetic tokens for the rest."""
     inp = W.draft_inputs(wl, seed=seed, device=device)
     hU, hh, hW1, hW2 = (host(inp[k]) for k in ("U", "h", "W1", "W2t"))
+    all_reqs = list(range(wl.R)) if reqs is None else list(reqs)
     if rnn:
-        ref = orc.draft_rnn(hU, hh, hW1, hW2, host(inp["W"]), host(inp["w"]), host(inp["anchor"]),
-                            seed=seed, cycle=cycle, reqs=reqs)
+        ref = oracle_pool.draft(orc.draft_rnn, all_reqs, hU, hh, hW1, hW2, host(inp["W"]),
+                                host(inp["w"]), host(inp["anchor"]), seed=seed, cycle=cycle)
     else:
-        ref = orc.draft_markov(hU, hh, hW1, hW2, host(inp["w"]), host(inp["anchor"]), seed=seed,
-                               cycle=cycle, reqs=reqs)
+        ref = oracle_pool.draft(orc.draft_markov, all_reqs, hU, hh, hW1, hW2, host(inp["w"]),
+                                host(inp["anchor"]), seed=seed, cycle=cycle)
     R, gamma = wl.R, wl.gamma
     rng = np.random.default_rng(seed + 1)
     x = rng.integers(0, wl.V, (R, gamma)).astype(np.int32)
@@ -50,8 +52,10 @@ def _gpu_verify(inp, x, logq, lse, A, tags, T, seed, cycle, N_dev=None):
 
 
 def _oracle_verify(orc, inp, x, logq, lse, A, tags, T, seed, cycle, reqs=None):
-    return orc.verify(host(T), tags, host(inp["anchor"]), x, logq, lse, host(inp["U"]),
-                      host(inp["W1"]), host(inp["W2t"]), A=A, seed=seed, cycle=cycle, reqs=reqs)
+    reqs = list(range(x.shape[0])) if reqs is None else list(reqs)
+    return oracle_pool.verify(orc.verify, reqs, host(T), tags, host(inp["anchor"]), x, logq, lse,
+                              host(inp["U"]), host(inp["W1"]), host(inp["W2t"]), A=A, seed=seed,
+                              cycle=cycle)
 
 
 SMALL = [
@@ -120,17 +124,24 @@ def test_verify_device_row_count(orc):
                    list(range(wl.R)), tags, wl.gamma)
 
 
-@pytest.mark.parametrize("name,reqs,ell_kind", [("qwen4b", [3, 60], "all"),
-                                                ("heavy", [9], "random"),
-                                                ("prod", [0, 400], "random")])
-def test_verify_full_size_sampled(orc, name, reqs, ell_kind):
+# every request at qwen4b, 64 spread over the batch elsewhere (first and last included)
+FULL_REQS = {"qwen4b": list(range(64)), "heavy": list(range(0, 256, 4)) + [255],
+             "prod": list(range(0, 512, 8)) + [511], "rnn": list(range(0, 128, 2)) + [127]}
+
+
+@pytest.mark.parametrize("name,ell_kind", [("qwen4b", "all"), ("heavy", "random"), ("prod", "random"),
+                                           ("rnn", "all")])
+def test_verify_full_size_sampled(orc, name, ell_kind):
     wl = W.WORKLOADS[name]
+    reqs = FULL_REQS[name]
+    rnn = wl.head == "rnn"
     rng = np.random.default_rng(5)
     ell = np.full(wl.R, wl.gamma) if ell_kind == "all" else rng.integers(0, wl.gamma + 1, wl.R)
-    case = _case(orc, wl, 6, 1, ell, reqs=reqs, device="cuda")
+    case = _case(orc, wl, 6, 1, ell, reqs=reqs, device="cuda", rnn=rnn)
     gpu = _gpu_verify(*case, 6, 1)
     ref = _oracle_verify(orc, *case, 6, 1, reqs=reqs)
     compare_verify(gpu, ref, reqs, case[5], wl.gamma)
+    assert int((ref["n_accept"][reqs] < ell[reqs]).sum()) > 0  # residuals exercised
 
 
 def test_malformed_tags_report_inval():
