@@ -16,7 +16,10 @@ draft, its own scheduler with its own K history, its own verification and
 anchors.  Every cycle compares the stages request by request:
 
 - draft: tokens exact, log q / c within 1e-4, lse within 1e-3 (tests/parity.py);
-- scheduler: verify lengths, K and Theta exactly;
+- scheduler: the kernel reproduces the oracle's scheduler bit for bit on the
+  confidences it was given; against the oracle's own chain, verify lengths and
+  K exactly and Theta within 1e-5 relative (the confidences agree within 1e-4
+  only, so the fixed-point sums differ in their last units);
 - verification: accepted counts and emitted tokens exactly, per-row log p and
   log-sum-exp within tolerance.
 
@@ -24,9 +27,9 @@ A near tie (a draft or final token whose oracle score gap is below 1e-3, an
 acceptance decision whose oracle margin is below 1e-4) is a counted flip.  A
 flipped request leaves that cycle's later comparisons; the scheduler sees the
 confidences of every request, so a flip can move verify lengths anywhere.  A
-scheduler difference is accepted as a flip only when the confidences agree
-within 1e-4 and the oracle's scheduler given the GPU's confidences reproduces the
-GPU's lengths, K and Theta bit for bit.  After a cycle with a flip the oracle's
+difference in verify lengths or K from the oracle's chain counts as a flip (the
+confidences agree within 1e-4, and the kernel matched the oracle's scheduler
+bit for bit on its own confidences).  After a cycle with a flip the oracle's
 chain continues from the GPU's anchors and K history (it follows the GPU only
 after a counted near tie).  Flips must stay below 0.1 % of the compared tokens.
 """
@@ -35,7 +38,7 @@ import pytest
 import torch
 
 import oracle_pool
-from parity import GAP_TOL, MARGIN_TOL, TOL_C, compare_draft, compare_verify, host, record
+from parity import TOL_C, compare_draft, compare_verify, host, record
 from speculative_decoding_drafter_markov_gb300 import _lib as dsp
 from speculative_decoding_drafter_markov_gb300 import workloads as W
 
@@ -125,18 +128,21 @@ def test_async_chain_matches_oracle_chain(orc, wl):
         flips, compared = flips + f, compared + n
         flipped = {rq for rq in range(R) if not np.array_equal(gd["x"][rq], od["x"][rq])}
         cycle_flip = bool(flipped)
-        same_sched = (np.array_equal(gs["ell"], os_["ell"]) and int(gs["K_out"][0]) == os_["K_out"]
-                      and float(gs["theta_best"][0]) == os_["theta_best"])
+        # the scheduler kernel itself, bit for bit, on the confidences it was given
+        chk = orc.schedule(gd["c"], sps, B_min, mode=orc.SCHED_ASYNC, K_in=int(host(k_in)[0]))
+        assert np.array_equal(chk["ell"], gs["ell"]) and chk["K_out"] == int(gs["K_out"][0])
+        assert chk["theta_best"] == float(gs["theta_best"][0])
+        # against the oracle's own chain: the confidences agree within 1e-4, not bit for
+        # bit, so Theta agrees to rounding and the integer decisions exactly, unless a
+        # comparison of the scan sat at a near tie
+        same_sched = np.array_equal(gs["ell"], os_["ell"]) and int(gs["K_out"][0]) == os_["K_out"]
         if not same_sched:
-            # allowed only as a consequence of confidences within tolerance
             assert np.abs(gd["c"] - od["c"]).max() <= TOL_C
-            chk = orc.schedule(gd["c"], sps, B_min, mode=orc.SCHED_ASYNC, K_in=int(host(k_in)[0]))
-            assert np.array_equal(chk["ell"], gs["ell"]) and chk["K_out"] == int(gs["K_out"][0])
-            assert chk["theta_best"] == float(gs["theta_best"][0])
             flips += 1
             record(1, 0)
             cycle_flip = True
         else:
+            assert abs(float(gs["theta_best"][0]) - os_["theta_best"]) <= 1e-5 * os_["theta_best"]
             assert n_rows == len(tags_o)
             assert np.array_equal(host(tags_dev)[:n_rows], tags_o)
             keep = [rq for rq in range(R) if rq not in flipped]
