@@ -162,10 +162,10 @@ typedef struct {
 } dspark_rnn_args;
 
 /* The h_k columns of W do not depend on the recurrence: W[:, 2r:] h_k is
- * formed for all (request, k) first, a plain bf16 GEMM run through cuBLASLt
- * (loaded at run time; with it missing, or for fp32, a CUDA-core kernel does
- * it).  The workspace holds the draft scratch, two [R, r] state buffers, the
- * [R gamma, 3r] fp32 projection and 4 MiB of GEMM scratch. */
+ * formed for all (request, k) first, one bf16 GEMM on the tensor cores
+ * (tcgen05; fp32, or shapes it does not take -- d or 2r + d not a multiple of
+ * 8 -- go to a CUDA-core kernel).  The workspace holds the draft scratch, two
+ * [R, r] state buffers and the [R gamma, 3r] fp32 projection. */
 DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a);
 DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_stream_t stream);
 

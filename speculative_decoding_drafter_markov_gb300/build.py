@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdspark.so")
-SOURCES = ["abi.cu", "diag.cu", "draft.cu", "draft_tc.cu", "gemm_lt.cu", "sched.cu", "sts.cu",
+SOURCES = ["abi.cu", "diag.cu", "draft.cu", "draft_tc.cu", "gemm_tc.cu", "sched.cu", "sts.cu",
            "train_loss.cu", "verify.cu", "verify_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 TU_FLAGS = {}
@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".{os.getpid()}.tmp"
-    res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"], capture_output=True, text=True)
+    res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
     os.replace(tmp, LIB)

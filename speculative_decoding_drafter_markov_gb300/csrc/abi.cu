@@ -126,13 +126,20 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         cudaError_t e = cudaMemsetAsync(cleared, 0, cleared_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft counters");
     }
-    if (use_tc && !rnn) {
-        // Markov head on the tensor cores: all the steps in one launch
+    if (use_tc) {
+        // on the tensor cores all the steps run in one launch (the RNN head's
+        // state updates between them, the first one included)
         st.k = k_first;
         st.step_index = k_first;
+        st.phase0 = k_first - 1;  // Markov: one synchronisation point per step
         st.nsteps = k_last - k_first + 1;
         st.x_prev = k_first == 1 ? a->anchor : a->x + (k_first - 2);
         st.x_stride = k_first == 1 ? 1 : a->gamma;
+        if (rnn) {
+            if (k_first != 1) return fail(DSPARK_ERR_INVAL, "RNN draft runs from step 1");
+            st.rnn = *rnn;
+            st.phase0 = 0;
+        }
         cudaError_t e = launch_draft_step_tc(st, s);
         return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft steps (tensor cores)");
     }
@@ -149,31 +156,22 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         rs.x_win = nullptr;
         return rs;
     };
+    // CUDA cores: one step (and, RNN head, one state update) per launch
     for (int k = k_first; k <= k_last; ++k) {
         const int32_t *xp = k == 1 ? a->anchor : a->x + (k - 2);
         const int xs = k == 1 ? 1 : a->gamma;
         if (rnn) {
-            // on the tensor cores the update of step k > k_first ran at the end of the
-            // previous step's launch, from that step's race winners
-            if (!use_tc || k == k_first) {
-                cudaError_t e = launch_rnn_step(rnn_update(k), s);
-                if (e != cudaSuccess) return cuda_fail(e, "rnn step");
-            }
+            cudaError_t e = launch_rnn_step(rnn_update(k), s);
+            if (e != cudaSuccess) return cuda_fail(e, "rnn step");
             st.A_op = A_rnn + (size_t)(k - 1) * a->r;
-            st.rnn_next_on = use_tc && k < k_last;
-            if (st.rnn_next_on) {
-                st.rnn_next = rnn_update(k + 1);
-                st.rnn_next.x_win = st.winners + (size_t)(k - 1) * a->R;  // step k's winners (counter index k)
-            }
         }
         st.k = k;
         st.step_index = k;
         st.nsteps = 1;
         st.x_prev = xp;
         st.x_stride = xs;
-        cudaError_t e = use_tc ? launch_draft_step_tc(st, s) : launch_draft_step(st, s);
-        if (e != cudaSuccess) return cuda_fail(e, use_tc ? "draft step (tensor cores)" : "draft step");
-        if (use_tc) continue;  // merged and scored inside the tensor-core step
+        cudaError_t e = launch_draft_step(st, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft step");
         rd.k = k;
         rd.x_prev = xp;
         rd.x_stride = xs;
@@ -286,12 +284,10 @@ DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_st
 }
 
 namespace {
-constexpr size_t kLtWorkspaceBytes = 4u << 20;  // cuBLASLt scratch of the h projection
-
 size_t rnn_ws_bytes(const dspark_rnn_args *a) {
     const dspark_draft_args &b = a->base;
     return draft_ws_bytes(&b, a->A) + 2 * dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
-           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r) + kLtWorkspaceBytes;
+           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
 }
 }  // namespace
 
@@ -317,14 +313,12 @@ DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_strea
     float *state1 = reinterpret_cast<float *>(p);
     p += dspark::align256(state_bytes);
     float *Hpre = reinterpret_cast<float *>(p);
-    p += dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
-    void *lt_ws = p;
     cudaError_t e = a->s0 ? cudaMemcpyAsync(state0, a->s0, state_bytes, cudaMemcpyDeviceToDevice, s)
                           : cudaMemsetAsync(state0, 0, state_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn state init");
     if (b.d > 0) {
-        if (b.dtype == DSPARK_BF16 && dspark::hproj_lt_available())
-            e = dspark::launch_hproj_lt(b.R * b.gamma, b.d, b.r, b.h, a->W, Hpre, lt_ws, kLtWorkspaceBytes, s);
+        if (dspark::hproj_tc_supported(b.R * b.gamma, b.d, b.r, b.dtype, b.h, a->W, Hpre))
+            e = dspark::launch_hproj_tc(b.R * b.gamma, b.d, b.r, b.h, a->W, Hpre, b.err, s);
         else
             e = dspark::launch_rnn_hproj(b.R * b.gamma, b.d, b.r, b.dtype, b.h, a->W, Hpre, s);
     } else {

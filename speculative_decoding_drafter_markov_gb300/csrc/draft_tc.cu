@@ -29,14 +29,15 @@ namespace {
 struct TcParams {
     int R, V, r, d, gamma;
     int k;       // first step of the launch (1..gamma)
-    int nsteps;  // steps k .. k + nsteps - 1 (Markov head; 1 for the RNN head)
+    int nsteps;  // steps k .. k + nsteps - 1
     int step_index;  // counter index of step k (1 for the first step since the counters were zeroed)
+    int phase0;      // cross-CTA synchronisation points earlier launches of the draft passed
     const __nv_bfloat16 *W1;
     const __nv_bfloat16 *W2t;  // [V, r] (the W_2^T tiles of the first step are pulled into L2 early)
     const int32_t *x_prev;  // token x_{k-1} of row i at x_prev[i * x_stride]
     int x_stride;
-    const float *A_op;  // RNN: operand of row i at A_op[i * a_stride], else null
-    int a_stride;
+    const float *A_op;  // RNN: operand of row i for step k at A_op[i * a_stride], else null
+    int a_stride;       // (step k + j: A_op + j r)
     const __nv_bfloat16 *h;  // [R, gamma, d]
     const float *w;          // [d + r]
     const float *sts_T;      // [gamma] or null
@@ -51,8 +52,7 @@ struct TcParams {
     int nparts;  // vocabulary ranges (CTAs per M-tile)
     int n_mtiles;
     int32_t *err;
-    RnnStep rnn_next;  // RNN head: the state update of step k + 1, run at the end of the launch
-    int rnn_next_on;
+    RnnStep rnn;  // RNN head: the state update's inputs (s_in holds s_{k-1})
 };
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
@@ -168,9 +168,10 @@ __device__ __forceinline__ int load_token(const TcParams &p, int grow, const int
 // the bias operand of the M-tile in the swizzled K-major layout: W_1[x_{k-1}]
 // (tokens in s.tok) or the split fp32 RNN operand; threads tid, tid + nthr, ...
 template <class P>
-__device__ __forceinline__ void gather_operand(const TcParams &p, const typename P::State &s, int m0, int tid,
-                                               int nthr) {
+__device__ __forceinline__ void gather_operand(const TcParams &p, const typename P::State &s, int m0, int k,
+                                               int tid, int nthr) {
     const int chunks_per_row = p.r / 8;
+    const float *A_k = P::KSPLIT == 2 ? p.A_op + (size_t)(k - p.k) * p.r : nullptr;
     for (int e = tid; e < P::MV * chunks_per_row; e += nthr) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int grow = m0 + row;
@@ -182,8 +183,9 @@ __device__ __forceinline__ void gather_operand(const TcParams &p, const typename
         } else {
             float xs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (grow < p.R) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.A_op + (size_t)grow * p.a_stride + c * 8);
-                const float4 a0 = src[0], a1 = src[1];
+                // written by other CTAs of the launch: read through L2
+                const float4 *src = reinterpret_cast<const float4 *>(A_k + (size_t)grow * p.a_stride + c * 8);
+                const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
                 xs[0] = a0.x; xs[1] = a0.y; xs[2] = a0.z; xs[3] = a0.w;
                 xs[4] = a1.x; xs[5] = a1.y; xs[6] = a1.z; xs[7] = a1.w;
             }
@@ -238,6 +240,61 @@ __device__ __forceinline__ void finalise_row(const TcParams &p, const DraftParti
     }
 }
 
+// Cross-CTA synchronisation point of the M-tile (all epilogue threads call it):
+// with `publish`, this CTA's writes so far become visible and it counts itself
+// (else it did so already); then it waits (bounded) until every CTA of the
+// M-tile has reached synchronisation point number `phase`.  Returns false (and
+// raises the abort flag) when the wait ran out or the CTA had aborted.
+template <class P>
+__device__ __forceinline__ bool mtile_sync(const TcParams &p, typename P::State &s, int *ctr, int phase, int et,
+                                           bool publish) {
+    if (publish) tc::named_bar_sync(1, tcp::kEpiThreads);
+    if (et == 0) {
+        if (publish) {
+            __threadfence();  // cumulative over the CTA's writes before the barrier
+            atomicAdd(ctr, 1);
+        }
+        *s.flag = !*s.abort_flag && wait_counter(ctr, phase * p.nparts, p.err) ? 1 : 0;
+    }
+    tc::named_bar_sync(1, tcp::kEpiThreads);
+    if (!*s.flag) {
+        *s.abort_flag = 1;
+        return false;
+    }
+    __threadfence();
+    return true;
+}
+
+// RNN head, eq. (6): the state update of step k for the M-tile's requests --
+// s_k and A_k = tanh(W_o z_k) from s_{k-1} and x_{k-1} (the launch's input
+// token for its first step, else step k-1's race winner) -- as tiles of 16
+// requests x 8 gate entries spread over the M-tile's CTAs, staged in the
+// operand region (free between two steps' contractions).
+template <class P>
+__device__ __forceinline__ void rnn_state_update(const TcParams &p, const typename P::State &s, int m0, int cv,
+                                                 int k, int et) {
+    static_assert(P::kABytes - P::kMergeBytes >= (int)rnn::tile_smem_bytes(256) && rnn::kThreads == tcp::kEpiThreads,
+                  "state-update tile in the operand region");
+    RnnStep rs = p.rnn;
+    if (((k - p.k) & 1) != 0) {  // the buffers alternate: s_in holds s_{k-1} at the launch's first step
+        rs.s_in = p.rnn.s_out;
+        rs.s_out = const_cast<float *>(p.rnn.s_in);
+    }
+    rs.k = k;
+    if (k == p.k) {
+        rs.x_prev = p.x_prev;
+        rs.x_stride = p.x_stride;
+        rs.x_win = nullptr;
+    } else {
+        rs.x_win = p.winners + (size_t)(p.step_index + (k - 1 - p.k) - 1) * p.R;
+    }
+    float *sh = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) + P::kMergeBytes);
+    const int ni = (p.r + rnn::kIB - 1) / rnn::kIB;
+    const int nq = (min(P::MV, p.R - m0) + rnn::kRB - 1) / rnn::kRB;
+    for (int t = cv; t < ni * nq; t += p.nparts)
+        rnn::step_tile<__nv_bfloat16>(rs, sh, (t % ni) * rnn::kIB, m0 + (t / ni) * rnn::kRB, et, EpiSync{});
+}
+
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
 // (m_tile, cv) owns requests m0 .. m0 + MV - 1 and the vocabulary tiles
 // cv, cv + nparts, cv + 2 nparts, ... (about an equal share).  Per step:
@@ -286,9 +343,12 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     __syncthreads();  // tokens, barriers, thresholds, TMEM
     P::ready(s);
 
-    // 2. first bias operand, before the W_2 / U streams compete for bandwidth
-    gather_operand<P>(p, s, m0, threadIdx.x, P::kThreads);
-    tc::fence_proxy_async_smem();
+    // 2. first bias operand, before the W_2 / U streams compete for bandwidth (the
+    //    RNN head's first operand needs the state update, below)
+    if (P::KSPLIT == 1) {
+        gather_operand<P>(p, s, m0, p.k, threadIdx.x, P::kThreads);
+        tc::fence_proxy_async_smem();
+    }
     __syncthreads();  // operand complete
 
     if (warp == tcp::kProducerWarp) {
@@ -303,7 +363,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         if (lane == 0) P::producer_u(s, &tmU, c0, tstride, ntiles, p.nsteps, p.k - 1, m0, p.err);
         __syncwarp();
     } else if (warp == tcp::kMmaWarp) {
-        if (lane == 0) P::mma(s, ntiles, kslabs, p.nsteps, p.err);
+        if (lane == 0) P::mma(s, ntiles, kslabs, p.nsteps, p.err, P::KSPLIT == 1 ? 1 : 0);
         __syncwarp();
     } else {
         const int et = threadIdx.x;
@@ -312,7 +372,16 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         const bool row_live = grow < p.R;
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         float *mg = P::merge_scratch(s);
-        for (int step = 0; step < p.nsteps; ++step) {
+        int phase = p.phase0;  // cross-CTA synchronisation points passed
+        if constexpr (P::KSPLIT == 2) {
+            // RNN head: the state update of the first step, then its operand A_k
+            rnn_state_update<P>(p, s, m0, cv, p.k, et);
+            if (mtile_sync<P>(p, s, ctr, ++phase, et, true)) {
+                gather_operand<P>(p, s, m0, p.k, et, tcp::kEpiThreads);
+                P::operand_written(s, et);
+            }
+        }
+        for (int step = 0; step < p.nsteps && !*s.abort_flag; ++step) {
             const int k = p.k + step, q = p.step_index + step;
             DraftPartial *part = p.part + (size_t)(q - 1) * p.R * p.nparts;
             unsigned long long *win = p.winners + (size_t)(q - 1) * p.R;
@@ -446,15 +515,9 @@ __global__ void __launch_bounds__(P::kThreads, 1)
             if (cv < P::MV && m0 + cv < p.R) confidence_row(p, k, m0 + cv, s.tok[cv], et, s.red);
 
             // wait (bounded) until every CTA of the M-tile has published this step
-            if (et == 0) *s.flag = !*s.abort_flag && wait_counter(ctr, q * p.nparts, p.err) ? 1 : 0;
-            tc::named_bar_sync(1, tcp::kEpiThreads);
-            if (!*s.flag) {
-                *s.abort_flag = 1;
-                break;
-            }
-            __threadfence();
+            if (!mtile_sync<P>(p, s, ctr, ++phase, et, false)) break;
             if (step + 1 < p.nsteps) {
-                // x_k of the M-tile's rows -> the next operand W_1[x_k], then the MMA warp goes
+                // x_k of the M-tile's rows (the next step's x_{k-1})
                 if (et < P::MV) {
                     int x = -1;
                     if (m0 + et < p.R) {
@@ -464,7 +527,14 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     s.tok[et] = x;
                 }
                 tc::named_bar_sync(1, tcp::kEpiThreads);
-                gather_operand<P>(p, s, m0, et, tcp::kEpiThreads);
+                if constexpr (P::KSPLIT == 2) {
+                    // RNN head: the state update of step k + 1 over the M-tile's CTAs,
+                    // then its operand A_{k+1}
+                    rnn_state_update<P>(p, s, m0, cv, k + 1, et);
+                    if (!mtile_sync<P>(p, s, ctr, ++phase, et, true)) break;
+                }
+                // the next operand (W_1[x_k], or A_{k+1}), then the MMA warp goes
+                gather_operand<P>(p, s, m0, k + 1, et, tcp::kEpiThreads);
                 P::operand_written(s, et);
             }
         }
@@ -492,26 +562,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     if (xp < 0 || xp >= p.V) xp = 0;
                 }
                 confidence_warp(p, p.k + si, gr, xp, lane);
-            }
-        }
-        // RNN head: the state update of step k + 1 for the M-tile's requests (x_k
-        // from this step's winner words, final for the M-tile once its CTAs are
-        // past the last wait), tiles of 16 requests x 8 entries over the M-tile's
-        // CTAs, staged in the operand region, which no MMA reads any more; the
-        // next launch gathers A_{k+1} from global memory
-        if constexpr (P::KSPLIT == 2) {
-            static_assert(P::kABytes - P::kMergeBytes >= (int)rnn::tile_smem_bytes(256) &&
-                              rnn::kThreads == tcp::kEpiThreads,
-                          "state-update tile in the operand region");
-            if (p.rnn_next_on && p.r <= 256 && !*s.abort_flag) {
-                tc::named_bar_sync(1, tcp::kEpiThreads);
-                float *sh = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) +
-                                                      P::kMergeBytes);
-                const int ni = (p.r + rnn::kIB - 1) / rnn::kIB;
-                const int nq = (min(P::MV, p.R - m0) + rnn::kRB - 1) / rnn::kRB;
-                for (int t = cv; t < ni * nq; t += p.nparts)
-                    rnn::step_tile<__nv_bfloat16>(p.rnn_next, sh, (t % ni) * rnn::kIB, m0 + (t / ni) * rnn::kRB, et,
-                                                  EpiSync{});
             }
         }
     }
@@ -553,8 +603,9 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     if (!encode_u_map(&tmU, p.U, p.R, p.gamma, p.V, P::MV)) return cudaErrorInvalidValue;
     TcParams tp;
     tp.R = p.R; tp.V = p.V; tp.r = p.r; tp.d = p.d; tp.gamma = p.gamma; tp.k = p.k;
-    tp.nsteps = p.A_op ? 1 : (p.nsteps > 0 ? p.nsteps : 1);
+    tp.nsteps = p.nsteps > 0 ? p.nsteps : 1;
     tp.step_index = p.step_index;
+    tp.phase0 = p.phase0;
     tp.h = static_cast<const __nv_bfloat16 *>(p.h); tp.w = p.w; tp.sts_T = p.sts_T;
     tp.counters = p.counters;
     tp.x = p.x_out; tp.logq = p.logq; tp.lse = p.lse; tp.c = p.c;
@@ -569,8 +620,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.winners = p.winners;
     tp.n_mtiles = n_mtiles;
     tp.err = p.err;
-    tp.rnn_next = p.rnn_next;
-    tp.rnn_next_on = P::KSPLIT == 2 && p.rnn_next_on;
+    tp.rnn = p.rnn;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;
@@ -615,6 +665,20 @@ bool encode_w2t_map(CUtensorMap *m, const void *W2t, int V, int r, int BN) {
     const cuuint32_t box[2] = {64, (cuuint32_t)BN};
     const cuuint32_t estr[2] = {1, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(W2t), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// a bf16 [rows, K] matrix with row stride ld elements (K-major): boxes of 64
+// K-elements (128 bytes, swizzled) x box_rows rows
+bool encode_kmajor_map(CUtensorMap *m, const void *base, int rows, int K, int ld, int box_rows) {
+    auto encode = encode_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -52,11 +52,13 @@ struct DraftStep {
     int *counters;                   // [number of M-tiles], zero at the start of the call
     unsigned long long *winners;     // [gamma, R] packed race winners, zero at the start of the call
     int step_index;                  // 1 for the first step launched since the counters were zeroed
-    int nsteps;                      // tensor-core Markov step: steps k .. k + nsteps - 1 in one launch
-    // tensor-core RNN step: when set, the launch ends with the state update of
-    // step k + 1 (rnn_next.x_win = this step's winners)
-    RnnStep rnn_next;
-    int rnn_next_on;
+    int nsteps;                      // tensor-core step: steps k .. k + nsteps - 1 in one launch
+    int phase0;                      // tensor-core step: cross-CTA synchronisation points that
+                                     // earlier launches of the same draft already passed
+    // tensor-core RNN head (A_op set): the operand of step k' of the launch is
+    // A_op + (k' - k) r; before it, the launch runs the state update of step k'
+    // from `rnn` (s_in: the buffer holding s_{k-1}; the buffers alternate)
+    RnnStep rnn;
 };
 int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
@@ -71,6 +73,7 @@ int sm_count();
 bool tc_available();
 bool tc_kernels_enabled();
 bool encode_w2t_map(CUtensorMap *m, const void *W2t, int V, int r, int BN);
+bool encode_kmajor_map(CUtensorMap *m, const void *base, int rows, int K, int ld, int box_rows);
 bool encode_u_map(CUtensorMap *m, const void *U, int R, int gamma, int V, int MV);
 void tc_grid_shape(int R, int V, int MV, int BN, int *nparts, int *n_mtiles);
 
@@ -99,10 +102,10 @@ cudaError_t launch_rnn_hproj(int M, int d, int r, int dtype, const void *h, cons
 // One recurrent step: gates from [s; W1[x_{k-1}]] and Hpre; updates state in
 // place, writes A[:, k-1, :] = tanh(W_o z_k).
 cudaError_t launch_rnn_step(const RnnStep &p, cudaStream_t s);
-// Hpre [M, 3r] = h [M, d] W[:, 2r:]^T on the tensor cores (bf16), through cuBLASLt
-bool hproj_lt_available();
-cudaError_t launch_hproj_lt(int M, int d, int r, const void *h, const void *W, float *Hpre, void *lt_ws,
-                            size_t lt_ws_bytes, cudaStream_t s);
+// Hpre [M, 3r] = h [M, d] W[:, 2r:]^T on the tensor cores (bf16, tcgen05, gemm_tc.cu)
+bool hproj_tc_supported(int M, int d, int r, int dtype, const void *h, const void *W, const float *Hpre);
+cudaError_t launch_hproj_tc(int M, int d, int r, const void *h, const void *W, float *Hpre, int32_t *err,
+                            cudaStream_t s);
 
 // ----- scheduler (Module E, Algorithm 1; async variant) ---------------------
 cudaError_t launch_schedule(const dspark_sched_args &a, cudaStream_t s);

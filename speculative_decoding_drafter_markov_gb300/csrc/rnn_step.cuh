@@ -8,8 +8,9 @@
 // 16-byte groups 4 ks, 4 ks + 16, ... of the 2r inputs, then a two-step shuffle
 // sum.  Rows are padded by 16 words: 16-byte aligned, and two weight rows read
 // by one quarter-warp sit 64 bytes apart in the banks.  kThreads threads run a
-// tile; `sync` is their barrier.  Used by the standalone update kernel and by
-// the tail of the tensor-core draft launch of the previous step.
+// tile; `sync` is their barrier.  Used by the standalone update kernel (the
+// CUDA-core path) and, between the steps, by the tensor-core draft launch that
+// runs all the steps.
 #pragma once
 
 #include "common.cuh"
@@ -82,10 +83,12 @@ __device__ void step_tile(const RnnStep &p, float *sh, int i0, int q0, int tid, 
 #pragma unroll
                 for (int k = 0; k < kVec; ++k) dst[k] = 0.f;
             } else if (j < r) {
+                // the state buffers alternate between steps and other CTAs of a
+                // multi-step launch write them: read through L2, not L1
                 const float *src = p.s_in + (size_t)rq * r + j;
 #pragma unroll
                 for (int k = 0; k < kVec; k += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(src + k);
+                    const float4 f = __ldcg(reinterpret_cast<const float4 *>(src + k));
                     dst[k] = f.x; dst[k + 1] = f.y; dst[k + 2] = f.z; dst[k + 3] = f.w;
                 }
             } else {
@@ -104,7 +107,7 @@ __device__ void step_tile(const RnnStep &p, float *sh, int i0, int q0, int tid, 
         for (int e = tid; e < kRB * K; e += kThreads) {
             const int q = e / K, j = e - q * K, rq = q0 + q;
             float v = 0.f;
-            if (rq < p.R) v = j < r ? p.s_in[(size_t)rq * r + j] : to_f32(W1[(size_t)s_xp[q] * r + (j - r)]);
+            if (rq < p.R) v = j < r ? __ldcg(p.s_in + (size_t)rq * r + j) : to_f32(W1[(size_t)s_xp[q] * r + (j - r)]);
             Zs[q * ld + j] = v;
         }
     }

@@ -241,9 +241,11 @@ struct Pipe {
         }
     }
 
-    // warp 17, lane 0: `nsteps` steps of `ntiles` tiles.  Step i > 0 starts once
-    // the epilogue has written its operand (phase i - 1 of `aready`).
-    __device__ static void mma(State &s, int ntiles, int kslabs, int nsteps, int32_t *err) {
+    // warp 17, lane 0: `nsteps` steps of `ntiles` tiles.  The operands of the
+    // first `a_ready` steps were written before the roles split; step i >= a_ready
+    // starts once the epilogue has written its operand (completion i - a_ready of
+    // `aready`).
+    __device__ static void mma(State &s, int ntiles, int kslabs, int nsteps, int32_t *err, int a_ready = 1) {
         constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
         // a descriptor moves with its operand: its low field is the shared
         // address >> 4, which no address of this CTA carries out of
@@ -253,8 +255,8 @@ struct Pipe {
         uint32_t phase = 0, tphase = 0;
         bool ok = true;
         for (int step = 0; step < nsteps && ok; ++step) {
-            if (step > 0) {
-                if (!tc::mbar_wait(s.aready, (uint32_t)(step - 1) & 1u, s.abort_flag, err)) break;
+            if (step >= a_ready) {
+                if (!tc::mbar_wait(s.aready, (uint32_t)(step - a_ready) & 1u, s.abort_flag, err)) break;
                 tc::tc_fence_after();
             }
             for (int tl = 0; tl < ntiles && ok; ++tl) {

@@ -147,6 +147,8 @@ RNN_SMALL = [
     W.small("rnn", R=3, gamma=3, V=257, r=8, d=8, dtype="f32"),
     W.small("rnn", R=70, gamma=3, V=2000, r=64, d=24),   # tensor cores, one M-tile of 128
     W.small("rnn", R=150, gamma=3, V=2000, r=64, d=24),  # tensor cores, 2 M-tiles (the second ragged)
+    W.small("rnn", R=40, gamma=4, V=3000, r=128, d=20),  # tensor-core draft, CUDA-core h projection (d % 8)
+    W.small("rnn", R=129, gamma=5, V=1024, r=256, d=72), # r = 256, two M-tiles, 2 K slabs of h
 ]
 
 
