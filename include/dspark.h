@@ -165,7 +165,8 @@ typedef struct {
  * formed for all (request, k) first, one bf16 GEMM on the tensor cores
  * (tcgen05; fp32, or shapes it does not take -- d or 2r + d not a multiple of
  * 8 -- go to a CUDA-core kernel).  The workspace holds the draft scratch, two
- * [R, r] state buffers and the [R gamma, 3r] fp32 projection. */
+ * [R, r] state buffers, the [R gamma, 3r] fp32 projection and 128 KiB per
+ * 128 requests for the bf16 operands the tensor-core steps prepare. */
 DSPARK_API size_t dspark_draft_rnn_workspace_size(const dspark_rnn_args *a);
 DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_stream_t stream);
 

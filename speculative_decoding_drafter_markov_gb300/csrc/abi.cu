@@ -106,7 +106,7 @@ size_t draft_ws_bytes(const dspark_draft_args *a, const float *A_rnn) {
 
 // the gamma sequential steps shared by both heads
 int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws, cudaStream_t s,
-                   const dspark::RnnStep *rnn, int k_first, int k_last) {
+                   const dspark::RnnStep *rnn, int k_first, int k_last, unsigned char *a_stage = nullptr) {
     using namespace dspark;
     DraftStep st = step_template(a, rnn ? A_rnn : nullptr);
     st.part = static_cast<DraftPartial *>(part_ws);
@@ -136,9 +136,10 @@ int run_draft_loop(const dspark_draft_args *a, const float *A_rnn, void *part_ws
         st.x_prev = k_first == 1 ? a->anchor : a->x + (k_first - 2);
         st.x_stride = k_first == 1 ? 1 : a->gamma;
         if (rnn) {
-            if (k_first != 1) return fail(DSPARK_ERR_INVAL, "RNN draft runs from step 1");
+            if (k_first != 1 || !a_stage) return fail(DSPARK_ERR_INVAL, "RNN draft runs from step 1");
             st.rnn = *rnn;
             st.phase0 = 0;
+            st.a_stage = a_stage;
         }
         cudaError_t e = launch_draft_step_tc(st, s);
         return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft steps (tensor cores)");
@@ -284,10 +285,13 @@ DSPARK_API int dspark_draft_markov_noalloc(const dspark_draft_args *a, dspark_st
 }
 
 namespace {
+// prepared operands of the tensor-core RNN step, one region per M-tile of 128 requests
+size_t rnn_stage_bytes(const dspark_draft_args &b) { return (size_t)((b.R + 127) / 128) * dspark::kRnnStageBytes; }
+
 size_t rnn_ws_bytes(const dspark_rnn_args *a) {
     const dspark_draft_args &b = a->base;
     return draft_ws_bytes(&b, a->A) + 2 * dspark::align256(sizeof(float) * (size_t)b.R * b.r) +
-           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
+           dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r) + rnn_stage_bytes(b);
 }
 }  // namespace
 
@@ -313,7 +317,11 @@ DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_strea
     float *state1 = reinterpret_cast<float *>(p);
     p += dspark::align256(state_bytes);
     float *Hpre = reinterpret_cast<float *>(p);
-    cudaError_t e = a->s0 ? cudaMemcpyAsync(state0, a->s0, state_bytes, cudaMemcpyDeviceToDevice, s)
+    p += dspark::align256(sizeof(float) * (size_t)b.R * b.gamma * 3 * b.r);
+    unsigned char *stage = reinterpret_cast<unsigned char *>(p);  // rows beyond R stay zero
+    cudaError_t e = cudaMemsetAsync(stage, 0, rnn_stage_bytes(b), s);
+    if (e != cudaSuccess) return cuda_fail(e, "rnn operand staging");
+    e = a->s0 ? cudaMemcpyAsync(state0, a->s0, state_bytes, cudaMemcpyDeviceToDevice, s)
                           : cudaMemsetAsync(state0, 0, state_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn state init");
     if (b.d > 0) {
@@ -330,7 +338,7 @@ DSPARK_API int dspark_draft_rnn(const dspark_rnn_args *a, void *ws, dspark_strea
     rs.W = a->W; rs.W1 = b.W1; rs.Hpre = Hpre; rs.A = a->A; rs.err = b.err;
     rs.s_in = state0;
     rs.s_out = state1;
-    rc = run_draft_loop(&b, a->A, part, s, &rs, 1, b.gamma);
+    rc = run_draft_loop(&b, a->A, part, s, &rs, 1, b.gamma, stage);
     if (rc != DSPARK_OK) return rc;
     if (a->s_out) {
         const float *last = (b.gamma & 1) ? state1 : state0;

@@ -53,6 +53,7 @@ struct TcParams {
     int n_mtiles;
     int32_t *err;
     RnnStep rnn;  // RNN head: the state update's inputs (s_in holds s_{k-1})
+    unsigned char *a_stage;  // RNN head: [n_mtiles][kRnnStageBytes] prepared operands
 };
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
@@ -266,15 +267,35 @@ __device__ __forceinline__ bool mtile_sync(const TcParams &p, typename P::State 
 }
 
 // RNN head, eq. (6): the state update of step k for the M-tile's requests --
-// s_k and A_k = tanh(W_o z_k) from s_{k-1} and x_{k-1} (the launch's input
-// token for its first step, else step k-1's race winner) -- as tiles of 16
-// requests x 8 gate entries spread over the M-tile's CTAs, staged in the
-// operand region (free between two steps' contractions).
+//   G = W[:, :2r] [s_{k-1} ; W_1[x_{k-1}]] + Hpre_k,
+//   s_k = sigma(G_g) s_{k-1} + (1 - sigma(G_g)) tanh(G_c),   A_k = tanh(G_o),
+// with x_{k-1} the launch's input token at its first step, else step k-1's race
+// winner.  Tiles of kRQ requests x kIE gate entries spread over the M-tile's
+// CTAs; a tile stages its 3 kIE weight rows and kRQ input vectors in fp32 in the
+// operand region (free between two steps' contractions).  Thread (ks, ii, qb)
+// takes the K inputs 4 (ks + 16 g), g = 0.., of entry ii for the kQB requests of
+// block qb (one weight load serves kQB requests), then 16 lanes sum by
+// shuffles.  Besides s_k and the fp32 A_k, each tile writes its 16-byte chunk of
+// the operand -- A_k split into bf16 hi + lo, in the shared-memory layout of the
+// contraction -- to the M-tile's staging buffer, which every CTA of the M-tile
+// then bulk-copies into its operand region.
+namespace rnnt {
+constexpr int kRQ = 32;  // requests per tile
+constexpr int kIE = 8;   // gate entries per tile (one 16-byte operand chunk)
+constexpr int kKS = 16;  // lanes sharing one (entry, request block)
+constexpr int kQB = 8;   // requests per thread
+static_assert(kKS * kIE * (kRQ / kQB) == tcp::kEpiThreads, "one thread per (ks, entry, request block)");
+// shared memory: [3 kIE + kRQ][2r + 4] fp32, [kRQ][kIE] fp32, kRQ tokens
+__host__ __device__ constexpr int smem_bytes(int r) {
+    return 4 * (3 * kIE + kRQ) * (2 * r + 4) + 4 * kRQ * kIE + 4 * kRQ;
+}
+}  // namespace rnnt
+
 template <class P>
-__device__ __forceinline__ void rnn_state_update(const TcParams &p, const typename P::State &s, int m0, int cv,
-                                                 int k, int et) {
-    static_assert(P::kABytes - P::kMergeBytes >= (int)rnn::tile_smem_bytes(256) && rnn::kThreads == tcp::kEpiThreads,
-                  "state-update tile in the operand region");
+__device__ __forceinline__ void rnn_state_update(const TcParams &p, const typename P::State &s, int m0, int m_tile,
+                                                 int cv, int k, int et) {
+    static_assert(P::kABytes - P::kMergeBytes >= rnnt::smem_bytes(256), "state-update tile in the operand region");
+    static_assert(P::kABytes == (int)kRnnStageBytes, "staging buffer holds one operand region");
     RnnStep rs = p.rnn;
     if (((k - p.k) & 1) != 0) {  // the buffers alternate: s_in holds s_{k-1} at the launch's first step
         rs.s_in = p.rnn.s_out;
@@ -288,11 +309,137 @@ __device__ __forceinline__ void rnn_state_update(const TcParams &p, const typena
     } else {
         rs.x_win = p.winners + (size_t)(p.step_index + (k - 1 - p.k) - 1) * p.R;
     }
-    float *sh = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) + P::kMergeBytes);
-    const int ni = (p.r + rnn::kIB - 1) / rnn::kIB;
-    const int nq = (min(P::MV, p.R - m0) + rnn::kRB - 1) / rnn::kRB;
-    for (int t = cv; t < ni * nq; t += p.nparts)
-        rnn::step_tile<__nv_bfloat16>(rs, sh, (t % ni) * rnn::kIB, m0 + (t / ni) * rnn::kRB, et, EpiSync{});
+    const int r = p.r, K = 2 * r, ld = K + 4, ldw = 2 * r + p.d;
+    float *Ws = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) + P::kMergeBytes);
+    float *Zs = Ws + 3 * rnnt::kIE * ld;
+    float *As = Zs + rnnt::kRQ * ld;
+    int *xs = reinterpret_cast<int *>(As + rnnt::kRQ * rnnt::kIE);
+    const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(rs.W);
+    unsigned char *stage = p.a_stage + (size_t)m_tile * kRnnStageBytes;
+    const int ni = r / rnnt::kIE;
+    const int nq = (min(P::MV, p.R - m0) + rnnt::kRQ - 1) / rnnt::kRQ;
+    const int ks = et % rnnt::kKS, ii = (et / rnnt::kKS) % rnnt::kIE, qb = et / (rnnt::kKS * rnnt::kIE);
+    const int cpr = K / 8;  // 16-byte chunks of a staged row
+    for (int t = cv; t < ni * nq; t += p.nparts) {
+        const int i0 = (t % ni) * rnnt::kIE, q0 = m0 + (t / ni) * rnnt::kRQ;
+        if (et < rnnt::kRQ) xs[et] = q0 + et < p.R ? rnn::token(rs, q0 + et) : 0;
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        // weight rows g r + i0 + e (g: gate, candidate, output) and the inputs
+        // [s_{k-1} ; W_1[x_{k-1}]] of the tile's requests, widened to fp32; the
+        // rows of W start on 16-byte boundaries only when 2r + d is a multiple of 8
+        if ((ldw & 7) == 0) {
+#pragma unroll 2
+            for (int e = et; e < 3 * rnnt::kIE * cpr; e += tcp::kEpiThreads) {
+                const int row = e / cpr, c = e - row * cpr;
+                const int g = row / rnnt::kIE, i = i0 + (row - g * rnnt::kIE);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(W + (size_t)(g * r + i) * ldw + c * 8);
+                float4 *dst = reinterpret_cast<float4 *>(Ws + row * ld + c * 8);
+                dst[0] = make_float4(tcp::bf16_lo(raw.x), tcp::bf16_hi(raw.x), tcp::bf16_lo(raw.y), tcp::bf16_hi(raw.y));
+                dst[1] = make_float4(tcp::bf16_lo(raw.z), tcp::bf16_hi(raw.z), tcp::bf16_lo(raw.w), tcp::bf16_hi(raw.w));
+            }
+        } else {
+            for (int e = et; e < 3 * rnnt::kIE * K; e += tcp::kEpiThreads) {
+                const int row = e / K, j = e - row * K;
+                const int g = row / rnnt::kIE, i = i0 + (row - g * rnnt::kIE);
+                Ws[row * ld + j] = __bfloat162float(W[(size_t)(g * r + i) * ldw + j]);
+            }
+        }
+#pragma unroll 2
+        for (int e = et; e < rnnt::kRQ * cpr; e += tcp::kEpiThreads) {
+            const int q = e / cpr, c = e - q * cpr, rq = q0 + q, j = c * 8;
+            float4 *dst = reinterpret_cast<float4 *>(Zs + q * ld + j);
+            if (rq >= p.R) {
+                dst[0] = dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (j < r) {
+                // the state buffers alternate between steps and other CTAs write them: L2 reads
+                const float4 *src = reinterpret_cast<const float4 *>(rs.s_in + (size_t)rq * r + j);
+                dst[0] = __ldcg(src);
+                dst[1] = __ldcg(src + 1);
+            } else {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xs[q] * r + (j - r));
+                dst[0] = make_float4(tcp::bf16_lo(raw.x), tcp::bf16_hi(raw.x), tcp::bf16_lo(raw.y), tcp::bf16_hi(raw.y));
+                dst[1] = make_float4(tcp::bf16_lo(raw.z), tcp::bf16_hi(raw.z), tcp::bf16_lo(raw.w), tcp::bf16_hi(raw.w));
+            }
+        }
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        float acc[rnnt::kQB][3];
+#pragma unroll
+        for (int q = 0; q < rnnt::kQB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = 0.f;
+        const float *wg = Ws + ii * ld, *wc = Ws + (rnnt::kIE + ii) * ld, *wo = Ws + (2 * rnnt::kIE + ii) * ld;
+        const float *zb = Zs + qb * rnnt::kQB * ld;
+        for (int j = 4 * ks; j < K; j += 4 * rnnt::kKS) {
+            const float4 a = *reinterpret_cast<const float4 *>(wg + j);
+            const float4 b = *reinterpret_cast<const float4 *>(wc + j);
+            const float4 c = *reinterpret_cast<const float4 *>(wo + j);
+#pragma unroll
+            for (int q = 0; q < rnnt::kQB; ++q) {
+                const float4 z = *reinterpret_cast<const float4 *>(zb + q * ld + j);
+                acc[q][0] = fmaf(a.w, z.w, fmaf(a.z, z.z, fmaf(a.y, z.y, fmaf(a.x, z.x, acc[q][0]))));
+                acc[q][1] = fmaf(b.w, z.w, fmaf(b.z, z.z, fmaf(b.y, z.y, fmaf(b.x, z.x, acc[q][1]))));
+                acc[q][2] = fmaf(c.w, z.w, fmaf(c.z, z.z, fmaf(c.y, z.y, fmaf(c.x, z.x, acc[q][2]))));
+            }
+        }
+#pragma unroll
+        for (int off = 1; off < rnnt::kKS; off <<= 1)
+#pragma unroll
+            for (int q = 0; q < rnnt::kQB; ++q) {
+                acc[q][0] += __shfl_xor_sync(0xffffffffu, acc[q][0], off);
+                acc[q][1] += __shfl_xor_sync(0xffffffffu, acc[q][1], off);
+                acc[q][2] += __shfl_xor_sync(0xffffffffu, acc[q][2], off);
+            }
+        if (ks == 0) {
+            const int i = i0 + ii;
+#pragma unroll
+            for (int q = 0; q < rnnt::kQB; ++q) {
+                const int ql = qb * rnnt::kQB + q, rq = q0 + ql;
+                float a_out = 0.f;
+                if (rq < p.R) {
+                    const float *hp = rs.Hpre + ((size_t)rq * p.gamma + (k - 1)) * (size_t)(3 * r);
+                    const float gg = acc[q][0] + hp[i], gc = acc[q][1] + hp[r + i], go = acc[q][2] + hp[2 * r + i];
+                    const float g = 1.0f / (1.0f + expf(-gg));
+                    rs.s_out[(size_t)rq * r + i] = g * Zs[ql * ld + i] + (1.0f - g) * tanhf(gc);
+                    a_out = tanhf(go);
+                    rs.A[((size_t)rq * p.gamma + (k - 1)) * (size_t)r + i] = a_out;
+                }
+                As[ql * rnnt::kIE + ii] = a_out;
+            }
+        }
+        tc::named_bar_sync(1, tcp::kEpiThreads);
+        // the operand chunk (entries i0 .. i0 + 7) of each request of the tile, hi and lo parts
+        if (et < rnnt::kRQ && q0 + et < p.R) {
+            const int row = q0 - m0 + et;
+            uint4 hi, lo;
+            tcp::split8(As + et * rnnt::kIE, hi, lo);
+            *reinterpret_cast<uint4 *>(stage + P::a_offset(row, i0 / 8, 0)) = hi;
+            *reinterpret_cast<uint4 *>(stage + P::a_offset(row, i0 / 8, 1)) = lo;
+        }
+        tc::named_bar_sync(1, tcp::kEpiThreads);  // the scratch is reused by the next tile
+    }
+    // the staged chunks are read by other CTAs' bulk copies (async proxy)
+    tc::fence_proxy_async_global();
+}
+
+// RNN head: one thread copies the M-tile's prepared operand (the kslabs used K
+// slabs of the hi and lo parts) from the staging buffer into the operand region
+// and, once it has landed, lets the MMA warp go.  `use` counts the copies of
+// the launch (the barrier's phase).
+template <class P>
+__device__ __forceinline__ bool rnn_load_operand(const TcParams &p, typename P::State &s, int m_tile, int use) {
+    const unsigned char *stage = p.a_stage + (size_t)m_tile * kRnnStageBytes;
+    const int kslabs = p.r / 64;
+    tc::fence_proxy_async_global();
+    tc::mbar_expect_tx(s.opbar, (uint32_t)(2 * kslabs * P::kSlabA));
+    for (int part = 0; part < 2; ++part)
+        for (int j = 0; j < kslabs; ++j) {
+            const int slab = j + 4 * part;
+            tc::bulk_load(s.sA + slab * P::kSlabA, stage + slab * P::kSlabA, (uint32_t)P::kSlabA, s.opbar);
+        }
+    if (!tc::mbar_wait_drain(s.opbar, (uint32_t)use & 1u, p.err)) {
+        *s.abort_flag = 1;
+        return false;
+    }
+    tc::mbar_arrive(s.aready);
+    return true;
 }
 
 // One launch runs draft steps k .. k + nsteps - 1 of one decoding cycle.  CTA
@@ -373,13 +520,12 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         const uint32_t c3 = philox_ctr3(p.cycle, 0);
         float *mg = P::merge_scratch(s);
         int phase = p.phase0;  // cross-CTA synchronisation points passed
+        int op_copies = 0;     // RNN head: operand copies issued
         if constexpr (P::KSPLIT == 2) {
             // RNN head: the state update of the first step, then its operand A_k
-            rnn_state_update<P>(p, s, m0, cv, p.k, et);
-            if (mtile_sync<P>(p, s, ctr, ++phase, et, true)) {
-                gather_operand<P>(p, s, m0, p.k, et, tcp::kEpiThreads);
-                P::operand_written(s, et);
-            }
+            rnn_state_update<P>(p, s, m0, m_tile, cv, p.k, et);
+            if (mtile_sync<P>(p, s, ctr, ++phase, et, true) && et == 0) rnn_load_operand<P>(p, s, m_tile, op_copies);
+            ++op_copies;
         }
         for (int step = 0; step < p.nsteps && !*s.abort_flag; ++step) {
             const int k = p.k + step, q = p.step_index + step;
@@ -529,13 +675,16 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 tc::named_bar_sync(1, tcp::kEpiThreads);
                 if constexpr (P::KSPLIT == 2) {
                     // RNN head: the state update of step k + 1 over the M-tile's CTAs,
-                    // then its operand A_{k+1}
-                    rnn_state_update<P>(p, s, m0, cv, k + 1, et);
+                    // then its operand A_{k+1} (prepared by those CTAs) is copied in
+                    rnn_state_update<P>(p, s, m0, m_tile, cv, k + 1, et);
                     if (!mtile_sync<P>(p, s, ctr, ++phase, et, true)) break;
+                    if (et == 0) rnn_load_operand<P>(p, s, m_tile, op_copies);
+                    ++op_copies;
+                } else {
+                    // the next operand W_1[x_k], then the MMA warp goes
+                    gather_operand<P>(p, s, m0, k + 1, et, tcp::kEpiThreads);
+                    P::operand_written(s, et);
                 }
-                // the next operand (W_1[x_k], or A_{k+1}), then the MMA warp goes
-                gather_operand<P>(p, s, m0, k + 1, et, tcp::kEpiThreads);
-                P::operand_written(s, et);
             }
         }
         // lse_k and log q_k of every step of the launch: (step, request) pairs of
@@ -621,6 +770,7 @@ cudaError_t launch_cfg(const DraftStep &p, int nparts, int n_mtiles, cudaStream_
     tp.n_mtiles = n_mtiles;
     tp.err = p.err;
     tp.rnn = p.rnn;
+    tp.a_stage = p.a_stage;
     auto kern = draft_step_tc<P>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes);
     if (e != cudaSuccess) return e;

@@ -59,7 +59,12 @@ struct DraftStep {
     // A_op + (k' - k) r; before it, the launch runs the state update of step k'
     // from `rnn` (s_in: the buffer holding s_{k-1}; the buffers alternate)
     RnnStep rnn;
+    unsigned char *a_stage;          // RNN: [n_mtiles][kRnnStageBytes] operands prepared for the
+                                     // bulk copy (rows beyond R zero)
 };
+// the RNN operand of one M-tile (128 rows x 256 K x hi/lo bf16) as the
+// tensor-core step lays it out in shared memory
+constexpr size_t kRnnStageBytes = 131072;
 int draft_step_nparts(int V);  // CUDA-core path: one partial per 64-entry slice
 cudaError_t launch_draft_step(const DraftStep &p, cudaStream_t s);
 // tensor-core path (bf16, r in {64, 128, 192, 256}, V % 8 == 0)

@@ -146,6 +146,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// bulk asynchronous copy global -> shared of `bytes` bytes (both addresses
+// 16-byte aligned, bytes a multiple of 16), completing on an mbarrier
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// orders this thread's generic-proxy global accesses with its later (or
+// another thread's, through a release/acquire) async-proxy accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // L2 policy for data read once (evict it before anything else)
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;

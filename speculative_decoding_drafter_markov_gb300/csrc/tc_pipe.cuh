@@ -58,7 +58,7 @@ struct Pipe {
     static constexpr int kOffB = kABytes;
     static constexpr int kOffU = kOffB + NS * kSlabB;
     static constexpr int kOffBar = kOffU + SU * kUBytes;
-    static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC + 1;
+    static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC + 2;
     static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
     static constexpr int kOffTok = kOffThr + 8 * MV;        // per-request tokens / metadata
     static constexpr int kOffMisc = kOffTok + 4 * MV;
@@ -77,6 +77,7 @@ struct Pipe {
         unsigned char *smem, *sA;
         uint64_t *fullB, *emptyB, *fullU, *emptyU, *tfull, *tempty;
         uint64_t *aready;  // operand of the next step written (multi-step launches)
+        uint64_t *opbar;   // bulk copy of a prepared operand into the operand region landed
         unsigned long long *thr;  // per request: the best packed race winner the CTA knows
         int *tok;          // MV ints of per-request scratch
         uint32_t *tmem_slot;
@@ -98,6 +99,7 @@ struct Pipe {
         s.tfull = bars + 2 * NS + 2 * SU;
         s.tempty = s.tfull + NACC;
         s.aready = s.tempty + NACC;
+        s.opbar = s.aready + 1;
         s.thr = reinterpret_cast<unsigned long long *>(s.smem + kOffThr);
         s.tok = reinterpret_cast<int *>(s.smem + kOffTok);
         s.tmem_slot = reinterpret_cast<uint32_t *>(s.smem + kOffMisc);
@@ -125,6 +127,7 @@ struct Pipe {
                 tc::mbar_init(&s.tempty[b], kEpiWarps);
             }
             tc::mbar_init(s.aready, 1);
+            tc::mbar_init(s.opbar, 1);
             *s.abort_flag = 0;
             *s.flag = 0;
             tc::fence_mbar_init();
@@ -143,10 +146,13 @@ struct Pipe {
         s.tmem_base = *s.tmem_slot;
     }
 
-    // 16-byte chunk c (8 bf16 along K) of MMA row `row` of split part `part` of A
+    // byte offset of 16-byte chunk c (8 bf16 along K) of MMA row `row` of split
+    // part `part` in the operand region (K-major, 128-byte swizzle, 64-wide slabs)
+    __host__ __device__ static constexpr int a_offset(int row, int c, int part) {
+        return ((c >> 3) + 4 * part) * kSlabA + (row >> 3) * 1024 + (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+    }
     __device__ static unsigned char *a_chunk(const State &s, int row, int c, int part) {
-        const int slab = (c >> 3) + 4 * part, cc = c & 7;
-        return s.sA + slab * kSlabA + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4);
+        return s.sA + a_offset(row, c, part);
     }
 
     // write operand chunk c of request row `row` (both copies when DUAL)
