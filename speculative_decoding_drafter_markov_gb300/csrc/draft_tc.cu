@@ -273,8 +273,8 @@ __device__ __forceinline__ bool mtile_sync(const TcParams &p, typename P::State 
 // winner.  Tiles of kRQ requests x kIE gate entries spread over the M-tile's
 // CTAs; a tile stages its 3 kIE weight rows and kRQ input vectors in fp32 in the
 // operand region (free between two steps' contractions).  Thread (ks, ii, qb)
-// takes the K inputs 4 (ks + 16 g), g = 0.., of entry ii for the kQB requests of
-// block qb (one weight load serves kQB requests), then 16 lanes sum by
+// takes the K inputs 4 (ks + kKS g), g = 0.., of entry ii for the kQB requests of
+// block qb (one weight load serves kQB requests), then kKS lanes sum by
 // shuffles.  Besides s_k and the fp32 A_k, each tile writes its 16-byte chunk of
 // the operand -- A_k split into bf16 hi + lo, in the shared-memory layout of the
 // contraction -- to the M-tile's staging buffer, which every CTA of the M-tile
@@ -282,126 +282,187 @@ __device__ __forceinline__ bool mtile_sync(const TcParams &p, typename P::State 
 namespace rnnt {
 constexpr int kRQ = 32;  // requests per tile
 constexpr int kIE = 8;   // gate entries per tile (one 16-byte operand chunk)
-constexpr int kKS = 16;  // lanes sharing one (entry, request block)
-constexpr int kQB = 8;   // requests per thread
+constexpr int kKS = 8;   // lanes sharing one (entry, request block)
+constexpr int kQB = 4;   // requests per thread
+constexpr int kWLoads = 3;  // 16-byte weight chunks per thread (r <= 256)
+constexpr int kZLoads = 4;  // 16-byte chunks of the state inputs per thread (r <= 256)
 static_assert(kKS * kIE * (kRQ / kQB) == tcp::kEpiThreads, "one thread per (ks, entry, request block)");
-// shared memory: [3 kIE + kRQ][2r + 4] fp32, [kRQ][kIE] fp32, kRQ tokens
+static_assert(kWLoads * tcp::kEpiThreads >= 3 * kIE * 64 && kZLoads * tcp::kEpiThreads >= kRQ * 64 &&
+                  (kZLoads / 2) * tcp::kEpiThreads >= kRQ * 32,
+              "r <= 256");
+// shared memory: [3 kIE + kRQ][2r + 4] fp32, the tile's pre-activations from
+// the h projection [kRQ][3 kIE] fp32, A_k [kRQ][kIE] fp32, kRQ tokens
 __host__ __device__ constexpr int smem_bytes(int r) {
-    return 4 * (3 * kIE + kRQ) * (2 * r + 4) + 4 * kRQ * kIE + 4 * kRQ;
+    return 4 * (3 * kIE + kRQ) * (2 * r + 4) + 4 * kRQ * 3 * kIE + 4 * kRQ * kIE + 4 * kRQ;
 }
 }  // namespace rnnt
+
+__device__ __forceinline__ float4 bf16x8_lo4(const uint4 &v) {
+    return make_float4(tcp::bf16_lo(v.x), tcp::bf16_hi(v.x), tcp::bf16_lo(v.y), tcp::bf16_hi(v.y));
+}
+__device__ __forceinline__ float4 bf16x8_hi4(const uint4 &v) {
+    return make_float4(tcp::bf16_lo(v.z), tcp::bf16_hi(v.z), tcp::bf16_lo(v.w), tcp::bf16_hi(v.w));
+}
 
 template <class P>
 __device__ __forceinline__ void rnn_state_update(const TcParams &p, const typename P::State &s, int m0, int m_tile,
                                                  int cv, int k, int et) {
     static_assert(P::kABytes - P::kMergeBytes >= rnnt::smem_bytes(256), "state-update tile in the operand region");
     static_assert(P::kABytes == (int)kRnnStageBytes, "staging buffer holds one operand region");
-    RnnStep rs = p.rnn;
-    if (((k - p.k) & 1) != 0) {  // the buffers alternate: s_in holds s_{k-1} at the launch's first step
-        rs.s_in = p.rnn.s_out;
-        rs.s_out = const_cast<float *>(p.rnn.s_in);
-    }
-    rs.k = k;
-    if (k == p.k) {
-        rs.x_prev = p.x_prev;
-        rs.x_stride = p.x_stride;
-        rs.x_win = nullptr;
-    } else {
-        rs.x_win = p.winners + (size_t)(p.step_index + (k - 1 - p.k) - 1) * p.R;
-    }
+    // the state buffers alternate: p.rnn.s_in holds s_{k-1} at the launch's first step
+    const bool odd = ((k - p.k) & 1) != 0;
+    const float *s_in = odd ? p.rnn.s_out : p.rnn.s_in;
+    float *s_out = odd ? const_cast<float *>(p.rnn.s_in) : p.rnn.s_out;
+    // x_{k-1}: the launch's input tokens at its first step, else step k-1's race winners
+    const unsigned long long *x_win =
+        k == p.k ? nullptr : p.winners + (size_t)(p.step_index + (k - 1 - p.k) - 1) * p.R;
     const int r = p.r, K = 2 * r, ld = K + 4, ldw = 2 * r + p.d;
     float *Ws = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(P::merge_scratch(s)) + P::kMergeBytes);
     float *Zs = Ws + 3 * rnnt::kIE * ld;
-    float *As = Zs + rnnt::kRQ * ld;
+    float *Hs = Zs + rnnt::kRQ * ld;
+    float *As = Hs + rnnt::kRQ * 3 * rnnt::kIE;
     int *xs = reinterpret_cast<int *>(As + rnnt::kRQ * rnnt::kIE);
-    const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(rs.W);
+    const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(p.rnn.W);
     unsigned char *stage = p.a_stage + (size_t)m_tile * kRnnStageBytes;
     const int ni = r / rnnt::kIE;
     const int nq = (min(P::MV, p.R - m0) + rnnt::kRQ - 1) / rnnt::kRQ;
     const int ks = et % rnnt::kKS, ii = (et / rnnt::kKS) % rnnt::kIE, qb = et / (rnnt::kKS * rnnt::kIE);
-    const int cpr = K / 8;  // 16-byte chunks of a staged row
+    const int cpr = K / 8;  // 16-byte chunks of a staged weight row
+    const int nw = 3 * rnnt::kIE * cpr;
+    const bool wvec = (ldw & 7) == 0;  // rows of W start on 16-byte boundaries
     for (int t = cv; t < ni * nq; t += p.nparts) {
         const int i0 = (t % ni) * rnnt::kIE, q0 = m0 + (t / ni) * rnnt::kRQ;
-        if (et < rnnt::kRQ) xs[et] = q0 + et < p.R ? rnn::token(rs, q0 + et) : 0;
+        if (et < rnnt::kRQ) {
+            int x = 0;
+            if (q0 + et < p.R) {
+                if (x_win) {
+                    x = winner_index(__ldcg(x_win + q0 + et));
+                    if (x < 0 || x >= p.V) x = 0;  // no winner: reported by the finaliser
+                } else {
+                    x = load_token(p, q0 + et, p.x_prev, p.x_stride);
+                }
+            }
+            xs[et] = x;
+        }
         tc::named_bar_sync(1, tcp::kEpiThreads);
-        // weight rows g r + i0 + e (g: gate, candidate, output) and the inputs
-        // [s_{k-1} ; W_1[x_{k-1}]] of the tile's requests, widened to fp32; the
-        // rows of W start on 16-byte boundaries only when 2r + d is a multiple of 8
-        if ((ldw & 7) == 0) {
-#pragma unroll 2
-            for (int e = et; e < 3 * rnnt::kIE * cpr; e += tcp::kEpiThreads) {
+        // All of a thread's loads in flight together: weight rows g r + i0 + e
+        // (g: gate, candidate, output), the inputs [s_{k-1} ; W_1[x_{k-1}]] of the
+        // tile's requests and their h-projection terms; then widened to fp32.
+        // the state part of the inputs moves as 16-byte chunks of 4 fp32, the
+        // embedding part as 16-byte chunks of 8 bf16
+        const int cs = r / 4, ce = r / 8;
+        uint4 wr[rnnt::kWLoads], zs[rnnt::kZLoads];
+#pragma unroll
+        for (int n = 0; n < rnnt::kWLoads; ++n) {
+            const int e = et + n * tcp::kEpiThreads;
+            if (wvec && e < nw) {
                 const int row = e / cpr, c = e - row * cpr;
                 const int g = row / rnnt::kIE, i = i0 + (row - g * rnnt::kIE);
-                const uint4 raw = *reinterpret_cast<const uint4 *>(W + (size_t)(g * r + i) * ldw + c * 8);
-                float4 *dst = reinterpret_cast<float4 *>(Ws + row * ld + c * 8);
-                dst[0] = make_float4(tcp::bf16_lo(raw.x), tcp::bf16_hi(raw.x), tcp::bf16_lo(raw.y), tcp::bf16_hi(raw.y));
-                dst[1] = make_float4(tcp::bf16_lo(raw.z), tcp::bf16_hi(raw.z), tcp::bf16_lo(raw.w), tcp::bf16_hi(raw.w));
+                wr[n] = *reinterpret_cast<const uint4 *>(W + (size_t)(g * r + i) * ldw + c * 8);
             }
-        } else {
+        }
+#pragma unroll
+        for (int n = 0; n < rnnt::kZLoads; ++n) {
+            const int e = et + n * tcp::kEpiThreads, q = e / cs, rq = q0 + q;
+            // the state buffers alternate between steps and other CTAs write them: L2 reads
+            if (e < rnnt::kRQ * cs && rq < p.R)
+                zs[n] = __ldcg(reinterpret_cast<const uint4 *>(s_in + (size_t)rq * r) + (e - q * cs));
+        }
+        for (int e = et; e < rnnt::kRQ * 3 * rnnt::kIE; e += tcp::kEpiThreads) {
+            const int q = e / (3 * rnnt::kIE), gi = e - q * 3 * rnnt::kIE, g = gi / rnnt::kIE;
+            const int rq = q0 + q, i = i0 + (gi - g * rnnt::kIE);
+            Hs[e] = rq < p.R ? p.rnn.Hpre[((size_t)rq * p.gamma + (k - 1)) * (size_t)(3 * r) + g * r + i] : 0.f;
+        }
+#pragma unroll
+        for (int n = 0; n < rnnt::kWLoads; ++n) {
+            const int e = et + n * tcp::kEpiThreads;
+            if (wvec && e < nw) {
+                const int row = e / cpr, c = e - row * cpr;
+                float4 *dst = reinterpret_cast<float4 *>(Ws + row * ld + c * 8);
+                dst[0] = bf16x8_lo4(wr[n]);
+                dst[1] = bf16x8_hi4(wr[n]);
+            }
+        }
+        if (!wvec) {
             for (int e = et; e < 3 * rnnt::kIE * K; e += tcp::kEpiThreads) {
                 const int row = e / K, j = e - row * K;
                 const int g = row / rnnt::kIE, i = i0 + (row - g * rnnt::kIE);
                 Ws[row * ld + j] = __bfloat162float(W[(size_t)(g * r + i) * ldw + j]);
             }
         }
-#pragma unroll 2
-        for (int e = et; e < rnnt::kRQ * cpr; e += tcp::kEpiThreads) {
-            const int q = e / cpr, c = e - q * cpr, rq = q0 + q, j = c * 8;
-            float4 *dst = reinterpret_cast<float4 *>(Zs + q * ld + j);
-            if (rq >= p.R) {
-                dst[0] = dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (j < r) {
-                // the state buffers alternate between steps and other CTAs write them: L2 reads
-                const float4 *src = reinterpret_cast<const float4 *>(rs.s_in + (size_t)rq * r + j);
-                dst[0] = __ldcg(src);
-                dst[1] = __ldcg(src + 1);
-            } else {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xs[q] * r + (j - r));
-                dst[0] = make_float4(tcp::bf16_lo(raw.x), tcp::bf16_hi(raw.x), tcp::bf16_lo(raw.y), tcp::bf16_hi(raw.y));
-                dst[1] = make_float4(tcp::bf16_lo(raw.z), tcp::bf16_hi(raw.z), tcp::bf16_lo(raw.w), tcp::bf16_hi(raw.w));
+#pragma unroll
+        for (int n = 0; n < rnnt::kZLoads; ++n) {
+            const int e = et + n * tcp::kEpiThreads, q = e / cs;
+            if (e < rnnt::kRQ * cs) {
+                const uint4 v = q0 + q < p.R ? zs[n] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(Zs + q * ld + 4 * (e - q * cs)) = v;
+            }
+        }
+        uint4 ze[rnnt::kZLoads / 2];
+#pragma unroll
+        for (int n = 0; n < rnnt::kZLoads / 2; ++n) {
+            const int e = et + n * tcp::kEpiThreads, q = e / ce, rq = q0 + q;
+            if (e < rnnt::kRQ * ce && rq < p.R)
+                ze[n] = *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xs[q] * r + 8 * (e - q * ce));
+        }
+#pragma unroll
+        for (int n = 0; n < rnnt::kZLoads / 2; ++n) {
+            const int e = et + n * tcp::kEpiThreads, q = e / ce;
+            if (e < rnnt::kRQ * ce) {
+                float4 *dst = reinterpret_cast<float4 *>(Zs + q * ld + r + 8 * (e - q * ce));
+                if (q0 + q < p.R) {
+                    dst[0] = bf16x8_lo4(ze[n]);
+                    dst[1] = bf16x8_hi4(ze[n]);
+                } else {
+                    dst[0] = dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
         tc::named_bar_sync(1, tcp::kEpiThreads);
-        float acc[rnnt::kQB][3];
+        // dot products on paired lanes: (even, odd) inputs of each float4 half
+        float2 acc[rnnt::kQB][3];
 #pragma unroll
-        for (int q = 0; q < rnnt::kQB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = 0.f;
+        for (int q = 0; q < rnnt::kQB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = make_float2(0.f, 0.f);
         const float *wg = Ws + ii * ld, *wc = Ws + (rnnt::kIE + ii) * ld, *wo = Ws + (2 * rnnt::kIE + ii) * ld;
-        const float *zb = Zs + qb * rnnt::kQB * ld;
+        const float *zb0 = Zs + qb * rnnt::kQB * ld;
         for (int j = 4 * ks; j < K; j += 4 * rnnt::kKS) {
             const float4 a = *reinterpret_cast<const float4 *>(wg + j);
             const float4 b = *reinterpret_cast<const float4 *>(wc + j);
             const float4 c = *reinterpret_cast<const float4 *>(wo + j);
 #pragma unroll
             for (int q = 0; q < rnnt::kQB; ++q) {
-                const float4 z = *reinterpret_cast<const float4 *>(zb + q * ld + j);
-                acc[q][0] = fmaf(a.w, z.w, fmaf(a.z, z.z, fmaf(a.y, z.y, fmaf(a.x, z.x, acc[q][0]))));
-                acc[q][1] = fmaf(b.w, z.w, fmaf(b.z, z.z, fmaf(b.y, z.y, fmaf(b.x, z.x, acc[q][1]))));
-                acc[q][2] = fmaf(c.w, z.w, fmaf(c.z, z.z, fmaf(c.y, z.y, fmaf(c.x, z.x, acc[q][2]))));
+                const float4 z = *reinterpret_cast<const float4 *>(zb0 + q * ld + j);
+                const float2 z0 = make_float2(z.x, z.y), z1 = make_float2(z.z, z.w);
+                acc[q][0] = fma2(make_float2(a.z, a.w), z1, fma2(make_float2(a.x, a.y), z0, acc[q][0]));
+                acc[q][1] = fma2(make_float2(b.z, b.w), z1, fma2(make_float2(b.x, b.y), z0, acc[q][1]));
+                acc[q][2] = fma2(make_float2(c.z, c.w), z1, fma2(make_float2(c.x, c.y), z0, acc[q][2]));
             }
         }
+        float sum[rnnt::kQB][3];
+#pragma unroll
+        for (int q = 0; q < rnnt::kQB; ++q)
+#pragma unroll
+            for (int g = 0; g < 3; ++g) sum[q][g] = acc[q][g].x + acc[q][g].y;
 #pragma unroll
         for (int off = 1; off < rnnt::kKS; off <<= 1)
 #pragma unroll
-            for (int q = 0; q < rnnt::kQB; ++q) {
-                acc[q][0] += __shfl_xor_sync(0xffffffffu, acc[q][0], off);
-                acc[q][1] += __shfl_xor_sync(0xffffffffu, acc[q][1], off);
-                acc[q][2] += __shfl_xor_sync(0xffffffffu, acc[q][2], off);
-            }
+            for (int q = 0; q < rnnt::kQB; ++q)
+#pragma unroll
+                for (int g = 0; g < 3; ++g) sum[q][g] += __shfl_xor_sync(0xffffffffu, sum[q][g], off);
         if (ks == 0) {
             const int i = i0 + ii;
 #pragma unroll
             for (int q = 0; q < rnnt::kQB; ++q) {
                 const int ql = qb * rnnt::kQB + q, rq = q0 + ql;
-                float a_out = 0.f;
+                const float *h3 = Hs + ql * 3 * rnnt::kIE + ii;
+                const float gg = sum[q][0] + h3[0], gc = sum[q][1] + h3[rnnt::kIE], go = sum[q][2] + h3[2 * rnnt::kIE];
+                const float g = 1.0f / (1.0f + expf(-gg));
+                const float a_out = tanhf(go);
                 if (rq < p.R) {
-                    const float *hp = rs.Hpre + ((size_t)rq * p.gamma + (k - 1)) * (size_t)(3 * r);
-                    const float gg = acc[q][0] + hp[i], gc = acc[q][1] + hp[r + i], go = acc[q][2] + hp[2 * r + i];
-                    const float g = 1.0f / (1.0f + expf(-gg));
-                    rs.s_out[(size_t)rq * r + i] = g * Zs[ql * ld + i] + (1.0f - g) * tanhf(gc);
-                    a_out = tanhf(go);
-                    rs.A[((size_t)rq * p.gamma + (k - 1)) * (size_t)r + i] = a_out;
+                    s_out[(size_t)rq * r + i] = g * Zs[ql * ld + i] + (1.0f - g) * tanhf(gc);
+                    p.rnn.A[((size_t)rq * p.gamma + (k - 1)) * (size_t)r + i] = a_out;
                 }
-                As[ql * rnnt::kIE + ii] = a_out;
+                As[ql * rnnt::kIE + ii] = rq < p.R ? a_out : 0.f;
             }
         }
         tc::named_bar_sync(1, tcp::kEpiThreads);
