@@ -173,6 +173,24 @@ __device__ __forceinline__ void gather_operand(const TcParams &p, const typename
                                                int tid, int nthr) {
     const int chunks_per_row = p.r / 8;
     const float *A_k = P::KSPLIT == 2 ? p.A_op + (size_t)(k - p.k) * p.r : nullptr;
+    if (P::KSPLIT == 1 && nthr == tcp::kEpiThreads) {
+        // the epilogue threads at a step boundary: all of a thread's row loads in
+        // flight together (MV rows x r / 8 chunks <= 8 per thread), then the stores
+        constexpr int kMax = P::MV * 32 / tcp::kEpiThreads;
+        uint4 v[kMax];
+#pragma unroll
+        for (int n = 0; n < kMax; ++n) {
+            const int e = tid + n * tcp::kEpiThreads, row = e / chunks_per_row, c = e - row * chunks_per_row;
+            const int xp = e < P::MV * chunks_per_row ? s.tok[row] : -1;
+            v[n] = xp >= 0 ? *reinterpret_cast<const uint4 *>(p.W1 + (size_t)xp * p.r + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int n = 0; n < kMax; ++n) {
+            const int e = tid + n * tcp::kEpiThreads, row = e / chunks_per_row, c = e - row * chunks_per_row;
+            if (e < P::MV * chunks_per_row) P::put_a(s, row, c, 0, v[n]);
+        }
+        return;
+    }
     for (int e = tid; e < P::MV * chunks_per_row; e += nthr) {
         const int row = e / chunks_per_row, c = e - row * chunks_per_row;
         const int grow = m0 + row;
@@ -525,6 +543,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     typename P::State s = P::carve(smem_raw);
     P::init(s);
+    P::init_identity(s);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
     const int m0 = m_tile * P::MV;
@@ -630,17 +649,23 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                             make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)k, (uint32_t)grow, c3), p.rk);
                         words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
                     }
+                    if constexpr (P::UMMA) {
+                        // U_k was added on the tensor cores
 #pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
-                        const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
+                        for (int j = 0; j < 16; ++j) z[j] = __uint_as_float(acc[j]);
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
-                                                               __uint_as_float(acc[8 * o + 2 * i + 1])),
-                                                   make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
-                            z[8 * o + 2 * i] = zz.x;
-                            z[8 * o + 2 * i + 1] = zz.y;
+                        for (int o = 0; o < 2; ++o) {
+                            const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
+                            const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
+                                                                   __uint_as_float(acc[8 * o + 2 * i + 1])),
+                                                       make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
+                                z[8 * o + 2 * i] = zz.x;
+                                z[8 * o + 2 * i + 1] = zz.y;
+                            }
                         }
                     }
                     row_feed16(st, z, vb, words);
@@ -648,11 +673,15 @@ __global__ void __launch_bounds__(P::kThreads, 1)
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const int col = cb + 4 * g;
-                        const uint2 uu = P::u_quad(sU, row, col);
-                        float z[4] = {__uint_as_float(acc[4 * g]) + tcp::bf16_lo(uu.x),
-                                      __uint_as_float(acc[4 * g + 1]) + tcp::bf16_hi(uu.x),
-                                      __uint_as_float(acc[4 * g + 2]) + tcp::bf16_lo(uu.y),
-                                      __uint_as_float(acc[4 * g + 3]) + tcp::bf16_hi(uu.y)};
+                        float z[4] = {__uint_as_float(acc[4 * g]), __uint_as_float(acc[4 * g + 1]),
+                                      __uint_as_float(acc[4 * g + 2]), __uint_as_float(acc[4 * g + 3])};
+                        if constexpr (!P::UMMA) {
+                            const uint2 uu = P::u_quad(sU, row, col);
+                            z[0] += tcp::bf16_lo(uu.x);
+                            z[1] += tcp::bf16_hi(uu.x);
+                            z[2] += tcp::bf16_lo(uu.y);
+                            z[3] += tcp::bf16_hi(uu.y);
+                        }
                         const int v0 = n0 + col;
                         const uint4 words =
                             philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), p.rk);
@@ -800,8 +829,11 @@ __global__ void wait_selfcheck_kernel(const int *flag, int target, int mode, uin
 
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
-using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;   // Markov, R <= 64
-using DraftM128 = tcp::Pipe<128, 128, 6, 2, 1>; // Markov, 128 requests per M-tile
+// (U_k added on the tensor cores with 128 requests per M-tile: 6 % faster at
+// R = 256 and 512; with 64 requests, where the identity block costs a W_2^T
+// slot, 5 % slower)
+using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;          // Markov, R <= 64
+using DraftM128 = tcp::Pipe<128, 128, 4, 2, 1, true>;  // Markov, 128 requests per M-tile
 using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

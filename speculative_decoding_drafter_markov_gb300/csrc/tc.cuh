@@ -258,6 +258,19 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzle
+// layout -- rows of 64 MN-consecutive bf16 (128 bytes) per K index, 8-row (K)
+// groups 1024 bytes apart, the next 64 MN elements `mn_stride` bytes further.
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16; // leading byte offset: along MN
+    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8-row groups along K
+    d |= (uint64_t)1u << 46;                          // descriptor version
+    d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B (K-major), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
