@@ -121,6 +121,39 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys &r
     return c;
 }
 
+// Philox-4x32-10 of counters (w0, w1, req, w3) for a fixed (w1, req), as the
+// draft forms them (w1 = step, req = request, w0 = vocabulary quad): the half of
+// round 1 and the multiply of round 2 that depend only on (w1, req) are formed
+// once per (step, request), so a call starts with one multiply in each of its
+// first two rounds.  The words equal philox4x32_10((w0, w1, req, w3), key).
+struct PhiloxRow {
+    uint32_t n0, n1, h2, l2;
+};
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t w1, uint32_t req, const PhiloxRoundKeys &rk) {
+    const uint64_t p1 = (uint64_t)req * 0xCD9E8D57ull;
+    PhiloxRow r;
+    r.n0 = (uint32_t)(p1 >> 32) ^ w1 ^ rk.k0[0];
+    r.n1 = (uint32_t)p1;
+    const uint64_t p0 = (uint64_t)r.n0 * 0xD2511F53ull;
+    r.h2 = (uint32_t)(p0 >> 32);
+    r.l2 = (uint32_t)p0;
+    return r;
+}
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t w0, uint32_t w3, const PhiloxRow &pr, const PhiloxRoundKeys &rk) {
+    const uint64_t q0 = (uint64_t)w0 * 0xD2511F53ull;
+    const uint32_t n2 = (uint32_t)(q0 >> 32) ^ w3 ^ rk.k1[0], n3 = (uint32_t)q0;
+    const uint64_t q1 = (uint64_t)n2 * 0xCD9E8D57ull;
+    uint4 c = make_uint4((uint32_t)(q1 >> 32) ^ pr.n1 ^ rk.k0[1], (uint32_t)q1, pr.h2 ^ n3 ^ rk.k1[1], pr.l2);
+#pragma unroll
+    for (int round = 2; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53ull;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57ull;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk.k0[round], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ rk.k1[round], (uint32_t)p0);
+    }
+    return c;
+}
+
 __device__ __forceinline__ uint32_t word_lane(const uint4 &w, int lane) {
     return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

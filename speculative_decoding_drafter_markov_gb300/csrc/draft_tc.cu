@@ -614,6 +614,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
 
             RowState st;
             row_init(st);
+            const PhiloxRow prow = philox_row((uint32_t)k, (uint32_t)grow, p.rk);
             // Filter thresholds shared by all CTAs: the step's winner word of a
             // request (win[row], raised by every CTA) holds the exact score of
             // some element of the row, so any value read from it is a valid
@@ -645,8 +646,7 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     float z[16];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
-                        const uint4 w4 = philox4x32_10(
-                            make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)k, (uint32_t)grow, c3), p.rk);
+                        const uint4 w4 = philox4x32_10((uint32_t)((vb >> 2) + g), c3, prow, p.rk);
                         words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
                     }
                     if constexpr (P::UMMA) {
