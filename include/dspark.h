@@ -32,7 +32,9 @@
  *   key = (seed lo, seed hi) and counter = (w0, w1, request, cycle << 2 | stream);
  *   stream 0 draft Gumbel noise (w0 = v / 4, w1 = step k, word v % 4),
  *   stream 1 acceptance uniforms (w0 = 0, w1 = position j, word 0),
- *   stream 2 residual / bonus Gumbel noise (w0 = v / 4, w1 = position).
+ *   stream 2 the residual / bonus draw (w0 = 0, w1 = position, word 0): one
+ *   uniform u per request, the token the first v whose cumulative weight
+ *   (fp32, vocabulary order) exceeds u times the total weight.
  *   A word w maps to u = ((w >> 9) + 1/2) 2^-23.  Only the low 30 bits of
  *   `cycle` enter the counter.
  */
@@ -219,7 +221,9 @@ DSPARK_API int dspark_build_tags(int32_t R, int32_t gamma, const int32_t *ell, i
 /* u from Philox stream 1; at the first rejection j* sample y from           */
 /* norm(max(0, p_{j*} - q_{j*+1})) (q recomputed from U, the bias operand and */
 /* W_2; p itself if the residual is empty); if all l_r tokens pass sample     */
-/* the bonus y from p_{l_r}.  Row i of T is the target's logits for position  */
+/* the bonus y from p_{l_r}, both by inverse CDF (one stream-2 uniform per   */
+/* request; the pages fix no sampler, any exact draw keeps the method        */
+/* lossless).  Row i of T is the target's logits for position                */
 /* tags[i] = (r, j), i.e. the distribution of x_{j+1} given x_0..x_j; rows    */
 /* are grouped by request with positions 0..l_r ascending, every request      */
 /* present (violations: DSPARK_ERR_INVAL in *err).                            */

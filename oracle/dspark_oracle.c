@@ -369,7 +369,9 @@ int oracle_schedule(int R, int gamma, const float *c, const double *sps, int B_m
 /* min(1, p_j(x)/q_{j+1}(x)); at the first rejection sample from            */
 /* norm(max(0, p_j - q_{j+1})); if all scheduled tokens pass, sample the     */
 /* bonus token from p_{l_r}.  Row (r, j) of T holds the target logits for   */
-/* x_{j+1} given x_0..x_j.                                                   */
+/* x_{j+1} given x_0..x_j.  The pages fix no sampler for the correction;    */
+/* it is drawn by inverse CDF with one uniform (any exact draw from the      */
+/* normalised residual keeps the method lossless).                           */
 /* ------------------------------------------------------------------------ */
 static double row_logsumexp(const void *T, size_t row, int V, int dtype) {
     double m = -INFINITY;
@@ -471,19 +473,36 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
             if (!any) /* degenerate p == q: fall back to p itself */
                 for (int v = 0; v < V; ++v) w[v] = exp(load_elem(T, row * (size_t)V + v, dtype) - lp);
         }
-        double best = -INFINITY, second = -INFINITY;
-        int y = -1, y2 = -1;
+        /* inverse-CDF draw from norm(w): one uniform u (stream 2, counter
+         * (0, n_r, request, cycle), word 0), the target u * sum(w), and the first
+         * v whose cumulative weight exceeds it */
+        double total = 0.0;
+        for (int v = 0; v < V; ++v) total += w[v];
+        double u2 = oracle_uniform(oracle_philox_word(seed, 0, (uint32_t)n_r, (uint32_t)rq, cycle, 2, 0));
+        double target = u2 * total;
+        double cum = 0.0, below = 0.0;
+        int y = -1;
         for (int v = 0; v < V; ++v) {
             if (!(w[v] > 0.0)) continue;
-            double score = log(w[v]) + gumbel(seed, (uint32_t)n_r, (uint32_t)rq, cycle, 2, v);
-            if (score > best) {
-                second = best;
-                y2 = y;
-                best = score;
-                y = v;
-            } else if (score > second) {
-                second = score;
-                y2 = v;
+            below = cum;
+            cum += w[v];
+            y = v; /* the last positive-weight index, if the target is never passed */
+            if (cum > target) break;
+        }
+        /* the closer CDF boundary of y, relative to the total, and the index on
+         * its other side (the draw a slightly different target would give) */
+        int y2 = -1;
+        double margin = INFINITY;
+        if (y >= 0 && total > 0.0) {
+            double lo = (target - below) / total, hi = (cum - target) / total;
+            if (lo <= hi) {
+                margin = lo;
+                for (int v = y - 1; v >= 0; --v)
+                    if (w[v] > 0.0) { y2 = v; break; }
+            } else {
+                margin = hi;
+                for (int v = y + 1; v < V; ++v)
+                    if (w[v] > 0.0) { y2 = v; break; }
             }
         }
         n_accept[rq] = n_r;
@@ -494,7 +513,7 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
             out_tokens[(size_t)rq * (gamma + 1) + j] = tok;
         }
         next_anchor[rq] = y;
-        if (gap) gap[rq] = best - second;
+        if (gap) gap[rq] = margin;
         if (runner) runner[rq] = y2;
     }
     free(first); free(count); free(w); free(b);

@@ -99,8 +99,12 @@ int oracle_schedule(int R, int gamma, const float *c, const double *sps, int B_m
  * [R] / [R, gamma + 1] / [N] arrays, written only for those requests.
  *   n_accept [R], out_tokens [R, gamma + 1] (-1 padded), next_anchor [R],
  *   lse_p [N], logp [N] (NaN on rows without a test), margin [N] =
- *   (log p - log q) - log u, gap [R] = top-two score gap of the final sample,
- *   runner [R] = the index with the second largest score of that sample.
+ *   (log p - log q) - log u.  The correction / bonus token y is drawn by
+ *   inverse CDF: u from Philox stream 2 (counter (0, n, request, cycle), word
+ *   0), y = the first v whose cumulative weight exceeds u * sum(w).
+ *   gap [R] = the distance of u * sum(w) to the nearer CDF boundary of y,
+ *   relative to sum(w); runner [R] = the index on the other side of that
+ *   boundary (-1 if none).
  * Returns 0, or -1 on malformed tags. */
 int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *T,
                   const int32_t *tags, const int32_t *anchor, const int32_t *x,

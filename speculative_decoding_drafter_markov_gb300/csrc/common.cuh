@@ -410,11 +410,10 @@ __device__ __forceinline__ DraftPartial load_partial_cg(const DraftPartial *q) {
     return DraftPartial{a.x, a.y, a.z, a.w, b.x, 0, 0, 0};
 }
 
-// Partial result of one (row, vocabulary slice) of verification phase 2:
-// the race over the residual max(0, p - q) and, as fallback / bonus, over p.
+// Partial result of one (row, vocabulary slice) of verification phase 2 on the
+// CUDA cores: the sums of the residual weights max(0, p - q) and of p.
 struct VerifyPartial {
-    float best_res, best_p;
-    int idx_res, idx_p;
+    float sum_res, sum_p;
 };
 
 // Race over weights w_v in (0, 1]: score ln w_v - ln E_v; the filter skips v

@@ -126,12 +126,14 @@ struct VerifyWs {
     int32_t *first_rej;    // [R]
     int32_t *ell;          // [R]
     int32_t *row_of;       // [R, gamma + 1]
-    VerifyPartial *part;   // [R, nparts]
+    VerifyPartial *part;   // [R, nparts] slice sums (CUDA-core phase 2)
     int *done;             // [kVerifyMaxMTiles] CTAs of an M-tile that published (tensor-core phase 2)
-    unsigned long long *win;  // [R] packed race winner of each request (tensor-core phase 2)
+    float *csum;           // [ceil(V / 16), R] sums of 16 consecutive weights (tensor-core phase 2)
+    float *stot;           // [R, kVerifyMaxParts] sums over each CTA's columns (tensor-core phase 2)
     int nparts;
 };
 constexpr int kVerifyMaxMTiles = 64;
+constexpr int kVerifyMaxParts = 256;
 size_t verify_ws_bytes(int R, int gamma, int V, int N);
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N);
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s);

@@ -13,9 +13,11 @@
 //                  independent, so the result is deterministic).
 //   verify_phase2  vocabulary-sliced like the draft step: per request it
 //                  recomputes q at the first rejected position (U + bias operand
-//                  x W_2, never stored) and races over max(0, p - q) and over p.
-//   verify_final   one CTA per request merges the slices and writes the
-//                  accepted tokens, the correction / bonus token and the anchor.
+//                  x W_2, never stored) and sums max(0, p - q) and p per slice.
+//   verify_final   one warp per request: the inverse-CDF draw of the correction
+//                  (or bonus) token over the slice sums, then over the chosen
+//                  slice's weights recomputed with phase 2's arithmetic, and the
+//                  accepted tokens, that token and the anchor.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -39,7 +41,6 @@ __global__ void verify_init(int R, int gamma, VerifyWs w) {
     if (i < R) {
         w.first_rej[i] = kNone;
         w.ell[i] = -1;
-        w.win[i] = 0ull;
     }
 }
 
@@ -156,11 +157,46 @@ __global__ void __launch_bounds__(256) verify_phase1(const dspark_verify_args a,
 }
 
 struct RowMeta {
-    int residual;   // 1: residual race needed, 0: bonus (p only), -1: skip
+    int residual;   // 1: residual draw, 0: bonus (p only), -1: skip
     int n;          // position of the final sample
     int row;        // flattened row of that position
     float lse_p, lse_q;
 };
+
+// The weights of vocabulary entries v0 .. v0 + 3 of one request: the residual
+// max(0, p - q) (zero unless the request rejected) and p; entries at or beyond V
+// weigh zero.  w2 points at the staged W_2^T row of v0 (rows ld apart), e at
+// the bias operand (W_1[x_n] or A_{n+1}); the same arithmetic serves the slice
+// sums and the final search, so both see the same weights.
+template <typename T, bool kRnn>
+__device__ __forceinline__ void slice_weights(const dspark_verify_args &a, const RowMeta &mt, const float *w2,
+                                              const float *e, int ld, int rq, int v0, float (&wr)[4],
+                                              float (&wp)[4]) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (mt.residual == 1) {
+        for (int i = 0; i < a.r; ++i) {
+            const float ev = e[i];
+            acc[0] = fmaf(ev, w2[i], acc[0]);
+            acc[1] = fmaf(ev, w2[ld + i], acc[1]);
+            acc[2] = fmaf(ev, w2[2 * ld + i], acc[2]);
+            acc[3] = fmaf(ev, w2[3 * ld + i], acc[3]);
+        }
+    }
+    const T *trow = static_cast<const T *>(a.T) + (size_t)mt.row * a.V;
+    const T *urow = static_cast<const T *>(a.U) + ((size_t)rq * a.gamma + mt.n) * (size_t)a.V;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int v = v0 + j;
+        wr[j] = wp[j] = 0.f;
+        if (v >= a.V) continue;
+        const float p = ex2((to_f32(trow[v]) - mt.lse_p) * kLog2e);
+        wp[j] = p;
+        if (mt.residual == 1) {
+            const float q = ex2((acc[j] + to_f32(urow[v]) - mt.lse_q) * kLog2e);
+            wr[j] = fmaxf(p - q, 0.f);
+        }
+    }
+}
 
 template <typename T, bool kRnn>
 __global__ void __launch_bounds__(kThreads) verify_phase2(const dspark_verify_args a, VerifyWs w) {
@@ -171,8 +207,6 @@ __global__ void __launch_bounds__(kThreads) verify_phase2(const dspark_verify_ar
     __shared__ RowMeta meta[kRowsPerPass];
     const T *W2t = static_cast<const T *>(a.W2t);
     const T *W1 = static_cast<const T *>(a.W1);
-    const T *U = static_cast<const T *>(a.U);
-    const T *Tm = static_cast<const T *>(a.T);
     const int slice = blockIdx.x, vbase = slice * kSliceV;
     for (int e = threadIdx.x; e < kSliceV * r; e += kThreads) {
         const int vv = e / r, i = e - vv * r, v = vbase + vv;
@@ -180,8 +214,6 @@ __global__ void __launch_bounds__(kThreads) verify_phase2(const dspark_verify_ar
     }
     const int quad = threadIdx.x & 15, sub = threadIdx.x >> 4;
     const int v0 = vbase + quad * 4;
-    const PhiloxKey key = philox_key(a.seed);
-    const uint32_t c3 = philox_ctr3(a.cycle, 2);
 
     for (int row0 = 0; row0 < a.R; row0 += kRowsPerPass) {
         __syncthreads();
@@ -227,114 +259,120 @@ __global__ void __launch_bounds__(kThreads) verify_phase2(const dspark_verify_ar
 
         const int rq = row0 + sub;
         const RowMeta mt = meta[sub];
-        Race res, pr;
-        race_init(res);
-        race_init(pr);
+        float sres = 0.f, sp = 0.f;  // this thread's 4 weights of the two draws
         if (rq < a.R && mt.residual >= 0 && v0 < a.V) {
+            float wr[4], wp[4];
+            slice_weights<T, kRnn>(a, mt, W2s + (quad * 4) * ld, Es + sub * ld, ld, rq, v0, wr, wp);
+            sres = (wr[0] + wr[1]) + (wr[2] + wr[3]);
+            sp = (wp[0] + wp[1]) + (wp[2] + wp[3]);
+        }
+        // the slice's sums over its 16 quads (a fixed tree)
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) {
+            sres += __shfl_xor_sync(0xffffffffu, sres, off);
+            sp += __shfl_xor_sync(0xffffffffu, sp, off);
+        }
+        if (quad == 0 && rq < a.R) w.part[(size_t)rq * w.nparts + slice] = VerifyPartial{sres, sp};
+    }
+}
+
+// One warp per request: the correction / bonus draw by inverse CDF over the
+// slice sums, then over the 64 weights of the chosen slice, recomputed with the
+// same arithmetic as phase 2.  A rejected position whose residual max(0, p - q)
+// came out empty (p equal to q to rounding everywhere) draws from p instead.
+template <typename T, bool kRnn>
+__global__ void __launch_bounds__(32) verify_final(const dspark_verify_args a, VerifyWs w) {
+    __shared__ float Es[512];  // the bias operand (r <= 512)
+    const int rq = blockIdx.x, lane = threadIdx.x;
+    const int ell = w.ell[rq];
+    if (ell < 0) {
+        if (lane == 0) write_outcome(a, w, rq, -1, -1);
+        return;
+    }
+    const int fr = w.first_rej[rq];
+    RowMeta mt;
+    mt.residual = fr < ell ? 1 : 0;
+    mt.n = fr < ell ? fr : ell;
+    mt.row = w.row_of[rq * (a.gamma + 1) + mt.n];
+    if (mt.row < 0) {
+        if (lane == 0) write_outcome(a, w, rq, -1, -1);
+        return;
+    }
+    mt.lse_p = w.lse_p[mt.row];
+    mt.lse_q = mt.residual ? a.lse[(size_t)rq * a.gamma + mt.n] : 0.f;
+    const VerifyPartial *part = w.part + (size_t)rq * w.nparts;
+    // the residual's total decides whether its draw is possible
+    float below = 0.f, total = 0.f;
+    bool use_res = mt.residual == 1;
+    if (use_res) {
+        warp_cdf_search(w.nparts, 0.f, INFINITY, [&](int i) { return part[i].sum_res; }, &below, &total);
+        use_res = total > 0.f;
+    }
+    if (!use_res) warp_cdf_search(w.nparts, 0.f, INFINITY, [&](int i) { return part[i].sum_p; }, &below, &total);
+    const float target = correction_uniform(a.seed, a.cycle, mt.n, rq) * total;
+    const int sl = use_res ? warp_cdf_search(w.nparts, 0.f, target, [&](int i) { return part[i].sum_res; }, &below)
+                           : warp_cdf_search(w.nparts, 0.f, target, [&](int i) { return part[i].sum_p; }, &below);
+    int y = -1;
+    if (sl >= 0) {
+        // the slice's 64 weights: lane l takes entries 4 (l % 16) .. + 3 (lanes 16-31 repeat them)
+        const int r = a.r, vbase = sl * kSliceV;
+        const T *W2t = static_cast<const T *>(a.W2t);
+        if (use_res) {
+            for (int i = lane; i < r; i += 32) {
+                float val;
+                if (kRnn) {
+                    val = a.A[((size_t)rq * a.gamma + mt.n) * (size_t)r + i];
+                } else {
+                    int xn = mt.n == 0 ? a.anchor[rq] : a.x[(size_t)rq * a.gamma + mt.n - 1];
+                    if (xn < 0 || xn >= a.V) xn = 0;
+                    val = to_f32(static_cast<const T *>(a.W1)[(size_t)xn * r + i]);
+                }
+                Es[i] = val;
+            }
+        }
+        float wv[4] = {0.f, 0.f, 0.f, 0.f};
+        const int quad = lane & 15, v0 = vbase + 4 * quad;
+        {
+            // the quad's weights, W_2^T read from global memory in phase 2's order
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (mt.residual) {
-                const float *e = Es + sub * ld;
-                const float *w0 = W2s + (quad * 4) * ld;
+            __syncwarp();
+            if (use_res) {
                 for (int i = 0; i < r; ++i) {
-                    const float ev = e[i];
-                    acc[0] = fmaf(ev, w0[i], acc[0]);
-                    acc[1] = fmaf(ev, w0[ld + i], acc[1]);
-                    acc[2] = fmaf(ev, w0[2 * ld + i], acc[2]);
-                    acc[3] = fmaf(ev, w0[3 * ld + i], acc[3]);
+                    const float ev = Es[i];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (v0 + j < a.V) acc[j] = fmaf(ev, to_f32(W2t[(size_t)(v0 + j) * r + i]), acc[j]);
                 }
             }
-            const uint4 words = philox4x32_10(
-                make_uint4((uint32_t)(v0 >> 2), (uint32_t)mt.n, (uint32_t)rq, c3), key);
-            const T *trow = Tm + (size_t)mt.row * a.V;
-            const T *urow = U + ((size_t)rq * a.gamma + mt.n) * (size_t)a.V;
+            const T *trow = static_cast<const T *>(a.T) + (size_t)mt.row * a.V;
+            const T *urow = static_cast<const T *>(a.U) + ((size_t)rq * a.gamma + mt.n) * (size_t)a.V;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int v = v0 + j;
                 if (v >= a.V) continue;
-                const float t = one_minus_uniform(word_lane(words, j));
                 const float p = ex2((to_f32(trow[v]) - mt.lse_p) * kLog2e);
-                race_feed(pr, p, t, v);
-                if (mt.residual) {
+                if (use_res) {
                     const float q = ex2((acc[j] + to_f32(urow[v]) - mt.lse_q) * kLog2e);
-                    race_feed(res, fmaxf(p - q, 0.f), t, v);
+                    wv[j] = fmaxf(p - q, 0.f);
+                } else {
+                    wv[j] = p;
                 }
             }
         }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) {
-            const float b1 = __shfl_xor_sync(0xffffffffu, res.best, off);
-            const int i1 = __shfl_xor_sync(0xffffffffu, res.idx, off);
-            const float b2 = __shfl_xor_sync(0xffffffffu, pr.best, off);
-            const int i2 = __shfl_xor_sync(0xffffffffu, pr.idx, off);
-            race_merge(res.best, res.idx, b1, i1);
-            race_merge(pr.best, pr.idx, b2, i2);
-        }
-        if (quad == 0 && rq < a.R)
-            w.part[(size_t)rq * w.nparts + slice] = VerifyPartial{res.best, pr.best, res.idx, pr.idx};
+        float b2 = 0.f;
+        const int e = warp_cdf_search(kSliceV, below, target,
+                                      [&](int i) {
+                                          const float x0 = __shfl_sync(0xffffffffu, wv[0], i >> 2),
+                                                      x1 = __shfl_sync(0xffffffffu, wv[1], i >> 2),
+                                                      x2 = __shfl_sync(0xffffffffu, wv[2], i >> 2),
+                                                      x3 = __shfl_sync(0xffffffffu, wv[3], i >> 2);
+                                          const int j = i & 3;
+                                          return j == 0 ? x0 : j == 1 ? x1 : j == 2 ? x2 : x3;
+                                      },
+                                      &b2);
+        y = e >= 0 ? vbase + e : -1;
     }
-}
-
-__global__ void __launch_bounds__(256) verify_final(const dspark_verify_args a, VerifyWs w) {
-    __shared__ float s_b1[256], s_b2[256];
-    __shared__ int s_i1[256], s_i2[256];
-    const int rq = blockIdx.x, tid = threadIdx.x;
-    float b1 = -INFINITY, b2 = -INFINITY;
-    int i1 = -1, i2 = -1;
-    for (int t = tid; t < w.nparts; t += blockDim.x) {
-        const VerifyPartial q = w.part[(size_t)rq * w.nparts + t];
-        race_merge(b1, i1, q.best_res, q.idx_res);
-        race_merge(b2, i2, q.best_p, q.idx_p);
-    }
-    s_b1[tid] = b1; s_i1[tid] = i1; s_b2[tid] = b2; s_i2[tid] = i2;
-    __syncthreads();
-    for (int half = blockDim.x / 2; half > 0; half >>= 1) {
-        if (tid < half) {
-            race_merge(s_b1[tid], s_i1[tid], s_b1[tid + half], s_i1[tid + half]);
-            race_merge(s_b2[tid], s_i2[tid], s_b2[tid + half], s_i2[tid + half]);
-        }
-        __syncthreads();
-    }
-    // A rejected position whose residual max(0, p - q) came out empty (p equal to
-    // q to rounding everywhere) samples p instead, with the same stream-2 noise:
-    // when the slices did not run that race, this CTA runs it over the whole row.
-    __shared__ int s_fallback;
-    if (tid == 0) {
-        const int ell = w.ell[rq];
-        s_fallback = ell >= 0 && w.first_rej[rq] < ell && s_i1[0] < 0 && s_i2[0] < 0;
-    }
-    __syncthreads();
-    if (s_fallback) {
-        const int n = w.first_rej[rq];
-        const int row = w.row_of[rq * (a.gamma + 1) + n];
-        Race pr;
-        race_init(pr);
-        if (row >= 0) {
-            const float lsep = w.lse_p[row] * kLog2e;
-            const PhiloxKey key = philox_key(a.seed);
-            const uint32_t c3 = philox_ctr3(a.cycle, 2);
-            for (int v0 = 4 * tid; v0 < a.V; v0 += 4 * blockDim.x) {
-                const uint4 words =
-                    philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)n, (uint32_t)rq, c3), key);
-                for (int j = 0; j < 4 && v0 + j < a.V; ++j) {
-                    const size_t at = (size_t)row * a.V + v0 + j;
-                    const float tv = a.dtype == DSPARK_BF16
-                                         ? __bfloat162float(static_cast<const __nv_bfloat16 *>(a.T)[at])
-                                         : static_cast<const float *>(a.T)[at];
-                    race_feed(pr, ex2(fmaf(tv, kLog2e, -lsep)), one_minus_uniform(word_lane(words, j)), v0 + j);
-                }
-            }
-        }
-        __syncthreads();
-        s_b2[tid] = pr.best;
-        s_i2[tid] = pr.idx;
-        __syncthreads();
-        for (int half = blockDim.x / 2; half > 0; half >>= 1) {
-            if (tid < half) race_merge(s_b2[tid], s_i2[tid], s_b2[tid + half], s_i2[tid + half]);
-            __syncthreads();
-        }
-    }
-    if (tid != 0) return;
-    write_outcome(a, w, rq, s_i1[0], s_i2[0]);
+    if (lane == 0) write_outcome(a, w, rq, use_res ? y : -1, use_res ? -1 : y);
 }
 
 template <typename T, bool kRnn>
@@ -354,7 +392,7 @@ size_t verify_ws_bytes(int R, int gamma, int V, int N) {
     return align256(sizeof(float) * (size_t)N) + align256(sizeof(int32_t) * (size_t)R) * 2 +
            align256(sizeof(int32_t) * (size_t)R * (gamma + 1)) +
            align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles) +
-           align256(sizeof(unsigned long long) * (size_t)R);
+           align256(sizeof(float) * (size_t)R * ((V + 15) / 16)) + align256(sizeof(float) * (size_t)R * kVerifyMaxParts);
 }
 
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
@@ -373,7 +411,9 @@ VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
     p += align256(sizeof(VerifyPartial) * (size_t)R * w.nparts);
     w.done = reinterpret_cast<int *>(p);
     p += align256(sizeof(int) * kVerifyMaxMTiles);
-    w.win = reinterpret_cast<unsigned long long *>(p);
+    w.csum = reinterpret_cast<float *>(p);
+    p += align256(sizeof(float) * (size_t)R * ((V + 15) / 16));
+    w.stot = reinterpret_cast<float *>(p);
     return w;
 }
 
@@ -402,7 +442,11 @@ cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaSt
     else
         e = rnn ? launch_phase2<float, true>(a, w, s) : launch_phase2<float, false>(a, w, s);
     if (e != cudaSuccess) return e;
-    verify_final<<<a.R, 256, 0, s>>>(a, wf);
+    if (a.dtype == DSPARK_BF16)
+        rnn ? verify_final<__nv_bfloat16, true><<<a.R, 32, 0, s>>>(a, wf)
+            : verify_final<__nv_bfloat16, false><<<a.R, 32, 0, s>>>(a, wf);
+    else
+        rnn ? verify_final<float, true><<<a.R, 32, 0, s>>>(a, wf) : verify_final<float, false><<<a.R, 32, 0, s>>>(a, wf);
     return cudaGetLastError();
 }
 

@@ -8,9 +8,9 @@
 namespace dspark {
 
 // [E] section 06 along the prefix: the accepted drafted tokens, then the
-// correction (residual winner i_res at the first rejection; the winner i_p of
-// the race over p when the residual was empty) or, all accepted, the bonus
-// token i_p; the next anchor is that token.  Requests missing from the batch
+// correction (the residual draw i_res at the first rejection; the draw i_p from
+// p when the residual was empty) or, all accepted, the bonus token i_p; the
+// next anchor is that token.  Requests missing from the batch
 // (ell < 0) get -1 everywhere.
 __device__ __forceinline__ void write_outcome(const dspark_verify_args &a, const VerifyWs &w, int rq, int i_res,
                                               int i_p) {
@@ -33,6 +33,61 @@ __device__ __forceinline__ void write_outcome(const dspark_verify_args &a, const
     a.n_accept[rq] = n;
     for (int j = 0; j <= a.gamma; ++j) out[j] = j < n ? a.x[(size_t)rq * a.gamma + j] : (j == n ? y : -1);
     a.next_anchor[rq] = y;
+}
+
+// The correction / bonus token is an inverse-CDF draw from the weights w (the
+// residual max(0, p - q), or p): one uniform u from Philox stream 2 with
+// counter (0, n, request, cycle << 2 | 2), word 0, the target u * sum(w), and the
+// first vocabulary entry whose cumulative weight exceeds it.  Sums run in fp32
+// in a fixed order (below), so the draw is deterministic.
+__device__ __forceinline__ float correction_uniform(uint64_t seed, uint64_t cycle, int n, int rq) {
+    const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)n, (uint32_t)rq, philox_ctr3(cycle, 2)),
+                                  philox_key(seed));
+    return uniform_of(w.x);
+}
+
+// One warp (all lanes) over cnt consecutive non-negative weights get(i), i <
+// cnt, taken 32 at a time with an inclusive warp scan and a running carry that
+// starts at `base` (the order of the additions is fixed).  With target >= 0:
+// returns the first i whose cumulative weight exceeds `target` and its
+// exclusive cumulative in *below; when the target is never passed (it sits at
+// the total, to rounding), the last i with a positive weight; -1 when all are
+// zero.  *total receives base + the sum of all cnt weights (the same
+// additions), when the scan ran to the end.
+template <class Get>
+__device__ __forceinline__ int warp_cdf_search(int cnt, float base, float target, Get &&get, float *below,
+                                               float *total = nullptr) {
+    const int lane = threadIdx.x & 31;
+    float carry = base, below_last = base;
+    int last = -1;
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+        const int i = i0 + lane;
+        float v = i < cnt ? get(i) : 0.f;
+        v = fmaxf(v, 0.f);  // NaN and negative weights count as zero
+        float incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const float cum_in = carry + incl, cum_ex = cum_in - v;
+        const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+        const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && cum_in > target);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            *below = __shfl_sync(0xffffffffu, cum_ex, l);
+            return i0 + l;
+        }
+        if (pos) {
+            const int l = 31 - __clz(pos);
+            last = i0 + l;
+            below_last = __shfl_sync(0xffffffffu, cum_ex, l);
+        }
+        carry = __shfl_sync(0xffffffffu, cum_in, 31);
+    }
+    *below = below_last;
+    if (total) *total = carry;
+    return last;
 }
 
 }  // namespace dspark

@@ -6,9 +6,10 @@
 // needs the draft logits of step n+1 again: U_{n+1} + (bias operand) W_2.
 // That contraction runs on tcgen05 exactly like the draft step (shared
 // pipeline in tc_pipe.cuh); the epilogue streams the target row p_n and the
-// base-logit row U_{n+1} of each request from global memory and runs two Gumbel
-// races with the stream-2 noise: over the residual and over p (the bonus
-// sample, and the fallback for an empty residual).
+// base-logit row U_{n+1} of each request from global memory, forms the weights
+// (the residual, or p for the bonus) and keeps only their 16-column chunk sums
+// and each CTA's total.  After the M-tile's CTAs meet, one warp per request
+// draws the token by inverse CDF with the stream-2 uniform: CTA, chunk, entry.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -32,20 +33,129 @@ constexpr int kStageBytes = 2 * kStagePieces * tcp::kEpiThreads * 16;
 
 struct VerifyTcParams {
     int R, V, r, gamma;
-    const __nv_bfloat16 *T, *U, *W1;
+    const __nv_bfloat16 *T, *U, *W1, *W2t;
     const float *A;  // RNN bias operands [R, gamma, r] or null
     const int32_t *anchor, *x;
     const float *lse;  // draft log-sum-exp [R, gamma]
     VerifyWs w;
     int nparts, n_mtiles, n_vtiles;
     uint64_t seed, cycle;
-    PhiloxRoundKeys rk;  // of seed
     int32_t *err;
     dspark_verify_args a;  // outputs and the rest of the call (the outcome writer)
 };
 
 __device__ __forceinline__ void cp_async_stage(uint4 *dst, const __nv_bfloat16 *src, uint32_t bytes, uint64_t pol) {
     tc::cp_async16(dst, src, bytes, pol);
+}
+
+// The correction / bonus draw of request rq by one warp (all lanes; lane 0's
+// result is the warp's): inverse CDF over this request's CTA totals (stot), then
+// over the chosen CTA's 16-column chunk sums (csum), then over the chosen
+// chunk's weights, recomputed here -- p exactly as the tile pass formed it, the
+// bias dot of q on the CUDA cores (two lanes per vocabulary entry) in place of
+// the tensor-core one; the two agree to a few fp32 ulps, and a target that lands
+// between them takes the chunk's last positive weight.  A rejected position
+// whose residual came out empty (p equal to q to rounding everywhere) draws from
+// p over the whole row.  The sums were written by other CTAs of this launch:
+// they are read through L2.
+template <class P>
+__device__ __noinline__ int draw_correction(const VerifyTcParams &p, int rq) {
+    const int lane = threadIdx.x & 31;
+    const int ell = p.w.ell[rq];
+    if (ell < 0) return -1;
+    const int fr = p.w.first_rej[rq];
+    const bool res = fr < ell;
+    const int n = res ? fr : ell;
+    const int row = p.w.row_of[rq * (p.gamma + 1) + n];
+    if (row < 0) return -1;
+    const float lsep = p.w.lse_p[row] * kLog2e;
+    const __nv_bfloat16 *trow = p.T + (size_t)row * p.V;
+    const float u = correction_uniform(p.seed, p.cycle, n, rq);
+    const float *tot = p.w.stot + (size_t)rq * kVerifyMaxParts;
+    auto get_tot = [&](int i) { return __ldcg(tot + i); };
+    float below = 0.f, total = 0.f;
+    warp_cdf_search(p.nparts, 0.f, INFINITY, get_tot, &below, &total);
+    if (res && !(total > 0.f)) {
+        auto pv = [&](int v) { return ex2(fmaf(__bfloat162float(trow[v]), kLog2e, -lsep)); };
+        warp_cdf_search(p.V, 0.f, INFINITY, pv, &below, &total);
+        return warp_cdf_search(p.V, 0.f, u * total, pv, &below);
+    }
+    const float target = u * total;
+    const int c = warp_cdf_search(p.nparts, 0.f, target, get_tot, &below);
+    if (c < 0) return -1;
+    int t_begin, ntl;
+    tcp::tile_range(c, p.nparts, p.n_vtiles, t_begin, ntl);
+    const int v_begin = t_begin * P::BN, v_end = min((t_begin + ntl) * P::BN, p.V);
+    const int ch0 = v_begin / 16;
+    float b1 = 0.f;
+    const int ch = warp_cdf_search((v_end - v_begin + 15) / 16, below, target,
+                                   [&](int i) { return __ldcg(p.w.csum + (size_t)(ch0 + i) * p.R + rq); }, &b1);
+    if (ch < 0) return -1;
+    const int vb = (ch0 + ch) * 16;
+    // entry j = lane / 2 of the chunk; lanes 2j and 2j + 1 split the bias dot in halves
+    const int j = lane >> 1, v = vb + j;
+    const bool inv = v < p.V;
+    const float pv = inv ? ex2(fmaf(__bfloat162float(trow[v]), kLog2e, -lsep)) : 0.f;
+    float diff = pv;  // p - q, or p
+    if (res) {
+        const int half = p.r / 2;  // a multiple of 32
+        const uint4 *w2 = reinterpret_cast<const uint4 *>(p.W2t + (size_t)(inv ? v : 0) * p.r + (lane & 1) * half);
+        float d = 0.f;
+        if (p.A) {
+            const float4 *av =
+                reinterpret_cast<const float4 *>(p.A + ((size_t)rq * p.gamma + n) * (size_t)p.r + (lane & 1) * half);
+            for (int k = 0; k < half / 8; ++k) {
+                const uint4 wr = w2[k];
+                const float4 a0 = av[2 * k], a1 = av[2 * k + 1];
+                const float bw[8] = {tcp::bf16_lo(wr.x), tcp::bf16_hi(wr.x), tcp::bf16_lo(wr.y), tcp::bf16_hi(wr.y),
+                                     tcp::bf16_lo(wr.z), tcp::bf16_hi(wr.z), tcp::bf16_lo(wr.w), tcp::bf16_hi(wr.w)};
+                const float ba[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) d = fmaf(ba[i], bw[i], d);
+            }
+        } else {
+            int xn = n == 0 ? p.anchor[rq] : p.x[(size_t)rq * p.gamma + n - 1];
+            if (xn < 0 || xn >= p.V) xn = 0;
+            const uint4 *e1 = reinterpret_cast<const uint4 *>(p.W1 + (size_t)xn * p.r + (lane & 1) * half);
+            for (int k = 0; k < half / 8; ++k) {
+                const uint4 wr = w2[k], er = e1[k];
+                const uint32_t ww[4] = {wr.x, wr.y, wr.z, wr.w}, ee[4] = {er.x, er.y, er.z, er.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    d = fmaf(tcp::bf16_lo(ee[i]), tcp::bf16_lo(ww[i]), d);
+                    d = fmaf(tcp::bf16_hi(ee[i]), tcp::bf16_hi(ww[i]), d);
+                }
+            }
+        }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        if (inv) {
+            const __nv_bfloat16 *urow = p.U + ((size_t)rq * p.gamma + n) * (size_t)p.V;
+            const float lseq = p.lse[(size_t)rq * p.gamma + n] * kLog2e;
+            const float q = ex2(fmaf(d + __bfloat162float(urow[v]), kLog2e, -lseq));
+            diff = pv - q;
+        }
+    }
+    const float wv = fmaxf(diff, 0.f);
+    const float wi = __shfl_sync(0xffffffffu, wv, 2 * (lane & 15));  // lane i < 16: entry i
+    float b2 = 0.f;
+    int e = warp_cdf_search(min(16, p.V - vb), b1, target, [&](int) { return wi; }, &b2);
+    if (e < 0) {
+        // the chunk's sum was positive but no recomputed weight is: its entry with
+        // the largest p - q (the lowest index among equals)
+        float dv = inv ? diff : -INFINITY;
+        int bi = j;
+#pragma unroll
+        for (int off = 2; off < 32; off <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, dv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (o > dv || (o == dv && oi < bi)) {
+                dv = o;
+                bi = oi;
+            }
+        }
+        e = bi;
+    }
+    return vb + e;
 }
 
 template <class P, bool STAGE>
@@ -144,16 +254,14 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         const float lsep = s_lsep[row] * kLog2e, lseq = s_lseq[row] * kLog2e;
         const __nv_bfloat16 *trow = p.T + (size_t)s_row[row] * p.V;
         const __nv_bfloat16 *urow = p.U + ((size_t)(row_live ? rq : 0) * p.gamma + (mode == 1 ? n : 0)) * (size_t)p.V;
-        const uint32_t c3 = philox_ctr3(p.cycle, 2);
         const uint64_t pol = tc::policy_evict_first();  // target and base rows are read once
-        // One race per request: over the residual max(0, p - q) at a rejected
-        // position (mode 1), over p for the bonus (mode 0).  Filter thresholds are
-        // shared like the draft's: per request in shared memory inside the CTA and
-        // through the request's winner word (p.w.win) across CTAs, which a leader
-        // thread per request exchanges once per tile; any value read there is the
-        // exact score of some element of the request's race.
-        float best = -INFINITY, thr = -INFINITY, C = 3.0e38f;
-        int idx = -1;
+        // One draw per request: by inverse CDF over the residual max(0, p - q) at a
+        // rejected position (mode 1), over p for the bonus (mode 0).  This pass
+        // forms the weights of each 16-column chunk, stores the chunk's sum
+        // (csum, chunk-major: a warp's 32 rows are one 128-byte line) and keeps
+        // this thread's running total; the draw itself follows the M-tile's
+        // synchronisation point.
+        float tot = 0.f;
         // staging (STAGE): chunk i of this thread lands in stage i % 2; the copy of
         // chunk i + 1 is in flight while chunk i is processed.  Without it, plain
         // loads at the start of each chunk.
@@ -174,9 +282,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         };
         if (STAGE) stage_chunk(0, t_begin * P::BN + col0);
         int ci = 0;
-        const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
-        unsigned long long *gwin = p.w.win + (row_live ? rq : m0);
-        unsigned long long g_next = leader ? tc::ld_relaxed_gpu_u64(gwin) : 0ull, g_sent = 0ull;
         P::epilogue(s, 0, t_begin * P::BN, P::BN, ntiles, p.err,
                     [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *) {
             const int vb = n0 + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
@@ -188,22 +293,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     tc::cp_async_wait<1>();
                 } else {
                     tc::cp_async_wait<0>();
-                }
-            }
-            if (leader && cofs == 0) {
-                const unsigned long long g = g_next, loc = P::read_thr(s, row);
-                if (loc > g && loc > g_sent) {
-                    atomicMax(gwin, loc);
-                    g_sent = loc;
-                }
-                if (g > loc) P::publish_thr(s, row, g);
-                g_next = tc::ld_relaxed_gpu_u64(gwin);
-            }
-            {
-                const float t2 = winner_score(P::read_thr(s, row));
-                if (t2 > thr) {
-                    thr = t2;
-                    C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
                 }
             }
             // the chunk of the target row (and of U_{n+1}): this thread's stage, or
@@ -225,21 +314,12 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 }
             }
             ++ci;
-            uint32_t words[16];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((vb >> 2) + g), (uint32_t)n, (uint32_t)rq, c3), p.rk);
-                words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
-            }
-            // race weights: residual max(0, p - q) (mode 1), p (mode 0), 0 (no race or
-            // beyond V: the stage holds zeros there, so only mode < 0 needs a mask);
-            // paired fp32 operations, two columns at a time
-            float wv[16], d[16];
-            uint32_t allneg = 0xFFFFFFFFu;
+            if (mode < 0 || vb >= c_end) return;
+            // weights: residual max(0, p - q) (mode 1) or p (mode 0), zero beyond V;
+            // paired fp32 operations, the chunk's sum in a fixed tree
             const float2 L2e = make_float2(kLog2e, kLog2e), nlp = make_float2(-lsep, -lsep),
-                         nlq = make_float2(-lseq, -lseq), C2 = make_float2(C, C),
-                         c0 = make_float2(1.0f - 1.0f / 16777216.0f, 1.0f - 1.0f / 16777216.0f);
-            const bool live_w = mode >= 0 && vb < p.V;
+                         nlq = make_float2(-lseq, -lseq);
+            float2 sum[8];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const uint32_t tt[4] = {tq[c].x, tq[c].y, tq[c].z, tq[c].w};
@@ -248,61 +328,39 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int j = 8 * c + 2 * i;
                     const float2 pa = fma2(make_float2(tcp::bf16_lo(tt[i]), tcp::bf16_hi(tt[i])), L2e, nlp);
-                    const float2 z = add2(make_float2(__uint_as_float(acc[j]), __uint_as_float(acc[j + 1])),
-                                          make_float2(tcp::bf16_lo(uu[i]), tcp::bf16_hi(uu[i])));
-                    const float2 qa = fma2(z, L2e, nlq);
-                    const float2 pv = make_float2(ex2(pa.x), ex2(pa.y));
-                    const float2 qv = make_float2(ex2(qa.x), ex2(qa.y));
-                    float2 w = pv;
+                    float2 w = make_float2(ex2(pa.x), ex2(pa.y));
                     if (mode == 1) {
-                        const float2 r = sub2(pv, qv);
+                        const float2 z = add2(make_float2(__uint_as_float(acc[j]), __uint_as_float(acc[j + 1])),
+                                              make_float2(tcp::bf16_lo(uu[i]), tcp::bf16_hi(uu[i])));
+                        const float2 qa = fma2(z, L2e, nlq);
+                        const float2 r = sub2(w, make_float2(ex2(qa.x), ex2(qa.y)));
                         w = make_float2(fmaxf(r.x, 0.f), fmaxf(r.y, 0.f));
                     }
-                    // columns at or beyond V (a ragged last chunk) read zeros, but p of a
-                    // zero logit is not zero: mask them
-                    wv[j] = live_w && vb + j < p.V ? w.x : 0.f;
-                    wv[j + 1] = live_w && vb + j + 1 < p.V ? w.y : 0.f;
-                    const float2 one_t = make_float2(__uint_as_float(((~words[j]) >> 9) | 0x3F800000u),
-                                                     __uint_as_float(((~words[j + 1]) >> 9) | 0x3F800000u));
-                    const float2 dd = fma2(make_float2(wv[j], wv[j + 1]), C2, sub2(c0, one_t));
-                    d[j] = dd.x;
-                    d[j + 1] = dd.y;
-                    allneg &= __float_as_uint(dd.x) & __float_as_uint(dd.y);
+                    sum[4 * c + i] = make_float2(vb + j < p.V ? w.x : 0.f, vb + j + 1 < p.V ? w.y : 0.f);
                 }
             }
-            // exact scores ln w - ln E of the survivors, a column at a time when some lane kept it
-            if (__any_sync(0xffffffffu, (int)allneg >= 0)) {
-                const float best0 = best;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (__any_sync(0xffffffffu, d[j] > 0.f)) {
-                        if (d[j] > 0.f) {
-                            const float score = kLn2 * lg2(wv[j]) - log_exp_variate(one_minus_uniform(words[j]));
-                            if (score > best) {
-                                best = score;
-                                idx = vb + j;
-                            }
-                        }
-                    }
-                }
-                if (best > best0) {
-                    if (best > thr) {
-                        thr = best;
-                        C = fminf(ex2(-thr * kLog2e) * kRaceSlack, 3.0e38f);
-                    }
-                    if (row_live) P::publish_thr(s, row, pack_winner(best, idx));
-                }
-            }
+            for (int wd = 4; wd > 0; wd >>= 1)
+#pragma unroll
+                for (int i = 0; i < wd; ++i) sum[i] = add2(sum[i], sum[i + wd]);
+            const float cs = sum[0].x + sum[0].y;
+            if (row_live) p.w.csum[(size_t)(vb >> 4) * p.R + rq] = cs;
+            tot += cs;
         });
-        // the CTA's best of each request into its winner word (ties: the lower index)
+        // this CTA's total of each request: its warps' totals in warp order
+        tc::named_bar_sync(1, tcp::kEpiThreads);  // every warp past its last accumulator
+        float *red = P::merge_scratch(s);
+        red[et] = tot;
         tc::named_bar_sync(1, tcp::kEpiThreads);
         if (et < P::MV && m0 + et < p.R) {
-            const unsigned long long loc = P::read_thr(s, et);
-            if (loc != 0ull) atomicMax(p.w.win + m0 + et, loc);
+            const int wstep = P::DUAL ? 2 : 4;  // warps holding the same request
+            float t2 = 0.f;
+            for (int w2 = et >> 5; w2 < tcp::kEpiWarps; w2 += wstep) t2 += red[w2 * 32 + (et & 31)];
+            p.w.stot[(size_t)(m0 + et) * kVerifyMaxParts + cv] = t2;
         }
 
         // Every CTA of the M-tile publishes, waits (bounded; the launch is cooperative,
-        // so all are resident) until all have, then finalises its share of the
+        // so all are resident) until all have, then draws its share of the
         // requests: rows cv, cv + nparts, ..., one warp per request.
         __threadfence();
         tc::named_bar_sync(1, tcp::kEpiThreads);
@@ -315,41 +373,12 @@ __global__ void __launch_bounds__(P::kThreads, 1)
             __threadfence();
             for (int i = cv, nn = 0; i < P::MV && m0 + i < p.R; i += p.nparts, ++nn) {
                 if (warp != nn % tcp::kEpiWarps) continue;
-                const int rq2 = m0 + i;
-                const unsigned long long wword = __ldcg(p.w.win + rq2);
-                const int iw = wword != 0ull ? winner_index(wword) : -1;
-                int i1 = -1, i2 = -1;
-                const int ell = p.w.ell[rq2], fr = p.w.first_rej[rq2];
-                if (ell >= 0 && fr < ell) i1 = iw;
-                else i2 = iw;
-                // a rejected position whose residual max(0, p - q) came out empty (p equal
-                // to q to rounding everywhere) samples p with the same noise: this warp
-                // runs that race over the whole row
-                if (ell >= 0 && fr < ell && i1 < 0) {
-                    const int row2 = p.w.row_of[rq2 * (p.gamma + 1) + fr];
-                    Race fb;
-                    race_init(fb);
-                    if (row2 >= 0) {
-                        const float lsep2 = p.w.lse_p[row2] * kLog2e;
-                        const uint32_t c3b = philox_ctr3(p.cycle, 2);
-                        const __nv_bfloat16 *trow2 = p.T + (size_t)row2 * p.V;
-                        for (int v0 = 4 * lane; v0 < p.V; v0 += 128) {
-                            const uint4 words =
-                                philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)fr, (uint32_t)rq2, c3b), p.rk);
-                            for (int j = 0; j < 4 && v0 + j < p.V; ++j)
-                                race_feed(fb, ex2(fmaf(__bfloat162float(trow2[v0 + j]), kLog2e, -lsep2)),
-                                          one_minus_uniform(word_lane(words, j)), v0 + j);
-                        }
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float c2 = __shfl_xor_sync(0xffffffffu, fb.best, off);
-                        const int j2 = __shfl_xor_sync(0xffffffffu, fb.idx, off);
-                        race_merge(fb.best, fb.idx, c2, j2);
-                    }
-                    i2 = fb.idx;
+                const int y = draw_correction<P>(p, m0 + i);
+                if (lane == 0) {
+                    const int ell = p.w.ell[m0 + i], fr = p.w.first_rej[m0 + i];
+                    const bool res = ell >= 0 && fr < ell;
+                    write_outcome(p.a, p.w, m0 + i, res ? y : -1, res ? -1 : y);
                 }
-                if (lane == 0) write_outcome(p.a, p.w, rq2, i1, i2);
             }
         } else {
             *s.abort_flag = 1;
@@ -380,12 +409,12 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.T = static_cast<const __nv_bfloat16 *>(a.T);
     tp.U = static_cast<const __nv_bfloat16 *>(a.U);
     tp.W1 = static_cast<const __nv_bfloat16 *>(a.W1);
+    tp.W2t = static_cast<const __nv_bfloat16 *>(a.W2t);
     tp.A = a.A;
     tp.anchor = a.anchor; tp.x = a.x; tp.lse = a.lse;
     tp.w = w;
     tp.nparts = nparts; tp.n_mtiles = mt; tp.n_vtiles = (a.V + P::BN - 1) / P::BN;
     tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
-    tp.rk = philox_round_keys(a.seed);
     tp.a = a;
     auto kern = verify_phase2_tc<P, STAGE>;
     const int smem = P::kBytes + (STAGE ? kStageBytes + 16 : 0);  // + 16: the stage starts on a 16-byte boundary

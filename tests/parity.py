@@ -23,6 +23,10 @@ TOL_LSE = 1e-3
 TOL_LOGP = 1e-4
 GAP_TOL = 1e-3
 MARGIN_TOL = 1e-4
+# the correction / bonus draw is an inverse CDF: its near ties are targets within
+# this fraction of the total weight of a CDF boundary (fp32 sums over the
+# vocabulary move a boundary by ~1e-6 of the total)
+CDF_TOL = 1e-4
 
 
 def host(t):
@@ -101,9 +105,9 @@ def compare_verify(gpu, ref, reqs, tags, gamma):
         assert np.array_equal(g_out[:n], r_out[:n])
         assert np.all(g_out[n + 1:] == -1)
         if g_out[n] != r_out[n]:
-            assert ref["gap"][rq] < GAP_TOL, (
+            assert ref["gap"][rq] < CDF_TOL, (
                 f"final token mismatch at request {rq}: gpu {g_out[n]} oracle {r_out[n]} "
-                f"gap {ref['gap'][rq]}")
+                f"CDF margin {ref['gap'][rq]}")
             assert g_out[n] == ref["runner"][rq], (
                 f"near-tie flip at request {rq} to {g_out[n]}, not the oracle's runner-up "
                 f"{ref['runner'][rq]}")

@@ -23,8 +23,10 @@ anchors.  Every cycle compares the stages request by request:
 - verification: accepted counts and emitted tokens exactly, per-row log p and
   log-sum-exp within tolerance.
 
-A near tie (a draft or final token whose oracle score gap is below 1e-3, an
-acceptance decision whose oracle margin is below 1e-4) is a counted flip.  A
+A near tie (a draft token whose oracle score gap is below 1e-3, a correction or
+bonus token whose inverse-CDF target lies within 1e-4 of the total weight from
+a CDF boundary, an acceptance decision whose oracle margin is below 1e-4) is a
+counted flip.  A
 flipped request leaves that cycle's later comparisons; the scheduler sees the
 confidences of every request, so a flip can move verify lengths anywhere.  A
 difference in verify lengths or K from the oracle's chain counts as a flip (the

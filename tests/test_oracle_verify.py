@@ -10,6 +10,8 @@ single-token rule, applied along the scheduled prefix; DSpark digest Appendix A)
   when the lossy backtracking search lets x_1 decide its own admission.
 * p == q accepts every scheduled token; p(x_1) = 0 rejects at the first position;
   the bonus token after a fully accepted prefix follows p.
+* The correction / bonus token is the inverse-CDF draw with one stream-2 uniform
+  (recomputed here with numpy's cumulative sums and searchsorted).
 """
 import numpy as np
 import pytest
@@ -214,18 +216,24 @@ def test_malformed_tags_rejected(orc):
             orc.verify(T, np.array(bad, np.int32), np.zeros(R, np.int32), x, lq, lq, U, W1, W2t)
 
 
-def test_final_sample_runner_up_by_brute_force(orc):
-    # l = 0: the final token is the Gumbel-max of log p_0 with stream-2 noise at position 0
-    R, V = 3, 30
+def test_final_sample_is_the_inverse_cdf_draw(orc):
+    # l = 0: the final token is the inverse-CDF draw from p_0 with one stream-2
+    # uniform (counter (0, position 0, request, cycle), word 0): the first v whose
+    # cumulative probability exceeds u; gap is the distance of u to the nearer
+    # boundary of that v's interval, runner the index on the other side
+    R, V = 40, 30
     rng = np.random.default_rng(12)
     U = rng.standard_normal((R, 1, V)).astype(np.float32)
     T_rows = rng.standard_normal((R, 2, V)).astype(np.float32)
     seed, cycle = 5, 9
     _, v = _draft_then_verify(orc, U, T_rows, np.zeros(R, np.int64), seed=seed, cycle=cycle)
     for rq in range(R):
-        logp = T_rows[rq, 0].astype(np.float64) - special.logsumexp(T_rows[rq, 0].astype(np.float64))
-        g = np.array([-np.log(-np.log(orc.uniform(orc.philox_word(seed, u // 4, 0, rq, cycle, 2, u % 4))))
-                      for u in range(V)])
-        order = np.argsort(-(logp + g), kind="stable")
-        assert v["out_tokens"][rq, 0] == order[0]
-        assert v["runner"][rq] == order[1]
+        p = special.softmax(T_rows[rq, 0].astype(np.float64))
+        cdf = np.cumsum(p)
+        u = orc.uniform(orc.philox_word(seed, 0, 0, rq, cycle, 2, 0))
+        y = int(np.searchsorted(cdf, u * cdf[-1], side="right"))
+        assert v["out_tokens"][rq, 0] == y
+        lo = u * cdf[-1] - (cdf[y - 1] if y > 0 else 0.0)
+        hi = cdf[y] - u * cdf[-1]
+        assert v["gap"][rq] == pytest.approx(min(lo, hi) / cdf[-1], abs=1e-12)
+        assert v["runner"][rq] == (y - 1 if lo <= hi else (y + 1 if y + 1 < V else -1))
