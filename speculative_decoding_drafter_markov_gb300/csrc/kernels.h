@@ -128,16 +128,18 @@ struct VerifyWs {
     int32_t *row_of;       // [R, gamma + 1]
     VerifyPartial *part;   // [R, nparts] slice sums (CUDA-core phase 2)
     int *done;             // [kVerifyMaxMTiles] CTAs of an M-tile that published (tensor-core phase 2)
+    int *tctr;             // [kVerifyMaxMTiles] vocabulary tiles taken per M-tile (tensor-core phase 2)
     float *csum;           // [ceil(V / 16), R] sums of 16 consecutive weights (tensor-core phase 2)
-    float *stot;           // [R, kVerifyMaxParts] sums over each CTA's columns (tensor-core phase 2)
+    unsigned long long *ttot;  // [tiles + ceil(tiles / 32), R] sums over each vocabulary tile, then over each
+                               // run of 32 tiles, fixed point 2^-47 (tensor-core phase 2; tiles <= ceil(V / 64))
     int nparts;
 };
 constexpr int kVerifyMaxMTiles = 64;
-constexpr int kVerifyMaxParts = 256;
 size_t verify_ws_bytes(int R, int gamma, int V, int N);
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N);
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s);
 bool verify_tc_supported(const dspark_verify_args &a);
+int verify_tc_tiles(const dspark_verify_args &a);  // vocabulary tiles of the tensor-core phase 2
 cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s);
 
 // ----- acceptance diagnostics and training losses ------------------------------------

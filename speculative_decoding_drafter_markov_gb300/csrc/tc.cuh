@@ -104,6 +104,11 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned 
     return v;
 }
 
+// fire-and-forget 64-bit integer addition in global memory (L2)
+__device__ __forceinline__ void red_add_u64(unsigned long long *ptr, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+
 // bounded wait until *ctr >= target (a counter other CTAs of the launch raise)
 __device__ __forceinline__ bool wait_counter_ge(const int *ctr, int target, int32_t *err,
                                                 uint64_t limit_ns = kWaitLimitNs) {

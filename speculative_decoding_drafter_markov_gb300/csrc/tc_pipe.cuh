@@ -3,8 +3,9 @@
 // D = A . W_2^T[tile]^T on tcgen05, where A (the bias operand of each request:
 // W_1[x] or the RNN vector A_k, bf16, K-major, 128-byte swizzle) is resident in
 // shared memory and W_2^T streams through a ring of 64-wide K slabs.  One CTA
-// owns one M-tile of MV requests and a set of BN-wide vocabulary tiles
-// (a contiguous range, or every nparts-th tile).  Warp roles (576 threads):
+// owns one M-tile of MV requests and a set of BN-wide vocabulary tiles (a
+// contiguous range, or tiles taken one at a time from a counter the M-tile's
+// CTAs share).  Warp roles (576 threads):
 //   warps 0..15  epilogue: every warp reads its own block of the accumulator
 //                straight from TMEM (no staging) and runs the caller's
 //                functor on it; synchronisation is per warp, through mbarriers.
@@ -352,6 +353,164 @@ struct Pipe {
         if (issued > 0) {  // the last MMAs must finish before TMEM is freed
             const int t = issued - 1;
             tc::mbar_wait_drain(&s.tfull[t % NACC], (uint32_t)(t / NACC) & 1u, err);
+        }
+    }
+
+    // ---- dynamic tile order ------------------------------------------------
+    // The CTAs of one M-tile take vocabulary tiles from a shared counter, so a
+    // CTA that streams faster takes more tiles and all finish together.  The
+    // producer takes the tiles and announces them to the MMA issuer and the
+    // epilogue through a ring of kTileRing words in shared memory: the word of
+    // the CTA's k-th tile is (k << 16) | (tile + 1), and tile + 1 == 0 marks
+    // the end.  The producer runs at most NACC + NS / kslabs + 1 tiles ahead of the slowest
+    // epilogue warp (its slab waits depend on the MMA, which waits for free
+    // accumulators), far less than the ring.
+    static constexpr int kTileRing = 32;
+
+    __device__ static uint32_t ring_word(int k, int tile) { return ((uint32_t)(k & 0xFFFF) << 16) | (uint32_t)(tile + 1); }
+
+    // ring words start as 0xFFFFFFFF, a tag no tile number below 65535 carries
+    __device__ static void ring_init(volatile uint32_t *ring) {
+        if (threadIdx.x < kTileRing) ring[threadIdx.x] = 0xFFFFFFFFu;
+    }
+
+    // the tile of local index k (-1: no more tiles, or an aborted launch); a
+    // bounded wait for the producer's word
+    __device__ static int ring_read(const volatile uint32_t *ring, int k, volatile int *abort_flag, int32_t *err) {
+        const uint32_t tag = (uint32_t)(k & 0xFFFF);
+        uint32_t w = ring[k % kTileRing];
+        if ((w >> 16) == tag) return (int)(w & 0xFFFFu) - 1;
+        const uint64_t t0 = tc::globaltimer_ns();
+        for (;;) {
+            __nanosleep(32);
+            w = ring[k % kTileRing];
+            if ((w >> 16) == tag) return (int)(w & 0xFFFFu) - 1;
+            if (*abort_flag) return -1;
+            if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+                *abort_flag = 1;
+                set_err(err, DSPARK_ERR_TIMEOUT);
+                return -1;
+            }
+        }
+    }
+
+    // warp 16, lane 0: take tiles from *ctr (n_vtiles in all) and stream their
+    // W_2^T slabs; the next tile is taken while the current one's slabs are issued
+    __device__ static void producer_w2_dyn(State &s, const CUtensorMap *tmB, volatile uint32_t *ring, int *ctr,
+                                           int n_vtiles, int kslabs, int32_t *err) {
+        int issued = 0, slot = 0;
+        uint32_t phase = 0;
+        int tile = atomicAdd(ctr, 1);
+        for (int k = 0;; ++k) {
+            if (tile >= n_vtiles) {
+                // the end, at this index and the next (the epilogue also asks for the
+                // tile after its current one, to stage its first chunk)
+                ring[k % kTileRing] = ring_word(k, -1);
+                ring[(k + 1) % kTileRing] = ring_word(k + 1, -1);
+                break;
+            }
+            ring[k % kTileRing] = ring_word(k, tile);
+            const int next = atomicAdd(ctr, 1);
+            bool ok = true;
+            for (int j = 0; j < kslabs; ++j) {
+                if (!tc::mbar_wait(&s.emptyB[slot], phase ^ 1u, s.abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc::mbar_expect_tx(&s.fullB[slot], (uint32_t)kSlabB);
+                tc::tma_load_2d(s.smem + kOffB + slot * kSlabB, tmB, &s.fullB[slot], j * 64, tile * BN);
+                ++issued;
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;  // the abort flag is up: the other roles stop on their own
+            tile = next;
+        }
+        for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)  // no copies left in flight
+            tc::mbar_wait_drain(&s.fullB[g % NS], (uint32_t)(g / NS) & 1u, err);
+    }
+
+    // warp 17, lane 0: the tiles the producer announces, after the operand is
+    // written (the first completion of `aready`)
+    __device__ static void mma_dyn(State &s, const volatile uint32_t *ring, int kslabs, int32_t *err) {
+        static_assert(SU == 0, "dynamic tiles stream no U ring");
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
+        const uint64_t a_desc0 = tc::smem_desc_k128(tc::smem_u32(s.sA));
+        const uint64_t b_desc0 = tc::smem_desc_k128(tc::smem_u32(s.smem + kOffB));
+        int issued = 0, slot = 0, b = 0;
+        uint32_t phase = 0, tphase = 0;
+        bool ok = tc::mbar_wait(s.aready, 0u, s.abort_flag, err);
+        if (ok) tc::tc_fence_after();
+        for (int k = 0; ok; ++k) {
+            if (ring_read(ring, k, s.abort_flag, err) < 0) break;
+            if (!tc::mbar_wait(&s.tempty[b], tphase ^ 1u, s.abort_flag, err)) break;
+            tc::tc_fence_after();
+            const uint32_t d = s.tmem_base + (uint32_t)(b * BN);
+            for (int j = 0; j < kslabs; ++j) {
+                if (!tc::mbar_wait(&s.fullB[slot], phase, s.abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint64_t bd = b_desc0 + (uint64_t)((slot * kSlabB) >> 4);
+                const uint64_t ad = a_desc0 + (uint64_t)((j * kSlabA) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int part = 0; part < KSPLIT; ++part)
+                        tc::umma_bf16(d, ad + (uint64_t)((4 * part * kSlabA + kk * 32) >> 4),
+                                      bd + (uint64_t)((kk * 32) >> 4), idesc,
+                                      (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                tc::umma_commit(&s.emptyB[slot]);
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc::umma_commit(&s.tfull[b]);
+            ++issued;
+            if (++b == NACC) {
+                b = 0;
+                tphase ^= 1u;
+            }
+        }
+        if (issued > 0) {
+            const int t = issued - 1;
+            tc::mbar_wait_drain(&s.tfull[t % NACC], (uint32_t)(t / NACC) & 1u, err);
+        }
+    }
+
+    // warps 0..15: as epilogue(), over the announced tiles; f(k, tile, cofs, acc)
+    // with k the CTA's tile count so far and tile the vocabulary tile
+    template <class F>
+    __device__ static void epilogue_dyn(State &s, const volatile uint32_t *ring, int32_t *err, F &&f) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const uint32_t taddr0 = s.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)epi_col0();
+        for (int k = 0;; ++k) {
+            const int b = k % NACC;
+            int tile = -1;
+            if (lane == 0) {
+                tile = ring_read(ring, k, s.abort_flag, err);
+                if (tile >= 0 && !tc::mbar_wait(&s.tfull[b], (uint32_t)(k / NACC) & 1u, s.abort_flag, err)) tile = -1;
+            }
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0) break;
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < CW / 16; ++h) {
+                uint32_t acc[16];
+                tc::tmem_ld16(taddr0 + (uint32_t)(b * BN + 16 * h), acc);
+                tc::tmem_wait_ld();
+                if (h == CW / 16 - 1) {
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&s.tempty[b]);
+                }
+                f(k, tile, 16 * h, acc);
+            }
         }
     }
 

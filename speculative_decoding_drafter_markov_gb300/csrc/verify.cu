@@ -34,10 +34,16 @@ constexpr int kRowsPerPass = 8;
 constexpr int kThreads = 128;
 constexpr int kNone = 0x7fffffff;
 
-__global__ void verify_init(int R, int gamma, VerifyWs w) {
+__global__ void verify_init(int R, int gamma, VerifyWs w, int ttot_words) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    // the tensor-core phase adds into its tile sums: zero them (16 bytes a store)
+    for (int j = i; 2 * j < ttot_words; j += gridDim.x * blockDim.x)
+        reinterpret_cast<uint4 *>(w.ttot)[j] = make_uint4(0u, 0u, 0u, 0u);
     if (i < R * (gamma + 1)) w.row_of[i] = -1;
-    if (i < kVerifyMaxMTiles) w.done[i] = 0;
+    if (i < kVerifyMaxMTiles) {
+        w.done[i] = 0;
+        w.tctr[i] = 0;
+    }
     if (i < R) {
         w.first_rej[i] = kNone;
         w.ell[i] = -1;
@@ -391,8 +397,8 @@ size_t verify_ws_bytes(int R, int gamma, int V, int N) {
     const int nparts = (V + kSliceV - 1) / kSliceV;
     return align256(sizeof(float) * (size_t)N) + align256(sizeof(int32_t) * (size_t)R) * 2 +
            align256(sizeof(int32_t) * (size_t)R * (gamma + 1)) +
-           align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles) +
-           align256(sizeof(float) * (size_t)R * ((V + 15) / 16)) + align256(sizeof(float) * (size_t)R * kVerifyMaxParts);
+           align256(sizeof(VerifyPartial) * (size_t)R * nparts) + align256(sizeof(int) * kVerifyMaxMTiles) * 2 +
+           align256(sizeof(float) * (size_t)R * ((V + 15) / 16)) + align256(sizeof(unsigned long long) * ((size_t)R * ((V + 63) / 64 + ((V + 63) / 64 + 31) / 32) + 1));
 }
 
 VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
@@ -411,15 +417,20 @@ VerifyWs verify_ws_carve(void *ws, int R, int gamma, int V, int N) {
     p += align256(sizeof(VerifyPartial) * (size_t)R * w.nparts);
     w.done = reinterpret_cast<int *>(p);
     p += align256(sizeof(int) * kVerifyMaxMTiles);
+    w.tctr = reinterpret_cast<int *>(p);
+    p += align256(sizeof(int) * kVerifyMaxMTiles);
     w.csum = reinterpret_cast<float *>(p);
     p += align256(sizeof(float) * (size_t)R * ((V + 15) / 16));
-    w.stot = reinterpret_cast<float *>(p);
+    w.ttot = reinterpret_cast<unsigned long long *>(p);
     return w;
 }
 
 cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaStream_t s) {
+    const bool tc = verify_tc_supported(a);
+    const int nt = tc ? verify_tc_tiles(a) : 0;
+    const int ttot_words = a.R * (nt + (nt + 31) / 32);  // rounded up to even below
     const int n_init = a.R * (a.gamma + 1) > kVerifyMaxMTiles ? a.R * (a.gamma + 1) : kVerifyMaxMTiles;  // >= R
-    verify_init<<<(n_init + 255) / 256, 256, 0, s>>>(a.R, a.gamma, w);
+    verify_init<<<(n_init + 255) / 256, 256, 0, s>>>(a.R, a.gamma, w, (ttot_words + 1) & ~1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.N > 0) {
@@ -432,7 +443,7 @@ cudaError_t launch_verify(const dspark_verify_args &a, const VerifyWs &w, cudaSt
     }
     const bool rnn = a.A != nullptr;
     VerifyWs wf = w;  // the tensor-core path sets its own partial count
-    if (verify_tc_supported(a)) {
+    if (tc) {
         // the last CTA of each M-tile merges the slices and writes the outcome itself
         e = launch_verify_phase2_tc(a, wf, s);
         return e;
