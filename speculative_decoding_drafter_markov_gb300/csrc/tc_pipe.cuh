@@ -403,10 +403,9 @@ struct Pipe {
         int tile = atomicAdd(ctr, 1);
         for (int k = 0;; ++k) {
             if (tile >= n_vtiles) {
-                // the end, at this index and the next (the epilogue also asks for the
-                // tile after its current one, to stage its first chunk)
-                ring[k % kTileRing] = ring_word(k, -1);
-                ring[(k + 1) % kTileRing] = ring_word(k + 1, -1);
+                // the end, at this index and the next three (the epilogue also asks
+                // for tiles ahead of its current one, to stage their chunks)
+                for (int j = 0; j < 4; ++j) ring[(k + j) % kTileRing] = ring_word(k + j, -1);
                 break;
             }
             ring[k % kTileRing] = ring_word(k, tile);

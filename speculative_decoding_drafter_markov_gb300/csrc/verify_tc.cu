@@ -26,13 +26,16 @@ namespace dspark {
 
 namespace {
 
-// Per-thread staging of the target and base rows: every epilogue thread copies
-// the 32 + 32 bytes of its next 16-column chunk with cp.async while it works on
-// the current one (two stages).  Stage s, piece k (0-1 target, 2-3 base, 16 B
-// each) of thread et sits at ((s 4 + k) kEpiThreads + et) 16: a warp's reads of
-// one piece are 32 consecutive 16-byte words (no bank conflicts).
+// Per-thread staging of the target and base rows in NST stages: every epilogue
+// thread copies the 32 + 32 bytes of its chunks NST - 1 ahead with cp.async
+// while it works on the current one.  Stage s, piece k (0-1 target, 2-3 base,
+// 16 B each) of thread et sits at ((s 4 + k) kEpiThreads + et) 16: a warp's reads
+// of one piece are 32 consecutive 16-byte words (no bank conflicts).
 constexpr int kStagePieces = 4;
-constexpr int kStageBytes = 2 * kStagePieces * tcp::kEpiThreads * 16;
+template <int NST>
+constexpr int stage_bytes() {
+    return NST * kStagePieces * tcp::kEpiThreads * 16;
+}
 
 struct VerifyTcParams {
     int R, V, r, gamma;
@@ -263,7 +266,7 @@ __device__ __noinline__ int draw_correction(const VerifyTcParams &p, const RowMe
     return vb + e;
 }
 
-template <class P, bool STAGE>
+template <class P, int NST>
 __global__ void __launch_bounds__(P::kThreads, 1)
     verify_phase2_tc(const __grid_constant__ CUtensorMap tmB, const VerifyTcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -369,13 +372,19 @@ __global__ void __launch_bounds__(P::kThreads, 1)
         // additions does not matter);
         // the draw itself follows the M-tile's synchronisation point.
         float tsum = 0.f;
-        // staging (STAGE): chunk i of this thread lands in stage i % 2; the copy of
-        // chunk i + 1 is in flight while chunk i is processed.  Without it, plain
-        // loads at the start of each chunk.
+        // staging (NST stages): chunk i of this thread lands in stage i % NST; the
+        // copies of chunks i + 1 .. i + NST - 1 are in flight while chunk i is
+        // processed (a chunk past the CTA's last tile is an empty copy group).
+        // Without (NST = 0), plain loads at the start of each chunk.
+        constexpr int CPT = P::CW / 16;  // a thread's chunks per tile
         uint4 *stage = reinterpret_cast<uint4 *>((reinterpret_cast<uintptr_t>(s.smem) + P::kBytes - 1024 + 15) &
                                                  ~static_cast<uintptr_t>(15));
+        auto chunk_vb = [&](int c) {  // vocabulary column of this thread's chunk c, or V: none
+            const int t = P::ring_read(s_ring, c / CPT, s.abort_flag, p.err);
+            return t >= 0 ? t * P::BN + col0 + 16 * (c % CPT) : p.V;
+        };
         auto stage_chunk = [&](int i, int vb) {
-            uint4 *dst = stage + (size_t)(i & 1) * kStagePieces * tcp::kEpiThreads + et;
+            uint4 *dst = stage + (size_t)(i % (NST > 0 ? NST : 1)) * kStagePieces * tcp::kEpiThreads + et;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const bool in = mode >= 0 && vb + 8 * c < p.V;
@@ -386,32 +395,20 @@ __global__ void __launch_bounds__(P::kThreads, 1)
             }
             tc::cp_async_commit();
         };
-        if (STAGE) {
-            const int t0 = P::ring_read(s_ring, 0, s.abort_flag, p.err);
-            if (t0 >= 0) stage_chunk(0, t0 * P::BN + col0);
-        }
+        if (NST > 0)
+            for (int c = 0; c < NST - 1; ++c) stage_chunk(c, chunk_vb(c));
         int ci = 0;
         P::epilogue_dyn(s, s_ring, p.err, [&](int k, int tile, int cofs, const uint32_t *acc) {
             const int vb = tile * P::BN + col0 + cofs;  // 16 columns vb .. vb + 15; V % 8 == 0
-            if (STAGE) {
-                // the next chunk: the rest of this warp's block, else the next tile's
-                int vnext = vb + 16;
-                if (cofs + 16 >= P::CW) {
-                    const int tn = P::ring_read(s_ring, k + 1, s.abort_flag, p.err);
-                    vnext = tn >= 0 ? tn * P::BN + col0 : p.V;
-                }
-                if (vnext < p.V) {
-                    stage_chunk(ci + 1, vnext);
-                    tc::cp_async_wait<1>();
-                } else {
-                    tc::cp_async_wait<0>();
-                }
+            if (NST > 0) {
+                stage_chunk(ci + NST - 1, chunk_vb(ci + NST - 1));
+                tc::cp_async_wait<(NST > 0 ? NST - 1 : 0)>();  // chunk ci has landed
             }
             // the chunk of the target row (and of U_{n+1}): this thread's stage, or
             // 16-byte loads (zeros beyond V)
             uint4 tq[2], uq[2];
-            if (STAGE) {
-                const uint4 *src = stage + (size_t)(ci & 1) * kStagePieces * tcp::kEpiThreads + et;
+            if (NST > 0) {
+                const uint4 *src = stage + (size_t)(ci % (NST > 0 ? NST : 1)) * kStagePieces * tcp::kEpiThreads + et;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     tq[c] = src[c * tcp::kEpiThreads];
@@ -494,16 +491,18 @@ __global__ void __launch_bounds__(P::kThreads, 1)
 }
 
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring (none), operand split>.
-// The 128-request configuration stages its rows (64 KB, with a shorter W_2^T ring);
-// measured against plain loads it was faster there and slower for 64 requests and
-// the RNN operand.  With the static row metadata, all within 227 KB.
+// The 128-request configuration stages its rows three deep (96 KB, with a W_2^T
+// ring of three slabs: the MMA is far ahead of the epilogue anyway); measured
+// against plain loads staging was faster there and slower for 64 requests and the
+// RNN operand, and three stages were 1-2 % faster than two with a five-slab ring.
+// With the static row metadata, all within 227 KB.
 using VerifyM64 = tcp::Pipe<64, 128, 9, 0, 1>;
-using VerifyM128 = tcp::Pipe<128, 128, 5, 0, 1>;
+using VerifyM128 = tcp::Pipe<128, 128, 3, 0, 1>;
 using VerifyRnn = tcp::Pipe<128, 64, 10, 0, 2>;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <class P, bool STAGE>
+template <class P, int NST>
 cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
     int nparts = 0, mt = 0;
     tc_grid_shape(a.R, a.V, P::MV, P::BN, &nparts, &mt);
@@ -522,8 +521,8 @@ cudaError_t launch_cfg(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s)
     tp.nparts = nparts; tp.n_mtiles = mt; tp.n_vtiles = (a.V + P::BN - 1) / P::BN;
     tp.seed = a.seed; tp.cycle = a.cycle; tp.err = a.err;
     tp.a = a;
-    auto kern = verify_phase2_tc<P, STAGE>;
-    const int smem = P::kBytes + (STAGE ? kStageBytes + 16 : 0);  // + 16: the stage starts on a 16-byte boundary
+    auto kern = verify_phase2_tc<P, NST>;
+    const int smem = P::kBytes + (NST > 0 ? stage_bytes<NST>() + 16 : 0);  // + 16: the stage starts on a 16-byte boundary
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // cooperative: the CTAs of an M-tile wait for one another before the final merge
@@ -547,9 +546,9 @@ int verify_tc_tiles(const dspark_verify_args &a) {
 }
 
 cudaError_t launch_verify_phase2_tc(const dspark_verify_args &a, VerifyWs &w, cudaStream_t s) {
-    if (a.A) return launch_cfg<VerifyRnn, false>(a, w, s);
-    if (a.R <= 64) return launch_cfg<VerifyM64, false>(a, w, s);
-    return launch_cfg<VerifyM128, true>(a, w, s);
+    if (a.A) return launch_cfg<VerifyRnn, 0>(a, w, s);
+    if (a.R <= 64) return launch_cfg<VerifyM64, 0>(a, w, s);
+    return launch_cfg<VerifyM128, 3>(a, w, s);
 }
 
 }  // namespace dspark
