@@ -543,6 +543,7 @@ struct Pipe {
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            if (SU > 0 && !UMMA) __syncwarp();  // the other lanes read the U tile lane 0 waited for
             tc::tc_fence_after();
             const unsigned char *sU = SU > 0 && !UMMA ? s.smem + kOffU + (tg % su) * kUBytes : nullptr;
 #pragma unroll 1

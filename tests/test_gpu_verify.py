@@ -156,3 +156,37 @@ def test_malformed_tags_report_inval():
                dev(z), inp["U"].cuda(), inp["W1"].cuda(), inp["W2t"].cuda(), err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == dsp.ERR_INVAL
+
+
+def test_verify_repeat_identical_with_dirty_workspace():
+    """The tensor-core verification is deterministic: the tile order is dynamic
+    (taken from a counter), but the draw's sums are indexed by vocabulary
+    position and the tile level is integer arithmetic, so repeated calls give
+    identical outputs bit for bit -- also when the caller's workspace holds
+    stale data from another call (the tile sums are zeroed by every call)."""
+    wl = W.small("heavy", R=300, gamma=4, V=20000, r=128, d=16)  # 3 M-tiles, ~157 tiles
+    rng = np.random.default_rng(11)
+    ell = rng.integers(0, wl.gamma + 1, wl.R)
+    inp = W.draft_inputs(wl, seed=9, device="cuda")
+    x = torch.as_tensor(rng.integers(0, wl.V, (wl.R, wl.gamma)).astype(np.int32), device="cuda")
+    logq = torch.as_tensor(rng.uniform(-3.0, -0.01, (wl.R, wl.gamma)).astype(np.float32), device="cuda")
+    lse = torch.as_tensor(rng.uniform(5.0, 15.0, (wl.R, wl.gamma)).astype(np.float32), device="cuda")
+    tags = W.tags_from_ell(ell)
+    T = W.target_logits(wl, inp["U"], inp["U_bonus"], tags, seed=9).cuda()
+    tags_d = torch.as_tensor(tags, device="cuda")
+    nbytes = dsp.verify_workspace_size(T, tags_d, inp["anchor"], x, logq, lse, inp["U"], inp["W1"],
+                                       inp["W2t"])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for fill in (0, 0xFF, 0x5A):
+        ws.fill_(fill)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = dsp.verify(T, tags_d, inp["anchor"], x, logq, lse, inp["U"], inp["W1"], inp["W2t"],
+                         seed=3, cycle=7, ws=ws, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, dsp.ERROR_NAMES[int(err.item())]
+        outs.append({k: host(v).copy() for k, v in out.items()})
+    for o in outs[1:]:
+        for k in outs[0]:
+            assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8)), k
+    assert (outs[0]["n_accept"] < ell).any()  # residual draws exercised
