@@ -244,11 +244,11 @@ class Cycle:
                                            self.out["logq"], self.out["lse"], inp["U"], inp["W1"],
                                            inp["W2t"], A=self.out.get("A"))
         self.vws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
-        # library kernels per cycle: the gamma Markov draft steps (one launch) or,
-        # RNN head, the h projection, the first step's state update, then one
-        # launch per step (which ends with the next step's update); schedule +
-        # build_tags; verify (init, phase 1, phase 2 with the final merge)
-        n_draft = 2 + gm if self.rnn else 1
+        # library kernels per cycle: the gamma draft steps in one launch (the RNN
+        # head's state updates inside it), after the RNN head's h projection (a
+        # tensor-core GEMM); schedule + build_tags; verify (init, phase 1, phase 2
+        # with the draw)
+        n_draft = 2 if self.rnn else 1
         self.launches_per_cycle = n_draft + 3 + (2 if self.sched else 0)
 
     def draft(self, cycle):
