@@ -498,7 +498,8 @@ def run_dspark(args, world, rank, local):
         bytes_launch += 3 * wl.r * (2 * wl.r + wl.d) * 2
     achieved = bytes_launch / (draft_us * 1e-6) / 1e9
     strict = draft_cycle_bytes_strict(wl) / (draft_us * 1e-6) / 1e9
-    draft_traffic = ncu_traffic("draft_step_tc", wl.name) if not cyc.rnn else (None, "RNN head: several launches")
+    draft_traffic = (ncu_traffic("draft_step_tc", wl.name) if not cyc.rnn
+                     else (None, "RNN head: the stage is two launches (h projection, steps)"))
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
