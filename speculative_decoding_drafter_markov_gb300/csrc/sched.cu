@@ -196,7 +196,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sc
     // 1. prefix survival products (Algorithm 1, line 1) and sort keys (line 2);
     //    the confidences are staged in shared memory with coalesced loads first
     float *c_s = reinterpret_cast<float *>(tmp);  // free until the sort
-    for (int e = tid; e < n; e += nt) c_s[e] = a.c[e];
+    {
+        float cv[IPT];  // all of a thread's loads in flight together
+#pragma unroll
+        for (int q = 0; q < IPT; ++q) cv[q] = tid + q * nt < n ? a.c[tid + q * nt] : 0.f;
+#pragma unroll
+        for (int q = 0; q < IPT; ++q)
+            if (tid + q * nt < n) c_s[tid + q * nt] = cv[q];
+    }
     __syncthreads();
     // one thread per entry (r, j): a_{r,j} as the same left-to-right product
     int in_pool = 0;
@@ -260,8 +267,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sc
     //    compare the values' bit patterns, which order like the values for
     //    non-negative finite doubles (else the fp64 comparison decides).
     long long *th = units;
-    for (int m = tid; m <= pool; m += nt) {
-        th[m] = __double_as_longlong(__dmul_rn(scaled_units(units[m]), a.sps[R + m - a.B_min]));
+    {
+        double spv[IPT + 1];  // the table entries of this thread's prefixes, loads in flight together
+#pragma unroll
+        for (int q = 0; q <= IPT; ++q) spv[q] = tid + q * nt <= pool ? a.sps[R + tid + q * nt - a.B_min] : 0.0;
+#pragma unroll
+        for (int q = 0; q <= IPT; ++q) {
+            const int m = tid + q * nt;
+            if (m <= pool) th[m] = __double_as_longlong(__dmul_rn(scaled_units(units[m]), spv[q]));
+        }
     }
     __syncthreads();
     long long best_th = 0;
