@@ -205,16 +205,27 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sc
             if (tid + q * nt < n) c_s[tid + q * nt] = cv[q];
     }
     __syncthreads();
-    // one thread per entry (r, j): a_{r,j} as the same left-to-right product
-    int in_pool = 0;
+    // one thread per request: the running products a_{r,1..G} (left to right, the
+    // rounding of Algorithm 1's products) in place of its confidences
     bool bad = false;
-    for (int e = tid; e < n; e += nt) {
-        const int rq = e / G, j = e - rq * G;
-        const float *cr = c_s + rq * G;
+    for (int rq = tid; rq < R; rq += nt) {
+        float *cr = c_s + rq * G;
         float prod = 1.0f;
-        for (int i = 0; i <= j; ++i) prod = __fmul_rn(prod, cr[i]);
-        const float cc = cr[j];
-        if (!(cc >= 0.0f && cc <= 1.0f)) bad = true;
+        for (int j = 0; j < G; ++j) {
+            const float cc = cr[j];
+            if (!(cc >= 0.0f && cc <= 1.0f)) bad = true;
+            prod = __fmul_rn(prod, cc);
+            cr[j] = prod;
+        }
+    }
+    __syncthreads();
+    // one thread per entry (r, j): its sort key
+    int in_pool = 0;
+#pragma unroll
+    for (int q = 0; q < IPT; ++q) {
+        const int e = tid + q * nt;
+        if (e >= n) continue;
+        const float prod = c_s[e];
         if (a.a) a.a[e] = prod;
         const uint32_t k30 = prod > 0.0f ? 0x3F800000u - __float_as_uint(prod) : kOutKey30;
         in_pool += prod > 0.0f;
