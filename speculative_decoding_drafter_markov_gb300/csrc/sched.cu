@@ -6,20 +6,24 @@
 // production section replaces the break by a top-K of the current order with K
 // taken from the confidences of two cycles earlier.
 //
-// One CTA does the whole decision (the pool holds at most 8192 entries):
+// A cluster of eight CTAs makes the decision (the pool holds at most 8192
+// entries, one per thread; CTA c holds positions 1024 c .. 1024 c + 1023):
 //   1. fp32 running products a (IEEE products, identical to any CPU);
 //   2. 30-bit sort keys 0x3F800000 - bits(a) (a in (0, 1]; 0x3FFFFFFF marks an
 //      entry outside the pool): ascending key order is a descending, and a
 //      stable sort of the entries in flat-index order breaks ties by
-//      (request, position).  Stable LSD radix sort in shared memory, 5-bit
-//      digits, 6 passes: each warp ranks its items with five ballots (the
-//      lanes sharing a digit), one block-wide scan over the (digit, warp)
-//      counts places them;
+//      (request, position).  Stable LSD radix sort in the cluster's shared
+//      memory, 5-bit digits, 6 passes: each warp ranks its entries with five
+//      ballots (the lanes sharing a digit); the (digit, warp) counts of the CTA
+//      and the digit counts of the CTAs before it place them, and each entry
+//      moves to the CTA that holds its new position;
 //   3. tau as an exact integer prefix sum in 2^-32 units;
 //   4. Theta(m) = (tau_m 2^-32) * SPS(R + m) for every prefix m in parallel;
 //      the synchronous stop is the first m with Theta(m) <= Theta(m-1), the
 //      capacity for cycle t+2 is argmax_m Theta(m) (smallest m on ties);
 //   5. l_r = largest admitted position of request r.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -90,36 +94,6 @@ constexpr uint32_t kOutKey30 = 0x3FFFFFFFu;  // sorts after every a in (0, 1]
 constexpr int kRadixBits = 5, kRadixPasses = 6, kBins = 1 << kRadixBits;
 constexpr int kHistLd = 33;  // (digit, warp) counts at d * 33 + w: no two digits share a bank
 
-// inclusive block scan of one int per thread (1024 threads)
-__device__ int block_inclusive_scan_int(int v, int *warp_tot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int t = warp_tot[lane];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, t, off);
-            if (lane >= off) t += o;
-        }
-        warp_tot[lane] = t;
-    }
-    __syncthreads();
-    const int prefix = warp > 0 ? warp_tot[warp - 1] : 0;
-    __syncthreads();
-    return v + prefix;
-}
-
-// Stable LSD radix sort of CAP = 1024 IPT words (sort key in bits 32..61, flat
-// index below) from `src`, result back in `src` (an even number of passes).
-// Warp w owns positions [32 IPT w, 32 IPT (w + 1)) of the current order, item i
-// of lane l being position 32 IPT w + 32 i + l, so (warp, item, lane) order is
-// sequence order and ranking the items in that order keeps the sort stable.
 // the lanes of the warp whose kRadixBits-bit digit is d, from the warp's
 // per-bit ballots
 __device__ __forceinline__ unsigned digit_lanes(const unsigned (&vote)[kRadixBits], int d) {
@@ -129,180 +103,178 @@ __device__ __forceinline__ unsigned digit_lanes(const unsigned (&vote)[kRadixBit
     return m;
 }
 
-template <int IPT>
-__device__ void radix_sort_keys(unsigned long long *src, unsigned long long *dst, int *hist, int *warp_tot) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int pass = 0; pass < kRadixPasses; ++pass) {
-        const int shift = 32 + kRadixBits * pass;
-        unsigned long long v[IPT];
-        int off[IPT];
-#pragma unroll
-        for (int i = 0; i < IPT; ++i) v[i] = src[32 * IPT * warp + 32 * i + lane];
-        // lane x keeps the running count of digit x over this warp's items
-        int cnt = 0;
-#pragma unroll
-        for (int i = 0; i < IPT; ++i) {
-            const int d = (int)(v[i] >> shift) & (kBins - 1);
-            unsigned vote[kRadixBits];
-#pragma unroll
-            for (int b = 0; b < kRadixBits; ++b) vote[b] = __ballot_sync(0xffffffffu, (d >> b) & 1);
-            const unsigned peers = digit_lanes(vote, d);
-            off[i] = __shfl_sync(0xffffffffu, cnt, d) + __popc(peers & lt_mask);
-            cnt += __popc(digit_lanes(vote, lane));
-        }
-        hist[lane * kHistLd + warp] = cnt;
-        __syncthreads();
-        // exclusive scan over (digit, warp) in digit-major order: 32 bins x 32 warps
-        const int hs = (tid >> 5) * kHistLd + (tid & 31);
-        const int c = hist[hs];
-        const int incl = block_inclusive_scan_int(c, warp_tot);
-        hist[hs] = incl - c;
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < IPT; ++i) {
-            const int d = (int)(v[i] >> shift) & (kBins - 1);
-            dst[hist[d * kHistLd + warp] + off[i]] = v[i];
-        }
-        __syncthreads();
-        unsigned long long *t = src;
-        src = dst;
-        dst = t;
-    }
-}
+constexpr int kClusterCtas = 8;          // CTAs of the scheduler's cluster
+constexpr int kCtaItems = kSchedThreads;  // sort positions per CTA: one per thread
 
-template <int IPT>
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sched_args a) {
-    constexpr int npad = kSchedThreads * IPT;
-    extern __shared__ unsigned long long sched_smem[];
-    unsigned long long *keys = sched_smem;                     // [npad] sorted entries
-    unsigned long long *tmp = keys + npad;                     // [npad] radix ping-pong
-    long long *units = reinterpret_cast<long long *>(tmp);     // [npad + 1] after the sort
-    int *ell_s = reinterpret_cast<int *>(tmp + npad + 1);      // [R]
+// The scheduler on a cluster of kClusterCtas CTAs (distributed shared memory):
+// CTA c holds positions c 1024 .. c 1024 + 1023 of the pool order (one entry a
+// thread), so every per-entry step runs on eight SMs; the radix passes exchange
+// the CTAs' digit counts and scatter the entries through the cluster's shared
+// memory, and the prefix sums and reductions combine the CTAs' parts in CTA
+// order.  Every CTA takes the same path (the decisions are cluster-wide), and
+// none leaves while another may still read its shared memory.
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSchedThreads)
+    schedule_cluster_kernel(const dspark_sched_args a) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int c = (int)cluster.block_rank();
+    __shared__ unsigned long long keys[2][kCtaItems];
+    __shared__ int hist[kBins * kHistLd];  // (digit, warp) counts, then their prefix in the CTA
+    __shared__ int dtot[kBins];             // this CTA's count of each digit (read by the others)
+    __shared__ int gbase[kBins];            // first position of this CTA's entries of each digit
     __shared__ long long warp_tot[32];
-    __shared__ int hist[kBins * kHistLd];
-    __shared__ int s_bad, s_pool, s_first;
-    __shared__ long long s_th[32];
-    __shared__ int s_arg[32];
-
-    const int R = a.R, G = a.gamma, n = R * G, tid = threadIdx.x, nt = blockDim.x;
+    __shared__ long long s_th[kCtaItems];   // Theta(m) for m = c 1024 + t + 1
+    __shared__ long long s_red_th[32];
+    __shared__ int s_red_m[32];
+    __shared__ int s_bad, s_pool, s_first;  // this CTA's parts, read by the others
+    __shared__ long long s_ctot, s_best_th, s_th0;
+    __shared__ int s_best_m;
+    const int R = a.R, G = a.gamma, n = R * G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int p0 = c * kCtaItems;  // this CTA's first position
     if (tid == 0) {
         s_bad = 0;
         s_pool = 0;
         s_first = 0x7fffffff;
     }
+    // the verify lengths start at 0 (atomic maxima follow, after cluster barriers)
+    for (int rq = c * kSchedThreads + tid; rq < R; rq += kClusterCtas * kSchedThreads) a.ell[rq] = 0;
     __syncthreads();
 
-    // 1. prefix survival products (Algorithm 1, line 1) and sort keys (line 2);
-    //    the confidences are staged in shared memory with coalesced loads first
-    float *c_s = reinterpret_cast<float *>(tmp);  // free until the sort
+    // 1. survival products (Algorithm 1, line 1): one thread per request whose
+    //    entries meet this CTA's range, the same left-to-right products; each
+    //    entry's key (line 2) in flat-index order
     {
-        float cv[IPT];  // all of a thread's loads in flight together
-#pragma unroll
-        for (int q = 0; q < IPT; ++q) cv[q] = tid + q * nt < n ? a.c[tid + q * nt] : 0.f;
-#pragma unroll
-        for (int q = 0; q < IPT; ++q)
-            if (tid + q * nt < n) c_s[tid + q * nt] = cv[q];
-    }
-    __syncthreads();
-    // one thread per request: the running products a_{r,1..G} (left to right, the
-    // rounding of Algorithm 1's products) in place of its confidences
-    bool bad = false;
-    for (int rq = tid; rq < R; rq += nt) {
-        float *cr = c_s + rq * G;
-        float prod = 1.0f;
-        for (int j = 0; j < G; ++j) {
-            const float cc = cr[j];
-            if (!(cc >= 0.0f && cc <= 1.0f)) bad = true;
-            prod = __fmul_rn(prod, cc);
-            cr[j] = prod;
+        const int rq0 = p0 / G, rq1 = min(R - 1, (p0 + kCtaItems - 1) / G);
+        bool bad = false;
+        int in_pool = 0;
+        const int rq = rq0 + tid;
+        if (p0 < n && rq <= rq1) {
+            const float *cr = a.c + (size_t)rq * G;
+            float prod = 1.0f;
+            for (int j = 0; j < G; ++j) {
+                const int e = rq * G + j;
+                const float cc = cr[j];
+                prod = __fmul_rn(prod, cc);
+                if (e < p0 || e >= p0 + kCtaItems) continue;
+                if (!(cc >= 0.0f && cc <= 1.0f)) bad = true;
+                if (a.a) a.a[e] = prod;
+                const uint32_t k30 = prod > 0.0f ? 0x3F800000u - __float_as_uint(prod) : kOutKey30;
+                in_pool += prod > 0.0f;
+                keys[0][e - p0] = ((unsigned long long)k30 << 32) | (unsigned)e;
+            }
         }
+        if (p0 + tid >= n) keys[0][tid] = ((unsigned long long)kOutKey30 << 32) | (unsigned)(p0 + tid);
+        if (bad) atomicExch(&s_bad, 1);
+        in_pool = __reduce_add_sync(0xffffffffu, in_pool);
+        if (lane == 0 && in_pool) atomicAdd(&s_pool, in_pool);
     }
-    __syncthreads();
-    // one thread per entry (r, j): its sort key
-    int in_pool = 0;
-#pragma unroll
-    for (int q = 0; q < IPT; ++q) {
-        const int e = tid + q * nt;
-        if (e >= n) continue;
-        const float prod = c_s[e];
-        if (a.a) a.a[e] = prod;
-        const uint32_t k30 = prod > 0.0f ? 0x3F800000u - __float_as_uint(prod) : kOutKey30;
-        in_pool += prod > 0.0f;
-        keys[e] = ((unsigned long long)k30 << 32) | (unsigned)e;
+    cluster.sync();
+    int bad = 0, pool = 0;
+    for (int q = 0; q < kClusterCtas; ++q) {
+        bad |= *cluster.map_shared_rank(&s_bad, q);
+        pool += *cluster.map_shared_rank(&s_pool, q);
     }
-    for (int rq = tid; rq < R; rq += nt) ell_s[rq] = 0;
-    if (bad) atomicExch(&s_bad, 1);
-    for (int e = n + tid; e < npad; e += nt) keys[e] = ((unsigned long long)kOutKey30 << 32) | (unsigned)e;
-    in_pool = __reduce_add_sync(0xffffffffu, in_pool);
-    if ((tid & 31) == 0 && in_pool) atomicAdd(&s_pool, in_pool);
-    __syncthreads();
-    if (s_bad) {
-        if (tid == 0) {
+    cluster.sync();  // every CTA has read the others' parts
+    if (bad) {
+        if (c == 0 && tid == 0) {
             set_err(a.err, DSPARK_ERR_RANGE);
             *a.K_out = 0;
             *a.theta_best = 0.0;
         }
-        for (int rq = tid; rq < R; rq += nt) a.ell[rq] = 0;
-        return;
+        return;  // every CTA: the decision is the cluster's
     }
 
-    // 2. stable radix sort, ascending keys
-    radix_sort_keys<IPT>(keys, tmp, hist, reinterpret_cast<int *>(warp_tot));
-    const int pool = s_pool;
-
-    // 3. tau in 2^-32 units: exact integer prefix sums of round(a * 2^32)
-    const int i0 = tid * IPT;
-    long long u[IPT];
-    long long local = 0;
+    // 2. stable LSD radix sort of the keys (bits 32..61), 5-bit digits: a warp
+    //    ranks its 32 entries with five ballots; the CTA's (digit, warp) counts,
+    //    the cluster's digit counts in CTA order and the rank give the new
+    //    position, and the entry moves to the CTA that holds it
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int cur = 0;
+    for (int pass = 0; pass < kRadixPasses; ++pass) {
+        const int shift = 32 + kRadixBits * pass;
+        const unsigned long long v = keys[cur][tid];
+        const int d = (int)(v >> shift) & (kBins - 1);
+        unsigned vote[kRadixBits];
 #pragma unroll
-    for (int q = 0; q < IPT; ++q) {
-        const int i = i0 + q;
-        u[q] = i < pool ? units_of(__uint_as_float(0x3F800000u - (unsigned)(keys[i] >> 32))) : 0;
-        local += u[q];
+        for (int b = 0; b < kRadixBits; ++b) vote[b] = __ballot_sync(0xffffffffu, (d >> b) & 1);
+        const int rank = __popc(digit_lanes(vote, d) & lt_mask);
+        hist[lane * kHistLd + warp] = __popc(digit_lanes(vote, lane));  // entries of digit `lane`
+        __syncthreads();
+        {
+            // warp d: the digit's counts over the CTA's warps, prefix and total
+            const int dd = warp, w = lane;
+            const int cnt = hist[dd * kHistLd + w];
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            hist[dd * kHistLd + w] = incl - cnt;
+            if (lane == 31) dtot[dd] = incl;
+        }
+        cluster.sync();
+        if (warp == 0) {
+            // digit `lane`: its count in every CTA; where this CTA's entries of it start
+            int tot = 0, before = 0;
+            for (int q = 0; q < kClusterCtas; ++q) {
+                const int t = *cluster.map_shared_rank(&dtot[lane], q);
+                tot += t;
+                if (q < c) before += t;
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            gbase[lane] = incl - tot + before;
+        }
+        __syncthreads();
+        const int pos = gbase[d] + hist[d * kHistLd + warp] + rank;
+        *cluster.map_shared_rank(&keys[cur ^ 1][pos & (kCtaItems - 1)], pos / kCtaItems) = v;
+        cluster.sync();  // every entry placed; the digit counts read
+        cur ^= 1;
     }
+
+    // 3. tau in 2^-32 units: exact integer prefix sums of round(a 2^32) over the
+    //    pool order, the CTAs' totals added in CTA order
+    const unsigned long long kv = keys[cur][tid];
+    const int i = p0 + tid;  // this entry's position
+    const long long u = i < pool ? units_of(__uint_as_float(0x3F800000u - (unsigned)(kv >> 32))) : 0;
+    const long long incl_u = block_inclusive_scan(u, warp_tot);
+    if (tid == kSchedThreads - 1) s_ctot = incl_u;
+    cluster.sync();
     const long long base = ((long long)R << 32);
-    long long run = block_inclusive_scan(local, warp_tot) - local + base;
-    if (tid == 0) units[0] = base;
-#pragma unroll
-    for (int q = 0; q < IPT; ++q) {
-        run += u[q];
-        units[i0 + q + 1] = run;
-    }
-    __syncthreads();
-
-    // 4. Theta(m) = (tau_m 2^-32) SPS(R + m) once per prefix m, in place of
-    //    units[m]: tau_m is exact in fp64 (units < 2^53, scaled by an exponent
-    //    shift), so the one rounded multiply is the oracle's.  fp64 runs at a
-    //    small fraction of the fp32 rate here, so the stop test and the argmax
-    //    compare the values' bit patterns, which order like the values for
-    //    non-negative finite doubles (else the fp64 comparison decides).
-    long long *th = units;
-    {
-        double spv[IPT + 1];  // the table entries of this thread's prefixes, loads in flight together
-#pragma unroll
-        for (int q = 0; q <= IPT; ++q) spv[q] = tid + q * nt <= pool ? a.sps[R + tid + q * nt - a.B_min] : 0.0;
-#pragma unroll
-        for (int q = 0; q <= IPT; ++q) {
-            const int m = tid + q * nt;
-            if (m <= pool) th[m] = __double_as_longlong(__dmul_rn(scaled_units(units[m]), spv[q]));
-        }
-    }
-    __syncthreads();
-    long long best_th = 0;
-    int best_m = 0x7fffffff;
-    int first = 0x7fffffff;
-    for (int m = tid; m <= pool; m += nt) {
-        const long long t = th[m];
-        if (best_m == 0x7fffffff || th_gt(t, best_th)) {  // m increases within a thread: smallest m on ties
-            best_th = t;
-            best_m = m;
-        }
-        if (m >= 1 && first == 0x7fffffff && th_le(t, th[m - 1])) first = m;
+    long long off_u = base;
+    for (int q = 0; q < c; ++q) off_u += *cluster.map_shared_rank(&s_ctot, q);
+    // 4. Theta(m) = (tau_m 2^-32) SPS(R + m) for the prefixes m = i + 1 (and m = 0
+    //    at CTA 0), compared by bit pattern like the values (non-negative finite
+    //    doubles), else by the fp64 comparison
+    const int m = i + 1;
+    const long long thm = m <= pool ? __double_as_longlong(__dmul_rn(scaled_units(off_u + incl_u),
+                                                                      a.sps[R + m - a.B_min]))
+                                    : 0;
+    s_th[tid] = thm;
+    if (c == 0 && tid == 0) s_th0 = __double_as_longlong(__dmul_rn(scaled_units(base), a.sps[R - a.B_min]));
+    cluster.sync();
+    // the stop test needs Theta(m - 1): the previous thread's, the previous CTA's
+    // last, or Theta(0)
+    long long prev = 0;
+    if (tid > 0)
+        prev = s_th[tid - 1];
+    else
+        prev = c == 0 ? s_th0 : *cluster.map_shared_rank(&s_th[kCtaItems - 1], c - 1);
+    const long long th0 = *cluster.map_shared_rank(&s_th0, 0);
+    int first = m <= pool && th_le(thm, prev) ? m : 0x7fffffff;
+    // argmax over m (larger Theta, then smaller m); CTA 0 also holds m = 0
+    long long best_th = m <= pool ? thm : 0;
+    int best_m = m <= pool ? m : 0x7fffffff;
+    if (c == 0 && tid == 0 && (best_m == 0x7fffffff || !th_gt(best_th, th0))) {
+        best_th = th0;
+        best_m = 0;
     }
     first = (int)__reduce_min_sync(0xffffffffu, (unsigned)first);
-    if ((tid & 31) == 0 && first != 0x7fffffff) atomicMin(&s_first, first);
-    // argmax over threads: larger Theta, then smaller m
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const long long th2 = __shfl_xor_sync(0xffffffffu, best_th, off);
@@ -313,14 +285,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sc
             best_m = m2;
         }
     }
-    if ((tid & 31) == 0) {
-        s_th[tid >> 5] = best_th;
-        s_arg[tid >> 5] = best_m;
+    if (lane == 0) {
+        s_red_th[warp] = best_th;
+        s_red_m[warp] = best_m;
+        if (first != 0x7fffffff) atomicMin(&s_first, first);
     }
     __syncthreads();
-    if (tid < 32) {
-        best_th = tid < (nt >> 5) ? s_th[tid] : 0;
-        best_m = tid < (nt >> 5) ? s_arg[tid] : 0x7fffffff;
+    if (warp == 0) {
+        best_th = s_red_th[lane];
+        best_m = s_red_m[lane];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const long long th2 = __shfl_xor_sync(0xffffffffu, best_th, off);
@@ -331,27 +304,43 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const dspark_sc
                 best_m = m2;
             }
         }
-        if (tid == 0) s_arg[0] = best_m;
+        if (lane == 0) {
+            s_best_th = best_th;
+            s_best_m = best_m;
+        }
     }
-    __syncthreads();
-    const int K_cap = s_arg[0];
-    int count = s_first == 0x7fffffff ? pool : s_first - 1;
+    cluster.sync();
+    // the cluster's argmax and first stop, from the CTAs' parts in CTA order
+    int K_cap = 0x7fffffff, stop = 0x7fffffff;
+    long long K_th = 0;
+    for (int q = 0; q < kClusterCtas; ++q) {
+        const int m2 = *cluster.map_shared_rank(&s_best_m, q);
+        const long long th2 = *cluster.map_shared_rank(&s_best_th, q);
+        if (m2 != 0x7fffffff && (K_cap == 0x7fffffff || th_gt(th2, K_th) || (th2 == K_th && m2 < K_cap))) {
+            K_th = th2;
+            K_cap = m2;
+        }
+        stop = min(stop, *cluster.map_shared_rank(&s_first, q));
+    }
+    int count = stop == 0x7fffffff ? pool : stop - 1;
     if (a.mode == DSPARK_SCHED_ASYNC && a.K_in != nullptr) {
         const int K = *a.K_in;
         if (K >= 0) count = min(K, pool);
     }
+    // Theta at the admitted point: Theta(0) or the entry's of position count - 1
+    if (count == 0) {
+        if (c == 0 && tid == 0) *a.theta_best = __longlong_as_double(th0);
+    } else if (count - 1 == i) {
+        *a.theta_best = __longlong_as_double(thm);
+    }
+    if (c == 0 && tid == 0) *a.K_out = K_cap;
 
-    // 5. verify lengths: l_r <- j for every admitted (r, j)
-    for (int i = tid; i < count; i += nt) {
-        const unsigned e = (unsigned)(keys[i] & 0xFFFFFFFFull);
-        atomicMax(&ell_s[e / G], (int)(e % G) + 1);
+    // 5. verify lengths: l_r <- j for every admitted (r, j) (its position < count)
+    if (i < count) {
+        const unsigned e = (unsigned)(kv & 0xFFFFFFFFull);
+        atomicMax(&a.ell[e / G], (int)(e % G) + 1);
     }
-    __syncthreads();
-    for (int rq = tid; rq < R; rq += nt) a.ell[rq] = ell_s[rq];
-    if (tid == 0) {
-        *a.K_out = K_cap;
-        *a.theta_best = __longlong_as_double(th[count]);
-    }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ----- flattened batch tags: rows (r, 0..l_r) in request order -----------------
@@ -387,35 +376,10 @@ __global__ void __launch_bounds__(1024) build_tags_kernel(int R, int gamma, cons
 
 }  // namespace
 
-static int sched_ipt(int n) {
-    int ipt = 1;
-    while (kSchedThreads * ipt < n) ipt <<= 1;
-    return ipt;
-}
-
-size_t schedule_smem_bytes(int R, int gamma) {
-    const int npad = kSchedThreads * sched_ipt(R * gamma);
-    return sizeof(unsigned long long) * (size_t)(2 * npad + 1) + sizeof(int) * (size_t)R;
-}
-
-template <int IPT>
-static cudaError_t launch_schedule_t(const dspark_sched_args &a, size_t smem, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel<IPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    schedule_kernel<IPT><<<1, kSchedThreads, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_schedule(const dspark_sched_args &a, cudaStream_t s) {
-    const size_t smem = schedule_smem_bytes(a.R, a.gamma);
-    switch (sched_ipt(a.R * a.gamma)) {
-        case 1: return launch_schedule_t<1>(a, smem, s);
-        case 2: return launch_schedule_t<2>(a, smem, s);
-        case 4: return launch_schedule_t<4>(a, smem, s);
-        case 8: return launch_schedule_t<8>(a, smem, s);
-        default: return cudaErrorInvalidValue;
-    }
+    if (a.R * a.gamma > kClusterCtas * kCtaItems) return cudaErrorInvalidValue;
+    schedule_cluster_kernel<<<kClusterCtas, kSchedThreads, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_build_tags(int R, int gamma, const int32_t *ell, int32_t *tags, int32_t *N_out,
