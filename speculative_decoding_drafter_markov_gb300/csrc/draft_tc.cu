@@ -130,11 +130,6 @@ __device__ __forceinline__ void confidence_warp(const TcParams &p, int k, int gr
     }
 }
 
-// barrier of the 16 epilogue warps
-struct EpiSync {
-    __device__ void operator()() const { tc::named_bar_sync(1, tcp::kEpiThreads); }
-};
-
 __device__ __forceinline__ int ld_acquire(const int *ptr) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
