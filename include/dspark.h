@@ -30,7 +30,11 @@
  *   the outputs of the affected rows are then unspecified.
  * - Sampling is deterministic given (seed, cycle): Philox-4x32-10 with
  *   key = (seed lo, seed hi) and counter = (w0, w1, request, cycle << 2 | stream);
- *   stream 0 draft Gumbel noise (w0 = v / 4, w1 = step k, word v % 4),
+ *   stream 0 the draft draw (w0 = b / 2 for vocabulary block b of 16 entries,
+ *   w1 = step k; words 2 (b % 2) and 2 (b % 2) + 1 are block b's uniforms u_b
+ *   and u'_b): the block is argmax_b ln S_b - ln(-ln u_b) (S_b the block's sum
+ *   of exp(z), ties to the lowest b), the token the first entry of that block
+ *   whose running sum of exp(z) exceeds u'_b S_b,
  *   stream 1 acceptance uniforms (w0 = 0, w1 = position j, word 0),
  *   stream 2 the residual / bonus draw (w0 = 0, w1 = position, word 0): one
  *   uniform u per request, the token the first v whose cumulative weight

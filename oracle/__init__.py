@@ -54,9 +54,9 @@ def bind(L):
     L.oracle_uniform.restype = ctypes.c_double
     L.oracle_philox_word.argtypes = [u64, u32, u32, u32, u64, u32, u32]
     L.oracle_philox_word.restype = u32
-    L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 8
+    L.oracle_draft_markov.argtypes = [i32] * 6 + [P] * 7 + [u64, u64, P, i32] + [P] * 10
     L.oracle_draft_markov.restype = i32
-    L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 9
+    L.oracle_draft_rnn.argtypes = [i32] * 6 + [P] * 9 + [u64, u64, P, i32] + [P] * 11
     L.oracle_draft_rnn.restype = i32
     L.oracle_schedule.argtypes = [i32, i32, P, P, i32, i32, i32, i32, P, P, P, P]
     L.oracle_schedule.restype = i32
@@ -128,15 +128,17 @@ def draft_markov(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, reqs=
     n = R if rl is None else len(rl)
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
-    gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma))
-    runner = np.full((n, gamma), -1, np.int32)
+    gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma)); cdf_gap = np.zeros((n, gamma))
+    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_markov(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(w),
                                    _p(sts), _p(anchor), seed, cycle, _p(rl), n, _p(x), _p(logq),
-                                   _p(lse), _p(c), _p(gap), _p(runner), _p(z), _p(logit))
+                                   _p(lse), _p(c), _p(gap), _p(runner), _p(cdf_gap),
+                                   _p(cdf_runner), _p(z), _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_markov failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, conf_logit=logit)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, cdf_gap=cdf_gap,
+               cdf_runner=cdf_runner, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out
@@ -162,15 +164,17 @@ def draft_rnn(U, h, W1, W2t, W, w, anchor, *, s0=None, seed=0, cycle=0, sts_T=No
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
     gap = np.zeros((n, gamma)); A = np.zeros((n, gamma, r)); logit = np.zeros((n, gamma))
-    runner = np.full((n, gamma), -1, np.int32)
+    cdf_gap = np.zeros((n, gamma))
+    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_rnn(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(W),
                                 _p(s0a), _p(w), _p(sts), _p(anchor), seed, cycle, _p(rl), n,
-                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(runner), _p(z),
-                                _p(A), _p(logit))
+                                _p(x), _p(logq), _p(lse), _p(c), _p(gap), _p(runner),
+                                _p(cdf_gap), _p(cdf_runner), _p(z), _p(A), _p(logit))
     if rc != 0:
         raise ValueError(f"oracle_draft_rnn failed ({rc})")
-    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, A=A, conf_logit=logit)
+    out = dict(x=x, logq=logq, lse=lse, c=c, gap=gap, runner=runner, cdf_gap=cdf_gap,
+               cdf_runner=cdf_runner, A=A, conf_logit=logit)
     if want_z:
         out["z"] = z
     return out

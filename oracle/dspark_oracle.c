@@ -70,24 +70,74 @@ uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t re
     return out[lane];
 }
 
-/* Standard Gumbel variate g = -log(-log u) for vocab entry v. */
-static double gumbel(uint64_t seed, uint32_t step, uint32_t req, uint64_t cycle,
-                     uint32_t stream, int v) {
-    uint32_t word = oracle_philox_word(seed, (uint32_t)(v / 4), step, req, cycle, stream,
-                                       (uint32_t)(v % 4));
-    double u = oracle_uniform(word);
-    return -log(-log(u));
-}
-
 /* ------------------------------------------------------------------------ */
 /* [D] eq. (4): p_k(v) = exp(U_k(v) + B_k(v)) / sum_u exp(U_k(u) + B_k(u)).  */
-/* Sampling by the Gumbel-max rule: x_k = argmax_v (z_v + g_v), ties to the  */
-/* lowest v.  Writes lse, the sampled index, log q of it and the gap        */
-/* between the two best perturbed scores.                                   */
+/* The pages fix the distribution, not how it is sampled; x_k is drawn in   */
+/* two levels, which together pick v with probability exactly p_k(v):       */
+/*   blocks: the vocabulary in blocks of DRAFT_BLOCK consecutive entries    */
+/*     (the last one may be shorter); block b has mass                      */
+/*     S_b = sum_{v in b} exp(z_v - m) for a fixed m (here the max of z);   */
+/*   level 1: the block by the Gumbel-max rule over the blocks' masses,     */
+/*     b* = argmax_b ln S_b + g_b, g_b = -log(-log u_b), ties to the lowest */
+/*     b -- block b wins with probability S_b / sum_b S_b;                  */
+/*   level 2: the entry of b* by inverse CDF: the first v of the block whose */
+/*     running sum of exp(z - m), in index order from the block's start,    */
+/*     exceeds u'_{b*} S_{b*} -- v with probability exp(z_v - m) / S_{b*}.  */
+/* Random words (stream 0): block b uses the Philox counter                 */
+/* (floor(b / 2), k, request, cycle << 2 | 0), word 2 (b mod 2) for u_b and */
+/* word 2 (b mod 2) + 1 for u'_b.                                           */
 /* ------------------------------------------------------------------------ */
+#define DRAFT_BLOCK 16
+
+static void block_words(uint64_t seed, uint32_t step, uint32_t req, uint64_t cycle, int b,
+                        double *u_race, double *u_entry) {
+    uint32_t ctr[4] = {(uint32_t)(b / 2), step, req, (uint32_t)(cycle << 2)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    *u_race = oracle_uniform(out[2 * (b % 2)]);
+    *u_entry = oracle_uniform(out[2 * (b % 2) + 1]);
+}
+
+/* Level 2 inside block b: the entry; optionally how close the target came  */
+/* to the nearer end of that entry's interval (a fraction of S_b) and the   */
+/* entry across that end (-1: none).                                         */
+static int block_entry(const double *z, int V, double m, int b, double u_entry,
+                       double *margin, int *across) {
+    int v0 = b * DRAFT_BLOCK, v1 = v0 + DRAFT_BLOCK < V ? v0 + DRAFT_BLOCK : V;
+    double S = 0.0;
+    for (int v = v0; v < v1; ++v) S += exp(z[v] - m);
+    double target = u_entry * S, cum = 0.0;
+    int pick = -1;
+    double lo = 0.0, hi = 0.0;
+    for (int v = v0; v < v1; ++v) {
+        double e = exp(z[v] - m);
+        if (cum + e > target) {
+            pick = v;
+            lo = target - cum;
+            hi = cum + e - target;
+            break;
+        }
+        cum += e;
+    }
+    if (pick < 0) { /* rounding put the target at the total: the last entry of positive mass */
+        for (int v = v1 - 1; v >= v0 && pick < 0; --v)
+            if (exp(z[v] - m) > 0.0) pick = v;
+    }
+    if (margin) *margin = (lo < hi ? lo : hi) / S;
+    if (across) *across = lo <= hi ? (pick - 1 >= v0 ? pick - 1 : -1) : (pick + 1 < v1 ? pick + 1 : -1);
+    return pick;
+}
+
+/* Writes lse, the sampled index x, log q of it and two near-tie records:   */
+/* gap / runner -- the difference between the two best block scores and    */
+/* the token the runner-up block gives at level 2; cdf_gap / cdf_runner --  */
+/* the level-2 target's distance to the nearer end of x's interval (a       */
+/* fraction of S_{b*}) and the entry across that end.                       */
 static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, uint32_t req,
                         uint64_t cycle, int32_t *x_out, double *logq_out, double *lse_out,
-                        double *gap_out, int32_t *runner_out) {
+                        double *gap_out, int32_t *runner_out, double *cdf_gap_out,
+                        int32_t *cdf_runner_out) {
     double m = -INFINITY;
     for (int v = 0; v < V; ++v)
         if (z[v] > m) m = z[v];
@@ -95,25 +145,45 @@ static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, ui
     for (int v = 0; v < V; ++v) S += exp(z[v] - m);
     double lse = m + log(S);
 
+    int nb = (V + DRAFT_BLOCK - 1) / DRAFT_BLOCK;
     double best = -INFINITY, second = -INFINITY;
     int arg = -1, arg2 = -1;
-    for (int v = 0; v < V; ++v) {
-        double score = z[v] + gumbel(seed, step, req, cycle, 0, v);
+    double u_race, u_entry;
+    for (int b = 0; b < nb; ++b) {
+        int v0 = b * DRAFT_BLOCK, v1 = v0 + DRAFT_BLOCK < V ? v0 + DRAFT_BLOCK : V;
+        double Sb = 0.0;
+        for (int v = v0; v < v1; ++v) Sb += exp(z[v] - m);
+        if (!(Sb > 0.0)) continue;
+        block_words(seed, step, req, cycle, b, &u_race, &u_entry);
+        double score = log(Sb) - log(-log(u_race));
         if (score > best) {
             second = best;
             arg2 = arg;
             best = score;
-            arg = v;
+            arg = b;
         } else if (score > second) {
             second = score;
-            arg2 = v;
+            arg2 = b;
         }
     }
-    *x_out = arg;
-    *logq_out = z[arg] - lse;
+    double margin;
+    int across;
+    block_words(seed, step, req, cycle, arg, &u_race, &u_entry);
+    int v = block_entry(z, V, m, arg, u_entry, &margin, &across);
+    *x_out = v;
+    *logq_out = z[v] - lse;
     *lse_out = lse;
     if (gap_out) *gap_out = best - second;
-    if (runner_out) *runner_out = arg2;
+    if (runner_out) {
+        int other = -1;
+        if (arg2 >= 0) {
+            block_words(seed, step, req, cycle, arg2, &u_race, &u_entry);
+            other = block_entry(z, V, m, arg2, u_entry, NULL, NULL);
+        }
+        *runner_out = other;
+    }
+    if (cdf_gap_out) *cdf_gap_out = margin;
+    if (cdf_runner_out) *cdf_runner_out = across;
 }
 
 /* [D] eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]]); the optional per-step
@@ -137,7 +207,8 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        int32_t *runner, double *z_out, double *logit) {
+                        int32_t *runner, double *cdf_gap, int32_t *cdf_runner, double *z_out,
+                        double *logit) {
     int n = reqs ? n_reqs : R;
     double *e = (double *)malloc(sizeof(double) * (size_t)r);
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
@@ -160,7 +231,8 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
             }
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
-                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL);
+                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL,
+                        cdf_gap ? &cdf_gap[o] : NULL, cdf_runner ? &cdf_runner[o] : NULL);
             const void *h_k = dtype == ORACLE_F32
                                   ? (const void *)((const float *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d)
                                   : (const void *)((const uint16_t *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d);
@@ -188,8 +260,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, int32_t *runner, double *z_out,
-                     double *A_out, double *logit) {
+                     double *lse, double *c, double *gap, int32_t *runner, double *cdf_gap,
+                     int32_t *cdf_runner, double *z_out, double *A_out, double *logit) {
     int n = reqs ? n_reqs : R;
     int zlen = 2 * r + d;
     double *s = (double *)malloc(sizeof(double) * (size_t)r);
@@ -234,7 +306,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
             }
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
-                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL);
+                        gap ? &gap[o] : NULL, runner ? &runner[o] : NULL,
+                        cdf_gap ? &cdf_gap[o] : NULL, cdf_runner ? &cdf_runner[o] : NULL);
             /* eq. (7) reads the embedding W_1[x_{k-1}], i.e. the middle block of z_k */
             const void *h_k = dtype == ORACLE_F32 ? (const void *)((const float *)h + hrow)
                                                   : (const void *)((const uint16_t *)h + hrow);

@@ -20,10 +20,12 @@
  * published definition.  Counter layout (a reading; the pages name no RNG):
  *   key     = (seed low 32 bits, seed high 32 bits)
  *   counter = (word0, word1, request, (cycle << 2) | stream)
- *   stream 0: draft Gumbel noise      word0 = v / 4, word1 = step k (1..gamma),
- *                                     output word v % 4 belongs to vocab entry v
+ *   stream 0: draft draw              word0 = b / 2 for vocabulary block b (16
+ *                                     entries), word1 = step k (1..gamma); words
+ *                                     2 (b % 2) and 2 (b % 2) + 1 are block b's
+ *                                     race and entry uniforms
  *   stream 1: acceptance uniforms     word0 = 0, word1 = row position j, word 0
- *   stream 2: residual / bonus Gumbel word0 = v / 4, word1 = row position
+ *   stream 2: residual / bonus draw   word0 = 0, word1 = row position, word 0
  *   stream 3: reserved for synthetic-input noise
  * Word to uniform: u = ((w >> 9) + 0.5) * 2^-23, strictly inside (0, 1).
  *
@@ -58,17 +60,22 @@ uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t re
  * position in that list.  Optional outputs may be NULL.
  *   U [R, gamma, V], h [R, gamma, d], W1 [V, r], W2t [V, r] (row v = column v
  *   of W_2), w [d + r] f32, sts_T [gamma] f32 or NULL, anchor [R].
- * Outputs: x [n, gamma], logq, lse, c [n, gamma], gap [n, gamma] = gap
- * between the two largest Gumbel-perturbed scores, runner [n, gamma] = the
- * index of the second largest (the token a near tie could swap in),
- * z [n, gamma, V] logits,
+ * x_k is drawn in two levels (16-entry vocabulary blocks by the Gumbel-max
+ * rule over their masses, then the entry of the winning block by inverse CDF).
+ * Outputs: x [n, gamma], logq, lse, c [n, gamma]; the near-tie records
+ * gap [n, gamma] = difference between the two best block scores, runner
+ * [n, gamma] = the token the runner-up block gives, cdf_gap [n, gamma] =
+ * distance of the entry draw's target to the nearer end of x's interval (a
+ * fraction of the block's mass), cdf_runner [n, gamma] = the entry across that
+ * end (-1: none); z [n, gamma, V] logits,
  * logit [n, gamma] = w^T [h_k ; W_1[x_{k-1}]] (the confidence logit). */
 int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const void *U, const void *h, const void *W1, const void *W2t,
                         const float *w, const float *sts_T, const int32_t *anchor,
                         uint64_t seed, uint64_t cycle, const int32_t *reqs, int n_reqs,
                         int32_t *x, double *logq, double *lse, double *c, double *gap,
-                        int32_t *runner, double *z, double *logit);
+                        int32_t *runner, double *cdf_gap, int32_t *cdf_runner, double *z,
+                        double *logit);
 
 /* RNN-head draft (eq. 6).  W [3r, 2r + d]: rows [0, r) gate, [r, 2r) candidate,
  * [2r, 3r) output.  s0 [R, r] f32 or NULL (zero).  Extra output: A [n, gamma, r],
@@ -78,8 +85,8 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
                      const void *W, const float *s0, const float *w, const float *sts_T,
                      const int32_t *anchor, uint64_t seed, uint64_t cycle,
                      const int32_t *reqs, int n_reqs, int32_t *x, double *logq,
-                     double *lse, double *c, double *gap, int32_t *runner, double *z,
-                     double *A, double *logit);
+                     double *lse, double *c, double *gap, int32_t *runner, double *cdf_gap,
+                     int32_t *cdf_runner, double *z, double *A, double *logit);
 
 /* Hardware-aware prefix scheduler (Module E, Algorithm 1; production async
  * variant).  c [R, gamma] f32; sps[i] = SPS(B_min + i) for i < B_count.

@@ -3,11 +3,18 @@
 Tolerances (absolute): log q, log p, confidences and confidence logits 1e-4;
 log-sum-exp 1e-3.
 Integer results (tokens, verify lengths, accepted counts) must match exactly,
-except a sampled token may differ where the oracle's two best Gumbel-perturbed
-scores are closer than 1e-3, and an acceptance decision may differ where the
-oracle's margin (log p - log q) - log u is below 1e-4 in magnitude.  A flipped
-sampled token must be exactly the oracle's runner-up (the index with the second
-largest perturbed score).  Such "flips" end the comparison of that request,
+except at a near tie of the oracle:
+- a drafted token is drawn in two levels (a Gumbel-max race over 16-entry
+  vocabulary blocks, then the entry of the winning block by inverse CDF); it may
+  differ where the oracle's two best block scores are closer than 1e-3 -- and
+  must then be the token the runner-up block gives -- or where the entry draw's
+  target lies within 1e-4 of the block's mass from an end of the drawn entry's
+  interval -- and must then be the entry across that end;
+- an acceptance decision may differ where the oracle's margin
+  (log p - log q) - log u is below 1e-4 in magnitude;
+- a correction or bonus token may differ where its inverse-CDF target lies
+  within 1e-4 of the total weight from a CDF boundary (the entry across it).
+Such "flips" end the comparison of that request,
 whose later steps legitimately diverge, and are counted: per comparison they
 must stay below 0.1 % of the compared tokens (at least one is allowed in a
 small case), and LEDGER sums them over the whole test session, where the total
@@ -52,6 +59,14 @@ def record(flips, compared):
     LEDGER["comparisons"] += 1
 
 
+def draft_near_tie(token, ref, t, k):
+    """True when `token` is what the oracle's draw of (t, k) gives after a near tie:
+    the runner-up block's token at a block-score gap below GAP_TOL, or the entry
+    across the nearer end of the drawn entry's interval at a margin below CDF_TOL."""
+    return ((ref["gap"][t, k] < GAP_TOL and token == ref["runner"][t, k]) or
+            (ref["cdf_gap"][t, k] < CDF_TOL and token == ref["cdf_runner"][t, k]))
+
+
 def compare_draft(gpu, ref, reqs, gamma):
     """gpu: dict of [R, gamma] host arrays; ref: oracle output for `reqs`."""
     flips, compared = 0, 0
@@ -64,12 +79,11 @@ def compare_draft(gpu, ref, reqs, gamma):
                 assert abs(gpu["conf_logit"][rq, k] - ref["conf_logit"][t, k]) <= TOL_LOGIT, (rq, k)
             compared += 1
             if gpu["x"][rq, k] != ref["x"][t, k]:
-                assert ref["gap"][t, k] < GAP_TOL, (
+                assert draft_near_tie(gpu["x"][rq, k], ref, t, k), (
                     f"token mismatch at request {rq} step {k + 1}: gpu {gpu['x'][rq, k]} "
-                    f"oracle {ref['x'][t, k]} with score gap {ref['gap'][t, k]}")
-                assert gpu["x"][rq, k] == ref["runner"][t, k], (
-                    f"near-tie flip at request {rq} step {k + 1} to {gpu['x'][rq, k]}, "
-                    f"not the oracle's runner-up {ref['runner'][t, k]}")
+                    f"oracle {ref['x'][t, k]}; block score gap {ref['gap'][t, k]} "
+                    f"(runner-up block's token {ref['runner'][t, k]}), entry CDF margin "
+                    f"{ref['cdf_gap'][t, k]} (entry across it {ref['cdf_runner'][t, k]})")
                 flips += 1
                 break
             assert abs(gpu["logq"][rq, k] - ref["logq"][t, k]) <= TOL_LOGQ, (rq, k)

@@ -23,7 +23,8 @@ anchors.  Every cycle compares the stages request by request:
 - verification: accepted counts and emitted tokens exactly, per-row log p and
   log-sum-exp within tolerance.
 
-A near tie (a draft token whose oracle score gap is below 1e-3, a correction or
+A near tie (a draft token whose oracle block-score gap is below 1e-3 or whose
+entry draw lies within 1e-4 of the block's mass from a CDF boundary, a correction or
 bonus token whose inverse-CDF target lies within 1e-4 of the total weight from
 a CDF boundary, an acceptance decision whose oracle margin is below 1e-4) is a
 counted flip.  A

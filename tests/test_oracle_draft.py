@@ -5,7 +5,13 @@
   transposed operand fails.
 * eq. (4): lse equals scipy's logsumexp of the logits; exp(log q) is the softmax
   probability of the sampled token.
-* Gumbel-max sampling: 10^6 sampled tokens follow softmax(U + B) (chi-square).
+* Sampling (a two-level draw: 16-entry vocabulary blocks by the Gumbel-max rule
+  over their masses, then the entry inside the winning block by inverse CDF):
+  10^6 sampled tokens follow softmax(U + B) (chi-square) on a vocabulary with
+  a short last block; with equal logits the draw reduces to a closed form in
+  the Philox words (the block with the largest race uniform, entry
+  floor(16 u')); the near-tie records follow from the block scores and the
+  cumulative sums, recomputed here from the words.
 * eq. (7): closed-form special cases (w = 0 gives 1/2; a weight vector that only
   sees the embedding part reads W_1[x_{k-1}], not W_1[x_k]; temperature divides
   the logit).
@@ -51,12 +57,11 @@ def test_lse_and_logq(orc):
     assert np.all(out["gap"] > 0)
 
 
-def test_gumbel_max_frequencies_match_softmax(orc):
-    # 1000 identical requests x 1000 cycles = 10^6 draws of x_1
-    R, V, r, d, cycles = 1000, 8, 4, 4, 1000
+def _chi_square_draws(orc, V, Urow, cycles=1000, R=1000, seed=1234):
+    """10^6 draws of x_1 (R identical requests x `cycles` cycles) against softmax."""
+    r, d = 4, 4
     rng = np.random.default_rng(11)
-    Urow = rng.standard_normal(V).astype(np.float32)
-    U = np.broadcast_to(Urow, (R, 1, V)).copy()
+    U = np.broadcast_to(Urow.astype(np.float32), (R, 1, V)).copy()
     W1 = (rng.standard_normal((V, r)) * 0.5).astype(np.float32)
     W2t = (rng.standard_normal((V, r)) * 0.5).astype(np.float32)
     h = np.zeros((R, 1, d), np.float32)
@@ -65,13 +70,43 @@ def test_gumbel_max_frequencies_match_softmax(orc):
     counts = np.zeros(V, np.int64)
     z = None
     for cyc in range(cycles):
-        out = orc.draft_markov(U, h, W1, W2t, w, anchor, seed=1234, cycle=cyc, want_z=(cyc == 0))
+        out = orc.draft_markov(U, h, W1, W2t, w, anchor, seed=seed, cycle=cyc, want_z=(cyc == 0))
         if z is None:
             z = out["z"][0, 0]
         counts += np.bincount(out["x"][:, 0], minlength=V)
     p = special.softmax(z)
-    res = stats.chisquare(counts, p * counts.sum())
-    assert res.pvalue > 1e-4, (counts, p)
+    return stats.chisquare(counts, p * counts.sum()).pvalue, counts, p
+
+
+def test_sampled_frequencies_match_softmax(orc):
+    # V = 40: blocks of 16, 16 and 8 entries; the logits give the blocks very
+    # different masses and spread each block's mass unevenly over its entries
+    V = 40
+    Urow = np.random.default_rng(5).standard_normal(V) * 1.5
+    Urow[16:32] -= 2.0
+    pval, counts, p = _chi_square_draws(orc, V, Urow)
+    assert pval > 1e-4, (counts, p)
+
+
+def test_equal_logits_reduce_to_the_words(orc):
+    """With every logit equal each block of 16 has the same mass, so level 1 picks
+    the block with the largest race uniform and level 2 the entry floor(16 u')."""
+    R, gamma, V, r, d = 3, 4, 64, 4, 2
+    U = np.zeros((R, gamma, V), np.float32)
+    W1 = np.zeros((V, r), np.float32)
+    W2t = np.zeros((V, r), np.float32)
+    h = np.zeros((R, gamma, d), np.float32)
+    w = np.zeros(d + r, np.float32)
+    anchor = np.arange(R, dtype=np.int32)
+    seed, cycle = 99, 7
+    out = orc.draft_markov(U, h, W1, W2t, w, anchor, seed=seed, cycle=cycle)
+    for rq in range(R):
+        for k in range(gamma):
+            u = [orc.uniform(orc.philox_word(seed, b // 2, k + 1, rq, cycle, 0, 2 * (b % 2))) for b in range(4)]
+            b = int(np.argmax(u))
+            ue = orc.uniform(orc.philox_word(seed, b // 2, k + 1, rq, cycle, 0, 2 * (b % 2) + 1))
+            assert out["x"][rq, k] == 16 * b + int(np.floor(16 * ue)), (rq, k)
+            assert out["logq"][rq, k] == pytest.approx(-np.log(V), abs=1e-12)
 
 
 def test_confidence_closed_forms(orc):
@@ -127,20 +162,40 @@ def test_bad_anchor_rejected(orc):
         orc.draft_markov(U, h, W1, W2t, w, anchor)
 
 
-def test_sample_gap_and_runner_up_by_brute_force(orc):
-    """The reported token is the argmax of z + g, the runner-up the second place and
-    the gap their difference, with g = -log(-log u) of the stream-0 Philox words
-    recomputed here word by word."""
+def test_sample_and_near_tie_records_by_brute_force(orc):
+    """The reported token, the block-score gap and the runner-up block's token, and
+    the entry draw's CDF margin and the entry across it, recomputed from the
+    stream-0 Philox words: block b (16 entries, the last one 8 here) takes words
+    2 (b mod 2) and 2 (b mod 2) + 1 of counter (b / 2, k, request, cycle)."""
     R, gamma, V, r, d = 2, 3, 40, 4, 2
     U, h, W1, W2t, w, anchor = _inputs(R, gamma, V, r, d, seed=4, scale=1.0)
     seed, cycle = 77, 5
     out = orc.draft_markov(U, h, W1, W2t, w, anchor, seed=seed, cycle=cycle, want_z=True)
+    blocks = [(0, 16), (16, 32), (32, 40)]
+
+    def word(b, k, rq, lane):
+        return orc.uniform(orc.philox_word(seed, b // 2, k + 1, rq, cycle, 0, 2 * (b % 2) + lane))
+
+    def entry(e, lo, u):
+        cum = np.cumsum(e[lo:])
+        target = u * cum[-1]
+        j = int(np.argmax(cum > target))
+        below = cum[j - 1] if j > 0 else 0.0
+        return lo + j, target - below, cum[j] - target, cum[-1]
+
     for rq in range(R):
         for k in range(gamma):
-            g = np.array([-np.log(-np.log(orc.uniform(orc.philox_word(seed, v // 4, k + 1, rq, cycle, 0, v % 4))))
-                          for v in range(V)])
-            score = out["z"][rq, k] + g
+            z = out["z"][rq, k]
+            e = np.exp(z - z.max())
+            score = np.array([np.log(e[a:b].sum()) - np.log(-np.log(word(i, k, rq, 0)))
+                              for i, (a, b) in enumerate(blocks)])
             order = np.argsort(-score, kind="stable")
-            assert out["x"][rq, k] == order[0]
-            assert out["runner"][rq, k] == order[1]
-            assert out["gap"][rq, k] == pytest.approx(score[order[0]] - score[order[1]], abs=1e-12)
+            b0, b1 = order[0], order[1]
+            x, lo, hi, S = entry(e[:blocks[b0][1]], blocks[b0][0], word(b0, k, rq, 1))
+            assert out["x"][rq, k] == x
+            assert out["gap"][rq, k] == pytest.approx(score[b0] - score[b1], abs=1e-12)
+            assert out["runner"][rq, k] == entry(e[:blocks[b1][1]], blocks[b1][0], word(b1, k, rq, 1))[0]
+            assert out["cdf_gap"][rq, k] == pytest.approx(min(lo, hi) / S, abs=1e-12)
+            first, last = blocks[b0][0], blocks[b0][1] - 1
+            expect = (x - 1 if x > first else -1) if lo <= hi else (x + 1 if x < last else -1)
+            assert out["cdf_runner"][rq, k] == expect
