@@ -329,27 +329,6 @@ def ncu_traffic(kernel, workload):
     return None, "no ncu capture at this workload"
 
 
-# Philox-4x32-10 throughput of this GPU's integer-multiply pipe: 20 32x32->64
-# multiplies (two 32-bit multiply slots each) per call of 4 words; a standalone
-# microbenchmark measured 518 G calls/s over 152 SMs (taken here as 2070 MHz, the
-# maximum clock; the clock was not sampled), 1.65 calls per SM per clock, the rate
-# of 64 multiply slots per SM per clock.
-PHILOX_CALLS_PER_SM_CLK = 518e9 / (152 * 2070e6)
-
-
-def philox_roofline(wl, draft_us, clk):
-    """The draft's plain-ALU floor: one Philox word per (request, step, vocabulary
-    entry), so R gamma V / 4 calls per cycle, against the multiply pipe's rate."""
-    calls = wl.R * wl.gamma * wl.V / 4
-    sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
-    peak = sm * PHILOX_CALLS_PER_SM_CLK * mhz * 1e6 / 1e9
-    achieved = calls / (draft_us * 1e-6) / 1e9
-    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "G Philox calls/s",
-            "frac": achieved / peak, "calls_per_launch": calls,
-            "peak_kind": f"{sm} SMs x {PHILOX_CALLS_PER_SM_CLK:.2f} calls per clock (measured) x {mhz:.0f} MHz"}
-
-
 def draft_step_bytes(wl, with_w2=True):
     """Algorithmic bytes of one draft step: U_k rows, W_2 streamed once, the
     gathered W_1 rows, h_k and w (fp32)."""
@@ -534,7 +513,6 @@ def run_dspark(args, world, rank, local):
         "roofline_w2_once_per_cycle": {"achieved": strict, "peak": hbm, "unit": "GB/s",
                                        "frac": strict / hbm,
                                        "algorithmic_bytes_per_launch": draft_cycle_bytes_strict(wl)},
-        "roofline_philox": philox_roofline(wl, draft_us, clk),
         "roofline_verify": _verify_roofline(wl, verified, rejected, args.steps, t_verify, hbm),
         "gpu_launches": args.steps * cyc.launches_per_cycle,
         "clocks": clk,

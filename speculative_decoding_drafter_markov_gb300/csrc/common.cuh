@@ -1,10 +1,12 @@
 // common.cuh -- device building blocks shared by the DSpark kernels.
 //
 // * Philox-4x32-10 (Salmon et al., SC'11) and the word -> uniform map.
-// * The running state of one row's fused epilogue: online max / sum-exp for the
-//   exact softmax normaliser of eq. (4) of the DSpark digest, and the Gumbel-max
-//   sample taken in "exponential race" form, argmax_v z_v - ln E_v with
-//   E_v = -ln u_v, which equals argmax_v z_v - ln(-ln u_v).
+// * The running state of one row's fused epilogue: the sum of exponentials for
+//   the exact softmax normaliser of eq. (4) of the DSpark digest, and its
+//   two-level draw: 16-entry vocabulary blocks raced by the Gumbel-max rule on
+//   their masses in "exponential race" form, argmax_b ln S_b - ln E_b with
+//   E_b = -ln u_b (which equals argmax_b ln S_b - ln(-ln u_b)), then the
+//   winning block's entry by inverse CDF.
 // * Error reporting into the caller's device error word.
 #pragma once
 
@@ -18,9 +20,6 @@ namespace dspark {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// multiplicative slack of the race pre-filter (far above the few-ulp error of
-// the fp32 products it guards)
-constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
 
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ void set_err(int32_t *err, int code) {
@@ -193,19 +192,18 @@ __device__ __forceinline__ float log_exp_variate(float t) {
 }
 
 // ---------------------------------------------------------------- epilogue state
-// One row's running fused-epilogue state.  `C` caches exp(m - best) * slack so
-// the race pre-filter costs one multiply and one compare per element: element v
-// can only beat `best` if E_v < exp(z_v - best), and E_v >= t_v = 1 - u_v, so it
-// is skipped whenever t_v >= exp(z_v - m) * C.
+// One row's running fused-epilogue state: the sum of exponentials for the
+// exact normaliser of eq. (4), and the two-level draw of x_k -- vocabulary
+// blocks of 16 entries raced by the Gumbel-max rule on their masses
+// (score ln S_b - ln E_b, E_b = -ln u_b), the winning block's entry drawn by
+// inverse CDF with its second uniform.
 struct RowState {
     float m;      // reference of the sum (the max of z, or below it; exp(z - m) stays finite)
     float mL;     // m * log2(e)
     float S;      // sum exp(z - m)
-    float best;   // best race score z - ln E of this thread's elements
-    float zbest;  // z of the best element
+    float best;   // best block score of this thread's blocks
+    float zbest;  // z of the entry drawn in that block
     int idx;      // its vocabulary index (-1: none yet)
-    float thr;    // filter threshold: a score some element of the row reached (>= best)
-    float C;      // exp(m - thr) * slack
 };
 
 __device__ __forceinline__ void row_init(RowState &s) {
@@ -215,73 +213,13 @@ __device__ __forceinline__ void row_init(RowState &s) {
     s.best = -INFINITY;
     s.zbest = 0.f;
     s.idx = -1;
-    s.thr = -INFINITY;
-    s.C = INFINITY;
 }
 
-__device__ __forceinline__ void row_refresh_C(RowState &s) {
-    s.C = ex2((s.m - s.thr) * kLog2e) * kRaceSlack;
-}
-
-// Raise the filter threshold to a score reached elsewhere in the same row (an
-// element below it cannot be the row's winner).
-__device__ __forceinline__ void row_raise_thr(RowState &s, float thr) {
-    if (thr > s.thr) {
-        s.thr = thr;
-        row_refresh_C(s);
-    }
-}
-
-// Feed four consecutive vocabulary entries v0..v0+3 (one Philox call).
-// kFull: all four are below V; otherwise entries at or beyond V are ignored.
-template <bool kFull = false>
-__device__ __forceinline__ void row_feed4(RowState &s, const float z[4], int v0, int V,
-                                          const uint4 &words) {
-    float zmax;
-    if (kFull) {
-        zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-    } else {
-        zmax = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (v0 + j < V) zmax = fmaxf(zmax, z[j]);
-    }
-    if (zmax > s.m) {
-        s.S *= ex2((s.m - zmax) * kLog2e);
-        s.m = zmax;
-        s.mL = zmax * kLog2e;
-        row_refresh_C(s);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (!kFull && v0 + j >= V) continue;
-        const float e = ex2(fmaf(z[j], kLog2e, -s.mL));
-        s.S += e;
-        const float t = one_minus_uniform(word_lane(words, j));
-        if (!(t >= e * s.C)) {
-            const float score = z[j] - log_exp_variate(t);
-            if (score > s.best) {
-                s.best = score;
-                s.idx = v0 + j;
-                s.zbest = z[j];
-                row_raise_thr(s, score);
-            }
-        }
-    }
-}
-
-// Feed 16 consecutive vocabulary entries v0..v0+15 of one row (all below V;
-// words[j] the Philox word of entry v0 + j).  All 32 lanes of the warp call it
-// together, each with its own row.
-//
 // The sum of exponentials runs against a reference m that only has to keep
 // the terms finite: it is the first block's maximum and moves up only when a
 // block's sum leaves [0, 2^64] (a term far above m, or a non-finite logit), so
 // a block needs no max and no rescale.  Any reference gives the same
-// lse = m + ln S.  The race filter keeps element j when e_j C > t_j
-// (e_j C = exp(z_j - thr) slack); a block whose 16 differences are all
-// negative -- one AND of their sign bits -- skips the exact scoring, and the
-// exact scoring of a column runs only when some lane of the warp kept it.
+// lse = m + ln S and the same block scores m + ln S_b.
 __device__ __forceinline__ void row_set_reference(RowState &s, const float (&z)[16]) {
     float mx[16];
 #pragma unroll
@@ -294,69 +232,84 @@ __device__ __forceinline__ void row_set_reference(RowState &s, const float (&z)[
     s.S = M == -INFINITY ? 0.f : s.S * ex2((s.m - M) * kLog2e);
     s.m = M;
     s.mL = M * kLog2e;
-    row_refresh_C(s);
 }
 
-__device__ __forceinline__ float block_exp_sum(const RowState &s, const float (&z)[16], float (&e)[16]) {
-    // arguments z log2(e) - m log2(e) two at a time; the pairwise sum tree adds
-    // j and j + 8, then j + 4, j + 2, j + 1, the same order as a scalar tree
+// The block's terms e_j = exp(z_j - m) and their sums over aligned runs of 2,
+// 4 and 8 entries (pr[i] = e_2i + e_2i+1, qd[i] = pr[2i] + pr[2i+1],
+// oc[i] = qd[2i] + qd[2i+1]); returns oc[0] + oc[1].  Arguments and sums two at
+// a time (each lane rounds like the scalar operation).
+__device__ __forceinline__ float block_exp_sums(const RowState &s, const float (&z)[16], float (&e)[16],
+                                                float (&pr)[8], float (&qd)[4], float (&oc)[2]) {
     const float2 L = make_float2(kLog2e, kLog2e), nm = make_float2(-s.mL, -s.mL);
-    float2 sum[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float2 arg = fma2(make_float2(z[2 * i], z[2 * i + 1]), L, nm);
         e[2 * i] = ex2(arg.x);
         e[2 * i + 1] = ex2(arg.y);
-        sum[i] = make_float2(e[2 * i], e[2 * i + 1]);
     }
 #pragma unroll
-    for (int w = 4; w > 0; w >>= 1)
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = add2(make_float2(e[4 * i], e[4 * i + 2]), make_float2(e[4 * i + 1], e[4 * i + 3]));
+        pr[2 * i] = t.x;
+        pr[2 * i + 1] = t.y;
+    }
 #pragma unroll
-        for (int i = 0; i < w; ++i) sum[i] = add2(sum[i], sum[i + w]);
-    return sum[0].x + sum[0].y;
+    for (int i = 0; i < 2; ++i) {
+        const float2 t = add2(make_float2(pr[4 * i], pr[4 * i + 2]), make_float2(pr[4 * i + 1], pr[4 * i + 3]));
+        qd[2 * i] = t.x;
+        qd[2 * i + 1] = t.y;
+    }
+    const float2 t = add2(make_float2(qd[0], qd[2]), make_float2(qd[1], qd[3]));
+    oc[0] = t.x;
+    oc[1] = t.y;
+    return oc[0] + oc[1];
 }
 
-__device__ __forceinline__ void row_feed16(RowState &s, const float (&z)[16], int v0, const uint32_t (&words)[16]) {
-    if (s.m == -INFINITY) row_set_reference(s, z);  // the row's first block in this thread
-    float e[16];
-    float sum = block_exp_sum(s, z, e);
-    if (!(sum <= 18446744073709551616.f)) {  // 2^64: move the reference up to this block's maximum
-        row_set_reference(s, z);
-        sum = block_exp_sum(s, z, e);
+template <int N>
+__device__ __forceinline__ float select_of(const float (&v)[N], int i) {
+    // v[i] by a tree of selects on the bits of i (registers only)
+    float w[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) w[j] = v[j];
+#pragma unroll
+    for (int h = N / 2, bit = N / 2; h > 0; h >>= 1, bit >>= 1)
+#pragma unroll
+        for (int j = 0; j < h; ++j) w[j] = (i & bit) ? w[j + h] : w[j];
+    return w[0];
+}
+
+// Level 2 of the draw inside one block: the first entry whose running sum of
+// e exceeds the target t = u' S_b, found by descending the aligned sums (go to
+// the right half when t reaches the left half's sum, less that sum).  A half
+// of zero mass is never entered, so the entry has e_j > 0 whatever the
+// roundings.  Returns j in 0..15.
+__device__ __forceinline__ int block_entry(float t, const float (&e)[16], const float (&pr)[8],
+                                           const float (&qd)[4], const float (&oc)[2]) {
+    const bool r1 = t >= oc[0] && oc[1] > 0.f;
+    t = r1 ? t - oc[0] : t;
+    const float qL = r1 ? qd[2] : qd[0], qR = r1 ? qd[3] : qd[1];
+    const bool r2 = t >= qL && qR > 0.f;
+    t = r2 ? t - qL : t;
+    const int qi = (r1 ? 2 : 0) | (r2 ? 1 : 0);
+    float pl[4], pg[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        pl[i] = pr[2 * i];
+        pg[i] = pr[2 * i + 1];
     }
-    s.S += sum;
-    // race filter: d_j = e_j C - t_j (C capped so that e_j = 0 gives d_j = -t_j);
-    // -t_j = (1 - 2^-24) - (1 + k' 2^-23) exactly (see one_minus_uniform)
-    const float Cc = fminf(s.C, 3.0e38f);
-    const float2 C2 = make_float2(Cc, Cc), c0 = make_float2(1.0f - 1.0f / 16777216.0f, 1.0f - 1.0f / 16777216.0f);
-    float d[16];
-    uint32_t allneg = 0xFFFFFFFFu;
+    const float pL = select_of(pl, qi), pR = select_of(pg, qi);
+    const bool r3 = t >= pL && pR > 0.f;
+    t = r3 ? t - pL : t;
+    const int pi = 2 * qi + (r3 ? 1 : 0);
+    float el[8], eg[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float2 one_t = make_float2(__uint_as_float(((~words[2 * i]) >> 9) | 0x3F800000u),
-                                         __uint_as_float(((~words[2 * i + 1]) >> 9) | 0x3F800000u));
-        const float2 dd = fma2(make_float2(e[2 * i], e[2 * i + 1]), C2, sub2(c0, one_t));
-        d[2 * i] = dd.x;
-        d[2 * i + 1] = dd.y;
-        allneg &= __float_as_uint(dd.x) & __float_as_uint(dd.y);
+        el[i] = e[2 * i];
+        eg[i] = e[2 * i + 1];
     }
-    if (__any_sync(0xffffffffu, (int)allneg >= 0)) {
-        const float best0 = s.best;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (__any_sync(0xffffffffu, d[j] > 0.f)) {
-                if (d[j] > 0.f) {
-                    const float score = z[j] - log_exp_variate(one_minus_uniform(words[j]));
-                    if (score > s.best) {
-                        s.best = score;
-                        s.idx = v0 + j;
-                        s.zbest = z[j];
-                    }
-                }
-            }
-        }
-        if (s.best > best0) row_raise_thr(s, s.best);
-    }
+    const float eL = select_of(el, pi), eR = select_of(eg, pi);
+    const bool r4 = t >= eL && eR > 0.f;
+    return 2 * pi + (r4 ? 1 : 0);
 }
 
 // A race winner as one 64-bit word whose unsigned order is the merge order
@@ -367,6 +320,34 @@ __device__ __forceinline__ unsigned long long pack_winner(float best, int idx) {
     const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
     return ((unsigned long long)ob << 32) | (uint32_t)~(uint32_t)idx;
 }
+
+// Feed one block of 16 consecutive vocabulary entries vb .. vb + 15 of a row
+// (vb a multiple of 16; entries at or beyond V carry z = -inf) with the
+// block's race word wr and entry word we.  The block's terms join the sum of
+// exponentials; its race score is formed and, when it beats `thr` (a packed
+// winner of the same row: this thread's best or a better one found elsewhere;
+// a block below it cannot win the row), the entry is drawn and the block
+// becomes this thread's best.  Returns whether it did.
+__device__ __forceinline__ bool block_feed16(RowState &s, const float (&z)[16], int vb, uint32_t wr, uint32_t we,
+                                             unsigned long long thr) {
+    if (s.m == -INFINITY) row_set_reference(s, z);  // the row's first block in this thread
+    float e[16], pr[8], qd[4], oc[2];
+    float S = block_exp_sums(s, z, e, pr, qd, oc);
+    if (!(S <= 18446744073709551616.f)) {  // 2^64: move the reference up to this block's maximum
+        row_set_reference(s, z);
+        S = block_exp_sums(s, z, e, pr, qd, oc);
+    }
+    s.S += S;
+    if (!(S > 0.f)) return false;  // no mass at this reference (entries beyond V, or far below m)
+    const float score = s.m + kLn2 * lg2(S) - log_exp_variate(one_minus_uniform(wr));
+    if (pack_winner(score, vb) <= thr) return false;
+    const int j = block_entry(uniform_of(we) * S, e, pr, qd, oc);
+    s.best = score;
+    s.idx = vb + j;
+    s.zbest = select_of(z, j);
+    return true;
+}
+
 __device__ __forceinline__ int winner_index(unsigned long long w) { return (int)~(uint32_t)w; }
 __device__ __forceinline__ float winner_score(unsigned long long w) {
     if (w == 0ull) return -INFINITY;
@@ -415,62 +396,5 @@ __device__ __forceinline__ DraftPartial load_partial_cg(const DraftPartial *q) {
 struct VerifyPartial {
     float sum_res, sum_p;
 };
-
-// Race over weights w_v in (0, 1]: score ln w_v - ln E_v; the filter skips v
-// when t_v >= w_v * C with C = exp(-best) * slack.
-struct Race {
-    float best;
-    int idx;
-    float C;
-};
-
-__device__ __forceinline__ void race_init(Race &r) {
-    r.best = -INFINITY;
-    r.idx = -1;
-    r.C = INFINITY;
-}
-
-__device__ __forceinline__ void race_feed(Race &r, float w, float t, int v) {
-    if (!(w > 0.f)) return;
-    if (t >= w * r.C) return;
-    const float score = kLn2 * lg2(w) - log_exp_variate(t);
-    if (score > r.best) {
-        r.best = score;
-        r.idx = v;
-        r.C = ex2(-r.best * kLog2e) * kRaceSlack;
-    }
-}
-
-// Four consecutive entries v0..v0+3 of one race (weights w[i] >= 0, words
-// from one Philox call): the filter for all four first, then the rare
-// survivors scored exactly in index order.
-__device__ __forceinline__ void race_feed4(Race &r, const float (&w)[4], const uint4 &words, int v0) {
-    unsigned pass = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float t = one_minus_uniform(word_lane(words, i));
-        if (w[i] > 0.f && t < w[i] * r.C) pass |= 1u << i;
-    }
-    if (pass) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (pass & (1u << i)) {
-                const float score = kLn2 * lg2(w[i]) - log_exp_variate(one_minus_uniform(word_lane(words, i)));
-                if (score > r.best) {
-                    r.best = score;
-                    r.idx = v0 + i;
-                    r.C = ex2(-r.best * kLog2e) * kRaceSlack;
-                }
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void race_merge(float &best, int &idx, float b2, int i2) {
-    if (i2 >= 0 && (idx < 0 || b2 > best || (b2 == best && i2 < idx))) {
-        best = b2;
-        idx = i2;
-    }
-}
 
 }  // namespace dspark

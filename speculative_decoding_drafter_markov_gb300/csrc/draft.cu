@@ -8,9 +8,10 @@
 //   draft_step_simt  vocabulary-sliced: each CTA owns 64 vocabulary entries,
 //                    keeps that slice of W_2 in shared memory, and for every
 //                    request contracts the bias operand with it, adds U_k and
-//                    folds the result into an online max / sum-exp and a
-//                    Gumbel race.  Output: one partial per (request, slice); no
-//                    logit ever reaches global memory.
+//                    folds the result into the sum of exponentials and the
+//                    two-level draw (its 16-entry blocks raced on their masses,
+//                    the entry of a block by inverse CDF).  Output: one partial
+//                    per (request, slice); no logit ever reaches global memory.
 //   draft_reduce     one CTA per request merges its partials in a fixed order
 //                    (deterministic), writes x_k, log q_k(x_k), lse_k and the
 //                    confidence c_k.
@@ -80,17 +81,57 @@ __global__ void __launch_bounds__(kThreads) draft_step_simt(const DraftStep p) {
             acc[2] = fmaf(ev, w0[2 * ld + i], acc[2]);
             acc[3] = fmaf(ev, w0[3 * ld + i], acc[3]);
         }
+        // Four lanes (quads 4i .. 4i + 3) hold vocabulary block b = v0 / 16 of this
+        // request: the block's maximum and quad sums by shuffles, the same block
+        // sum and race score in each of the four, then level 2 of the draw from
+        // the block's aligned sums; the lane whose quad holds the drawn entry
+        // keeps the block as its candidate.  Entries at or beyond V carry
+        // z = -inf (weight 0); a block wholly beyond V has no mass.
         RowState st;
         row_init(st);
-        if (row < p.R && v0 < p.V) {
-            const T *Urow = U + ((size_t)row * p.gamma + (p.k - 1)) * (size_t)p.V;
-            float z[4];
+        {
+            const T *Urow = U + ((size_t)min(row, p.R - 1) * p.gamma + (p.k - 1)) * (size_t)p.V;
+            float z[4], e[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                z[j] = (v0 + j < p.V) ? acc[j] + to_f32(Urow[v0 + j]) : -INFINITY;
-            const uint4 words = philox4x32_10(
-                make_uint4((uint32_t)(v0 >> 2), (uint32_t)p.k, (uint32_t)row, c3), key);
-            row_feed4(st, z, v0, p.V, words);
+            for (int j = 0; j < 4; ++j) z[j] = (v0 + j < p.V) ? acc[j] + to_f32(Urow[v0 + j]) : -INFINITY;
+            float mb = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const float mL = mb * kLog2e;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e[j] = mb == -INFINITY ? 0.f : ex2(fmaf(z[j], kLog2e, -mL));
+            const float p0 = e[0] + e[1], p1 = e[2] + e[3], qs = p0 + p1;
+            const int base = threadIdx.x & ~3;
+            float q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[i] = __shfl_sync(0xffffffffu, qs, base + i);
+            const float o0 = q[0] + q[1], o1 = q[2] + q[3], Sb = o0 + o1;
+            if (row < p.R && mb > -INFINITY && Sb > 0.f) {
+                st.m = mb;
+                st.mL = mL;
+                st.S = qs;  // the request's sum over the slice is the sum of its quads
+                const int vb = v0 & ~15, qi_self = quad & 3;
+                const uint4 words = philox4x32_10(
+                    make_uint4((uint32_t)(vb >> 5), (uint32_t)p.k, (uint32_t)row, c3), key);
+                const bool odd = (vb & 16) != 0;
+                const uint32_t wr = odd ? words.z : words.x, we = odd ? words.w : words.y;
+                const float score = mb + kLn2 * lg2(Sb) - log_exp_variate(one_minus_uniform(wr));
+                float t = uniform_of(we) * Sb;
+                const bool r1 = t >= o0 && o1 > 0.f;
+                t = r1 ? t - o0 : t;
+                const float qL = r1 ? q[2] : q[0], qR = r1 ? q[3] : q[1];
+                const bool r2 = t >= qL && qR > 0.f;
+                t = r2 ? t - qL : t;
+                if (((r1 ? 2 : 0) | (r2 ? 1 : 0)) == qi_self) {
+                    const bool r3 = t >= p0 && p1 > 0.f;
+                    t = r3 ? t - p0 : t;
+                    const float eL = r3 ? e[2] : e[0], eR = r3 ? e[3] : e[1];
+                    const int j = 2 * (r3 ? 1 : 0) + (t >= eL && eR > 0.f ? 1 : 0);
+                    st.best = score;
+                    st.idx = v0 + j;
+                    st.zbest = select_of(z, j);
+                }
+            }
         }
         // merge the 16 quads of this request (lanes differing in bits 0..3)
 #pragma unroll
@@ -135,7 +176,7 @@ __global__ void __launch_bounds__(kReduceThreads) draft_reduce_kernel(const Draf
     __syncthreads();
     for (int half = kReduceThreads / 2; half > 0; half >>= 1) {
         if (tid < half) {
-            RowState a{s_m[tid], s_m[tid] * kLog2e, s_S[tid], s_b[tid], s_z[tid], s_i[tid], s_b[tid], 0.f};
+            RowState a{s_m[tid], s_m[tid] * kLog2e, s_S[tid], s_b[tid], s_z[tid], s_i[tid]};
             row_merge(a, s_m[tid + half], s_S[tid + half], s_b[tid + half], s_z[tid + half],
                       s_i[tid + half]);
             s_m[tid] = a.m; s_S[tid] = a.S; s_b[tid] = a.best; s_z[tid] = a.zbest; s_i[tid] = a.idx;

@@ -2,8 +2,9 @@
 //
 // DSpark digest eq. (5): B_k = W_1[x_{k-1}] W_2 (Markov head) or eq. (6)
 // B_k = W_2^T tanh(W_o z_k) (RNN head), contracted on tcgen05 into TMEM and
-// consumed in place by the eq. (4) epilogue: U_k add, online max / sum-exp,
-// Philox Gumbel race.  No logit reaches global memory.  The pipeline (TMA rings
+// consumed in place by the eq. (4) epilogue: U_k add, sum of exponentials,
+// the two-level draw (16-entry blocks raced on their masses with Philox
+// words, the winning block's entry by inverse CDF).  No logit reaches global memory.  The pipeline (TMA rings
 // of W_2^T slabs and U_k tiles, MMA warp, per-warp TMEM epilogue) is tc_pipe.cuh;
 // this file supplies the bias operand, the per-tile epilogue and the merge.
 //
@@ -610,16 +611,18 @@ __global__ void __launch_bounds__(P::kThreads, 1)
             RowState st;
             row_init(st);
             const PhiloxRow prow = philox_row((uint32_t)k, (uint32_t)grow, p.rk);
-            // Filter thresholds shared by all CTAs: the step's winner word of a
-            // request (win[row], raised by every CTA) holds the exact score of
-            // some element of the row, so any value read from it is a valid
-            // threshold, however stale.  Once per tile one thread per request
-            // (the leader) forwards the CTA's best when it beats what it last saw
-            // and brings the global best into the CTA; its read is issued a tile
-            // ahead so the L2 latency stays off the tile loop.
+            // Thresholds shared by all CTAs: a block only needs its entry drawn when
+            // it beats the row's best block so far, wherever that was found.  The
+            // step's winner word of a request (win[row], raised by every CTA) holds
+            // the packed score of some block of the row, so any value read from it
+            // is a valid threshold, however stale.  Once per tile one thread per
+            // request (the leader) forwards the CTA's best when it beats what it
+            // last saw and brings the global best into the CTA; its read is issued
+            // a tile ahead so the L2 latency stays off the tile loop.
             const bool leader = row_live && warp < (P::DUAL ? 2 : 4);
             unsigned long long *gwin = win + (row_live ? grow : m0);
             unsigned long long g_next = leader ? tc::ld_relaxed_gpu_u64(gwin) : 0ull, g_sent = 0ull;
+            uint2 w_odd = make_uint2(0u, 0u);  // the odd block's words of the last Philox call
             P::epilogue(s, step * ntiles, c0, tstride, ntiles, p.err,
                         [&](int, int n0, int cofs, const uint32_t *acc, const unsigned char *sU) {
                 if (leader && cofs == 0) {
@@ -631,59 +634,50 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     if (g > loc) P::publish_thr(s, row, g);
                     g_next = tc::ld_relaxed_gpu_u64(gwin);
                 }
-                // the row's best score so far, wherever it was found, filters this thread
-                row_raise_thr(st, winner_score(P::read_thr(s, row)));
-                const float best0 = st.best;
-                const int cb = col0 + cofs, vb = n0 + cb;  // the chunk's first column: in the tile, in V
-                if (vb + 16 <= c1) {
-                    // whole chunk in range: the Philox words first (independent chains), then the block
-                    uint32_t words[16];
-                    float z[16];
+                const int cb = col0 + cofs, vb = n0 + cb;  // the block's first column: in the tile, in V
+                if (vb >= c1) return;
+                // block b = vb / 16 draws words 2 (b mod 2), 2 (b mod 2) + 1 of the Philox
+                // call (b / 2, k, request, cycle): an even block and the odd one after it,
+                // when the same warp takes it next, share one call
+                uint32_t wr, we;
+                const bool odd = (vb & 16) != 0;
+                if (!odd || cofs == 0) {
+                    const uint4 w4 = philox4x32_10((uint32_t)(vb >> 5), c3, prow, p.rk);
+                    wr = odd ? w4.z : w4.x;
+                    we = odd ? w4.w : w4.y;
+                    w_odd = make_uint2(w4.z, w4.w);
+                } else {
+                    wr = w_odd.x;
+                    we = w_odd.y;
+                }
+                float z[16];
+                if constexpr (P::UMMA) {
+                    // U_k was added on the tensor cores
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint4 w4 = philox4x32_10((uint32_t)((vb >> 2) + g), c3, prow, p.rk);
-                        words[4 * g] = w4.x; words[4 * g + 1] = w4.y; words[4 * g + 2] = w4.z; words[4 * g + 3] = w4.w;
-                    }
-                    if constexpr (P::UMMA) {
-                        // U_k was added on the tensor cores
+                    for (int j = 0; j < 16; ++j) z[j] = __uint_as_float(acc[j]);
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) z[j] = __uint_as_float(acc[j]);
-                    } else {
+                    for (int o = 0; o < 2; ++o) {
+                        const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
+                        const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
-                        for (int o = 0; o < 2; ++o) {
-                            const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
-                            const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
-                                                                   __uint_as_float(acc[8 * o + 2 * i + 1])),
-                                                       make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
-                                z[8 * o + 2 * i] = zz.x;
-                                z[8 * o + 2 * i + 1] = zz.y;
-                            }
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
+                                                               __uint_as_float(acc[8 * o + 2 * i + 1])),
+                                                   make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
+                            z[8 * o + 2 * i] = zz.x;
+                            z[8 * o + 2 * i + 1] = zz.y;
                         }
-                    }
-                    row_feed16(st, z, vb, words);
-                } else if (vb < c1 && row_live) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = cb + 4 * g;
-                        float z[4] = {__uint_as_float(acc[4 * g]), __uint_as_float(acc[4 * g + 1]),
-                                      __uint_as_float(acc[4 * g + 2]), __uint_as_float(acc[4 * g + 3])};
-                        if constexpr (!P::UMMA) {
-                            const uint2 uu = P::u_quad(sU, row, col);
-                            z[0] += tcp::bf16_lo(uu.x);
-                            z[1] += tcp::bf16_hi(uu.x);
-                            z[2] += tcp::bf16_lo(uu.y);
-                            z[3] += tcp::bf16_hi(uu.y);
-                        }
-                        const int v0 = n0 + col;
-                        const uint4 words =
-                            philox4x32_10(make_uint4((uint32_t)(v0 >> 2), (uint32_t)k, (uint32_t)grow, c3), p.rk);
-                        row_feed4<false>(st, z, v0, c1, words);
                     }
                 }
-                if (row_live && st.best > best0) P::publish_thr(s, row, pack_winner(st.best, st.idx));
+                if (vb + 16 > c1) {
+                    // the vocabulary ends inside this block
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (vb + j >= c1) z[j] = -INFINITY;
+                }
+                if (block_feed16(st, z, vb, wr, we, P::read_thr(s, row)) && row_live)
+                    P::publish_thr(s, row, pack_winner(st.best, st.idx));
             });
 
             // The next step needs only x_k: fold the CTA's winner of each request (its
