@@ -128,8 +128,8 @@ def draft_markov(U, h, W1, W2t, w, anchor, *, seed=0, cycle=0, sts_T=None, reqs=
     n = R if rl is None else len(rl)
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
-    gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma)); cdf_gap = np.zeros((n, gamma))
-    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma), -1, np.int32)
+    gap = np.zeros((n, gamma)); logit = np.zeros((n, gamma)); cdf_gap = np.zeros((n, gamma, 2))
+    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma, 2), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_markov(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(w),
                                    _p(sts), _p(anchor), seed, cycle, _p(rl), n, _p(x), _p(logq),
@@ -164,8 +164,8 @@ def draft_rnn(U, h, W1, W2t, W, w, anchor, *, s0=None, seed=0, cycle=0, sts_T=No
     x = np.zeros((n, gamma), np.int32)
     logq = np.zeros((n, gamma)); lse = np.zeros((n, gamma)); c = np.zeros((n, gamma))
     gap = np.zeros((n, gamma)); A = np.zeros((n, gamma, r)); logit = np.zeros((n, gamma))
-    cdf_gap = np.zeros((n, gamma))
-    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma), -1, np.int32)
+    cdf_gap = np.zeros((n, gamma, 2))
+    runner = np.full((n, gamma), -1, np.int32); cdf_runner = np.full((n, gamma, 2), -1, np.int32)
     z = np.zeros((n, gamma, V)) if want_z else None
     rc = lib().oracle_draft_rnn(R, gamma, V, r, d, dt, _p(U), _p(h), _p(W1), _p(W2t), _p(W),
                                 _p(s0a), _p(w), _p(sts), _p(anchor), seed, cycle, _p(rl), n,
@@ -219,8 +219,8 @@ def verify(T, tags, anchor, x, logq, lse, U, W1, W2t, *, A=None, seed=0, cycle=0
     out = np.full((R, gamma + 1), -1, np.int32)
     nxt = np.full(R, -1, np.int32)
     lse_p = np.full(N, np.nan); logp = np.full(N, np.nan); margin = np.full(N, np.nan)
-    gap = np.full(R, np.nan)
-    runner = np.full(R, -1, np.int32)
+    gap = np.full((R, 2), np.nan)
+    runner = np.full((R, 2), -1, np.int32)
     rc = lib().oracle_verify(R, gamma, V, r, dt, N, _p(T), _p(tags), _p(anchor), _p(x), _p(logq),
                              _p(lse), _p(U), _p(W1), _p(W2t), _p(Aa), seed, cycle, _p(rl), n,
                              _p(n_acc), _p(out), _p(nxt), _p(lse_p), _p(logp), _p(margin), _p(gap),

@@ -99,11 +99,11 @@ static void block_words(uint64_t seed, uint32_t step, uint32_t req, uint64_t cyc
     *u_entry = oracle_uniform(out[2 * (b % 2) + 1]);
 }
 
-/* Level 2 inside block b: the entry; optionally how close the target came  */
-/* to the nearer end of that entry's interval (a fraction of S_b) and the   */
-/* entry across that end (-1: none).                                         */
+/* Level 2 inside block b: the entry; optionally the target's distances to  */
+/* the lower and upper ends of that entry's interval (fractions of S_b) and */
+/* the entries of the block across them (-1: none).                         */
 static int block_entry(const double *z, int V, double m, int b, double u_entry,
-                       double *margin, int *across) {
+                       double margin[2], int across[2]) {
     int v0 = b * DRAFT_BLOCK, v1 = v0 + DRAFT_BLOCK < V ? v0 + DRAFT_BLOCK : V;
     double S = 0.0;
     for (int v = v0; v < v1; ++v) S += exp(z[v] - m);
@@ -124,16 +124,22 @@ static int block_entry(const double *z, int V, double m, int b, double u_entry,
         for (int v = v1 - 1; v >= v0 && pick < 0; --v)
             if (exp(z[v] - m) > 0.0) pick = v;
     }
-    if (margin) *margin = (lo < hi ? lo : hi) / S;
-    if (across) *across = lo <= hi ? (pick - 1 >= v0 ? pick - 1 : -1) : (pick + 1 < v1 ? pick + 1 : -1);
+    if (margin) {
+        margin[0] = lo / S;
+        margin[1] = hi / S;
+    }
+    if (across) {
+        across[0] = pick - 1 >= v0 ? pick - 1 : -1;
+        across[1] = pick + 1 < v1 && exp(z[pick + 1] - m) > 0.0 ? pick + 1 : -1;
+    }
     return pick;
 }
 
-/* Writes lse, the sampled index x, log q of it and two near-tie records:   */
+/* Writes lse, the sampled index x, log q of it and the near-tie records:  */
 /* gap / runner -- the difference between the two best block scores and    */
-/* the token the runner-up block gives at level 2; cdf_gap / cdf_runner --  */
-/* the level-2 target's distance to the nearer end of x's interval (a       */
-/* fraction of S_{b*}) and the entry across that end.                       */
+/* the token the runner-up block gives at level 2; cdf_gap[2] /             */
+/* cdf_runner[2] -- the level-2 target's distances to the lower and upper   */
+/* ends of x's interval (fractions of S_{b*}) and the entries across them.  */
 static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, uint32_t req,
                         uint64_t cycle, int32_t *x_out, double *logq_out, double *lse_out,
                         double *gap_out, int32_t *runner_out, double *cdf_gap_out,
@@ -166,10 +172,10 @@ static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, ui
             arg2 = b;
         }
     }
-    double margin;
-    int across;
+    double margin[2];
+    int across[2];
     block_words(seed, step, req, cycle, arg, &u_race, &u_entry);
-    int v = block_entry(z, V, m, arg, u_entry, &margin, &across);
+    int v = block_entry(z, V, m, arg, u_entry, margin, across);
     *x_out = v;
     *logq_out = z[v] - lse;
     *lse_out = lse;
@@ -182,8 +188,14 @@ static void sample_step(const double *z, int V, uint64_t seed, uint32_t step, ui
         }
         *runner_out = other;
     }
-    if (cdf_gap_out) *cdf_gap_out = margin;
-    if (cdf_runner_out) *cdf_runner_out = across;
+    if (cdf_gap_out) {
+        cdf_gap_out[0] = margin[0];
+        cdf_gap_out[1] = margin[1];
+    }
+    if (cdf_runner_out) {
+        cdf_runner_out[0] = across[0];
+        cdf_runner_out[1] = across[1];
+    }
 }
 
 /* [D] eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]]); the optional per-step
@@ -232,7 +244,7 @@ int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
                         gap ? &gap[o] : NULL, runner ? &runner[o] : NULL,
-                        cdf_gap ? &cdf_gap[o] : NULL, cdf_runner ? &cdf_runner[o] : NULL);
+                        cdf_gap ? &cdf_gap[2 * o] : NULL, cdf_runner ? &cdf_runner[2 * o] : NULL);
             const void *h_k = dtype == ORACLE_F32
                                   ? (const void *)((const float *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d)
                                   : (const void *)((const uint16_t *)h + ((size_t)rq * gamma + (k - 1)) * (size_t)d);
@@ -307,7 +319,7 @@ int oracle_draft_rnn(int R, int gamma, int V, int r, int d, int dtype,
             if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
             sample_step(z, V, seed, (uint32_t)k, (uint32_t)rq, cycle, &x[o], &logq[o], &lse[o],
                         gap ? &gap[o] : NULL, runner ? &runner[o] : NULL,
-                        cdf_gap ? &cdf_gap[o] : NULL, cdf_runner ? &cdf_runner[o] : NULL);
+                        cdf_gap ? &cdf_gap[2 * o] : NULL, cdf_runner ? &cdf_runner[2 * o] : NULL);
             /* eq. (7) reads the embedding W_1[x_{k-1}], i.e. the middle block of z_k */
             const void *h_k = dtype == ORACLE_F32 ? (const void *)((const float *)h + hrow)
                                                   : (const void *)((const uint16_t *)h + hrow);
@@ -562,21 +574,18 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
             y = v; /* the last positive-weight index, if the target is never passed */
             if (cum > target) break;
         }
-        /* the closer CDF boundary of y, relative to the total, and the index on
-         * its other side (the draw a slightly different target would give) */
-        int y2 = -1;
-        double margin = INFINITY;
+        /* the distances of the target to the two ends of y's interval, relative
+         * to the total, and the positive-weight indices across them (the draws a
+         * slightly lower or higher target would give) */
+        int y_lo = -1, y_hi = -1;
+        double d_lo = INFINITY, d_hi = INFINITY;
         if (y >= 0 && total > 0.0) {
-            double lo = (target - below) / total, hi = (cum - target) / total;
-            if (lo <= hi) {
-                margin = lo;
-                for (int v = y - 1; v >= 0; --v)
-                    if (w[v] > 0.0) { y2 = v; break; }
-            } else {
-                margin = hi;
-                for (int v = y + 1; v < V; ++v)
-                    if (w[v] > 0.0) { y2 = v; break; }
-            }
+            d_lo = (target - below) / total;
+            d_hi = (cum - target) / total;
+            for (int v = y - 1; v >= 0 && y_lo < 0; --v)
+                if (w[v] > 0.0) y_lo = v;
+            for (int v = y + 1; v < V && y_hi < 0; ++v)
+                if (w[v] > 0.0) y_hi = v;
         }
         n_accept[rq] = n_r;
         for (int j = 0; j <= gamma; ++j) {
@@ -586,8 +595,14 @@ int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *
             out_tokens[(size_t)rq * (gamma + 1) + j] = tok;
         }
         next_anchor[rq] = y;
-        if (gap) gap[rq] = margin;
-        if (runner) runner[rq] = y2;
+        if (gap) {
+            gap[2 * (size_t)rq] = d_lo;
+            gap[2 * (size_t)rq + 1] = d_hi;
+        }
+        if (runner) {
+            runner[2 * (size_t)rq] = y_lo;
+            runner[2 * (size_t)rq + 1] = y_hi;
+        }
     }
     free(first); free(count); free(w); free(b);
     return status;

@@ -64,10 +64,10 @@ uint32_t oracle_philox_word(uint64_t seed, uint32_t w0, uint32_t w1, uint32_t re
  * rule over their masses, then the entry of the winning block by inverse CDF).
  * Outputs: x [n, gamma], logq, lse, c [n, gamma]; the near-tie records
  * gap [n, gamma] = difference between the two best block scores, runner
- * [n, gamma] = the token the runner-up block gives, cdf_gap [n, gamma] =
- * distance of the entry draw's target to the nearer end of x's interval (a
- * fraction of the block's mass), cdf_runner [n, gamma] = the entry across that
- * end (-1: none); z [n, gamma, V] logits,
+ * [n, gamma] = the token the runner-up block gives, cdf_gap [n, gamma, 2] =
+ * distances of the entry draw's target to the lower and upper ends of x's
+ * interval (fractions of the block's mass), cdf_runner [n, gamma, 2] = the
+ * entries across those ends (-1: none); z [n, gamma, V] logits,
  * logit [n, gamma] = w^T [h_k ; W_1[x_{k-1}]] (the confidence logit). */
 int oracle_draft_markov(int R, int gamma, int V, int r, int d, int dtype,
                         const void *U, const void *h, const void *W1, const void *W2t,
@@ -109,9 +109,9 @@ int oracle_schedule(int R, int gamma, const float *c, const double *sps, int B_m
  *   (log p - log q) - log u.  The correction / bonus token y is drawn by
  *   inverse CDF: u from Philox stream 2 (counter (0, n, request, cycle), word
  *   0), y = the first v whose cumulative weight exceeds u * sum(w).
- *   gap [R] = the distance of u * sum(w) to the nearer CDF boundary of y,
- *   relative to sum(w); runner [R] = the index on the other side of that
- *   boundary (-1 if none).
+ *   gap [R, 2] = the distances of u * sum(w) to the lower and upper ends of
+ *   y's interval, relative to sum(w); runner [R, 2] = the positive-weight
+ *   indices across those ends (-1 if none).
  * Returns 0, or -1 on malformed tags. */
 int oracle_verify(int R, int gamma, int V, int r, int dtype, int N, const void *T,
                   const int32_t *tags, const int32_t *anchor, const int32_t *x,

@@ -164,7 +164,8 @@ def test_bad_anchor_rejected(orc):
 
 def test_sample_and_near_tie_records_by_brute_force(orc):
     """The reported token, the block-score gap and the runner-up block's token, and
-    the entry draw's CDF margin and the entry across it, recomputed from the
+    the entry draw's distances to both ends of the drawn entry's interval with the
+    entries across them, recomputed from the
     stream-0 Philox words: block b (16 entries, the last one 8 here) takes words
     2 (b mod 2) and 2 (b mod 2) + 1 of counter (b / 2, k, request, cycle)."""
     R, gamma, V, r, d = 2, 3, 40, 4, 2
@@ -195,7 +196,8 @@ def test_sample_and_near_tie_records_by_brute_force(orc):
             assert out["x"][rq, k] == x
             assert out["gap"][rq, k] == pytest.approx(score[b0] - score[b1], abs=1e-12)
             assert out["runner"][rq, k] == entry(e[:blocks[b1][1]], blocks[b1][0], word(b1, k, rq, 1))[0]
-            assert out["cdf_gap"][rq, k] == pytest.approx(min(lo, hi) / S, abs=1e-12)
+            assert out["cdf_gap"][rq, k, 0] == pytest.approx(lo / S, abs=1e-12)
+            assert out["cdf_gap"][rq, k, 1] == pytest.approx(hi / S, abs=1e-12)
             first, last = blocks[b0][0], blocks[b0][1] - 1
-            expect = (x - 1 if x > first else -1) if lo <= hi else (x + 1 if x < last else -1)
-            assert out["cdf_runner"][rq, k] == expect
+            assert out["cdf_runner"][rq, k, 0] == (x - 1 if x > first else -1)
+            assert out["cdf_runner"][rq, k, 1] == (x + 1 if x < last else -1)

@@ -219,8 +219,8 @@ def test_malformed_tags_rejected(orc):
 def test_final_sample_is_the_inverse_cdf_draw(orc):
     # l = 0: the final token is the inverse-CDF draw from p_0 with one stream-2
     # uniform (counter (0, position 0, request, cycle), word 0): the first v whose
-    # cumulative probability exceeds u; gap is the distance of u to the nearer
-    # boundary of that v's interval, runner the index on the other side
+    # cumulative probability exceeds u; gap holds the distances of u to the
+    # lower and upper ends of that v's interval, runner the indices across them
     R, V = 40, 30
     rng = np.random.default_rng(12)
     U = rng.standard_normal((R, 1, V)).astype(np.float32)
@@ -235,5 +235,7 @@ def test_final_sample_is_the_inverse_cdf_draw(orc):
         assert v["out_tokens"][rq, 0] == y
         lo = u * cdf[-1] - (cdf[y - 1] if y > 0 else 0.0)
         hi = cdf[y] - u * cdf[-1]
-        assert v["gap"][rq] == pytest.approx(min(lo, hi) / cdf[-1], abs=1e-12)
-        assert v["runner"][rq] == (y - 1 if lo <= hi else (y + 1 if y + 1 < V else -1))
+        assert v["gap"][rq, 0] == pytest.approx(lo / cdf[-1], abs=1e-12)
+        assert v["gap"][rq, 1] == pytest.approx(hi / cdf[-1], abs=1e-12)
+        assert v["runner"][rq, 0] == (y - 1 if y > 0 else -1)
+        assert v["runner"][rq, 1] == (y + 1 if y + 1 < V else -1)
