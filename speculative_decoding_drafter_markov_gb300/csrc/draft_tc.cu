@@ -539,7 +539,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     typename P::State s = P::carve(smem_raw);
     P::init(s);
-    P::init_identity(s);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.n_mtiles, cv = blockIdx.x / p.n_mtiles;
     const int m0 = m_tile * P::MV;
@@ -651,23 +650,17 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                     we = w_odd.y;
                 }
                 float z[16];
-                if constexpr (P::UMMA) {
-                    // U_k was added on the tensor cores
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) z[j] = __uint_as_float(acc[j]);
-                } else {
+                for (int o = 0; o < 2; ++o) {
+                    const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
+                    const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const uint4 uu = P::u_oct(sU, row, cb + 8 * o);
-                        const uint32_t u[4] = {uu.x, uu.y, uu.z, uu.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
-                                                               __uint_as_float(acc[8 * o + 2 * i + 1])),
-                                                   make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
-                            z[8 * o + 2 * i] = zz.x;
-                            z[8 * o + 2 * i + 1] = zz.y;
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 zz = add2(make_float2(__uint_as_float(acc[8 * o + 2 * i]),
+                                                           __uint_as_float(acc[8 * o + 2 * i + 1])),
+                                               make_float2(tcp::bf16_lo(u[i]), tcp::bf16_hi(u[i])));
+                        z[8 * o + 2 * i] = zz.x;
+                        z[8 * o + 2 * i + 1] = zz.y;
                     }
                 }
                 if (vb + 16 > c1) {
@@ -818,11 +811,8 @@ __global__ void wait_selfcheck_kernel(const int *flag, int target, int mode, uin
 
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
-// (U_k added on the tensor cores with 128 requests per M-tile: 6 % faster at
-// R = 256 and 512; with 64 requests, where the identity block costs a W_2^T
-// slot, 5 % slower)
 using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;          // Markov, R <= 64
-using DraftM128 = tcp::Pipe<128, 128, 4, 2, 1, true>;  // Markov, 128 requests per M-tile
+using DraftM128 = tcp::Pipe<128, 128, 6, 2, 1>;  // Markov, 128 requests per M-tile
 using DraftRnn = tcp::Pipe<128, 64, 6, 2, 2>;   // RNN (fp32 operand split hi/lo)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

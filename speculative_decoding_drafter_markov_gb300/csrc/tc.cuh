@@ -55,6 +55,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// The same with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of polling.  A role that waits
+// most of the time (the producers and the MMA issuer while the epilogue is the
+// bottleneck) then takes no issue slots from the warps sharing its scheduler.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait for the phase with the given parity; false on timeout (which
 // raises the CTA's abort flag and reports DSPARK_ERR_TIMEOUT) or when another
 // role already aborted.
@@ -62,13 +80,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
                                           int32_t *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0u) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) break;
-            __nanosleep(64);
-        }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) break;
     }
     *abort_flag = 1;
     set_err(err, DSPARK_ERR_TIMEOUT);
@@ -79,12 +94,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // and MMAs in flight land before its shared memory or TMEM is released.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 15u) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-            __nanosleep(64);
-        }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
     set_err(err, DSPARK_ERR_TIMEOUT);
     return false;
@@ -258,19 +270,6 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
     d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
     d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
-    d |= (uint64_t)1u << 46;                          // descriptor version
-    d |= (uint64_t)2u << 61;                          // 128-byte swizzle
-    return d;
-}
-
-// Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzle
-// layout -- rows of 64 MN-consecutive bf16 (128 bytes) per K index, 8-row (K)
-// groups 1024 bytes apart, the next 64 MN elements `mn_stride` bytes further.
-__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t mn_stride) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
-    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16; // leading byte offset: along MN
-    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8-row groups along K
     d |= (uint64_t)1u << 46;                          // descriptor version
     d |= (uint64_t)2u << 61;                          // 128-byte swizzle
     return d;

@@ -40,15 +40,9 @@ constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kUWarp = 18;
 
-template <int MV_, int BN_, int NS_, int SU_, int KSPLIT_, bool UMMA_ = false>
+template <int MV_, int BN_, int NS_, int SU_, int KSPLIT_>
 struct Pipe {
     static constexpr int MV = MV_, BN = BN_, NS = NS_, SU = SU_, KSPLIT = KSPLIT_;
-    // UMMA: the U tile is added on the tensor cores -- an identity block I
-    // (row m holds 1 at K index m mod MV) times the U tile read as an MN-major
-    // operand (K = the tile's requests) accumulates U_k into the same TMEM
-    // accumulator as the bias, so the epilogue reads the logits z directly; the
-    // U slot is freed by the MMA commit instead of by the epilogue warps.
-    static constexpr bool UMMA = UMMA_;
     static constexpr bool DUAL = MV == 64;
     static constexpr bool WITH_U = SU > 0;
     static constexpr int kThreads = kEpiThreads + (WITH_U ? 96 : 64);  // epilogue, producer(s), MMA
@@ -62,11 +56,9 @@ struct Pipe {
     static constexpr int kTmemCols = NACC * BN;
     static constexpr int CW = DUAL ? BN / 8 : BN / 4;  // accumulator columns per warp
     static constexpr int TPR = DUAL ? 8 : 4;           // epilogue threads per request
-    static constexpr int kIdSlabs = UMMA ? MV / 64 : 0;  // identity block: MV K positions
     static constexpr int kOffB = kABytes;
     static constexpr int kOffU = kOffB + NS * kSlabB;
-    static constexpr int kOffId = kOffU + SU * kUBytes;
-    static constexpr int kOffBar = kOffId + kIdSlabs * kSlabA;
+    static constexpr int kOffBar = kOffU + SU * kUBytes;
     static constexpr int kNumBars = 2 * NS + 2 * SU + 2 * NACC + 2;
     static constexpr int kOffThr = kOffBar + 8 * kNumBars;  // per-request filter thresholds
     static constexpr int kOffTok = kOffThr + 8 * MV;        // per-request tokens / metadata
@@ -81,7 +73,6 @@ struct Pipe {
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
     static_assert(CW == 16 || CW == 32, "TMEM load width");
     static_assert(MV == 64 || MV == 128, "M-tile rows");
-    static_assert(!UMMA || SU > 0, "the U tiles come through the U ring");
 
     struct State {
         unsigned char *smem, *sA;
@@ -130,7 +121,7 @@ struct Pipe {
             }
             for (int i = 0; i < SU; ++i) {
                 tc::mbar_init(&s.fullU[i], 1);
-                tc::mbar_init(&s.emptyU[i], UMMA ? 1 : kEpiWarps);  // the MMA commit, or every epilogue warp
+                tc::mbar_init(&s.emptyU[i], kEpiWarps);  // every epilogue warp
             }
             for (int b = 0; b < NACC; ++b) {
                 tc::mbar_init(&s.tfull[b], 1);
@@ -147,23 +138,6 @@ struct Pipe {
             tc::tmem_alloc(s.tmem_slot, kTmemCols);
             tc::tmem_relinquish();
             tc::tc_fence_before();
-        }
-    }
-
-    // all threads, before the CTA barrier that follows init (UMMA): the identity
-    // block, K-major with the 128-byte swizzle like the operand
-    __device__ static void init_identity(const State &s) {
-        if constexpr (UMMA) {
-            unsigned char *id = s.smem + kOffId;
-            for (int e = threadIdx.x; e < kIdSlabs * kSlabA / 16; e += blockDim.x)
-                reinterpret_cast<uint4 *>(id)[e] = make_uint4(0u, 0u, 0u, 0u);
-            __syncthreads();
-            if (threadIdx.x < kArows) {
-                const int m = threadIdx.x, k = m % MV, c = k >> 3;
-                unsigned char *chunk = id + (c >> 3) * kSlabA + (m >> 3) * 1024 + (m & 7) * 128 + (((c & 7) ^ (m & 7)) << 4);
-                reinterpret_cast<uint16_t *>(chunk)[k & 7] = 0x3F80u;  // bf16 1.0
-            }
-            tc::fence_proxy_async_smem();
         }
     }
 
@@ -285,7 +259,6 @@ struct Pipe {
         const uint64_t a_desc0 = tc::smem_desc_k128(tc::smem_u32(s.sA));
         const uint64_t b_desc0 = tc::smem_desc_k128(tc::smem_u32(s.smem + kOffB));
         int issued = 0, slot = 0, b = 0;  // W_2^T ring slot and accumulator of the next MMAs
-        int issued_tiles = 0;             // tiles whose bias MMAs were issued (U ring position)
         uint32_t phase = 0, tphase = 0;
         bool ok = true;
         for (int step = 0; step < nsteps && ok; ++step) {
@@ -322,26 +295,6 @@ struct Pipe {
                     }
                 }
                 if (!ok) break;
-                if constexpr (UMMA) {
-                    // + I . U_tile: K = the tile's MV requests, 16 at a time; the U tile is
-                    // the MN-major operand (64-column boxes kUBox apart, 8-row groups 1024 B)
-                    const int su_slot = issued_tiles % SU;
-                    if (!tc::mbar_wait(&s.fullU[su_slot], (uint32_t)(issued_tiles / SU) & 1u, s.abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    constexpr uint32_t idesc_u = tc::idesc_bf16_f32(128, BN) | (1u << 16);  // B MN-major
-                    const uint64_t id0 = tc::smem_desc_k128(tc::smem_u32(s.smem + kOffId));
-                    const uint64_t u0 = tc::smem_desc_mn128(tc::smem_u32(s.smem + kOffU + su_slot * kUBytes),
-                                                            (uint32_t)kUBox);
-#pragma unroll
-                    for (int kk = 0; kk < MV / 16; ++kk)
-                        tc::umma_bf16(d, id0 + (uint64_t)(((kk >> 2) * kSlabA + (kk & 3) * 32) >> 4),
-                                      u0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_u, 1u);
-                    tc::umma_commit(&s.emptyU[su_slot]);
-                }
-                ++issued_tiles;
                 tc::umma_commit(&s.tfull[b]);
                 ++issued;
                 if (++b == NACC) {
@@ -538,14 +491,14 @@ struct Pipe {
             int ok = 1;
             if (lane == 0) {
                 ok = tc::mbar_wait(&s.tfull[b], (uint32_t)(tg / NACC) & 1u, s.abort_flag, err) ? 1 : 0;
-                if (ok && SU > 0 && !UMMA)
+                if (ok && SU > 0)
                     ok = tc::mbar_wait(&s.fullU[tg % su], (uint32_t)(tg / su) & 1u, s.abort_flag, err) ? 1 : 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (SU > 0 && !UMMA) __syncwarp();  // the other lanes read the U tile lane 0 waited for
+            if (SU > 0) __syncwarp();  // the other lanes read the U tile lane 0 waited for
             tc::tc_fence_after();
-            const unsigned char *sU = SU > 0 && !UMMA ? s.smem + kOffU + (tg % su) * kUBytes : nullptr;
+            const unsigned char *sU = SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr;
 #pragma unroll 1
             for (int h = 0; h < CW / 16; ++h) {
                 uint32_t acc[16];
@@ -559,7 +512,7 @@ struct Pipe {
                 f(t, col0 + t * tstride, 16 * h, acc, sU);
             }
             __syncwarp();
-            if (SU > 0 && !UMMA && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
+            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
         }
     }
 
