@@ -55,24 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// The same with a suspend-time hint: the thread sleeps until the phase
-// completes or about `hint_ns` pass, instead of polling.  A role that waits
-// most of the time (the producers and the MMA issuer while the epilogue is the
-// bottleneck) then takes no issue slots from the warps sharing its scheduler.
-constexpr uint32_t kSuspendHintNs = 1000000u;
-
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return done != 0;
-}
-
 // Bounded wait for the phase with the given parity; false on timeout (which
 // raises the CTA's abort flag and reports DSPARK_ERR_TIMEOUT) or when another
 // role already aborted.
@@ -80,10 +62,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
                                           int32_t *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_suspend(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) break;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) break;
+            __nanosleep(64);
+        }
     }
     *abort_flag = 1;
     set_err(err, DSPARK_ERR_TIMEOUT);
@@ -94,9 +79,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // and MMAs in flight land before its shared memory or TMEM is released.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
     const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_suspend(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(64);
+        }
     }
     set_err(err, DSPARK_ERR_TIMEOUT);
     return false;
