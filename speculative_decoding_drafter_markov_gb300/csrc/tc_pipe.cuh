@@ -51,7 +51,12 @@ struct Pipe {
     static constexpr int kABytes = 4 * KSPLIT * kSlabA; // r <= 256
     static constexpr int kSlabB = BN * 128;             // one 64-wide K slab of W_2^T
     static constexpr int kUBox = MV * 128;              // 64 vocabulary columns of U
-    static constexpr int kUBytes = (BN / 64) * kUBox;
+    // The U tile travels in UH parts of at most 128 columns, one ring slot each
+    // (a 256-column tile would not fit two whole U tiles next to the operand and
+    // the W_2^T ring); the epilogue warps of a part release its slot.
+    static constexpr int UH = BN > 128 ? BN / 128 : 1;
+    static constexpr int kUCols = BN / UH;               // columns of a part
+    static constexpr int kUBytes = (kUCols / 64) * kUBox;  // bytes of a part (one slot)
     static constexpr int NACC = 512 / BN > 4 ? 4 : 512 / BN;  // TMEM accumulators
     static constexpr int kTmemCols = NACC * BN;
     static constexpr int CW = DUAL ? BN / 8 : BN / 4;  // accumulator columns per warp
@@ -71,7 +76,8 @@ struct Pipe {
     static_assert(kBytes <= 232448, "shared memory budget");
     static_assert(kMergeBytes <= kABytes, "merge scratch");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
-    static_assert(CW == 16 || CW == 32, "TMEM load width");
+    static_assert(CW == 16 || CW == 32 || CW == 64, "TMEM load width");
+    static_assert(UH == 1 || (!DUAL && kUCols % CW == 0), "a warp's columns lie in one U part");
     static_assert(MV == 64 || MV == 128, "M-tile rows");
 
     struct State {
@@ -121,7 +127,7 @@ struct Pipe {
             }
             for (int i = 0; i < SU; ++i) {
                 tc::mbar_init(&s.fullU[i], 1);
-                tc::mbar_init(&s.emptyU[i], kEpiWarps);  // every epilogue warp
+                tc::mbar_init(&s.emptyU[i], kEpiWarps / UH);  // every epilogue warp of the part
             }
             for (int b = 0; b < NACC; ++b) {
                 tc::mbar_init(&s.tfull[b], 1);
@@ -164,12 +170,14 @@ struct Pipe {
 
     // eight columns col .. col + 7 (col a multiple of 8) of a U tile row
     __device__ static uint4 u_oct(const unsigned char *sU, int row, int col) {
+        col &= kUCols - 1;  // within the part that holds it
         const int h = col >> 6, cc = col & 63;
         return *reinterpret_cast<const uint4 *>(sU + h * kUBox + row * 128 + (((cc >> 3) ^ (row & 7)) << 4));
     }
 
     // one quad of a U tile (64-column boxes, 128-byte swizzle)
     __device__ static uint2 u_quad(const unsigned char *sU, int row, int col) {
+        col &= kUCols - 1;  // within the part that holds it
         const int h = col >> 6, cc = col & 63;
         return *reinterpret_cast<const uint2 *>(sU + h * kUBox + row * 128 +
                                                 ((((cc >> 3) ^ (row & 7))) << 4) + ((cc & 7) << 1));
@@ -215,32 +223,35 @@ struct Pipe {
         }
     }
 
-    // warp 18, lane 0: the U tiles of the same steps and tiles; U of step i is
-    // position u_k0 + i of requests m0 ..
+    // warp 18, lane 0: the U tiles of the same steps and tiles, UH parts per
+    // tile in order; U of step i is position u_k0 + i of requests m0 ..
     __device__ static void producer_u(State &s, const CUtensorMap *tmU, int col0, int tstride, int ntiles,
                                       int nsteps, int u_k0, int m0, int32_t *err) {
         if (SU > 0) {
             // U is read once: keep it from displacing W_2^T, which the next steps reuse
             const uint64_t pol = tc::policy_evict_first();
             constexpr int su = SU > 0 ? SU : 1;
-            const int total = nsteps * ntiles;
-            int issued = 0, st = 0, step = 0, t = 0;  // ring slot, step and tile of load `issued`
+            const int total = nsteps * ntiles * UH;
+            int issued = 0, st = 0, step = 0, t = 0, part = 0;  // ring slot, step, tile and part of load `issued`
             uint32_t phase = 0;
             for (int g = 0; g < total; ++g) {
                 if (!tc::mbar_wait(&s.emptyU[st], phase ^ 1u, s.abort_flag, err)) break;
                 unsigned char *dst = s.smem + kOffU + st * kUBytes;
-                const int n0 = col0 + t * tstride;
+                const int n0 = col0 + t * tstride + part * kUCols;
                 tc::mbar_expect_tx(&s.fullU[st], (uint32_t)kUBytes);
-                for (int h = 0; h < BN / 64; ++h)
+                for (int h = 0; h < kUCols / 64; ++h)
                     tc::tma_load_3d_hint(dst + h * kUBox, tmU, &s.fullU[st], n0 + h * 64, u_k0 + step, m0, pol);
                 ++issued;
                 if (++st == su) {
                     st = 0;
                     phase ^= 1u;
                 }
-                if (++t == ntiles) {
-                    t = 0;
-                    ++step;
+                if (++part == UH) {
+                    part = 0;
+                    if (++t == ntiles) {
+                        t = 0;
+                        ++step;
+                    }
                 }
             }
             for (int g = issued - su < 0 ? 0 : issued - su; g < issued; ++g)
@@ -478,7 +489,7 @@ struct Pipe {
     // rows 16 at a time and call f(t, n0, cofs, acc, sU) on each chunk (t: tile
     // within this call; n0 = col0 + t tstride: first vocabulary entry of the
     // tile; cofs: the chunk's offset within the warp's CW columns; acc: its 16
-    // values; sU: the tile's U, or null).  The accumulator is released once its
+    // values; sU: the ring slot of the U part that holds this warp's columns, or null).  The accumulator is released once its
     // last chunk has been read.  Barrier phases continue from tile number tg0
     // (the tiles of earlier steps of the launch).  Per-warp flow, no CTA barrier.
     template <class F>
@@ -488,17 +499,18 @@ struct Pipe {
         constexpr int su = SU > 0 ? SU : 1;
         for (int t = 0; t < ntiles; ++t) {
             const int tg = tg0 + t, b = tg % NACC;
+            const int ug = tg * UH + epi_col0() / kUCols;  // this warp's U part in the ring order
             int ok = 1;
             if (lane == 0) {
                 ok = tc::mbar_wait(&s.tfull[b], (uint32_t)(tg / NACC) & 1u, s.abort_flag, err) ? 1 : 0;
                 if (ok && SU > 0)
-                    ok = tc::mbar_wait(&s.fullU[tg % su], (uint32_t)(tg / su) & 1u, s.abort_flag, err) ? 1 : 0;
+                    ok = tc::mbar_wait(&s.fullU[ug % su], (uint32_t)(ug / su) & 1u, s.abort_flag, err) ? 1 : 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (SU > 0) __syncwarp();  // the other lanes read the U tile lane 0 waited for
             tc::tc_fence_after();
-            const unsigned char *sU = SU > 0 ? s.smem + kOffU + (tg % su) * kUBytes : nullptr;
+            const unsigned char *sU = SU > 0 ? s.smem + kOffU + (ug % su) * kUBytes : nullptr;
 #pragma unroll 1
             for (int h = 0; h < CW / 16; ++h) {
                 uint32_t acc[16];
@@ -512,7 +524,7 @@ struct Pipe {
                 f(t, col0 + t * tstride, 16 * h, acc, sU);
             }
             __syncwarp();
-            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[tg % su]);
+            if (SU > 0 && lane == 0) tc::mbar_arrive(&s.emptyU[ug % su]);
         }
     }
 
