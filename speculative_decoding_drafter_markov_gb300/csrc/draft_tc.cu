@@ -811,7 +811,7 @@ __global__ void wait_selfcheck_kernel(const int *flag, int target, int mode, uin
 
 // pipeline configurations
 // Pipe<requests per M-tile, vocabulary tile, W_2^T slab ring, U ring, operand split>
-using DraftM64 = tcp::Pipe<64, 128, 6, 4, 1>;          // Markov, R <= 64
+using DraftM64 = tcp::Pipe<64, 256, 3, 4, 1>;   // Markov, R <= 64 (U in 128-column parts)
 using DraftM128 = tcp::Pipe<128, 256, 2, 3, 1>;  // Markov, 128 requests per M-tile (U in 128-column parts)
 using DraftRnn = tcp::Pipe<128, 128, 2, 2, 2>;  // RNN (fp32 operand split hi/lo: 128 KB, so a 2-slot W_2^T ring)
 

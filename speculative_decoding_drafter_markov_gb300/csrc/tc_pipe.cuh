@@ -77,7 +77,8 @@ struct Pipe {
     static_assert(kMergeBytes <= kABytes, "merge scratch");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
     static_assert(CW == 16 || CW == 32 || CW == 64, "TMEM load width");
-    static_assert(UH == 1 || (!DUAL && kUCols % CW == 0), "a warp's columns lie in one U part");
+    static_assert(UH == 1 || (kUCols % CW == 0 && (!DUAL || (BN / 2) % kUCols == 0)),
+                  "a warp's columns lie in one U part");
     static_assert(MV == 64 || MV == 128, "M-tile rows");
 
     struct State {
