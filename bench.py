@@ -2,8 +2,9 @@
 """Benchmark of the DSpark per-cycle hot path on GB300.
 
 One step = one decoding cycle of the workload: the gamma-step Markov draft
-(fused bias contraction + exact softmax normaliser + Gumbel-max sample +
-confidence, per step) followed by verification of every drafted token of the
+(fused bias contraction + exact softmax normaliser + the two-level sample --
+16-entry blocks raced on their masses, the entry by inverse CDF -- + confidence,
+per step) followed by verification of every drafted token of the
 flattened batch (the qwen4b workload verifies all R * (gamma + 1) rows; workloads
 with a profiled SPS table also run the prefix scheduler and verify only the
 scheduled rows).
