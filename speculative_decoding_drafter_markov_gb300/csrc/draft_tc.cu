@@ -58,47 +58,8 @@ struct TcParams {
 };
 
 // eq. (7): c_k = sigma(w^T [h_k ; W_1[x_{k-1}]] / T_k) of one request (token
-// xp = x_{k-1}), by all epilogue threads, reduced in a fixed order through
-// `red` (16 floats of shared memory).
-__device__ __forceinline__ void confidence_row(const TcParams &p, int k, int grow, int xp, int et, float *red) {
-    const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
-    const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
-    float dot = 0.f;
-    if ((p.d & 7) == 0) {
-        const int hc = p.d / 8, nc = hc + p.r / 8;
-        for (int ch = et; ch < nc; ch += tcp::kEpiThreads) {
-            const uint4 raw = ch < hc ? *reinterpret_cast<const uint4 *>(h + ch * 8)
-                                      : *reinterpret_cast<const uint4 *>(e + (ch - hc) * 8);
-            const float *wv = p.w + ch * 8;  // w = [w_h ; w_e] lines up with [h ; e]
-            const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                dot = fmaf(wv[2 * i], tcp::bf16_lo(v[i]), dot);
-                dot = fmaf(wv[2 * i + 1], tcp::bf16_hi(v[i]), dot);
-            }
-        }
-    } else {
-        for (int j = et; j < p.d + p.r; j += tcp::kEpiThreads)
-            dot = fmaf(p.w[j], __bfloat162float(j < p.d ? h[j] : e[j - p.d]), dot);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if ((et & 31) == 0) red[et >> 5] = dot;
-    tc::named_bar_sync(1, tcp::kEpiThreads);
-    if (et == 0) {
-        float sum = 0.f;
-        for (int i = 0; i < tcp::kEpiThreads / 32; ++i) sum += red[i];
-        const float T_k = p.sts_T ? p.sts_T[k - 1] : 1.0f;
-        const size_t o = (size_t)grow * p.gamma + (k - 1);
-        p.c[o] = 1.0f / (1.0f + expf(-sum / T_k));
-        if (p.conf_logit) p.conf_logit[o] = sum;
-    }
-    tc::named_bar_sync(1, tcp::kEpiThreads);
-}
-
-// The same for one request by one warp (lanes over 16-byte chunks, four in
-// flight, then a fixed shuffle tree; lane 0 writes): the confidences deferred
-// to the end of the launch.
+// xp = x_{k-1}) by one warp: lanes over 16-byte chunks, four in flight, then a
+// fixed shuffle tree; lane 0 writes.  Computed after the launch's last step.
 __device__ __forceinline__ void confidence_warp(const TcParams &p, int k, int grow, int xp, int lane) {
     const __nv_bfloat16 *h = p.h + ((size_t)grow * p.gamma + (k - 1)) * (size_t)p.d;
     const __nv_bfloat16 *e = p.W1 + (size_t)xp * p.r;
@@ -526,12 +487,10 @@ __device__ __forceinline__ bool rnn_load_operand(const TcParams &p, typename P::
 // (bounded wait; the launch is cooperative, so all are resident) each reads
 // the winners x_k of its rows and gathers the next operand W_1[x_k] right away
 // -- the producer has already streamed the next step's first W_2^T slabs and U
-// tiles.  While it waits for the other CTAs, CTA cv computes the confidence
-// of row cv (one row per CTA hides behind the wait; the rows beyond the
-// M-tile's CTA count, with more requests than CTAs, are deferred).  Nothing
-// else sits between two steps: the rows' lse_k and log q_k (which need every
-// CTA's partial) and the deferred confidences (x_{k-1} from the per-step
-// winner words) are computed after the last step, spread over the CTAs' warps.
+// tiles.  Nothing else sits between two steps: the rows' lse_k and log q_k
+// (which need every CTA's partial) and the confidences c_k (x_{k-1} from the
+// per-step winner words) are computed after the last step, spread over the
+// CTAs' warps.
 template <class P>
 __global__ void __launch_bounds__(P::kThreads, 1)
     draft_step_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmU,
@@ -728,10 +687,6 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 }
             }
 
-            // while the other CTAs finish: the confidence c_k of local row cv
-            // (x_{k-1} is still in s.tok)
-            if (cv < P::MV && m0 + cv < p.R) confidence_row(p, k, m0 + cv, s.tok[cv], et, s.red);
-
             // wait (bounded) until every CTA of the M-tile has published this step
             if (!mtile_sync<P>(p, s, ctr, ++phase, et, false)) break;
             if (step + 1 < p.nsteps) {
@@ -768,12 +723,12 @@ __global__ void __launch_bounds__(P::kThreads, 1)
                 if (m0 + i < p.R)
                     finalise_row(p, p.part + (size_t)(p.step_index + si - 1) * p.R * p.nparts, m0 + i, p.k + si, lane);
             }
-            // deferred confidences: local rows nparts .. MV - 1 of every step; x_{k-1}
-            // is the launch's input token for its first step, else the previous
-            // step's winner (as the operand took it)
-            const int nrest = P::MV - p.nparts;
-            for (int pi = cv * tcp::kEpiWarps + warp; pi < p.nsteps * nrest; pi += p.nparts * tcp::kEpiWarps) {
-                const int si = pi / nrest, gr = m0 + p.nparts + (pi - si * nrest);
+            // the confidences c_k of every (step, request) pair of the M-tile, spread
+            // over all its CTAs' warps (kept off the step boundary, where the slowest
+            // CTA of the M-tile would carry them); x_{k-1} is the launch's input token
+            // for its first step, else the previous step's winner (as the operand took it)
+            for (int pi = cv * tcp::kEpiWarps + warp; pi < p.nsteps * P::MV; pi += p.nparts * tcp::kEpiWarps) {
+                const int si = pi / P::MV, gr = m0 + (pi - si * P::MV);
                 if (gr >= p.R) continue;
                 int xp;
                 if (si == 0) {
